@@ -1,0 +1,316 @@
+"""Independent checks ("pins") of the CPU oracle.
+
+Each ``check_*`` function takes the oracle function it checks as an argument and
+raises AssertionError on a mismatch, so that the same check can run against the
+real oracle (tests/test_oracle_*.py) and against deliberately broken copies of
+it (tests/test_oracle_mutations.py), showing that a plausible mistake is caught.
+
+The expected values never come from the oracle itself: they come from the
+pages' printed values (tests/golden/), exact rational arithmetic
+(``fractions.Fraction``), torch's float8_e4m3fn cast (a library routine that
+shares nothing with the oracle), brute force, or invariants.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------
+# exact helpers
+# ---------------------------------------------------------------------------
+def rn_f32(r: Fraction) -> Fraction:
+    """Round a rational to the nearest IEEE binary32 value, ties to even
+    (finite range only).  Written from the IEEE definition: quantum 2^(e-23)
+    for normal numbers, 2^-149 below 2^-126."""
+    if r == 0:
+        return Fraction(0)
+    sign = -1 if r < 0 else 1
+    a = abs(r)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    n = a / quantum
+    k = round(n)  # Fraction.__round__ rounds half to even
+    return sign * k * quantum
+
+
+def bf16_values(rng, shape, scale=1.0):
+    """Random bf16-representable float32 values (rounded by torch)."""
+    x = torch.from_numpy((rng.standard_normal(shape) * scale).astype(np.float32))
+    return x.to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line)
+    return rows
+
+
+def closed_forms():
+    out = {}
+    for row in read_golden("closed_forms.txt"):
+        k, v = row.split("=")
+        out[k.strip()] = int(v.strip())
+    return out
+
+
+# ---------------------------------------------------------------------------
+# INT8
+# ---------------------------------------------------------------------------
+def int8_expected_exact(row):
+    """Codes and scale of one row by exact rational arithmetic + IEEE rounding."""
+    amax = max(abs(Fraction(float(v))) for v in row)
+    s = rn_f32(amax / 127)
+    if s == 0:
+        return [0] * len(row), 0.0
+    codes = []
+    for v in row:
+        q = rn_f32(Fraction(float(v)) / s)
+        c = round(q)  # half to even
+        codes.append(max(-127, min(127, c)))
+    return codes, float(s)
+
+
+def check_int8_exact(int8_quantize, seed=0, rows=64, D=16):
+    rng = np.random.default_rng(seed)
+    x = bf16_values(rng, (rows, D))
+    x[::7, 3] *= 40.0  # outlier channel
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    codes, scales = int8_quantize(x)
+    for i in range(rows):
+        ec, es = int8_expected_exact(x[i])
+        assert float(scales[i]) == es, (i, float(scales[i]), es)
+        assert [int(c) for c in codes[i]] == ec, (i, codes[i], ec)
+
+
+def check_int8_ties(int8_quantize):
+    """Rows whose scale is exactly 1/8 (amax = 127/8), so x/s = k + 1/2 exactly."""
+    s = 0.125
+    amax = 127 * s
+    halves = [0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 125.5, 126.5, -126.5]
+    expect = [0, 2, 2, 4, 0, -2, -2, 126, 126, -126]  # round half to even
+    row = np.array([amax] + [h * s for h in halves], dtype=np.float32)
+    codes, scale = int8_quantize(row[None, :])
+    assert float(scale[0]) == s
+    assert int(codes[0, 0]) == 127
+    assert [int(c) for c in codes[0, 1:]] == expect, codes
+
+
+def check_int8_invariants(int8_quantize, int8_dequantize, seed=1):
+    rng = np.random.default_rng(seed)
+    x = bf16_values(rng, (200, 256))
+    x[:, [3, 77, 140, 201]] *= 8.0
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    codes, s = int8_quantize(x)
+    assert codes.dtype == np.int8
+    assert codes.min() >= -127 and codes.max() <= 127
+    xh = int8_dequantize(codes, s)
+    err = np.abs(x.astype(np.float64) - xh)
+    bound = (0.5 + 127 * 2.0 ** -24) * s.astype(np.float64)[:, None]
+    assert np.all(err <= bound)
+    i = np.argmax(np.abs(x), axis=1)
+    assert np.all(np.abs(codes[np.arange(len(x)), i]) == 127)
+    c2, s2 = int8_quantize(-x)
+    assert np.array_equal(c2, -codes) and np.array_equal(s2, s)
+    cz, sz = int8_quantize(np.zeros((3, 256), np.float32))
+    assert not cz.any() and not sz.any()
+
+
+# ---------------------------------------------------------------------------
+# E4M3 / E2M1 / NVFP4
+# ---------------------------------------------------------------------------
+def torch_e4m3_values():
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+
+
+def check_e4m3_decode(e4m3_value):
+    ours = e4m3_value(np.arange(256, dtype=np.uint8))
+    ref = torch_e4m3_values()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def check_e4m3_encode(e4m3_encode_satfinite, seed=2):
+    ref_vals = torch_e4m3_values()[:0x7F]
+    mids = (ref_vals[:-1] + ref_vals[1:]) / 2
+    rng = np.random.default_rng(seed)
+    t = np.concatenate([ref_vals, mids, rng.uniform(0, 448, 20000), np.exp(rng.uniform(-12, 6, 20000)),
+                        [2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11]])
+    t = t.astype(np.float32).astype(np.float64)
+    ours = e4m3_encode_satfinite(t)
+    ref = torch.from_numpy(t.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref), np.nonzero(ours != ref)
+    big = e4m3_encode_satfinite(np.array([448.0, 449.0, 470.0, 1e6]))
+    assert list(big) == [0x7E] * 4
+
+
+def check_e2m1_grid(e2m1_value):
+    golden = [float(v) for v in read_golden("e2m1_grid.txt")]
+    assert list(e2m1_value(np.arange(8))) == golden
+    assert list(e2m1_value(np.arange(8, 16))) == [-v for v in golden]
+
+
+def check_e2m1_ties(e2m1_encode):
+    # midpoints between neighbours go to the code with mantissa bit 0 (even code)
+    y = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, 7.0, 100.0, 0.3, -0.1, -0.0, 0.0, 5.5])
+    expect = [0, 2, 2, 4, 4, 6, 6, 8, 14, 7, 7, 1, 8, 8, 0, 7]
+    assert [int(c) for c in e2m1_encode(y)] == expect
+
+
+def check_nibble_order(pack_nibbles):
+    for row in read_golden("nibble_order.txt"):
+        lhs, rhs = row.split("->")
+        codes = np.array([int(t, 16) for t in lhs.split()], dtype=np.uint8)
+        packed = [int(t, 16) for t in rhs.split()]
+        assert [int(b) for b in pack_nibbles(codes)] == packed
+
+
+def nvfp4_expected_exact(row, gs):
+    """One row by exact rationals: fp32 steps by rn_f32, the E4M3 step by torch's
+    cast, the E2M1 step by brute-force nearest with ties to the even code."""
+    gs = Fraction(float(np.float32(gs)))
+    grid = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+    codes, scales = [], []
+    for g0 in range(0, len(row), 16):
+        grp_f = [float(v) for v in row[g0:g0 + 16]]
+        grp = [Fraction(v) for v in grp_f]
+        amax = max(abs(v) for v in grp)
+        t = rn_f32(amax / 6)
+        t2 = rn_f32(t * gs)
+        sf = int(torch.tensor([float(t2)], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+        if float(t2) > 448:
+            sf = 0x7E
+        sd = Fraction(float(torch.tensor([sf], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32)[0]))
+        scales.append(sf)
+        for v, vf in zip(grp, grp_f):
+            if sd == 0:
+                codes.append(0)
+                continue
+            y = rn_f32(rn_f32(v * gs) / sd)
+            a = abs(y)
+            best = min(range(8), key=lambda i: (abs(a - grid[i]), i % 2))
+            neg = y < 0 or (y == 0 and math.copysign(1.0, vf) < 0)
+            codes.append(best | (8 if neg else 0))
+    return codes, scales
+
+
+def check_nvfp4_exact(nvfp4_quantize, unpack_nibbles, seed=3, gs_list=(1.0, None)):
+    rng = np.random.default_rng(seed)
+    x = bf16_values(rng, (24, 64))
+    x[0, :16] = 0.0
+    x[1, 16:32] = 1e-4
+    x[2, 5] = -0.0
+    x[3, :] *= 30.0
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    for gs in gs_list:
+        if gs is None:
+            gs = float(np.float32(448.0 * 6.0) / np.float32(np.max(np.abs(x))))
+        codes, scales = nvfp4_quantize(x, gs)
+        c = unpack_nibbles(codes)
+        for i in range(x.shape[0]):
+            ec, es = nvfp4_expected_exact(x[i], gs)
+            assert [int(v) for v in scales[i]] == es, (gs, i)
+            assert [int(v) for v in c[i]] == ec, (gs, i)
+
+
+def check_nvfp4_invariants(nvfp4_quantize, nvfp4_dequantize, e4m3_value, seed=4):
+    rng = np.random.default_rng(seed)
+    x = bf16_values(rng, (100, 256))
+    for gs in (1.0, float(np.float32(2688.0) / np.float32(np.max(np.abs(x))))):
+        codes, scales = nvfp4_quantize(x, gs)
+        xh = nvfp4_dequantize(codes, scales, gs)
+        sd = e4m3_value(scales).repeat(16, axis=1) / np.float64(np.float32(gs))
+        err = np.abs(x - xh)
+        # largest gap of the E2M1 grid is 2 (between 4 and 6); within a group whose
+        # scale was rounded, |y| <= 6 * (1 + 2^-4); so the error is at most one grid gap.
+        assert np.all(err <= 2.0 * sd + 1e-12)
+        small = np.abs(x) * np.float64(np.float32(gs)) / np.maximum(e4m3_value(scales).repeat(16, axis=1), 1e-30) <= 4.0
+        assert np.all(err[small] <= 0.5 * sd[small] * (1 + 2.0 ** -18) + 1e-12)
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+def tiny_case(rng, G=3, L=17, D=8):
+    q = rng.standard_normal((G, D))
+    k = rng.standard_normal((L, D))
+    v = rng.standard_normal((L, D))
+    return q, k, v
+
+
+def check_attend_brute(attend, attend_brute, seed=5):
+    rng = np.random.default_rng(seed)
+    for (G, L, D) in [(1, 1, 8), (3, 17, 8), (6, 40, 16), (4, 33, 16), (2, 5, 8)]:
+        q, k, v = tiny_case(rng, G, L, D)
+        sm = 1.0 / math.sqrt(D)
+        o, s = attend(q, k, v, sm)
+        ob, sb = attend_brute(q.tolist(), k.tolist(), v.tolist(), sm)
+        assert np.max(np.abs(o - np.array(ob))) < 1e-12
+        assert np.max(np.abs(s - np.array(sb))) < 1e-12
+
+
+def check_split_merge(attend, attend_split, seed=6):
+    rng = np.random.default_rng(seed)
+    q, k, v = tiny_case(rng, 6, 96, 16)
+    sm = 0.25
+    o, s = attend(q, k, v, sm)
+    for bounds in ([(0, 96)], [(0, 48), (48, 96)], [(0, 16), (16, 17), (17, 80), (80, 96)],
+                   [(0, 0), (0, 96), (96, 96)], [(i, i + 16) for i in range(0, 96, 16)]):
+        om, sm_ = attend_split(q, k, v, sm, bounds)
+        assert np.max(np.abs(om - o)) < 1e-12
+        assert np.max(np.abs(sm_ - s)) < 1e-12
+
+
+def check_merge_not_average(attend, merge, seed=7):
+    """The page's warning: averaging partial outputs is not the attention result."""
+    rng = np.random.default_rng(seed)
+    q, k, v = tiny_case(rng, 2, 64, 8)
+    k[:32] *= 3.0
+    o1, s1 = attend(q, k[:32], v[:32], 1.0)
+    o2, s2 = attend(q, k[32:], v[32:], 1.0)
+    o, _ = attend(q, k, v, 1.0)
+    om, _ = merge(np.stack([o1, o2]), np.stack([s1, s2]))
+    assert np.max(np.abs(om - o)) < 1e-12
+    assert np.max(np.abs((o1 + o2) / 2 - o)) > 1e-3
+
+
+def check_attention_invariants(attend, probabilities, seed=8):
+    rng = np.random.default_rng(seed)
+    q, k, v = tiny_case(rng, 6, 50, 16)
+    p = probabilities(q, k, 0.3)
+    assert np.max(np.abs(p.sum(axis=1) - 1.0)) < 1e-14
+    # identical keys -> mean of V
+    kk = np.repeat(k[:1], 50, axis=0)
+    o, _ = attend(q, kk, v, 0.3)
+    assert np.max(np.abs(o - v.mean(axis=0)[None, :])) < 1e-12
+    # single token -> that V row, exactly
+    o, s = attend(q, k[:1], v[:1], 0.3)
+    assert np.array_equal(o, np.repeat(v[:1], 6, axis=0))
+    assert np.allclose(s, 0.3 * (q @ k[0]), atol=1e-14)
+    # empty context
+    o, s = attend(q, k[:0], v[:0], 0.3)
+    assert not o.any() and np.all(np.isneginf(s))
+    # identical queries in a group -> identical outputs
+    qq = np.repeat(q[:1], 6, axis=0)
+    o, _ = attend(qq, k, v, 0.3)
+    assert np.max(np.abs(o - o[:1])) == 0.0
+    # one dominant logit -> that row of V
+    kd = k.copy()
+    kd[17] = q[0] * 1e3
+    o, _ = attend(q[:1], kd, v, 1.0)
+    assert np.max(np.abs(o[0] - v[17])) < 1e-12

@@ -1,0 +1,80 @@
+"""The oracle's attention against brute force and invariants (CPU only)."""
+import numpy as np
+
+from oracle import attention, brute, layout
+from tests import oracle_pins as pins
+
+
+def test_attend_matches_pure_python_brute_force():
+    pins.check_attend_brute(attention.attend, brute.attend_brute)
+
+
+def test_split_then_merge_equals_unsplit():
+    pins.check_split_merge(attention.attend, attention.attend_split)
+
+
+def test_merge_is_not_an_average():
+    pins.check_merge_not_average(attention.attend, attention.merge)
+
+
+def test_attention_invariants():
+    pins.check_attention_invariants(attention.attend, attention.probabilities)
+
+
+def test_merge_skips_empty_segments():
+    o = np.ones((3, 2, 4))
+    s = np.array([[0.0, -np.inf], [-np.inf, -np.inf], [0.0, -np.inf]])
+    om, sm = attention.merge(o, s)
+    assert np.allclose(om[0], 1.0) and not om[1].any()
+    assert np.isclose(sm[0], np.log(2.0)) and np.isneginf(sm[1])
+
+
+def _paged_pool(rng, fmt, L, D, Hkv, perm):
+    P = 16
+    npages = -(-L // P)
+    k = pins.bf16_values(rng, (L, Hkv, D))
+    v = pins.bf16_values(rng, (L, Hkv, D))
+    pools = {}
+    for name, x in (("k", k), ("v", v)):
+        c, s = attention.quantize_rows(fmt, x.reshape(-1, D))
+        c = c.reshape(L, Hkv, -1)
+        cp = np.zeros((npages, Hkv, P, c.shape[-1]), np.uint8)
+        sp = None if s is None else np.full((npages, Hkv, P) + s.shape[1:], 0, s.dtype)
+        slots = layout.token_slots(perm, L, P)
+        for h in range(Hkv):
+            layout.scatter_rows(cp, slots, h, c[:, h])
+            if sp is not None:
+                layout.scatter_rows(sp, slots, h, s.reshape(L, Hkv, *s.shape[1:])[:, h])
+        pools[name + "_codes"], pools[name + "_scales"] = cp, sp
+    return pools
+
+
+def test_block_table_permutation_does_not_change_the_result():
+    rng = np.random.default_rng(11)
+    L, D, Hkv, G = 70, 16, 2, 3
+    npages = -(-L // 16)
+    q = pins.bf16_values(rng, (1, Hkv * G, D))
+    for fmt in ("int8", "nvfp4", "bf16"):
+        state = rng.bit_generator.state
+        outs = []
+        for perm in (np.arange(npages), rng.permutation(npages)):
+            rng.bit_generator.state = state
+            pools = _paged_pool(np.random.default_rng(5), fmt, L, D, Hkv, perm)
+            o, s = attention.paged_decode(fmt, pools, q, perm[None, :], [L], 0.25)
+            outs.append((o, s))
+        assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_paged_decode_equals_dense_attend_over_dequantized_rows():
+    rng = np.random.default_rng(12)
+    L, D, Hkv, G = 45, 16, 2, 2
+    perm = rng.permutation(3)
+    pools = _paged_pool(rng, "int8", L, D, Hkv, perm)
+    q = pins.bf16_values(rng, (1, Hkv * G, D))
+    o, s = attention.paged_decode("int8", pools, q, perm[None, :], [L], 0.25)
+    slots = layout.token_slots(perm, L, 16)
+    for h in range(Hkv):
+        k = attention.cache_rows("int8", pools["k_codes"], pools["k_scales"], slots, h)
+        v = attention.cache_rows("int8", pools["v_codes"], pools["v_scales"], slots, h)
+        ob, sb = brute.attend_brute(q[0, h * G:(h + 1) * G].tolist(), k.tolist(), v.tolist(), 0.25)
+        assert np.max(np.abs(o[0, h * G:(h + 1) * G] - np.array(ob))) < 1e-12

@@ -1,0 +1,101 @@
+"""Planted mistakes in (copies of) the oracle must be caught by the pins.
+
+Each mutant is a plausible slip — a wrong tie rule, a reciprocal instead of a
+division, a wrong bias, a swapped nibble, an averaged merge, a dropped scale —
+applied to the oracle on the CPU only.  A pin that lets a mutant pass would not
+be pinning anything.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention, formats
+from tests import oracle_pins as pins
+
+
+def _fails(check, *args):
+    with pytest.raises(AssertionError):
+        check(*args)
+
+
+def test_int8_mutants_are_caught():
+    def half_away(x):
+        x = np.asarray(x, np.float32)
+        s = (np.max(np.abs(x), -1) / np.float32(127)).astype(np.float32)
+        q = x / s[..., None]
+        c = np.clip(np.sign(q) * np.floor(np.abs(q) + 0.5), -127, 127)
+        return c.astype(np.int8), s
+
+    def reciprocal(x):
+        x = np.asarray(x, np.float32)
+        s = (np.max(np.abs(x), -1) / np.float32(127)).astype(np.float32)
+        q = (x * (np.float32(1) / s)[..., None]).astype(np.float32)
+        return np.clip(np.rint(q), -127, 127).astype(np.int8), s
+
+    def scale128(x):
+        x = np.asarray(x, np.float32)
+        s = (np.max(np.abs(x), -1) / np.float32(128)).astype(np.float32)
+        return np.clip(np.rint(x / s[..., None]), -127, 127).astype(np.int8), s
+
+    _fails(pins.check_int8_ties, half_away)
+    _fails(pins.check_int8_exact, reciprocal, 0, 512, 64)
+    _fails(pins.check_int8_exact, scale128)
+
+
+def test_fp8_fp4_mutants_are_caught():
+    def bias8(b):
+        return formats.e4m3_value(b) / 2.0
+
+    def ties_up(t):
+        t = np.asarray(t, np.float64)
+        grid = formats._E4M3_POS
+        idx = np.clip(np.searchsorted(grid, np.abs(t), side="right"), 1, len(grid) - 1)
+        lo, hi = idx - 1, idx
+        pick = np.abs(t) - grid[lo] >= grid[hi] - np.abs(t)
+        return np.where(pick, hi, lo).astype(np.uint8)
+
+    def swapped_grid(c):
+        g = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 4.0, 3.0, 6.0])
+        c = np.asarray(c, np.int64)
+        return np.where(c & 8, -1.0, 1.0) * g[c & 7]
+
+    def swapped_nibbles(c):
+        c = np.asarray(c, np.uint8)
+        return (c[..., 1::2] | (c[..., 0::2] << 4)).astype(np.uint8)
+
+    def amax_over_4(x, gs):
+        return formats.nvfp4_quantize(np.asarray(x, np.float32) * np.float32(1.5), gs)
+
+    _fails(pins.check_e4m3_decode, bias8)
+    _fails(pins.check_e4m3_encode, ties_up)
+    _fails(pins.check_e2m1_grid, swapped_grid)
+    _fails(pins.check_nibble_order, swapped_nibbles)
+    _fails(pins.check_nvfp4_exact, amax_over_4, formats.unpack_nibbles)
+
+
+def test_attention_mutants_are_caught():
+    from oracle import brute
+
+    def no_scale(q, k, v, sm):
+        return attention.attend(q, k, v, 1.0)
+
+    def transposed_v(q, k, v, sm):
+        o, s = attention.attend(q, k, v, sm)
+        return o[:, ::-1], s
+
+    def averaged(outs, lses):
+        return np.mean(outs, axis=0), np.max(lses, axis=0)
+
+    def split_with_average(q, k, v, sm, bounds):
+        outs, lses = zip(*[attention.attend(q, k[b:e], v[b:e], sm) for b, e in bounds])
+        return averaged(np.stack(outs), np.stack(lses))
+
+    def lse_without_log(q, k, v, sm):
+        o, s = attention.attend(q, k, v, sm)
+        p = attention.probabilities(q, k, sm)
+        return o, s - np.log(1.0 / p.max(axis=1)) * 0 + 0.5
+
+    _fails(pins.check_attend_brute, no_scale, brute.attend_brute)
+    _fails(pins.check_attend_brute, transposed_v, brute.attend_brute)
+    _fails(pins.check_attend_brute, lse_without_log, brute.attend_brute)
+    _fails(pins.check_split_merge, attention.attend, split_with_average)
+    _fails(pins.check_merge_not_average, attention.attend, averaged)
