@@ -1,0 +1,255 @@
+/*
+ * kvq.h — C ABI of libkvq: a quantized paged KV cache for GB300 (sm_103a).
+ *
+ * Three operations, each one kernel launch (or two) on the caller's stream:
+ *
+ *   kvq_quant_append            quantize new K/V rows and scatter them into pool slots
+ *   kvq_paged_decode_attention  split-KV (flash-decoding) GQA decode attention that
+ *                               reads the quantized pages directly
+ *   kvq_split_merge             log-sum-exp combine of the per-split partial results
+ *
+ * plus host helpers (byte accounting, split planning, workspace sizing, errors).
+ *
+ * Sources (the pages that define the operations):
+ *   [int8-kv]   "half-the-memory-int8-kv-cache" (Making a ternary reasoning model
+ *               fast in vLLM), sections "An 8-bit cache was already available" and
+ *               "Read the compressed cache without copying it first".
+ *   [long-ctx]  "long-context-attention-and-lessons", section "Give more GPU
+ *               workers a piece of the attention calculation".
+ *   [nvfp4]     "Building an NVFP4 KV cache for a hybrid Qwen model", sections
+ *               "How 2,048 bytes became 576" and "Writing and reading the packed cache".
+ *   [capstone]  "Smaller KV cache, faster first token", section "Lever two:
+ *               block-sparse attention with BLASST" (one KV block is loaded once
+ *               for a whole GQA group).
+ *
+ * Conventions for every call
+ *   - Pointers named "device" are CUDA device pointers on the current device;
+ *     "host" pointers are ordinary host memory.  The caller owns all memory
+ *     (pools, workspace, outputs) and the stream; the library allocates nothing
+ *     and, unless KVQ_CHECKED is given, never synchronizes, so raw calls can be
+ *     captured into a CUDA graph.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Every call returns a kvq_status; on failure kvq_last_error() returns a
+ *     message (thread-local).  No exception or abort crosses the ABI.
+ *   - Errors found on the device (an out-of-range page id or slot, a bounded
+ *     wait that ran out) never fault or trap: the kernel skips the access, sets a
+ *     bit in a device status word and finishes.  KVQ_CHECKED reads that word
+ *     before returning; raw callers read it with kvq_read_status().
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,    /* a null pointer, bad size or inconsistent argument */
+  KVQ_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (see below) */
+  KVQ_ERR_WORKSPACE = 3,      /* workspace or plan buffer too small */
+  KVQ_ERR_CUDA = 4,           /* a CUDA runtime call failed */
+  KVQ_ERR_DEVICE_CHECK = 5,   /* the device status word reports invalid metadata */
+  KVQ_ERR_DEVICE_TIMEOUT = 6  /* a bounded device wait ran out */
+} kvq_status;
+
+/* ---- cache formats ([int8-kv], [nvfp4]) --------------------------------- */
+enum {
+  KVQ_FMT_BF16 = 0,  /* bf16 values, no scales (comparison format) */
+  KVQ_FMT_INT8 = 1,  /* int8 codes + one fp32 scale per (token, KV head), scale = absmax/127 */
+  KVQ_FMT_NVFP4 = 2  /* E2M1 codes, 2 per byte (element 2j low nibble), one E4M3 scale per
+                        16 elements, one fp32 global scale per tensor; x = fp4*scale/global */
+};
+
+/* ---- output dtypes ------------------------------------------------------ */
+enum { KVQ_OUT_F32 = 0, KVQ_OUT_BF16 = 1 };
+
+/* ---- flags --------------------------------------------------------------- */
+enum {
+  KVQ_CHECKED = 1u,    /* validate metadata on the host, synchronize, read the device
+                          status word; not graph-capturable ([nvfp4] "Testing the cache
+                          without loading the model": the checked API syncs) */
+  KVQ_SKIP_MERGE = 2u  /* decode only: leave the split partials in the workspace and
+                          do not launch the merge (the caller calls kvq_split_merge) */
+};
+
+/* device status word bits (kvq_read_status) */
+enum {
+  KVQ_DEV_BAD_PAGE = 1,      /* block-table entry outside [0, num_pages) */
+  KVQ_DEV_BAD_SEQLEN = 2,    /* seq_len < 0 or > max_pages_per_seq * page_size */
+  KVQ_DEV_BAD_PLAN = 4,      /* plan entry outside the batch / split range */
+  KVQ_DEV_TIMEOUT = 8,       /* a pipeline wait gave up */
+  KVQ_DEV_BAD_SLOT = 16,     /* append: slot >= num_pages * page_size */
+  KVQ_DEV_NONFINITE = 32     /* append (checked): a non-finite input value */
+};
+
+/*
+ * The paged pool ([capstone] "Why KV capacity drives TTFT under load": the cache
+ * is managed in fixed-size blocks, like virtual-memory pages).
+ *
+ * Layout (all arrays dense, row-major, device memory, base 256-byte aligned):
+ *   k_codes, v_codes   [num_pages][num_kv_heads][page_size][row_bytes]
+ *                      row_bytes = 2*head_dim (BF16), head_dim (INT8), head_dim/2 (NVFP4)
+ *   k_scales, v_scales INT8:  [num_pages][num_kv_heads][page_size] float
+ *                      NVFP4: [num_pages][num_kv_heads][page_size][head_dim/16] E4M3 bytes
+ *                      BF16:  unused (NULL)
+ * Slot s is row (s % page_size) of page (s / page_size).  Each (page, KV head)
+ * block is contiguous, so one page of one head streams as one 16-byte-aligned
+ * block; the scales live in their own arrays so that code rows stay aligned
+ * (the pages' vLLM layout put a 4-byte scale after each 256-byte row, which
+ * blocked wide loads: [int8-kv] "Read the compressed cache without copying it first").
+ *
+ * Supported: page_size 16; head_dim 128 or 256 (NVFP4: 256); any num_kv_heads >= 1.
+ * NVFP4 global scales must be finite and > 0 and must stay fixed while entries
+ * are live ([nvfp4] "How 2,048 bytes became 576").
+ */
+typedef struct kvq_cache {
+  void* k_codes;
+  void* v_codes;
+  void* k_scales;
+  void* v_scales;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t format;         /* KVQ_FMT_* */
+  float k_global_scale;   /* NVFP4 only */
+  float v_global_scale;   /* NVFP4 only */
+} kvq_cache;
+
+/* ---- host helpers: byte accounting ([int8-kv], [nvfp4]) ----------------- */
+
+/* K+V bytes one token occupies in one layer (codes + scales, all KV heads):
+ * BF16 4*D*Hkv, INT8 2*(D+4)*Hkv (520 per head at D=256), NVFP4 2*(D/2+D/16)*Hkv
+ * (576 per token per layer at 2 heads, D=256).  Returns -1 for an unknown format
+ * or a non-positive size.  Host only; no GPU needed. */
+int64_t kvq_bytes_per_token(int32_t format, int32_t num_kv_heads, int32_t head_dim);
+
+/* Sizes in bytes of one codes array and one scales array of a pool (each of K and
+ * V has one of each).  Host only.  Returns KVQ_OK or KVQ_ERR_INVALID_ARG. */
+int kvq_cache_array_bytes(int32_t format, int32_t num_pages, int32_t page_size,
+                          int32_t num_kv_heads, int32_t head_dim,
+                          int64_t* codes_bytes, int64_t* scales_bytes);
+
+/* ---- kv_quant_append ([int8-kv] "An 8-bit cache was already available";
+ *      [nvfp4] "Writing and reading the packed cache") ---------------------- */
+/*
+ * Quantize n_tokens new rows of K and V and write them into the pool.
+ *   k_new, v_new   device, bf16 [n_tokens][num_kv_heads][head_dim]
+ *   slot_mapping   device, int64 [n_tokens]; token i goes to slot slot_mapping[i];
+ *                  a negative slot means "do not write" (padding).  Valid slots must
+ *                  be unique within a call; KVQ_CHECKED rejects duplicates.
+ *   dev_status     device int32 word (nullable).  Slots >= num_pages*page_size are
+ *                  skipped and set KVQ_DEV_BAD_SLOT there; with KVQ_CHECKED a
+ *                  non-finite input sets KVQ_DEV_NONFINITE.  KVQ_CHECKED needs it.
+ * INT8: per (token, head) s = fp32(absmax/127), code = clamp(rne(fp32(x/s)),-127,127),
+ *       s == 0 gives zero codes.
+ * NVFP4: per group of 16: t = fp32(amax/6), scale byte = E4M3_rne_satfinite(fp32(t*gs)),
+ *       code = E2M1_rne_satfinite(fp32(fp32(x*gs)/scale)) with the sign of x, zero
+ *       codes when the scale is 0; element 2j in the low nibble.
+ * BF16: the rows are copied.
+ * Overwriting a slot that holds older data is allowed.
+ */
+int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_new,
+                     const int64_t* slot_mapping, int64_t n_tokens,
+                     int32_t* dev_status, uint32_t flags, void* stream);
+
+/* ---- split planning ([long-ctx]: split-KV; the split count trades merge
+ *      overhead against parallelism) ----------------------------------------- */
+/*
+ * Choose, on the host, how many splits each sequence gets and write a plan:
+ *   plan[0..batch]               split_offsets: sequence b owns partial slots
+ *                                [plan[b], plan[b+1]), plan[0] = 0, plan[batch] = total
+ *   plan[batch+1 .. batch+total] the order in which work items are launched: split
+ *                                indices sorted by decreasing page count
+ * Split s of a sequence with n pages and S splits covers pages
+ * [floor(s*n/S), floor((s+1)*n/S)) — whole pages, sizes differing by at most one.
+ *   seq_lens        host int32 [batch], each >= 0
+ *   split_override  > 0: S_b = clamp(split_override, 1, max(n_pages_b, 1));
+ *                   0: automatic — about one work item per resident CTA slot:
+ *                   pages per item = max(4, ceil(Hkv * total_pages / target_ctas))
+ *   target_ctas     concurrent CTAs to plan for; 0 = measured on the current device
+ *                   (SM count x resident decode CTAs per SM for this format/head_dim)
+ *   plan            host int32 buffer of plan_capacity entries (nullable for a size query)
+ *   total_splits, max_splits  out (always written when the inputs are valid)
+ * Returns KVQ_ERR_WORKSPACE if plan is NULL or shorter than batch + 1 + total.
+ * The plan must be copied to the device before kvq_paged_decode_attention.
+ */
+int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch,
+                    int32_t split_override, int32_t target_ctas,
+                    int32_t* plan, int64_t plan_capacity,
+                    int32_t* total_splits, int32_t* max_splits);
+
+/* Workspace bytes for a decode call: a 256-byte status block, then
+ * lse_part float[total_splits][num_q_heads] (padded to 256 bytes), then
+ * o_part float[total_splits][num_q_heads][head_dim].  The status block must be
+ * zero before the first call (e.g. cudaMemset once); the library only ORs bits
+ * into it and kvq_read_status clears it. */
+size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int32_t head_dim);
+
+/* Device pointers to the partials inside a workspace (host pointer arithmetic). */
+int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_heads,
+                           int32_t head_dim, float** o_part, float** lse_part);
+
+/* ---- paged_decode_attention ([long-ctx] split-KV; [int8-kv] "Read the
+ *      compressed cache without copying it first": dequantize in registers) --- */
+/*
+ * out[b][g] = softmax(sm_scale * q[b][g] . K_b^T) . V_b for every sequence b and
+ * query head g, with K_b/V_b the dequantized cache rows of KV head g / (Hq/Hkv)
+ * (consecutive query heads share a KV head), tokens 0..seq_lens[b]-1 in the order
+ * of the block table.  One CTA handles one (split, KV head) work item and loads
+ * each page once for the whole query-head group.
+ *   q              device bf16 [batch][num_q_heads][head_dim]
+ *   sm_scale       softmax scale, normally 1/sqrt(head_dim)
+ *   block_tables   device int32 [batch][max_pages_per_seq]; page j of sequence b
+ *   seq_lens       device int32 [batch]
+ *   plan           device int32, the kvq_plan_splits output for these seq_lens
+ *   workspace      device, >= kvq_decode_workspace_bytes(total_splits, Hq, D)
+ *   out            device, [batch][num_q_heads][head_dim] float or bf16 (out_dtype)
+ *   lse_out        device float [batch][num_q_heads] (nullable): natural-log
+ *                  log-sum-exp of the scaled logits (-inf for an empty context)
+ * An empty context gives out = 0.  Tokens past seq_len in the last page are never
+ * read into the softmax, whatever their slots hold.  Sequences with a single
+ * split are written directly; the others are combined by the merge kernel on the
+ * same stream (unless KVQ_SKIP_MERGE).
+ * Supported: num_q_heads % num_kv_heads == 0 and 1 <= num_q_heads/num_kv_heads <= 8.
+ */
+int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t batch,
+                               int32_t num_q_heads, float sm_scale,
+                               const int32_t* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, const int32_t* plan,
+                               int32_t total_splits, void* workspace, size_t workspace_bytes,
+                               void* out, int32_t out_dtype, float* lse_out,
+                               uint32_t flags, void* stream);
+
+/* ---- split_merge ([long-ctx]: merge with the normalisation terms; averaging
+ *      the partial outputs would be wrong) ------------------------------------ */
+/*
+ * For every sequence with S_b = split_offsets[b+1]-split_offsets[b] >= 2 and query
+ * head g: M = max_s lse[s], w_s = exp(lse[s] - M), out = sum_s w_s o[s] / sum_s w_s,
+ * lse_out = M + log(sum_s w_s); empty splits (lse = -inf) have weight 0.  Rows are
+ * o_part[(split_offsets[b]+s)*num_q_heads + g][head_dim], lse_part likewise.
+ * Sequences with S_b = 1 are skipped (the decode kernel wrote them directly).
+ *   o_part, lse_part, split_offsets  device; out, lse_out (nullable) device.
+ */
+int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* split_offsets,
+                    int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                    void* out, int32_t out_dtype, float* lse_out, void* stream);
+
+/* Synchronize `stream`, read and clear a device status word (the first int32 of a
+ * decode workspace, or an append dev_status).  *bits receives the KVQ_DEV_* bits.
+ * Returns KVQ_OK, KVQ_ERR_DEVICE_CHECK or KVQ_ERR_DEVICE_TIMEOUT. */
+int kvq_read_status(void* dev_status, void* stream, int32_t* bits);
+
+/* Last error message of the calling thread ("" if none). */
+const char* kvq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

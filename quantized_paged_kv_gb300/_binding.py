@@ -1,0 +1,194 @@
+"""ctypes binding of libkvq.so — argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/kvq.h)
+and does nothing but turn torch tensors into device pointers, torch streams into
+cudaStream_t handles, and non-zero status codes into exceptions.  All of the work
+runs in the library's sm_103a kernels; there is no fallback: if libkvq.so is
+missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkvq.so")
+
+KVQ_FMT_BF16, KVQ_FMT_INT8, KVQ_FMT_NVFP4 = 0, 1, 2
+KVQ_OUT_F32, KVQ_OUT_BF16 = 0, 1
+KVQ_CHECKED, KVQ_SKIP_MERGE = 1, 2
+KVQ_DEV_BAD_PAGE, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_BAD_PLAN = 1, 2, 4
+KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_SLOT, KVQ_DEV_NONFINITE = 8, 16, 32
+FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4}
+
+# every symbol include/kvq.h declares
+EXPORTS = (
+    "kvq_bytes_per_token", "kvq_cache_array_bytes", "kvq_quant_append", "kvq_plan_splits",
+    "kvq_decode_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
+    "kvq_split_merge", "kvq_read_status", "kvq_last_error",
+)
+
+
+class KvqCacheStruct(ctypes.Structure):
+    _fields_ = [
+        ("k_codes", c_void_p), ("v_codes", c_void_p), ("k_scales", c_void_p), ("v_scales", c_void_p),
+        ("num_pages", c_int32), ("page_size", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
+        ("format", c_int32), ("k_global_scale", c_float), ("v_global_scale", c_float),
+    ]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"[kvq status {code}] {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """Load libkvq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "or python -m quantized_paged_kv_gb300.build")
+    L = ctypes.CDLL(LIB_PATH)
+    P = c_void_p
+    sig = {
+        "kvq_bytes_per_token": (c_int64, [c_int32, c_int32, c_int32]),
+        "kvq_cache_array_bytes": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32, POINTER(c_int64), POINTER(c_int64)]),
+        "kvq_quant_append": (c_int32, [POINTER(KvqCacheStruct), P, P, P, c_int64, P, c_uint32, P]),
+        "kvq_plan_splits": (c_int32, [POINTER(KvqCacheStruct), POINTER(c_int32), c_int32, c_int32, c_int32,
+                                      POINTER(c_int32), c_int64, POINTER(c_int32), POINTER(c_int32)]),
+        "kvq_decode_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
+        "kvq_workspace_partials": (c_int32, [P, c_int32, c_int32, c_int32, POINTER(c_void_p), POINTER(c_void_p)]),
+        "kvq_paged_decode_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P, c_int32,
+                                                 P, P, c_int32, P, c_size_t, P, c_int32, P, c_uint32, P]),
+        "kvq_split_merge": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P, c_int32, P, P]),
+        "kvq_read_status": (c_int32, [P, P, POINTER(c_int32)]),
+        "kvq_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise KvqError(rc, f"{name}: {lib().kvq_last_error().decode()}")
+
+
+def _need(t, dtype, name, device=True):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+# ----------------------------------------------------------------- host helpers
+def kvq_bytes_per_token(fmt, num_kv_heads, head_dim):
+    return int(lib().kvq_bytes_per_token(FORMATS.get(fmt, fmt), num_kv_heads, head_dim))
+
+
+def kvq_cache_array_bytes(fmt, num_pages, page_size, num_kv_heads, head_dim):
+    cb, sb = c_int64(), c_int64()
+    _check(lib().kvq_cache_array_bytes(FORMATS.get(fmt, fmt), num_pages, page_size, num_kv_heads, head_dim,
+                                       ctypes.byref(cb), ctypes.byref(sb)), "kvq_cache_array_bytes")
+    return cb.value, sb.value
+
+
+def kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim):
+    return int(lib().kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim))
+
+
+def kvq_plan_splits(cache_struct, seq_lens, split_override=0, target_ctas=0):
+    """seq_lens: host int sequence.  Returns (plan int32 CPU tensor, total_splits, max_splits)."""
+    sl = torch.as_tensor(list(seq_lens), dtype=torch.int32)
+    B = sl.numel()
+    total, mx = c_int32(), c_int32()
+    L = lib()
+    rc = L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
+                           split_override, target_ctas, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    if rc not in (0, 3):  # 3 = KVQ_ERR_WORKSPACE (size query)
+        _check(rc, "kvq_plan_splits")
+    plan = torch.zeros(B + 1 + total.value, dtype=torch.int32)
+    _check(L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
+                             split_override, target_ctas, plan.numpy().ctypes.data_as(POINTER(c_int32)),
+                             plan.numel(), ctypes.byref(total), ctypes.byref(mx)), "kvq_plan_splits")
+    return plan, total.value, mx.value
+
+
+def kvq_workspace_partials(workspace, total_splits, num_q_heads, head_dim):
+    o, l = c_void_p(), c_void_p()
+    _check(lib().kvq_workspace_partials(_ptr(workspace), total_splits, num_q_heads, head_dim, ctypes.byref(o),
+                                        ctypes.byref(l)), "kvq_workspace_partials")
+    return o.value, l.value
+
+
+def kvq_read_status(dev_status, stream=None):
+    """Returns (status code, bits) without raising."""
+    bits = c_int32()
+    rc = lib().kvq_read_status(_ptr(dev_status), _stream(stream), ctypes.byref(bits))
+    return rc, bits.value
+
+
+def kvq_last_error():
+    return lib().kvq_last_error().decode()
+
+
+# ----------------------------------------------------------------- device calls
+def kvq_quant_append(cache_struct, k_new, v_new, slot_mapping, dev_status=None, flags=0, stream=None):
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    n = slot_mapping.numel()
+    if k_new.shape != v_new.shape or k_new.shape[0] != n:
+        raise ValueError("k_new / v_new must be [n_tokens, Hkv, D] and match slot_mapping")
+    _check(lib().kvq_quant_append(ctypes.byref(cache_struct), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n,
+                                  _ptr(dev_status), flags, _stream(stream)), "kvq_quant_append")
+
+
+def kvq_paged_decode_attention(cache_struct, q, sm_scale, block_tables, seq_lens, plan, total_splits, workspace,
+                               out, lse_out=None, flags=0, stream=None):
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(plan, torch.int32, "plan")
+    _need(workspace, torch.uint8, "workspace")
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    _need(out, out.dtype, "out")
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out")
+    B, Hq, _ = q.shape
+    od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
+    _check(lib().kvq_paged_decode_attention(
+        ctypes.byref(cache_struct), _ptr(q), B, Hq, float(sm_scale), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), _ptr(plan), total_splits, _ptr(workspace), workspace.numel(), _ptr(out), od, _ptr(lse_out),
+        flags, _stream(stream)), "kvq_paged_decode_attention")
+
+
+def kvq_split_merge(o_part_ptr, lse_part_ptr, split_offsets, batch, num_q_heads, head_dim, out, lse_out=None,
+                    stream=None):
+    od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
+    _check(lib().kvq_split_merge(c_void_p(o_part_ptr), c_void_p(lse_part_ptr), _ptr(split_offsets), batch,
+                                 num_q_heads, head_dim, _ptr(out), od, _ptr(lse_out), _stream(stream)),
+           "kvq_split_merge")

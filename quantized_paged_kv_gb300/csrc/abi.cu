@@ -1,0 +1,451 @@
+// abi.cu — the extern "C" entry points declared in include/kvq.h: argument
+// validation, the host split planner, TMA tensor-map encoding and kernel dispatch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return code;
+}
+
+int succeed() {
+  g_error.clear();
+  return KVQ_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int64_t row_bytes(int format, int D) {
+  switch (format) {
+    case KVQ_FMT_BF16: return 2LL * D;
+    case KVQ_FMT_INT8: return D;
+    case KVQ_FMT_NVFP4: return D / 2;
+    default: return -1;
+  }
+}
+
+int64_t scale_row_bytes(int format, int D) {
+  switch (format) {
+    case KVQ_FMT_BF16: return 0;
+    case KVQ_FMT_INT8: return 4;
+    case KVQ_FMT_NVFP4: return D / 16;
+    default: return -1;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates the shape (and, if `pointers`, the device arrays) of a cache.
+int check_cache(const kvq_cache* c, bool pointers) {
+  if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
+  if (c->format != KVQ_FMT_BF16 && c->format != KVQ_FMT_INT8 && c->format != KVQ_FMT_NVFP4)
+    return fail(KVQ_ERR_INVALID_ARG, "unknown cache format %d", c->format);
+  if (c->page_size != 16) return fail(KVQ_ERR_UNSUPPORTED, "page_size %d: only 16 is implemented", c->page_size);
+  if (c->head_dim != 128 && c->head_dim != 256)
+    return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d: only 128 and 256 are implemented", c->head_dim);
+  if (c->format == KVQ_FMT_NVFP4 && c->head_dim != 256)
+    return fail(KVQ_ERR_UNSUPPORTED, "NVFP4 is implemented for head_dim 256 only");
+  if (c->num_kv_heads < 1) return fail(KVQ_ERR_INVALID_ARG, "num_kv_heads %d < 1", c->num_kv_heads);
+  if (c->num_pages < 1) return fail(KVQ_ERR_INVALID_ARG, "num_pages %d < 1", c->num_pages);
+  if ((int64_t)c->num_pages * c->num_kv_heads * c->page_size > 0x7FFFFFFFLL)
+    return fail(KVQ_ERR_UNSUPPORTED, "num_pages * num_kv_heads * page_size exceeds 2^31 rows");
+  if (c->format == KVQ_FMT_NVFP4) {
+    if (!(std::isfinite(c->k_global_scale) && c->k_global_scale > 0.f && std::isfinite(c->v_global_scale) &&
+          c->v_global_scale > 0.f))
+      return fail(KVQ_ERR_INVALID_ARG, "NVFP4 global scales must be finite and > 0");
+  }
+  if (pointers) {
+    if (!c->k_codes || !c->v_codes) return fail(KVQ_ERR_INVALID_ARG, "code arrays are NULL");
+    if (!aligned16(c->k_codes) || !aligned16(c->v_codes))
+      return fail(KVQ_ERR_INVALID_ARG, "code arrays must be 16-byte aligned");
+    if (c->format != KVQ_FMT_BF16) {
+      if (!c->k_scales || !c->v_scales) return fail(KVQ_ERR_INVALID_ARG, "scale arrays are NULL");
+      if (!aligned16(c->k_scales) || !aligned16(c->v_scales))
+        return fail(KVQ_ERR_INVALID_ARG, "scale arrays must be 16-byte aligned");
+    }
+  }
+  return KVQ_OK;
+}
+
+// --------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 5-D map over a codes array [num_pages][Hkv][16 rows][row_bytes]: dimensions
+// (innermost first) 128 bytes of a row half, 16 rows (stride row_bytes), row
+// halves (stride 128), KV heads (stride 16 * row_bytes), pages.  One box = the
+// `hg` consecutive heads of one page, landing in shared memory as
+// [head][half][row][128 bytes] with the 128-byte swizzle the decode kernel's
+// ldmatrix addressing expects.
+int make_code_map(CUtensorMap* map, void* base, int64_t num_pages, int64_t hkv, int64_t rbytes, int hg) {
+  auto fn = encode_fn();
+  if (!fn) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[5] = {128, 16, static_cast<cuuint64_t>(rbytes / 128), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(rbytes), 128, static_cast<cuuint64_t>(16 * rbytes),
+                                 static_cast<cuuint64_t>(16 * rbytes * hkv)};
+  const cuuint32_t box[5] = {128, 16, static_cast<cuuint32_t>(rbytes / 128), static_cast<cuuint32_t>(hg), 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return KVQ_OK;
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// KV heads per decode work item for a cache (0 if no kernel exists for it).
+int heads_per_cta(const kvq_cache* c) {
+  kvq::DecodeInstance inst;
+  if (!kvq::decode_instance(c->format, c->head_dim, &inst)) return 0;
+  return gcd_int(c->num_kv_heads, inst.consumer_warps);
+}
+
+// --------------------------------------------------------------- decode instances
+int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
+  if (!kvq::decode_instance(format, D, inst))
+    return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for format %d head_dim %d", format, D);
+  static std::mutex mu;
+  static bool done[64][3][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  bool& d = done[dev][format][D == 256 ? 1 : 0];
+  if (!d) {
+    e = cudaFuncSetAttribute(inst->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, inst->smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+    d = true;
+  }
+  return KVQ_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+int64_t kvq_bytes_per_token(int32_t format, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || head_dim % 16 != 0) return -1;
+  const int64_t rb = row_bytes(format, head_dim), sb = scale_row_bytes(format, head_dim);
+  if (rb < 0 || sb < 0) return -1;
+  return 2 * (rb + sb) * num_kv_heads;
+}
+
+int kvq_cache_array_bytes(int32_t format, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                          int32_t head_dim, int64_t* codes_bytes, int64_t* scales_bytes) {
+  if (num_pages < 0 || page_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 16 != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "bad pool shape");
+  const int64_t rb = row_bytes(format, head_dim), sb = scale_row_bytes(format, head_dim);
+  if (rb < 0) return fail(KVQ_ERR_INVALID_ARG, "unknown cache format %d", format);
+  const int64_t rows = (int64_t)num_pages * num_kv_heads * page_size;
+  if (codes_bytes) *codes_bytes = rows * rb;
+  if (scales_bytes) *scales_bytes = rows * sb;
+  return succeed();
+}
+
+int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                     int64_t n_tokens, int32_t* dev_status, uint32_t flags, void* stream) {
+  int rc = check_cache(cache, true);
+  if (rc) return rc;
+  if (n_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "n_tokens %lld < 0", (long long)n_tokens);
+  if (n_tokens == 0) return succeed();
+  if (!k_new || !v_new || !slot_mapping) return fail(KVQ_ERR_INVALID_ARG, "k_new, v_new or slot_mapping is NULL");
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(KVQ_ERR_INVALID_ARG, "k_new / v_new must be 16-byte aligned");
+  if (n_tokens > ((int64_t)1 << 40) / cache->num_kv_heads)
+    return fail(KVQ_ERR_UNSUPPORTED, "too many rows in one append");
+  const bool checked = flags & KVQ_CHECKED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t capacity = (int64_t)cache->num_pages * cache->page_size;
+  if (checked) {
+    if (!dev_status) return fail(KVQ_ERR_INVALID_ARG, "KVQ_CHECKED append needs dev_status");
+    std::vector<int64_t> slots(n_tokens);
+    cudaError_t e = cudaMemcpyAsync(slots.data(), slot_mapping, n_tokens * sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading slot_mapping");
+    std::vector<int64_t> valid;
+    valid.reserve(n_tokens);
+    for (int64_t i = 0; i < n_tokens; ++i) {
+      if (slots[i] >= capacity)
+        return fail(KVQ_ERR_INVALID_ARG, "slot_mapping[%lld] = %lld >= capacity %lld", (long long)i,
+                    (long long)slots[i], (long long)capacity);
+      if (slots[i] >= 0) valid.push_back(slots[i]);
+    }
+    std::sort(valid.begin(), valid.end());
+    const auto dup = std::adjacent_find(valid.begin(), valid.end());
+    if (dup != valid.end()) return fail(KVQ_ERR_INVALID_ARG, "duplicate valid slot %lld in one append", (long long)*dup);
+  }
+  kvq::AppendParams p{};
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.slots = slot_mapping;
+  p.k_codes = static_cast<uint8_t*>(cache->k_codes);
+  p.v_codes = static_cast<uint8_t*>(cache->v_codes);
+  p.k_scales = static_cast<uint8_t*>(cache->k_scales);
+  p.v_scales = static_cast<uint8_t*>(cache->v_scales);
+  p.status = dev_status;
+  p.n_tokens = n_tokens;
+  p.capacity = capacity;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.check_finite = checked ? 1 : 0;
+  p.k_gs = cache->k_global_scale;
+  p.v_gs = cache->v_global_scale;
+  cudaError_t e = kvq::launch_append(cache->format, cache->head_dim, p, st);
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  if (checked) {
+    int32_t bits = 0;
+    rc = kvq_read_status(dev_status, stream, &bits);
+    if (rc) return rc;
+  }
+  return succeed();
+}
+
+int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch, int32_t split_override,
+                    int32_t target_ctas, int32_t* plan, int64_t plan_capacity, int32_t* total_splits,
+                    int32_t* max_splits) {
+  int rc = check_cache(cache, false);
+  if (rc) return rc;
+  if (batch < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", batch);
+  if (!seq_lens || !total_splits || !max_splits) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  if (split_override < 0 || target_ctas < 0) return fail(KVQ_ERR_INVALID_ARG, "negative split_override / target_ctas");
+  const int P = cache->page_size;
+  std::vector<int64_t> npages(batch);
+  int64_t total_pages = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (seq_lens[b] < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_lens[%d] = %d < 0", b, seq_lens[b]);
+    npages[b] = (seq_lens[b] + P - 1) / P;
+    total_pages += npages[b];
+  }
+  std::vector<int32_t> splits(batch, 1);
+  if (split_override > 0) {
+    for (int b = 0; b < batch; ++b)
+      splits[b] = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(split_override, std::max<int64_t>(npages[b], 1))));
+  } else {
+    int64_t target = target_ctas;
+    if (target == 0) {
+      kvq::DecodeInstance inst;
+      rc = prepare_instance(cache->format, cache->head_dim, &inst);
+      if (rc) return rc;
+      int dev = 0, sms = 0, per_sm = 0;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inst.kernel, inst.threads, inst.smem_bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "querying SM count / occupancy");
+      target = (int64_t)sms * std::max(per_sm, 1);
+    }
+    const int hgs = heads_per_cta(cache);
+    if (hgs <= 0) return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this cache");
+    const int64_t units = total_pages * (cache->num_kv_heads / hgs);  // (page, head group) units
+    const int64_t chunk = std::max<int64_t>(4, (units + target - 1) / std::max<int64_t>(target, 1));
+    for (int b = 0; b < batch; ++b)
+      splits[b] = static_cast<int32_t>(std::max<int64_t>(1, (npages[b] + chunk - 1) / chunk));
+  }
+  int64_t total = 0;
+  int32_t mx = 0;
+  for (int b = 0; b < batch; ++b) {
+    total += splits[b];
+    mx = std::max(mx, splits[b]);
+  }
+  if (total > 0x7FFFFFFF / std::max(cache->num_kv_heads, 1)) return fail(KVQ_ERR_UNSUPPORTED, "too many splits");
+  *total_splits = static_cast<int32_t>(total);
+  *max_splits = mx;
+  if (!plan || plan_capacity < batch + 1 + total)
+    return fail(KVQ_ERR_WORKSPACE, "plan needs %lld int32 entries", (long long)(batch + 1 + total));
+  plan[0] = 0;
+  for (int b = 0; b < batch; ++b) plan[b + 1] = plan[b] + splits[b];
+  // launch order: longest work items first (pages of split s of sequence b)
+  std::vector<std::pair<int64_t, int32_t>> items;
+  items.reserve(total);
+  for (int b = 0; b < batch; ++b)
+    for (int s = 0; s < splits[b]; ++s) {
+      const int64_t pb = (int64_t)s * npages[b] / splits[b], pe = (int64_t)(s + 1) * npages[b] / splits[b];
+      items.emplace_back(pe - pb, plan[b] + s);
+    }
+  std::stable_sort(items.begin(), items.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+  for (int64_t i = 0; i < total; ++i) plan[batch + 1 + i] = items[i].second;
+  return succeed();
+}
+
+size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int32_t head_dim) {
+  if (total_splits < 0 || num_q_heads < 0 || head_dim < 0) return 0;
+  const size_t rows = (size_t)total_splits * num_q_heads;
+  return 256 + align256(rows * sizeof(float)) + rows * head_dim * sizeof(float);
+}
+
+int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_heads, int32_t head_dim,
+                           float** o_part, float** lse_part) {
+  if (!workspace || !o_part || !lse_part || total_splits < 0 || num_q_heads < 0 || head_dim < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "bad workspace arguments");
+  const size_t rows = (size_t)total_splits * num_q_heads;
+  char* base = static_cast<char*>(workspace);
+  *lse_part = reinterpret_cast<float*>(base + 256);
+  *o_part = reinterpret_cast<float*>(base + 256 + align256(rows * sizeof(float)));
+  return succeed();
+}
+
+int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t batch, int32_t num_q_heads,
+                               float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, const int32_t* plan, int32_t total_splits,
+                               void* workspace, size_t workspace_bytes, void* out, int32_t out_dtype,
+                               float* lse_out, uint32_t flags, void* stream) {
+  int rc = check_cache(cache, true);
+  if (rc) return rc;
+  if (batch < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", batch);
+  if (!q || !block_tables || !seq_lens || !plan || !workspace || !out)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer argument");
+  if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                cache->num_kv_heads);
+  const int G = num_q_heads / cache->num_kv_heads;
+  if (G > 8) return fail(KVQ_ERR_UNSUPPORTED, "query heads per KV head %d > 8", G);
+  if (max_pages_per_seq < 1) return fail(KVQ_ERR_INVALID_ARG, "max_pages_per_seq %d < 1", max_pages_per_seq);
+  if (total_splits < batch) return fail(KVQ_ERR_INVALID_ARG, "total_splits %d < batch %d", total_splits, batch);
+  if ((int64_t)total_splits * cache->num_kv_heads > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "bad out_dtype");
+  if (!(std::isfinite(sm_scale))) return fail(KVQ_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(KVQ_ERR_INVALID_ARG, "q / out must be 16-byte aligned and workspace 256-byte aligned");
+  const int D = cache->head_dim;
+  const size_t need = kvq_decode_workspace_bytes(total_splits, num_q_heads, D);
+  if (workspace_bytes < need)
+    return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool checked = flags & KVQ_CHECKED;
+  if (checked) {
+    // host-side validation of the plan (the kernel also checks every entry it uses)
+    std::vector<int32_t> h(batch + 1 + total_splits);
+    cudaError_t e = cudaMemcpyAsync(h.data(), plan, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading plan");
+    if (h[0] != 0 || h[batch] != total_splits) return fail(KVQ_ERR_INVALID_ARG, "plan offsets do not span total_splits");
+    for (int b = 0; b < batch; ++b)
+      if (h[b + 1] <= h[b]) return fail(KVQ_ERR_INVALID_ARG, "plan gives sequence %d no split", b);
+    std::vector<int32_t> order(h.begin() + batch + 1, h.end());
+    std::sort(order.begin(), order.end());
+    for (int i = 0; i < total_splits; ++i)
+      if (order[i] != i) return fail(KVQ_ERR_INVALID_ARG, "plan launch order is not a permutation");
+  }
+  kvq::DecodeInstance inst;
+  rc = prepare_instance(cache->format, D, &inst);
+  if (rc) return rc;
+  const int hg = heads_per_cta(cache);
+  if (hg <= 0 || cache->num_kv_heads % hg != 0) return fail(KVQ_ERR_UNSUPPORTED, "bad KV head grouping");
+  CUtensorMap tk, tv;
+  rc = make_code_map(&tk, cache->k_codes, cache->num_pages, cache->num_kv_heads, row_bytes(cache->format, D), hg);
+  if (rc) return rc;
+  rc = make_code_map(&tv, cache->v_codes, cache->num_pages, cache->num_kv_heads, row_bytes(cache->format, D), hg);
+  if (rc) return rc;
+  float *o_part = nullptr, *lse_part = nullptr;
+  kvq_workspace_partials(workspace, total_splits, num_q_heads, D, &o_part, &lse_part);
+  kvq::DecodeParams p{};
+  p.q = q;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.plan = plan;
+  p.k_scales = static_cast<const uint8_t*>(cache->k_scales);
+  p.v_scales = static_cast<const uint8_t*>(cache->v_scales);
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.out = out;
+  p.lse_out = lse_out;
+  p.status = static_cast<int32_t*>(workspace);
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = cache->num_pages;
+  p.total_splits = total_splits;
+  p.heads_per_cta = hg;
+  p.out_bf16 = out_dtype == KVQ_OUT_BF16;
+  p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+  p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
+  p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
+  cudaError_t e = kvq::launch_decode(cache->format, D, tk, tv, p, total_splits * (cache->num_kv_heads / hg), st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (!(flags & KVQ_SKIP_MERGE) && total_splits > batch) {
+    e = kvq::launch_merge(o_part, lse_part, plan, batch, num_q_heads, D, out, p.out_bf16, lse_out, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  if (checked) {
+    int32_t bits = 0;
+    rc = kvq_read_status(workspace, stream, &bits);
+    if (rc) return rc;
+  }
+  return succeed();
+}
+
+int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* split_offsets, int32_t batch,
+                    int32_t num_q_heads, int32_t head_dim, void* out, int32_t out_dtype, float* lse_out,
+                    void* stream) {
+  if (!o_part || !lse_part || !split_offsets || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer argument");
+  if (batch < 1 || num_q_heads < 1) return fail(KVQ_ERR_INVALID_ARG, "batch / num_q_heads < 1");
+  if (head_dim != 128 && head_dim != 256) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "bad out_dtype");
+  if (!aligned16(o_part) || !aligned16(out)) return fail(KVQ_ERR_INVALID_ARG, "o_part / out must be 16-byte aligned");
+  cudaError_t e = kvq::launch_merge(o_part, lse_part, split_offsets, batch, num_q_heads, head_dim, out,
+                                    out_dtype == KVQ_OUT_BF16, lse_out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return succeed();
+}
+
+int kvq_read_status(void* dev_status, void* stream, int32_t* bits) {
+  if (!dev_status) return fail(KVQ_ERR_INVALID_ARG, "dev_status is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev_status, 0, sizeof(v), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (bits) *bits = v;
+  if (v & KVQ_DEV_TIMEOUT) return fail(KVQ_ERR_DEVICE_TIMEOUT, "a device pipeline wait timed out (status 0x%x)", v);
+  if (v) return fail(KVQ_ERR_DEVICE_CHECK, "device status 0x%x (bad page/seq_len/plan/slot or non-finite input)", v);
+  return succeed();
+}
+
+const char* kvq_last_error(void) { return g_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,704 @@
+// decode.cuh — split-KV GQA decode attention over a paged INT8 / NVFP4 / BF16 cache.
+//
+// What it computes: for every (sequence b, query head g) the softmax-weighted sum
+// of the dequantized V rows, with logits sm_scale * q . k_hat over the sequence's
+// tokens (split-KV / flash-decoding: "long-context-attention-and-lessons", section
+// "Give more GPU workers a piece of the attention calculation").  Codes are
+// dequantized in registers and never written back as a converted copy
+// ("half-the-memory-int8-kv-cache", section "Read the compressed cache without
+// copying it first").  One loaded page serves the whole GQA group ("Smaller KV
+// cache, faster first token", section "Lever two": one KV block is loaded once
+// for a whole group of query heads).
+//
+// Work item (one CTA, one per SM): one split (a range of whole pages) of one
+// sequence for a group of HG consecutive KV heads, HG = gcd(Hkv, CW) where CW is
+// the number of consumer warps (4 at D = 256, 8 at D = 128).  The pool keeps the
+// KV heads of a page next to each other, so the HG heads' code blocks of a page
+// are one contiguous region and travel as ONE TMA box per tensor (16 KB at
+// D = 256 INT8 with 4 heads); a 1-D bulk copy brings their scales.  Few large
+// copies per page keep a single producer thread ahead of the consumers.
+//
+//   * warp CW (producer): lane 0 walks the split's pages through the block table
+//     (page ids staged in shared memory 32 at a time by the whole warp) and, per
+//     page, waits for the stage to be free, then issues the K and V boxes
+//     (128-byte swizzle) and the two scale copies, completing on the stage's
+//     mbarrier (expect-tx bytes).
+//   * warps 0..CW-1 (consumers): warp w owns KV head w % HG and, if CW / HG > 1,
+//     every (CW/HG)-th page.  Per page (16 tokens) a warp computes S = q K^T for
+//     its G <= 8 query heads with mma.m16n8k16 (heads are the M rows, tokens the N
+//     columns, D the reduction), runs the online softmax on the accumulator
+//     fragment, and accumulates O^T = V^T P'^T (D is the M dimension, heads the N
+//     columns, tokens the reduction), so that S's accumulator layout is directly
+//     P's operand layout.  Integer codes enter the tensor cores as exact f16
+//     integers; the per-token INT8 scales are applied to the logits (K) and folded
+//     into P (V); NVFP4 group scales multiply the operands (products of an E2M1
+//     and an E4M3 value are exact in f16).  P' is split into hi + lo halves of two
+//     MMAs, so P carries ~22 bits.
+//   * epilogue: the warps of a head merge (m, l, O) in shared memory; a sequence
+//     with one split writes `out` directly, otherwise (o, lse) partials.
+//
+// All waits are bounded (%globaltimer); on timeout the kernel sets
+// KVQ_DEV_TIMEOUT in the status word and stops instead of spinning.
+#pragma once
+
+#include "kvq_internal.h"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+
+constexpr int kPage = 16;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxStages = 32;
+
+template <int FMT, int D>
+struct DecodeTraits;
+
+template <int D>
+struct DecodeTraits<KVQ_FMT_INT8, D> {
+  static constexpr bool kBf16Mma = false;
+  static constexpr int kRow = D;        // code bytes per token row
+  static constexpr int kScaleRow = 4;   // scale bytes per token row (one fp32)
+};
+
+template <int D>
+struct DecodeTraits<KVQ_FMT_BF16, D> {
+  static constexpr bool kBf16Mma = true;
+  static constexpr int kRow = 2 * D;
+  static constexpr int kScaleRow = 0;
+};
+
+template <>
+struct DecodeTraits<KVQ_FMT_NVFP4, 256> {
+  static constexpr bool kBf16Mma = false;
+  static constexpr int kRow = 128;
+  static constexpr int kScaleRow = 16;  // one E4M3 byte per 16 elements
+};
+
+// consumer warps per CTA: 4 (+1 producer = 5 warps, up to 255 registers) at D =
+// 256; 8 (+1 = 9 warps, <= 168 registers, enough at D = 128) at D = 128.
+template <int D>
+constexpr int consumer_warps() { return 8; }
+
+template <int FMT, int D>
+struct DecodeLayout {
+  using T = DecodeTraits<FMT, D>;
+  static constexpr int kCW = consumer_warps<D>();
+  static constexpr int kThreads = (kCW + 1) * 32;
+  static constexpr int kHeadCode = kPage * T::kRow;        // one head's K (or V) code block of a page
+  static constexpr int kHeadScale = kPage * T::kScaleRow;  // one head's K (or V) scale block of a page
+  static constexpr int kKSteps = D / 16;
+  static constexpr int kMTiles = D / 16;
+  // q fragments per consumer warp: [k-step][dA / dB part][8 head rows][8 halves]
+  static constexpr int kQBytes = kKSteps * 2 * 128;
+  // shared-memory stage ring: what is left of 227 KB after alignment slack, the
+  // q tiles, the barriers and the page-id buffer
+  static constexpr int kRingBytes = (227 * 1024 - 1024 - kCW * kQBytes - 2 * kMaxStages * 8 - 2 * 32 * 4) / 1024 * 1024;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kCW * kQBytes + 2 * kMaxStages * 8 + 2 * 32 * 4;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  // epilogue reuses the code region: O[warp][8 heads][D] + m, l [warp][8]
+  static constexpr int kEpilogueBytes = kCW * 8 * D * 4 + 2 * kCW * 8 * 4;
+};
+
+// Stage count for a head group of `hg` heads: as many stages as fit the ring,
+// at most kMaxStages, and a multiple of the number of warps per head.  Page i goes
+// to stage i % stages and to the head's warp (i % warps-per-head); with the
+// stage count a multiple of warps-per-head every stage has a fixed set of
+// consumer warps, each of which consumed the stage's previous page itself before
+// waiting on the next one, so a parity wait can never be satisfied by a barrier
+// that is still two phases behind.
+template <int FMT, int D>
+__host__ __device__ inline int decode_stages(int hg) {
+  using Lo = DecodeLayout<FMT, D>;
+  const int wph = Lo::kCW / hg;
+  const int stage = 2 * hg * (Lo::kHeadCode + Lo::kHeadScale);
+  int n = Lo::kRingBytes / stage;
+  n = n < kMaxStages ? n : kMaxStages;
+  return n / wph * wph;
+}
+
+// byte address (shared window) of 16-byte chunk `chunk` (0..kRow/16-1) of token
+// row t in a swizzled head block starting at `block` (1024-byte aligned): the
+// block is [row half][16 rows][128 bytes], chunk index XOR-ed with t % 8.
+__device__ __forceinline__ uint32_t swz(uint32_t block, int t, int chunk) {
+  return block + (chunk >> 3) * (kPage * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+}
+
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }  // k in [-126, 127]
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeParams p) {
+  using T = DecodeTraits<FMT, D>;
+  using Lo = DecodeLayout<FMT, D>;
+  constexpr int CW = Lo::kCW;
+  constexpr int KS = Lo::kKSteps;
+
+  // the merge kernel is launched as a programmatic dependent: let it be scheduled
+  // (it waits for this grid's results before reading them)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int HG = p.heads_per_cta;
+  const int WPH = CW / HG;
+  const int NST = decode_stages<FMT, D>(HG);
+  const int stage_code = 2 * HG * Lo::kHeadCode;
+  const int stage_scale = 2 * HG * Lo::kHeadScale;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* codes = smem;                                   // NST x [K heads][V heads]
+  uint8_t* scales = smem + NST * stage_code;               // NST x [K heads][V heads]
+  uint8_t* qfrag = smem + Lo::kRingBytes;                  // CW x kQBytes
+  uint64_t* full = reinterpret_cast<uint64_t*>(qfrag + CW * Lo::kQBytes);
+  uint64_t* empty = full + kMaxStages;
+  int* pid_s = reinterpret_cast<int*>(empty + kMaxStages);  // [2][32] page ids
+
+  const int Hkv = p.num_kv_heads;
+  const int NHG = Hkv / HG;
+  const int order = blockIdx.x / NHG;
+  const int hg = blockIdx.x - order * NHG;
+  const int G = p.num_q_heads / Hkv;
+  const int32_t* offs = p.plan;
+
+  // ---- which split of which sequence
+  const int item = p.plan[p.batch + 1 + order];
+  if (item < 0 || item >= p.total_splits) {
+    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
+    return;
+  }
+  int lo = 0, hi = p.batch;  // largest b with offs[b] <= item
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offs[mid] <= item) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int nsplit = offs[b + 1] - offs[b];
+  const int s = item - offs[b];
+  if (nsplit <= 0 || s < 0 || s >= nsplit) {
+    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
+    return;
+  }
+  int L = p.seq_lens[b];
+  if (L < 0 || L > p.max_pages * kPage) {
+    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
+    L = L < 0 ? 0 : p.max_pages * kPage;
+  }
+  const int npages = (L + kPage - 1) / kPage;
+  const int page_begin = static_cast<int>((int64_t)s * npages / nsplit);
+  const int page_end = static_cast<int>((int64_t)(s + 1) * npages / nsplit);
+  const int n = page_end - page_begin;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], HG);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == CW) {
+    // ================================================================ producer
+    const int32_t* bt = p.block_tables + (size_t)b * p.max_pages + page_begin;
+    auto page_id = [&](int j) -> int {  // validated page id of split page j (or -1)
+      int v = -1;
+      if (j < n) {
+        v = bt[j];
+        if (v < 0 || v >= p.num_pages) {
+          atomicOr(p.status, KVQ_DEV_BAD_PAGE);
+          v = -1;
+        }
+      }
+      return v;
+    };
+    pid_s[lane] = page_id(lane);
+    __syncwarp();
+    bool ok = true;
+    int issued = 0, st = 0, rnd = 0;  // next page's stage and ring round
+    const size_t head0 = (size_t)hg * HG;
+    for (int base = 0, buf = 0; base < n; base += 32, buf ^= 1) {
+      const int nxt = page_id(base + 32 + lane);  // prefetch the next 32 ids
+      if (lane == 0) {
+        const int cnt = min(32, n - base);
+        for (int k = 0; k < cnt; ++k) {
+          const int pg = pid_s[buf * 32 + k];
+          if (rnd > 0 && !mbar_wait(&empty[st], (rnd - 1) & 1, kWaitLimitNs)) {
+            atomicOr(p.status, KVQ_DEV_TIMEOUT);
+            ok = false;
+            break;
+          }
+          if (pg >= 0) {
+            uint8_t* kc = codes + st * stage_code;
+            mbar_arrive_expect_tx(&full[st], stage_code + stage_scale);
+            tma_load_5d(kc, &tm_k, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
+            tma_load_5d(kc + HG * Lo::kHeadCode, &tm_v, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
+            if constexpr (T::kScaleRow > 0) {
+              uint8_t* ks = scales + st * stage_scale;
+              const size_t off = ((size_t)pg * Hkv + head0) * Lo::kHeadScale;
+              bulk_load(ks, p.k_scales + off, HG * Lo::kHeadScale, &full[st]);
+              bulk_load(ks + HG * Lo::kHeadScale, p.v_scales + off, HG * Lo::kHeadScale, &full[st]);
+            }
+          } else {
+            mbar_arrive(&full[st]);  // nothing to load; the stage keeps stale bytes (status flagged)
+          }
+          ++issued;
+          if (++st == NST) {
+            st = 0;
+            ++rnd;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+      if (!ok) break;
+      pid_s[(buf ^ 1) * 32 + lane] = nxt;
+      __syncwarp();
+    }
+    // Drain: before this warp (and so the CTA) can exit, every copy it issued has
+    // landed; normally the consumers already waited for all of them.
+    if (lane == 0) {  // only lane 0 counted `issued`
+      for (int idx = max(0, issued - NST); idx < issued; ++idx) {
+        if (!mbar_wait(&full[idx % NST], (idx / NST) & 1, kWaitLimitNs)) {
+          atomicOr(p.status, KVQ_DEV_TIMEOUT);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ================================================================== consumers
+  const int hl = warp % HG;   // head within the group
+  const int grp = warp / HG;  // page subset of this head's warps
+  const int h = hg * HG + hl;
+  const int r = lane >> 2;    // head row of S / P, token group of V^T fragments
+  const int c = lane & 3;
+  const int hq = h * G + r;
+  const bool head_ok = r < G;
+  const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.num_q_heads + hq) * D;
+  uint8_t* myq = qfrag + warp * Lo::kQBytes;
+
+  // ---- q fragments (A operand rows = heads), staged once per warp in shared
+  // memory and read per page with ldmatrix.  Column (k) order per format,
+  // matching the K fragments below: k-step j pairs (2c, 2c+1) with d dA(j, c) +
+  // {0, 1} and (2c+8, 2c+9) with dB(j, c) + {0, 1}.
+  float qk_scale;
+  {
+    uint32_t raw[KS][2];
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      int dA, dB;
+      if constexpr (FMT == KVQ_FMT_INT8) {
+        dA = 16 * j + 4 * c;
+        dB = dA + 2;
+      } else if constexpr (FMT == KVQ_FMT_BF16) {
+        dA = 16 * j + 2 * c;
+        dB = dA + 8;
+      } else {
+        dA = 32 * (j >> 1) + 8 * c + 4 * (j & 1);
+        dB = dA + 2;
+      }
+      raw[j][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + dA) : 0u;
+      raw[j][1] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + dB) : 0u;
+    }
+    float qs = p.sm_scale_log2;
+    if constexpr (!T::kBf16Mma) {
+      // bf16 -> f16 exactly: scale the head's row by a power of two so that its
+      // largest |q| lands in [2^14, 2^15); every element within 2^28 of it is then
+      // exactly representable in f16.  The power of two is undone on the logits.
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
+          amax = fmaxf(amax, fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      int k = 0;
+      if (amax > 0.f) {
+        int e;
+        frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
+        k = min(126, max(-126, 15 - e));
+      }
+      const float up = pow2f(k);
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
+          raw[j][u] = h2_as_u32(__floats2half2_rn(__low2float(v) * up, __high2float(v) * up));
+        }
+      }
+      qs *= pow2f(-k);
+      if constexpr (FMT == KVQ_FMT_NVFP4) qs *= p.k_gs_inv;
+    }
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      uint32_t* m0 = reinterpret_cast<uint32_t*>(myq + (2 * j) * 128 + r * 16 + c * 4);
+      m0[0] = raw[j][0];
+      m0[32] = raw[j][1];  // next matrix (dB part), +128 bytes
+    }
+    qk_scale = qs;
+  }
+  __syncwarp();
+  const uint32_t qbase = smem_addr(myq) + ((lane >> 3) * 8 + (lane & 7)) * 16;
+  // Per-lane byte offsets of the swizzled ldmatrix rows inside a head block,
+  // one per value of (chunk & 7) of the iteration (the XOR with the row index
+  // only touches the low three chunk bits; see swz()).  V (INT8, transposed):
+  // matrix m = lane/8 is token block m%2, chunk 2 cp + m/2.
+  [[maybe_unused]] uint32_t voff[4];
+  if constexpr (FMT == KVQ_FMT_INT8) {
+    const int mm = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int v4 = 0; v4 < 4; ++v4) voff[v4] = (8 * (mm & 1) + rr) * 128 + (((2 * v4 + (mm >> 1)) ^ rr) << 4);
+  }
+
+  float oacc[Lo::kMTiles][4];
+#pragma unroll
+  for (int mt = 0; mt < Lo::kMTiles; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+  float m_run = -INFINITY;  // running max (log2 domain) of head r
+  float l_run = 0.f;        // this lane's part of the running sum of head r
+
+  bool alive = true;
+  int st = grp, rnd = 0;  // stage and ring round of page `idx`
+  for (int idx = grp; idx < n; idx += WPH) {
+    const bool got = mbar_wait(&full[st], rnd & 1, kWaitLimitNs);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) atomicOr(p.status, KVQ_DEV_TIMEOUT);
+      alive = false;
+      break;
+    }
+    const uint32_t kblk = smem_addr(codes + st * stage_code + hl * Lo::kHeadCode);
+    const uint32_t vblk = kblk + HG * Lo::kHeadCode;
+    const uint8_t* ksc = scales + st * stage_scale + hl * Lo::kHeadScale;
+    const uint8_t* vsc = ksc + HG * Lo::kHeadScale;
+    const int tok0 = (page_begin + idx) * kPage;
+    const int nvalid = min(kPage, L - tok0);
+
+    // ---------------------------------------------------------- S = q K^T
+    float sacc[2][2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) sacc[i][u][0] = sacc[i][u][1] = sacc[i][u][2] = sacc[i][u][3] = 0.f;
+
+    // chunk groups of 4 x 16-byte chunks; q fragments of the group's k-steps are
+    // fetched from shared memory (two k-steps per ldmatrix.x4).
+    constexpr int QPG = FMT == KVQ_FMT_INT8 ? 4 : (FMT == KVQ_FMT_BF16 ? 2 : 8);  // k-steps per group
+    constexpr int NCG = KS / QPG;
+    [[maybe_unused]] uint32_t ksw[2][4];
+    if constexpr (FMT == KVQ_FMT_NVFP4) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 srow = *reinterpret_cast<const uint4*>(ksc + (8 * i + r) * 16);
+        ksw[i][0] = srow.x; ksw[i][1] = srow.y; ksw[i][2] = srow.z; ksw[i][3] = srow.w;
+      }
+    }
+#pragma unroll
+    for (int cg = 0; cg < NCG; ++cg) {
+      uint32_t qa[QPG][2];
+#pragma unroll
+      for (int jj = 0; jj < QPG / 2; ++jj)
+        ldsm_x4(qbase + (cg * (QPG / 2) + jj) * 512, qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj + 1][0],
+                qa[2 * jj + 1][1]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint32_t w[4];
+        ldsm_x4(swz(kblk, 8 * i + (lane & 7), 4 * cg + (lane >> 3)), w[0], w[1], w[2], w[3]);
+        if constexpr (FMT == KVQ_FMT_INT8) {
+          // chunk = 16 d's = one k-step; lane gets bytes 4c..4c+3 of row 8i+r:
+          // k (2c, 2c+1) <- d 16ch+4c+{0,1}, k (2c+8, 2c+9) <- d 16ch+4c+{2,3}.
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t x = w[m] ^ 0x80808080u;
+            mma16816<false>(sacc[i][m & 1], qa[m][0], 0u, qa[m][1], 0u, i8pair_to_h2<0x4140>(x),
+                            i8pair_to_h2<0x4342>(x));
+          }
+        } else if constexpr (FMT == KVQ_FMT_BF16) {
+          // chunk = 8 d's; k-step uses chunks 2j (k 2c..) and 2j+1 (k 2c+8..).
+          mma16816<true>(sacc[i][0], qa[0][0], 0u, qa[0][1], 0u, w[0], w[1]);
+          mma16816<true>(sacc[i][1], qa[1][0], 0u, qa[1][1], 0u, w[2], w[3]);
+        } else {
+          // NVFP4: chunk = 32 d's; lane gets bytes 4c..4c+3 = d 32ch+8c..+7, split
+          // into k-steps (ch, 0) and (ch, 1); the group scale of d is 2ch + c/2.
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int ch = 4 * cg + m;
+            const uint32_t bsel = 2 * (ch & 1) + (c >> 1);
+            const __half2 sdh = u32_as_h2(e4m3x2_to_h2(prmt(ksw[i][ch >> 1], 0u, bsel | (bsel << 4))));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[m] >> (16 * hh)) & 0xFFu)), sdh));
+              const uint32_t b1 =
+                  h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[m] >> (16 * hh + 8)) & 0xFFu)), sdh));
+              mma16816<false>(sacc[i][hh], qa[2 * m + hh][0], 0u, qa[2 * m + hh][1], 0u, b0, b1);
+            }
+          }
+        }
+      }
+    }
+
+    // ---------------------------------------------------------- online softmax
+    // lane holds head r, tokens 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c (n-tile 1).
+    const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+    float z[4];
+    z[0] = sacc[0][0][0] + sacc[0][1][0];
+    z[1] = sacc[0][0][1] + sacc[0][1][1];
+    z[2] = sacc[1][0][0] + sacc[1][1][0];
+    z[3] = sacc[1][0][1] + sacc[1][1][1];
+    float ks4[4] = {1.f, 1.f, 1.f, 1.f};
+    if constexpr (FMT == KVQ_FMT_INT8) {
+      const float2 a = *reinterpret_cast<const float2*>(ksc + 8 * c);
+      const float2 bb = *reinterpret_cast<const float2*>(ksc + 32 + 8 * c);
+      ks4[0] = a.x; ks4[1] = a.y; ks4[2] = bb.x; ks4[3] = bb.y;
+    }
+    float pmax = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      z[u] = (tk[u] < nvalid) ? z[u] * ks4[u] * qk_scale : -INFINITY;
+      pmax = fmaxf(pmax, z[u]);
+    }
+    pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 1));
+    pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 2));
+    const float m_new = fmaxf(m_run, pmax);
+    const float alpha = exp2f(m_run - m_new);  // m_run = -inf -> 0
+    m_run = m_new;
+    float pr[4];
+    float psum = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pr[u] = exp2f(z[u] - m_new);  // masked tokens: exp2(-inf) = 0
+      psum += pr[u];
+    }
+    l_run = l_run * alpha + psum;
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);      // head 2c
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);  // head 2c+1
+#pragma unroll
+      for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+        oacc[mt][0] *= a0;
+        oacc[mt][1] *= a1;
+        oacc[mt][2] *= a0;
+        oacc[mt][3] *= a1;
+      }
+    }
+    // P' (B operand of O^T = V^T P'^T): INT8 folds the V scale of the token in.
+    float pv[4];
+    if constexpr (FMT == KVQ_FMT_INT8) {
+      const float2 a = *reinterpret_cast<const float2*>(vsc + 8 * c);
+      const float2 bb = *reinterpret_cast<const float2*>(vsc + 32 + 8 * c);
+      const float vs4[4] = {a.x, a.y, bb.x, bb.y};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pv[u] = (tk[u] < nvalid) ? pr[u] * vs4[u] : 0.f;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pv[u] = pr[u];
+    }
+    uint32_t phi[2], plo[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if constexpr (T::kBf16Mma) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(pv[2 * u], pv[2 * u + 1]);
+        const __nv_bfloat162 ll =
+            __floats2bfloat162_rn(pv[2 * u] - __low2float(hh), pv[2 * u + 1] - __high2float(hh));
+        phi[u] = *reinterpret_cast<const uint32_t*>(&hh);
+        plo[u] = *reinterpret_cast<const uint32_t*>(&ll);
+      } else {
+        const __half2 hh = __floats2half2_rn(pv[2 * u], pv[2 * u + 1]);
+        const __half2 ll = __floats2half2_rn(pv[2 * u] - __low2float(hh), pv[2 * u + 1] - __high2float(hh));
+        phi[u] = h2_as_u32(hh);
+        plo[u] = h2_as_u32(ll);
+      }
+    }
+
+    // ---------------------------------------------------------- O^T += V^T P'^T
+    const bool partial = nvalid < kPage;
+    if constexpr (FMT == KVQ_FMT_INT8) {
+      // ldmatrix.trans of int8 pairs: lane gets [V[t][de], V[t][do], V[t+1][de], V[t+1][do]]
+      // with t = 8tb+2c, de = 16ch+2r, do = de+1 -> m-tile ch rows r (de) and r+8 (do).
+      uint32_t vb[4];
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) vb[v4] = vblk + voff[v4];
+#pragma unroll
+      for (int cp = 0; cp < Lo::kMTiles / 2; ++cp) {
+        uint32_t w[4];
+        ldsm_x4_t(vb[cp & 3] + (cp >> 2) * (kPage * 128), w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t x0 = w[2 * u] ^ 0x80808080u;
+          const uint32_t x1 = w[2 * u + 1] ^ 0x80808080u;
+          const uint32_t a0 = i8pair_to_h2<0x4240>(x0), a1 = i8pair_to_h2<0x4341>(x0);
+          const uint32_t a2 = i8pair_to_h2<0x4240>(x1), a3 = i8pair_to_h2<0x4341>(x1);
+          mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, phi[0], phi[1]);
+          mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, plo[0], plo[1]);
+        }
+      }
+    } else if constexpr (FMT == KVQ_FMT_BF16) {
+      // m-tile mt: rows r <- d 16mt+r (chunk 2mt), r+8 <- d 16mt+8+r (chunk 2mt+1)
+      const uint32_t m0 = (2 * c < nvalid ? 0x0000FFFFu : 0u) | (2 * c + 1 < nvalid ? 0xFFFF0000u : 0u);
+      const uint32_t m1 = (8 + 2 * c < nvalid ? 0x0000FFFFu : 0u) | (9 + 2 * c < nvalid ? 0xFFFF0000u : 0u);
+#pragma unroll
+      for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+        const int mm = lane >> 3;
+        const int trow = 8 * (mm >> 1) + (lane & 7);
+        uint32_t w[4];
+        ldsm_x4_t(swz(vblk, trow, 2 * mt + (mm & 1)), w[0], w[1], w[2], w[3]);
+        if (partial) {  // unwritten slots may hold NaN bit patterns: zero them
+          w[0] &= m0; w[1] &= m0; w[2] &= m1; w[3] &= m1;
+        }
+        mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], phi[0], phi[1]);
+        mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
+      }
+    } else {
+      // NVFP4: lane gets b16 (4 nibbles = d 32ch+4r..+3) of tokens t, t+1 (t = 8tb+2c);
+      // regroup nibbles into per-d token pairs; group scale of those d's = 2ch + r/4.
+      const uint4 sa0 = *reinterpret_cast<const uint4*>(vsc + (2 * c) * 16);
+      const uint4 sb0 = *reinterpret_cast<const uint4*>(vsc + (2 * c + 1) * 16);
+      const uint4 sa1 = *reinterpret_cast<const uint4*>(vsc + (8 + 2 * c) * 16);
+      const uint4 sb1 = *reinterpret_cast<const uint4*>(vsc + (9 + 2 * c) * 16);
+      const uint32_t swa[2][4] = {{sa0.x, sa0.y, sa0.z, sa0.w}, {sa1.x, sa1.y, sa1.z, sa1.w}};
+      const uint32_t swb[2][4] = {{sb0.x, sb0.y, sb0.z, sb0.w}, {sb1.x, sb1.y, sb1.z, sb1.w}};
+      const uint32_t vmask[2] = {
+          (2 * c < nvalid ? 0x0000FFFFu : 0u) | (2 * c + 1 < nvalid ? 0xFFFF0000u : 0u),
+          (8 + 2 * c < nvalid ? 0x0000FFFFu : 0u) | (9 + 2 * c < nvalid ? 0xFFFF0000u : 0u)};
+#pragma unroll
+      for (int cp = 0; cp < 4; ++cp) {
+        const int mm = lane >> 3;
+        const int trow = 8 * (mm & 1) + (lane & 7);
+        uint32_t w[4];
+        ldsm_x4_t(swz(vblk, trow, 2 * cp + (mm >> 1)), w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int ch = 2 * cp + u;
+          const uint32_t bsel = 2 * (ch & 1) + (r >> 2);
+          uint32_t a[2][4];  // [tb][d offset 0..3] f16x2 over the token pair
+#pragma unroll
+          for (int tb = 0; tb < 2; ++tb) {
+            const uint32_t wd = w[2 * u + tb];
+            const uint32_t lo4 = wd & 0x0F0F0F0Fu;
+            const uint32_t hi4 = (wd >> 4) & 0x0F0F0F0Fu;
+            const uint32_t ev = lo4 | (lo4 >> 12);  // byte0: d0 pair, byte1: d2 pair
+            const uint32_t od = hi4 | (hi4 >> 12);  // byte0: d1 pair, byte1: d3 pair
+            uint32_t sv = e4m3x2_to_h2(prmt(swa[tb][ch >> 1], swb[tb][ch >> 1], bsel | ((bsel + 4) << 4)));
+            sv &= vmask[tb];  // unwritten slots may hold NaN scales
+            const __half2 svh = u32_as_h2(sv);
+            a[tb][0] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(ev & 0xFFu)), svh));
+            a[tb][1] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(od & 0xFFu)), svh));
+            a[tb][2] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((ev >> 8) & 0xFFu)), svh));
+            a[tb][3] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((od >> 8) & 0xFFu)), svh));
+          }
+          // m-tile 2ch: rows r <- d 32ch+4r, r+8 <- +1; m-tile 2ch+1: +2, +3
+          mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], phi[0], phi[1]);
+          mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], plo[0], plo[1]);
+          mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], phi[0], phi[1]);
+          mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], plo[0], plo[1]);
+        }
+      }
+    }
+    (void)partial;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    st += WPH;
+    if (st >= NST) {
+      st -= NST;
+      ++rnd;
+    }
+  }
+
+  // ================================================================== epilogue
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  if (!alive) {
+    m_run = -INFINITY;
+    l_run = 0.f;
+  }
+  // all consumer warps are past their last page, so every stage has landed and
+  // been read: the code region can be reused.
+  asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+  float* red_o = reinterpret_cast<float*>(codes);  // [CW][8][D]
+  float* red_m = red_o + CW * 8 * D;                // [CW][8]
+  float* red_l = red_m + CW * 8;                    // [CW][8]
+  {
+    float* ow = red_o + warp * 8 * D;
+#pragma unroll
+    for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+      int da, db;
+      if constexpr (FMT == KVQ_FMT_INT8) {
+        da = 16 * mt + 2 * r;
+        db = da + 1;
+      } else if constexpr (FMT == KVQ_FMT_BF16) {
+        da = 16 * mt + r;
+        db = da + 8;
+      } else {
+        da = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1);
+        db = da + 1;
+      }
+      ow[(2 * c) * D + da] = oacc[mt][0];
+      ow[(2 * c + 1) * D + da] = oacc[mt][1];
+      ow[(2 * c) * D + db] = oacc[mt][2];
+      ow[(2 * c + 1) * D + db] = oacc[mt][3];
+    }
+    if (c == 0) {
+      red_m[warp * 8 + r] = m_run;
+      red_l[warp * 8 + r] = l_run;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+
+  const int tid = threadIdx.x;  // 0 .. CW*32-1
+  const bool direct = nsplit == 1;
+  constexpr float kLn2 = 0.69314718055994530942f;
+  // outputs of the group: HG heads x G query heads x D/4 float4 columns
+  for (int e4 = tid; e4 < HG * G * (D / 4); e4 += CW * 32) {
+    const int hh = e4 / (G * (D / 4));
+    const int rem = e4 - hh * G * (D / 4);
+    const int g = rem / (D / 4);
+    const int d = (rem - g * (D / 4)) * 4;
+    float M = -INFINITY;
+    for (int j = 0; j < WPH; ++j) M = fmaxf(M, red_m[(hh + j * HG) * 8 + g]);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lse = -INFINITY;
+    if (M != -INFINITY) {
+      float Lsum = 0.f;
+      for (int j = 0; j < WPH; ++j) {
+        const int w = hh + j * HG;
+        const float wt = exp2f(red_m[w * 8 + g] - M);
+        Lsum += red_l[w * 8 + g] * wt;
+        const float4 ow = *reinterpret_cast<const float4*>(red_o + (w * 8 + g) * D + d);
+        o.x += ow.x * wt;
+        o.y += ow.y * wt;
+        o.z += ow.z * wt;
+        o.w += ow.w * wt;
+      }
+      float inv = 1.f / Lsum;
+      if constexpr (FMT == KVQ_FMT_NVFP4) inv *= p.v_gs_inv;
+      o.x *= inv;
+      o.y *= inv;
+      o.z *= inv;
+      o.w *= inv;
+      lse = (M + log2f(Lsum)) * kLn2;
+    }
+    const int qh = (hg * HG + hh) * G + g;
+    if (direct) {
+      const size_t off = ((size_t)b * p.num_q_heads + qh) * D + d;
+      if (p.out_bf16) {
+        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off);
+        ob[0] = __floats2bfloat162_rn(o.x, o.y);
+        ob[1] = __floats2bfloat162_rn(o.z, o.w);
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + off) = o;
+      }
+      if (d == 0 && p.lse_out) p.lse_out[(size_t)b * p.num_q_heads + qh] = lse;
+    } else {
+      const size_t row = (size_t)item * p.num_q_heads + qh;
+      *reinterpret_cast<float4*>(p.o_part + row * D + d) = o;
+      if (d == 0) p.lse_part[row] = lse;
+    }
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,44 @@
+// decode_launch.cu — the decode kernel instances (format x head_dim) and their launchers.
+#include "decode.cuh"
+
+namespace kvq {
+namespace {
+
+template <int FMT, int D>
+DecodeInstance instance_of() {
+  using Lo = DecodeLayout<FMT, D>;
+  return DecodeInstance{reinterpret_cast<const void*>(&decode_kernel<FMT, D>), Lo::kSmemBytes, Lo::kThreads, Lo::kCW,
+                        DecodeTraits<FMT, D>::kRow};
+}
+
+template <int FMT, int D>
+cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                     cudaStream_t stream) {
+  using Lo = DecodeLayout<FMT, D>;
+  decode_kernel<FMT, D><<<grid, Lo::kThreads, Lo::kSmemBytes, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_instance(int format, int head_dim, DecodeInstance* out) {
+  if (format == KVQ_FMT_INT8 && head_dim == 256) *out = instance_of<KVQ_FMT_INT8, 256>();
+  else if (format == KVQ_FMT_INT8 && head_dim == 128) *out = instance_of<KVQ_FMT_INT8, 128>();
+  else if (format == KVQ_FMT_BF16 && head_dim == 256) *out = instance_of<KVQ_FMT_BF16, 256>();
+  else if (format == KVQ_FMT_BF16 && head_dim == 128) *out = instance_of<KVQ_FMT_BF16, 128>();
+  else if (format == KVQ_FMT_NVFP4 && head_dim == 256) *out = instance_of<KVQ_FMT_NVFP4, 256>();
+  else return false;
+  return true;
+}
+
+cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, int grid, cudaStream_t stream) {
+  if (format == KVQ_FMT_INT8 && head_dim == 256) return launch_t<KVQ_FMT_INT8, 256>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_INT8 && head_dim == 128) return launch_t<KVQ_FMT_INT8, 128>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_BF16 && head_dim == 256) return launch_t<KVQ_FMT_BF16, 256>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_BF16 && head_dim == 128) return launch_t<KVQ_FMT_BF16, 128>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_NVFP4 && head_dim == 256) return launch_t<KVQ_FMT_NVFP4, 256>(tk, tv, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

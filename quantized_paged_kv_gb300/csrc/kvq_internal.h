@@ -1,0 +1,66 @@
+// kvq_internal.h — declarations shared by the library's translation units
+// (kernel parameter blocks and the per-format launchers).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+struct DecodeParams {
+  const void* q;               // bf16 [B][Hq][D]
+  const int32_t* block_tables; // [B][max_pages]
+  const int32_t* seq_lens;     // [B]
+  const int32_t* plan;         // [B+1] split offsets, then [total] launch order
+  const uint8_t* k_scales;     // pool scale arrays (INT8 / NVFP4)
+  const uint8_t* v_scales;
+  float* o_part;               // [total][Hq][D]
+  float* lse_part;             // [total][Hq]
+  void* out;                   // [B][Hq][D] f32 or bf16
+  float* lse_out;              // [B][Hq] or null
+  int32_t* status;             // device status word
+  int32_t batch, num_q_heads, num_kv_heads, max_pages, num_pages, total_splits;
+  int32_t heads_per_cta;       // KV heads per work item (a divisor of num_kv_heads)
+  int32_t out_bf16;
+  float sm_scale_log2;         // sm_scale * log2(e)
+  float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scale
+};
+
+struct AppendParams {
+  const uint16_t* k_new;       // bf16 [N][Hkv][D]
+  const uint16_t* v_new;
+  const int64_t* slots;        // [N]
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  uint8_t* k_scales;
+  uint8_t* v_scales;
+  int32_t* status;             // nullable
+  int64_t n_tokens;
+  int64_t capacity;            // num_pages * page_size
+  int32_t num_kv_heads;
+  int32_t check_finite;
+  float k_gs, v_gs;            // NVFP4 global scales
+};
+
+// Per-(format, head_dim) decode instance description.
+struct DecodeInstance {
+  const void* kernel;          // __global__ function
+  int smem_bytes;
+  int threads;
+  int consumer_warps;          // KV heads per work item = gcd(num_kv_heads, consumer_warps)
+  int row_bytes;               // code bytes per token row
+};
+
+bool decode_instance(int format, int head_dim, DecodeInstance* out);
+cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
+                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
+                         cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,130 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every symbol
+include/kvq.h declares, and its host-only helpers (byte accounting, split
+planning, workspace layout, argument validation) behave as documented."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from tests import harness as H
+from tests import oracle_pins as pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    H.ensure_built()
+    import quantized_paged_kv_gb300 as k
+    return k
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_header_symbol(kvq):
+    syms = header_symbols()
+    assert len(syms) >= 10
+    lib = ctypes.CDLL(kvq._binding.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert sorted(kvq._binding.EXPORTS) == syms
+
+
+def test_bytes_per_token_matches_the_pages(kvq):
+    cf = pins.closed_forms()
+    assert kvq.kvq_bytes_per_token("int8", 1, 256) == cf["int8_bytes_per_token_head_D256"]
+    assert kvq.kvq_bytes_per_token("bf16", 1, 256) == cf["bf16_bytes_per_token_head_D256"]
+    assert kvq.kvq_bytes_per_token("nvfp4", 2, 256) == cf["nvfp4_bytes_per_token_layer_2H_D256"]
+    assert kvq.kvq_bytes_per_token("nvfp4", 1, 256) == cf["nvfp4_bytes_per_kv_head_D256"]
+    assert 16 * kvq.kvq_bytes_per_token("bf16", 4, 256) == cf["bf16_bytes_per_token_16L_4H_D256"]
+    assert kvq.kvq_bytes_per_token("int8", 8, 128) == 8 * 2 * (128 + 4)
+    assert kvq.kvq_bytes_per_token(7, 1, 256) == -1
+    cb, sb = kvq.kvq_cache_array_bytes("nvfp4", 10, 16, 2, 256)
+    assert (cb, sb) == (10 * 2 * 16 * 128, 10 * 2 * 16 * 16)
+    cb, sb = kvq.kvq_cache_array_bytes("int8", 3, 16, 4, 256)
+    assert (cb, sb) == (3 * 4 * 16 * 256, 3 * 4 * 16 * 4)
+
+
+def _struct(kvq, fmt="int8", pages=4096, Hkv=4, D=256):
+    return kvq._binding.KvqCacheStruct(None, None, None, None, pages, 16, Hkv, D, kvq._binding.FORMATS[fmt], 1.0, 1.0)
+
+
+def _check_plan(plan, seq_lens, total, override=None):
+    B = len(seq_lens)
+    offs = plan[:B + 1]
+    order = plan[B + 1:]
+    assert offs[0] == 0 and offs[-1] == total
+    assert sorted(order.tolist()) == list(range(total))
+    sizes = {}
+    for b, L in enumerate(seq_lens):
+        n = -(-L // 16)
+        S = offs[b + 1] - offs[b]
+        assert S >= 1
+        if override:
+            assert S == max(1, min(override, max(n, 1)))
+        bounds = [(s * n // S, (s + 1) * n // S) for s in range(S)]
+        assert bounds[0][0] == 0 and bounds[-1][1] == n
+        assert all(bounds[i][1] == bounds[i + 1][0] for i in range(S - 1))
+        assert max(e - b_ for b_, e in bounds) - min(e - b_ for b_, e in bounds) <= 1
+        for s, (b0, e0) in enumerate(bounds):
+            sizes[int(offs[b]) + s] = e0 - b0
+    got = [sizes[int(i)] for i in order]
+    assert got == sorted(got, reverse=True)  # longest work first
+
+
+def test_planner_override_and_auto(kvq):
+    s = _struct(kvq)
+    rng = np.random.default_rng(0)
+    for seq_lens in ([32768], [512], [0], [1, 17, 300, 0, 64], rng.integers(512, 8193, 64).tolist()):
+        for ov in (1, 2, 4, 64):
+            plan, total, mx = kvq.kvq_plan_splits(s, seq_lens, ov, 0)
+            _check_plan(plan.numpy(), seq_lens, total, ov)
+        plan, total, mx = kvq.kvq_plan_splits(s, seq_lens, 0, 152)
+        _check_plan(plan.numpy(), seq_lens, total)
+    plan, total, _ = kvq.kvq_plan_splits(s, [32768], 0, 152)
+    # 4 KV heads form one head group (4 consumer warps at D = 256): 2048 page units
+    # over 152 CTAs -> 14 pages per item -> 147 splits
+    assert total == 147
+    s8 = _struct(kvq, pages=4096, Hkv=8, D=128)
+    plan, total, _ = kvq.kvq_plan_splits(s8, [32768], 0, 152)
+    assert total == 147  # 8 heads = one group of the 8 consumer warps at D = 128
+
+
+def test_workspace_layout(kvq):
+    n = kvq.kvq_decode_workspace_bytes(38, 24, 256)
+    assert n == 256 + ((38 * 24 * 4 + 255) // 256) * 256 + 38 * 24 * 256 * 4
+
+
+def test_host_validation_errors(kvq):
+    L = kvq.lib()
+    s = _struct(kvq, pages=4)
+    s.page_size = 32
+    total, mx = ctypes.c_int32(), ctypes.c_int32()
+    lens = (ctypes.c_int32 * 1)(10)
+    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    assert rc == 2 and "page_size" in kvq.kvq_last_error()
+    s.page_size = 16
+    s.format = 2
+    s.head_dim = 128
+    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    assert rc == 2
+    s.head_dim = 256
+    s.k_global_scale = 0.0
+    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    assert rc == 1
+    s.k_global_scale = 1.0
+    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    assert rc == 3 and total.value == 1  # size query
+    # device calls refuse NULL / misaligned arguments before touching the GPU
+    rc = L.kvq_quant_append(ctypes.byref(s), None, None, None, 4, None, 0, None)
+    assert rc == 1
+    rc = L.kvq_paged_decode_attention(ctypes.byref(s), None, 1, 4, 0.1, None, 1, None, None, 1, None, 0, None, 0,
+                                      None, 0, None)
+    assert rc == 1
+    assert L.kvq_split_merge(None, None, None, 1, 1, 256, None, 0, None, None) == 1

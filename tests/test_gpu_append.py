@@ -1,0 +1,151 @@
+"""kvq_quant_append on the GPU against the oracle: codes and scales bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oatt
+from oracle import formats as ofmt
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    H.ensure_built()
+
+
+def _rows(rng, n, Hkv, D, kind):
+    x = rng.standard_normal((n, Hkv, D)).astype(np.float32)
+    if kind == "outliers":
+        x[:, :, [3, 40, 77, 200 % D]] *= 8.0
+    elif kind == "spikes":
+        x[rng.random(x.shape) < 0.01] *= 20.0
+    elif kind == "edge":
+        x[0] = 0.0                                    # all-zero rows -> scale 0, codes 0
+        x[1] *= 1e-30                                 # tiny (subnormal-scale) rows
+        x[2] = np.where(rng.random((Hkv, D)) < 0.5, -0.0, 0.0)
+        x[3] *= 3e4                                   # large
+        x[4, :, :] = 1.0                              # constant row
+        x[5, :, 0] = 127.0 / 8                        # exact INT8 midpoints: scale = 1/8
+        x[5, :, 1:11] = (np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 125.5, 126.5, -126.5]) / 8)
+        x[5, :, 11:] = 0.0
+    return torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def _append_and_compare(fmt, Hkv, D, kind, n=300, num_pages=64, gs=(1.0, 1.0), seed=0):
+    from quantized_paged_kv_gb300 import KVCache
+
+    rng = np.random.default_rng(seed)
+    k, v = _rows(rng, n, Hkv, D, kind), _rows(rng, n, Hkv, D, kind)
+    if gs == "tensor":
+        gs = (float(ofmt.nvfp4_tensor_global_scale(k)), float(ofmt.nvfp4_tensor_global_scale(v)))
+    cap = num_pages * 16
+    slots = rng.permutation(cap)[:n].astype(np.int64)
+    slots[::17] = -1                                   # padding tokens: not written
+    cache = KVCache(fmt, num_pages, Hkv, D, k_global_scale=gs[0], v_global_scale=gs[1], fill=H.SENTINEL)
+    dev = lambda a: torch.from_numpy(a).to("cuda")
+    cache.append(dev(k).to(torch.bfloat16), dev(v).to(torch.bfloat16), dev(slots))
+    torch.cuda.synchronize()
+    kc, vc, ks, vs = H.gpu_views_numpy(cache)
+    valid = slots >= 0
+    for x, codes, scales, g in ((k, kc, ks, gs[0]), (v, vc, vs, gs[1])):
+        for h in range(Hkv):
+            c_exp, s_exp = oatt.quantize_rows(fmt, x[valid, h, :], g)
+            sl = slots[valid]
+            got_c = codes[sl // 16, h, sl % 16]
+            assert np.array_equal(got_c, c_exp), (fmt, kind, h, np.argwhere(got_c != c_exp)[:5])
+            if s_exp is not None:
+                got_s = scales[sl // 16, h, sl % 16]
+                assert np.array_equal(got_s.view(np.uint8), np.asarray(s_exp).view(np.uint8)), (fmt, kind, h)
+    # slots that were not written keep the sentinel
+    written = np.zeros(cap, bool)
+    written[slots[valid]] = True
+    assert np.all(kc.reshape(num_pages, Hkv, 16, -1).transpose(0, 2, 1, 3).reshape(cap, Hkv, -1)[~written] == H.SENTINEL)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kind", ["normal", "outliers", "spikes", "edge"])
+def test_int8_append_bit_exact(D, kind):
+    _append_and_compare("int8", 4, D, kind)
+
+
+@pytest.mark.parametrize("kind", ["normal", "outliers", "spikes", "edge"])
+@pytest.mark.parametrize("gs", [(1.0, 1.0), "tensor", (0.37, 1234.5)])
+def test_nvfp4_append_bit_exact(kind, gs):
+    _append_and_compare("nvfp4", 2, 256, kind, gs=gs)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_bf16_append_copies(D):
+    _append_and_compare("bf16", 3, D, "normal")
+
+
+def test_nvfp4_scale_rounding_sweep():
+    """Group maxima that put fp32(amax/6 * gs) on and between every E4M3 value
+    (midpoints included) and across the subnormal range."""
+    from quantized_paged_kv_gb300 import KVCache
+
+    vals = ofmt.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    targets = np.concatenate([vals, mids, mids * (1 + 2 ** -20), mids * (1 - 2 ** -20)])
+    amax = (targets * 6.0).astype(np.float32)
+    amax = torch.from_numpy(amax).to(torch.bfloat16).to(torch.float32).numpy()
+    n = (len(amax) + 15) // 16
+    x = np.zeros((n, 1, 256), np.float32)
+    flat = x.reshape(-1, 16)
+    flat[: len(amax), 5] = amax
+    flat[: len(amax), 6] = -amax * 0.6
+    flat[: len(amax), 7] = amax * 0.25
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    cache = KVCache("nvfp4", (n + 15) // 16, 1, 256, fill=H.SENTINEL)
+    slots = np.arange(n, dtype=np.int64)
+    xt = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    cache.append(xt, xt, torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    kc, _, ks, _ = H.gpu_views_numpy(cache)
+    c_exp, s_exp = ofmt.nvfp4_quantize(x[:, 0, :], 1.0)
+    assert np.array_equal(ks[slots // 16, 0, slots % 16], s_exp)
+    assert np.array_equal(kc[slots // 16, 0, slots % 16], c_exp)
+
+
+def test_slot_overwrite():
+    from quantized_paged_kv_gb300 import KVCache
+
+    rng = np.random.default_rng(5)
+    cache = KVCache("int8", 4, 2, 128, fill=H.SENTINEL)
+    slots = torch.tensor([3, 9, 40], dtype=torch.int64, device="cuda")
+    for it in range(2):
+        k = _rows(rng, 3, 2, 128, "normal")
+        kt = torch.from_numpy(k).to(torch.bfloat16).cuda()
+        cache.append(kt, kt, slots)
+    torch.cuda.synchronize()
+    kc, _, ks, _ = H.gpu_views_numpy(cache)
+    c_exp, s_exp = oatt.quantize_rows("int8", k[:, 1, :])
+    sl = slots.cpu().numpy()
+    assert np.array_equal(kc[sl // 16, 1, sl % 16], c_exp)
+    assert np.array_equal(ks[sl // 16, 1, sl % 16], s_exp)
+
+
+def test_checked_append_rejects_bad_metadata():
+    from quantized_paged_kv_gb300 import KVCache, KvqError
+
+    cache = KVCache("int8", 2, 1, 128, fill=H.SENTINEL)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = torch.randn(3, 1, 128, device="cuda").to(torch.bfloat16)
+    with pytest.raises(KvqError) as e:
+        cache.append(k, k, torch.tensor([1, 5, 1], device="cuda"), dev_status=status, checked=True)
+    assert e.value.code == 1 and "duplicate" in str(e.value)
+    with pytest.raises(KvqError) as e:
+        cache.append(k, k, torch.tensor([1, 5, 32], device="cuda"), dev_status=status, checked=True)
+    assert e.value.code == 1
+    bad = k.clone()
+    bad[1, 0, 7] = float("inf")
+    with pytest.raises(KvqError) as e:
+        cache.append(bad, k, torch.tensor([1, 5, 6], device="cuda"), dev_status=status, checked=True)
+    assert e.value.code == 5
+    # raw mode: an out-of-range slot is skipped and reported in the status word
+    cache.append(k, k, torch.tensor([0, 99, 2], device="cuda"), dev_status=status)
+    from quantized_paged_kv_gb300 import kvq_read_status
+    rc, bits = kvq_read_status(status)
+    assert rc == 5 and bits & 16

@@ -1,0 +1,198 @@
+"""paged_decode_attention + split_merge on the GPU against the float64 oracle.
+
+The oracle attends over pools it built itself from the same seeded bf16 inputs
+(codes equal the GPU's bit for bit, see test_gpu_append.py): the comparison
+isolates the kernel's arithmetic and layout handling from quantization error.
+Tolerance: max-abs 2e-3 (fp32 output) / 1e-2 (bf16 output).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_paged_kv_gb300 import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    H.ensure_built()
+
+
+def _check(wl, fmt, split=0, out_dtype=None, units=None, target_ctas=0, gs=None):
+    od = out_dtype or wl.out_dtype
+    gs = H.global_scales(wl, fmt) if gs is None else gs
+    seqs = None if units is None else sorted({b for b, _ in units})
+    cache = H.gpu_cache(wl, fmt, gs)  # every sequence, as the benchmark runs it
+    out, lse, plan = H.run_decode(cache, wl, split=split, out_dtype=od, target_ctas=target_ctas)
+    pools = H.oracle_pools(wl, fmt, gs, seqs=seqs)
+    ref, ref_lse = H.oracle_decode(wl, fmt, pools, units=units)
+    sel = np.isfinite(ref_lse) | (wl.seq_lens[:, None] == 0)
+    if units is not None:
+        mask = np.zeros_like(sel)
+        for b, h in units:
+            mask[b, h * wl.G:(h + 1) * wl.G] = True
+        sel &= mask
+    err = np.abs(out - ref)[sel]
+    assert np.all(np.isfinite(out[sel]))
+    bound = H.tol(od)
+    if od == "bf16" and np.abs(ref[sel]).max() > 2.5:
+        # stress data with large outputs: bf16 rounding alone is up to 2^-8 |ref|
+        bound = np.maximum(bound, 2.0 ** -8 * np.abs(ref[sel]))
+    assert np.all(err <= bound), (fmt, split, od, err.max())
+    fin = sel & np.isfinite(ref_lse)
+    le = np.abs(lse[fin] - ref_lse[fin])
+    assert le.size == 0 or le.max() < 1e-3, le.max()
+    assert np.all(np.isneginf(lse[sel & ~np.isfinite(ref_lse)]))
+    return plan, err.max()
+
+
+@pytest.mark.parametrize("split", [1, 4, 0])
+def test_tiny_int8(split):
+    wl = W.make("tiny_int8")
+    plan, _ = _check(wl, "int8", split)
+    if split:
+        assert plan.total_splits == split
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
+@pytest.mark.parametrize("D,Hq,Hkv", [(256, 24, 4), (128, 32, 8), (256, 8, 8), (128, 16, 2)])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_ragged_batch(fmt, D, Hq, Hkv, out_dtype):
+    if fmt == "nvfp4" and D != 256:
+        pytest.skip("NVFP4 is implemented for D = 256")
+    wl = W.make("serving_int8", lens=("list", [1, 17, 300, 0, 64, 1000]), seed=7)
+    wl.Hq, wl.Hkv, wl.D = Hq, Hkv, D
+    if out_dtype == "f32":  # large values; the bf16-output cases keep N(0, 0.5^2) as the bf16 workloads do
+        wl.outlier_channels, wl.outlier_gain = 4, 8.0
+    for split in (1, 3, 0):
+        _check(wl, fmt, split, out_dtype=out_dtype)
+
+
+def test_bf16_output_with_large_values():
+    wl = W.make("tiny_int8", lens=("list", [1, 40, 700]), seed=8)
+    _check(wl, "int8", 2, out_dtype="bf16")
+
+
+def test_group_sizes_1_to_8():
+    for G in (1, 2, 3, 5, 7, 8):
+        wl = W.make("tiny_int8", lens=("list", [203, 45]), seed=11)
+        wl.Hkv = 2
+        wl.Hq = 2 * G
+        _check(wl, "int8", 2)
+
+
+def test_empty_context_gives_zero_and_neg_inf():
+    wl = W.make("tiny_int8", lens=("list", [0, 33]), seed=3)
+    cache = H.gpu_cache(wl, "int8")
+    for split in (1, 5):
+        out, lse, _ = H.run_decode(cache, wl, split=split)
+        assert np.all(out[0] == 0.0) and np.all(np.isneginf(lse[0]))
+
+
+def test_single_token_returns_its_value_row():
+    wl = W.make("tiny_int8", lens=("list", [1]), seed=4)
+    pools = H.oracle_pools(wl, "int8")
+    cache = H.gpu_cache(wl, "int8")
+    out, _, _ = H.run_decode(cache, wl, split=1)
+    from oracle import attention as oatt
+    for h in range(wl.Hkv):
+        v = oatt.cache_rows("int8", pools["v_codes"], pools["v_scales"], wl.slots(0), h)[0]
+        assert np.max(np.abs(out[0, h * wl.G:(h + 1) * wl.G] - v[None, :])) < 1e-5
+
+
+def test_block_table_permutation_is_bit_identical():
+    wl = W.make("tiny_int8", lens=("list", [700, 77]), seed=5)
+    a = H.run_decode(H.gpu_cache(wl, "int8"), wl, split=3)[0]
+    wl2 = W.make("tiny_int8", lens=("list", [700, 77]), seed=5)
+    perm = np.random.default_rng(1).permutation(wl2.num_pages).astype(np.int32)
+    wl2.block_tables = perm[wl2.block_tables]
+    b = H.run_decode(H.gpu_cache(wl2, "int8"), wl2, split=3)[0]
+    assert np.array_equal(a, b)
+
+
+def test_skip_merge_then_split_merge_matches():
+    from quantized_paged_kv_gb300 import DecodePlan, decode, kvq_split_merge
+
+    wl = W.make("tiny_int8", lens=("list", [900, 333, 16]), seed=9)
+    cache = H.gpu_cache(wl, "int8")
+    full, lse_full, _ = H.run_decode(cache, wl, split=4)
+    q = torch.from_numpy(wl.q()).to(torch.bfloat16).cuda()
+    out = torch.full((wl.B, wl.Hq, wl.D), float("nan"), device="cuda")
+    lse = torch.full((wl.B, wl.Hq), float("nan"), device="cuda")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=4)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    sl = torch.from_numpy(wl.seq_lens).cuda()
+    decode(cache, plan, q, bt, sl, out, wl.sm_scale, lse_out=lse, skip_merge=True)
+    o_ptr, l_ptr = plan.partials()
+    kvq_split_merge(o_ptr, l_ptr, plan.plan, wl.B, wl.Hq, wl.D, out, lse)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), full)
+    assert np.array_equal(lse.cpu().numpy(), lse_full)
+
+
+def test_checked_mode_reports_bad_metadata():
+    from quantized_paged_kv_gb300 import DecodePlan, KvqError, decode
+
+    wl = W.make("tiny_int8", lens=("list", [64, 64]), seed=2)
+    cache = H.gpu_cache(wl, "int8")
+    q = torch.from_numpy(wl.q()).to(torch.bfloat16).cuda()
+    out = torch.empty((wl.B, wl.Hq, wl.D), device="cuda")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=2)
+    sl = torch.from_numpy(wl.seq_lens).cuda()
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    bad = bt.clone()
+    bad[1, 2] = wl.num_pages + 5          # page id out of range: skipped, flagged
+    with pytest.raises(KvqError) as e:
+        decode(cache, plan, q, bad, sl, out, wl.sm_scale, checked=True)
+    assert e.value.code == 5
+    bad_len = sl.clone()
+    bad_len[0] = 10**6                    # longer than the block table
+    with pytest.raises(KvqError) as e:
+        decode(cache, plan, q, bt, bad_len, out, wl.sm_scale, checked=True)
+    assert e.value.code == 5
+    bad_plan = plan.plan.clone()
+    bad_plan[wl.B + 1] = 99               # launch order is not a permutation
+    plan.plan = bad_plan
+    with pytest.raises(KvqError) as e:
+        decode(cache, plan, q, bt, sl, out, wl.sm_scale, checked=True)
+    assert e.value.code == 1
+    # after the errors the context is still usable and a good call is exact
+    good = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=2)
+    decode(cache, good, q, bt, sl, out, wl.sm_scale, checked=True)
+
+
+def test_nan_sentinels_in_unwritten_tail_slots_do_not_leak():
+    for fmt in ("int8", "nvfp4", "bf16"):
+        wl = W.make("tiny_int8", lens=("list", [33, 5, 47]), seed=6)
+        _check(wl, fmt, 2)
+
+
+# ---------------------------------------------------------------- full-size workloads
+# (launch configuration of bench.py: automatic split plan, sampled (b, h) units)
+def test_long_int8_full_size_sampled():
+    wl = W.make("long_int8")
+    for split in (0, 16, 64):
+        _check(wl, "int8", split, units=[(0, 0), (0, 3)])
+
+
+def test_long_int8_bf16_cache_full_size_sampled():
+    wl = W.make("long_int8")
+    _check(wl, "bf16", 0, units=[(0, 1)])
+
+
+def test_serving_int8_full_size_sampled():
+    wl = W.make("serving_int8")
+    order = np.argsort(wl.seq_lens)
+    units = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 3)]
+    _check(wl, "int8", 0, units=units)
+
+
+def test_long_nvfp4_full_size_sampled():
+    wl = W.make("long_nvfp4")
+    order = np.argsort(wl.seq_lens)
+    units = [(int(order[0]), 1), (int(order[-1]), 2)]
+    _check(wl, "nvfp4", 0, units=units)
