@@ -161,28 +161,36 @@ int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_ne
 /* ---- split planning ([long-ctx]: split-KV; the split count trades merge
  *      overhead against parallelism) ----------------------------------------- */
 /*
- * Choose, on the host, how many splits each sequence gets and write a plan:
- *   plan[0..batch]               split_offsets: sequence b owns partial slots
- *                                [plan[b], plan[b+1]), plan[0] = 0, plan[batch] = total
- *   plan[batch+1 .. batch+total] the order in which work items are launched: split
- *                                indices sorted by decreasing page count
+ * Choose, on the host, how many splits each sequence gets and how the work is
+ * spread over persistent CTAs, and write the plan:
+ *   plan[0..batch]            split_offsets: sequence b owns splits (and partial
+ *                             slots) [plan[b], plan[b+1]); plan[0] = 0, plan[batch] = total
+ *   plan[batch+1]             C = *num_ctas, the number of persistent CTAs
+ *   plan[batch+2 .. +C+1]     CTA offsets: CTA c works through item list entries
+ *                             [off[c], off[c+1]), off[0] = 0, off[C] = total * NHG
+ *   then total * NHG items    item = split * NHG + head group, NHG = Hkv / HG, where
+ *                             HG = gcd(Hkv, consumer warps of the kernel: 8 at D = 256,
+ *                             12 at D = 128) KV heads are handled together
  * Split s of a sequence with n pages and S splits covers pages
  * [floor(s*n/S), floor((s+1)*n/S)) — whole pages, sizes differing by at most one.
+ * Items are packed onto the C CTAs longest first, each onto the CTA with the least
+ * work so far, so an uneven batch runs in one wave.
  *   seq_lens        host int32 [batch], each >= 0
  *   split_override  > 0: S_b = clamp(split_override, 1, max(n_pages_b, 1));
- *                   0: automatic — about one work item per resident CTA slot:
- *                   pages per item = max(4, ceil(Hkv * total_pages / target_ctas))
- *   target_ctas     concurrent CTAs to plan for; 0 = measured on the current device
- *                   (SM count x resident decode CTAs per SM for this format/head_dim)
+ *                   0: automatic — pages per split = max(4, ceil(NHG * total_pages / C))
+ *   target_ctas     CTAs to plan for; 0 = measured on the current device (SM count
+ *                   x resident decode CTAs per SM for this format/head_dim);
+ *                   C = min(target_ctas, total * NHG)
  *   plan            host int32 buffer of plan_capacity entries (nullable for a size query)
- *   total_splits, max_splits  out (always written when the inputs are valid)
- * Returns KVQ_ERR_WORKSPACE if plan is NULL or shorter than batch + 1 + total.
- * The plan must be copied to the device before kvq_paged_decode_attention.
+ *   total_splits, num_ctas  out (always written when the inputs are valid)
+ * Returns KVQ_ERR_WORKSPACE if plan is NULL or shorter than
+ * batch + 3 + C + total * NHG.  The plan must be copied to the device before
+ * kvq_paged_decode_attention.
  */
 int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch,
                     int32_t split_override, int32_t target_ctas,
                     int32_t* plan, int64_t plan_capacity,
-                    int32_t* total_splits, int32_t* max_splits);
+                    int32_t* total_splits, int32_t* num_ctas);
 
 /* Workspace bytes for a decode call: a 256-byte status block, then
  * lse_part float[total_splits][num_q_heads] (padded to 256 bytes), then
@@ -201,13 +209,15 @@ int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_
  * out[b][g] = softmax(sm_scale * q[b][g] . K_b^T) . V_b for every sequence b and
  * query head g, with K_b/V_b the dequantized cache rows of KV head g / (Hq/Hkv)
  * (consecutive query heads share a KV head), tokens 0..seq_lens[b]-1 in the order
- * of the block table.  One CTA handles one (split, KV head) work item and loads
- * each page once for the whole query-head group.
+ * of the block table.  Each of the num_ctas persistent CTAs works through its
+ * list of (split, KV-head group) items and loads each page once for the whole
+ * query-head group.
  *   q              device bf16 [batch][num_q_heads][head_dim]
  *   sm_scale       softmax scale, normally 1/sqrt(head_dim)
  *   block_tables   device int32 [batch][max_pages_per_seq]; page j of sequence b
  *   seq_lens       device int32 [batch]
- *   plan           device int32, the kvq_plan_splits output for these seq_lens
+ *   plan           device int32, the kvq_plan_splits output for these seq_lens;
+ *                  total_splits and num_ctas are its two outputs
  *   workspace      device, >= kvq_decode_workspace_bytes(total_splits, Hq, D)
  *   out            device, [batch][num_q_heads][head_dim] float or bf16 (out_dtype)
  *   lse_out        device float [batch][num_q_heads] (nullable): natural-log
@@ -222,7 +232,8 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
                                int32_t num_q_heads, float sm_scale,
                                const int32_t* block_tables, int32_t max_pages_per_seq,
                                const int32_t* seq_lens, const int32_t* plan,
-                               int32_t total_splits, void* workspace, size_t workspace_bytes,
+                               int32_t total_splits, int32_t num_ctas,
+                               void* workspace, size_t workspace_bytes,
                                void* out, int32_t out_dtype, float* lse_out,
                                uint32_t flags, void* stream);
 

@@ -67,7 +67,7 @@ def lib():
         "kvq_decode_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
         "kvq_workspace_partials": (c_int32, [P, c_int32, c_int32, c_int32, POINTER(c_void_p), POINTER(c_void_p)]),
         "kvq_paged_decode_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P, c_int32,
-                                                 P, P, c_int32, P, c_size_t, P, c_int32, P, c_uint32, P]),
+                                                 P, P, c_int32, c_int32, P, c_size_t, P, c_int32, P, c_uint32, P]),
         "kvq_split_merge": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P, c_int32, P, P]),
         "kvq_read_status": (c_int32, [P, P, POINTER(c_int32)]),
         "kvq_last_error": (ctypes.c_char_p, []),
@@ -120,20 +120,21 @@ def kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim):
 
 
 def kvq_plan_splits(cache_struct, seq_lens, split_override=0, target_ctas=0):
-    """seq_lens: host int sequence.  Returns (plan int32 CPU tensor, total_splits, max_splits)."""
+    """seq_lens: host int sequence.  Returns (plan int32 CPU tensor, total_splits, num_ctas)."""
     sl = torch.as_tensor(list(seq_lens), dtype=torch.int32)
     B = sl.numel()
-    total, mx = c_int32(), c_int32()
+    total, nctas = c_int32(), c_int32()
     L = lib()
     rc = L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
-                           split_override, target_ctas, None, 0, ctypes.byref(total), ctypes.byref(mx))
+                           split_override, target_ctas, None, 0, ctypes.byref(total), ctypes.byref(nctas))
     if rc not in (0, 3):  # 3 = KVQ_ERR_WORKSPACE (size query)
         _check(rc, "kvq_plan_splits")
-    plan = torch.zeros(B + 1 + total.value, dtype=torch.int32)
+    # head groups per item <= num_kv_heads, so this bounds the plan length
+    plan = torch.zeros(B + 3 + nctas.value + total.value * cache_struct.num_kv_heads, dtype=torch.int32)
     _check(L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
                              split_override, target_ctas, plan.numpy().ctypes.data_as(POINTER(c_int32)),
-                             plan.numel(), ctypes.byref(total), ctypes.byref(mx)), "kvq_plan_splits")
-    return plan, total.value, mx.value
+                             plan.numel(), ctypes.byref(total), ctypes.byref(nctas)), "kvq_plan_splits")
+    return plan, total.value, nctas.value
 
 
 def kvq_workspace_partials(workspace, total_splits, num_q_heads, head_dim):
@@ -166,8 +167,8 @@ def kvq_quant_append(cache_struct, k_new, v_new, slot_mapping, dev_status=None, 
                                   _ptr(dev_status), flags, _stream(stream)), "kvq_quant_append")
 
 
-def kvq_paged_decode_attention(cache_struct, q, sm_scale, block_tables, seq_lens, plan, total_splits, workspace,
-                               out, lse_out=None, flags=0, stream=None):
+def kvq_paged_decode_attention(cache_struct, q, sm_scale, block_tables, seq_lens, plan, total_splits, num_ctas,
+                               workspace, out, lse_out=None, flags=0, stream=None):
     _need(q, torch.bfloat16, "q")
     _need(block_tables, torch.int32, "block_tables")
     _need(seq_lens, torch.int32, "seq_lens")
@@ -182,7 +183,8 @@ def kvq_paged_decode_attention(cache_struct, q, sm_scale, block_tables, seq_lens
     od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
     _check(lib().kvq_paged_decode_attention(
         ctypes.byref(cache_struct), _ptr(q), B, Hq, float(sm_scale), _ptr(block_tables), block_tables.shape[1],
-        _ptr(seq_lens), _ptr(plan), total_splits, _ptr(workspace), workspace.numel(), _ptr(out), od, _ptr(lse_out),
+        _ptr(seq_lens), _ptr(plan), total_splits, num_ctas, _ptr(workspace), workspace.numel(), _ptr(out), od,
+        _ptr(lse_out),
         flags, _stream(stream)), "kvq_paged_decode_attention")
 
 

@@ -54,7 +54,7 @@ class DecodePlan:
     workspace it needs (status word zeroed once)."""
 
     def __init__(self, cache, seq_lens, num_q_heads, split_override=0, target_ctas=0, device="cuda"):
-        plan, self.total_splits, self.max_splits = B.kvq_plan_splits(
+        plan, self.total_splits, self.num_ctas = B.kvq_plan_splits(
             cache.struct, [int(x) for x in seq_lens], split_override, target_ctas)
         self.plan_host = plan
         self.plan = plan.to(device)
@@ -73,4 +73,4 @@ def decode(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, 
            stream=None):
     flags = (B.KVQ_CHECKED if checked else 0) | (B.KVQ_SKIP_MERGE if skip_merge else 0)
     B.kvq_paged_decode_attention(cache.struct, q, sm_scale, block_tables, seq_lens, plan.plan, plan.total_splits,
-                                 plan.workspace, out, lse_out, flags, stream)
+                                 plan.num_ctas, plan.workspace, out, lse_out, flags, stream)

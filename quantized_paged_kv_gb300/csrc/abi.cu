@@ -126,20 +126,11 @@ int make_code_map(CUtensorMap* map, void* base, int64_t num_pages, int64_t hkv, 
   return KVQ_OK;
 }
 
-int gcd_int(int a, int b) {
-  while (b) {
-    const int t = a % b;
-    a = b;
-    b = t;
-  }
-  return a;
-}
-
 // KV heads per decode work item for a cache (0 if no kernel exists for it).
 int heads_per_cta(const kvq_cache* c) {
   kvq::DecodeInstance inst;
   if (!kvq::decode_instance(c->format, c->head_dim, &inst)) return 0;
-  return gcd_int(c->num_kv_heads, inst.consumer_warps);
+  return inst.head_group(c->num_kv_heads);
 }
 
 // --------------------------------------------------------------- decode instances
@@ -245,12 +236,15 @@ int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_ne
 
 int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch, int32_t split_override,
                     int32_t target_ctas, int32_t* plan, int64_t plan_capacity, int32_t* total_splits,
-                    int32_t* max_splits) {
+                    int32_t* num_ctas) {
   int rc = check_cache(cache, false);
   if (rc) return rc;
   if (batch < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", batch);
-  if (!seq_lens || !total_splits || !max_splits) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  if (!seq_lens || !total_splits || !num_ctas) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
   if (split_override < 0 || target_ctas < 0) return fail(KVQ_ERR_INVALID_ARG, "negative split_override / target_ctas");
+  const int hgs = heads_per_cta(cache);
+  if (hgs <= 0) return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this cache");
+  const int nhg = cache->num_kv_heads / hgs;
   const int P = cache->page_size;
   std::vector<int64_t> npages(batch);
   int64_t total_pages = 0;
@@ -259,54 +253,75 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
     npages[b] = (seq_lens[b] + P - 1) / P;
     total_pages += npages[b];
   }
+  int64_t target = target_ctas;
+  if (target == 0) {
+    kvq::DecodeInstance inst;
+    rc = prepare_instance(cache->format, cache->head_dim, &inst);
+    if (rc) return rc;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inst.kernel, inst.threads, inst.smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "querying SM count / occupancy");
+    target = (int64_t)sms * std::max(per_sm, 1);
+  }
+  target = std::max<int64_t>(target, 1);
   std::vector<int32_t> splits(batch, 1);
   if (split_override > 0) {
     for (int b = 0; b < batch; ++b)
       splits[b] = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(split_override, std::max<int64_t>(npages[b], 1))));
   } else {
-    int64_t target = target_ctas;
-    if (target == 0) {
-      kvq::DecodeInstance inst;
-      rc = prepare_instance(cache->format, cache->head_dim, &inst);
-      if (rc) return rc;
-      int dev = 0, sms = 0, per_sm = 0;
-      cudaError_t e = cudaGetDevice(&dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inst.kernel, inst.threads, inst.smem_bytes);
-      if (e != cudaSuccess) return cuda_fail(e, "querying SM count / occupancy");
-      target = (int64_t)sms * std::max(per_sm, 1);
-    }
-    const int hgs = heads_per_cta(cache);
-    if (hgs <= 0) return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this cache");
-    const int64_t units = total_pages * (cache->num_kv_heads / hgs);  // (page, head group) units
-    const int64_t chunk = std::max<int64_t>(4, (units + target - 1) / std::max<int64_t>(target, 1));
+    const int64_t units = total_pages * nhg;  // (page, head group) units
+    const int64_t chunk = std::max<int64_t>(4, (units + target - 1) / target);
     for (int b = 0; b < batch; ++b)
       splits[b] = static_cast<int32_t>(std::max<int64_t>(1, (npages[b] + chunk - 1) / chunk));
   }
   int64_t total = 0;
-  int32_t mx = 0;
-  for (int b = 0; b < batch; ++b) {
-    total += splits[b];
-    mx = std::max(mx, splits[b]);
-  }
-  if (total > 0x7FFFFFFF / std::max(cache->num_kv_heads, 1)) return fail(KVQ_ERR_UNSUPPORTED, "too many splits");
+  for (int b = 0; b < batch; ++b) total += splits[b];
+  if (total * nhg > 0x7FFFFFFF / 2) return fail(KVQ_ERR_UNSUPPORTED, "too many splits");
+  const int64_t n_items = total * nhg;
+  const int64_t C = std::min<int64_t>(target, n_items);  // persistent CTAs
   *total_splits = static_cast<int32_t>(total);
-  *max_splits = mx;
-  if (!plan || plan_capacity < batch + 1 + total)
-    return fail(KVQ_ERR_WORKSPACE, "plan needs %lld int32 entries", (long long)(batch + 1 + total));
+  *num_ctas = static_cast<int32_t>(C);
+  const int64_t need = batch + 1 + 1 + (C + 1) + n_items;
+  if (!plan || plan_capacity < need)
+    return fail(KVQ_ERR_WORKSPACE, "plan needs %lld int32 entries", (long long)need);
   plan[0] = 0;
   for (int b = 0; b < batch; ++b) plan[b + 1] = plan[b] + splits[b];
-  // launch order: longest work items first (pages of split s of sequence b)
+  // Items (split, head group) with their page counts; longest first, each onto the
+  // CTA with the least work so far (a page costs 1, an item's fixed prologue and
+  // epilogue are counted as 8 pages).
   std::vector<std::pair<int64_t, int32_t>> items;
-  items.reserve(total);
+  items.reserve(n_items);
   for (int b = 0; b < batch; ++b)
     for (int s = 0; s < splits[b]; ++s) {
       const int64_t pb = (int64_t)s * npages[b] / splits[b], pe = (int64_t)(s + 1) * npages[b] / splits[b];
-      items.emplace_back(pe - pb, plan[b] + s);
+      for (int g = 0; g < nhg; ++g) items.emplace_back(pe - pb, (plan[b] + s) * nhg + g);
     }
   std::stable_sort(items.begin(), items.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
-  for (int64_t i = 0; i < total; ++i) plan[batch + 1 + i] = items[i].second;
+  std::vector<std::vector<int32_t>> bins(C);
+  std::vector<std::pair<int64_t, int32_t>> heap;  // (load, cta) min-heap
+  heap.reserve(C);
+  for (int32_t cta = 0; cta < C; ++cta) heap.emplace_back(0, cta);
+  auto cmp = [](const auto& a, const auto& b) { return a.first > b.first || (a.first == b.first && a.second > b.second); };
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  for (const auto& it : items) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    auto& top = heap.back();
+    bins[top.second].push_back(it.second);
+    top.first += it.first + 8;
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  int32_t* hdr = plan + batch + 1;
+  hdr[0] = static_cast<int32_t>(C);
+  int32_t* cta_off = hdr + 1;
+  int32_t* out_items = cta_off + C + 1;
+  cta_off[0] = 0;
+  for (int64_t cta = 0; cta < C; ++cta) {
+    cta_off[cta + 1] = cta_off[cta] + static_cast<int32_t>(bins[cta].size());
+    std::copy(bins[cta].begin(), bins[cta].end(), out_items + cta_off[cta]);
+  }
   return succeed();
 }
 
@@ -330,8 +345,8 @@ int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_
 int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t batch, int32_t num_q_heads,
                                float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq,
                                const int32_t* seq_lens, const int32_t* plan, int32_t total_splits,
-                               void* workspace, size_t workspace_bytes, void* out, int32_t out_dtype,
-                               float* lse_out, uint32_t flags, void* stream) {
+                               int32_t num_ctas, void* workspace, size_t workspace_bytes, void* out,
+                               int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
   int rc = check_cache(cache, true);
   if (rc) return rc;
   if (batch < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", batch);
@@ -344,6 +359,7 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   if (G > 8) return fail(KVQ_ERR_UNSUPPORTED, "query heads per KV head %d > 8", G);
   if (max_pages_per_seq < 1) return fail(KVQ_ERR_INVALID_ARG, "max_pages_per_seq %d < 1", max_pages_per_seq);
   if (total_splits < batch) return fail(KVQ_ERR_INVALID_ARG, "total_splits %d < batch %d", total_splits, batch);
+  if (num_ctas < 1) return fail(KVQ_ERR_INVALID_ARG, "num_ctas %d < 1", num_ctas);
   if ((int64_t)total_splits * cache->num_kv_heads > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "bad out_dtype");
   if (!(std::isfinite(sm_scale))) return fail(KVQ_ERR_INVALID_ARG, "sm_scale must be finite");
@@ -357,17 +373,29 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   const bool checked = flags & KVQ_CHECKED;
   if (checked) {
     // host-side validation of the plan (the kernel also checks every entry it uses)
-    std::vector<int32_t> h(batch + 1 + total_splits);
+    const int hgc = heads_per_cta(cache);
+    if (hgc <= 0) return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this cache");
+    const int nhg_checked = cache->num_kv_heads / hgc;
+    if (num_ctas > (int64_t)total_splits * nhg_checked)
+      return fail(KVQ_ERR_INVALID_ARG, "num_ctas %d exceeds the number of work items", num_ctas);
+    std::vector<int32_t> h(batch + 1 + 1 + (num_ctas + 1) + (size_t)total_splits * nhg_checked);
     cudaError_t e = cudaMemcpyAsync(h.data(), plan, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "reading plan");
     if (h[0] != 0 || h[batch] != total_splits) return fail(KVQ_ERR_INVALID_ARG, "plan offsets do not span total_splits");
     for (int b = 0; b < batch; ++b)
       if (h[b + 1] <= h[b]) return fail(KVQ_ERR_INVALID_ARG, "plan gives sequence %d no split", b);
-    std::vector<int32_t> order(h.begin() + batch + 1, h.end());
+    const int64_t C = h[batch + 1];
+    const int64_t n_items = (int64_t)total_splits * nhg_checked;
+    if (C != num_ctas) return fail(KVQ_ERR_INVALID_ARG, "plan CTA count %lld != num_ctas %d", (long long)C, num_ctas);
+    const int32_t* co = h.data() + batch + 2;
+    if (co[0] != 0 || co[C] != n_items) return fail(KVQ_ERR_INVALID_ARG, "plan CTA offsets do not span the items");
+    for (int64_t i = 0; i < C; ++i)
+      if (co[i + 1] < co[i]) return fail(KVQ_ERR_INVALID_ARG, "plan CTA offsets decrease");
+    std::vector<int32_t> order(co + C + 1, co + C + 1 + n_items);
     std::sort(order.begin(), order.end());
-    for (int i = 0; i < total_splits; ++i)
-      if (order[i] != i) return fail(KVQ_ERR_INVALID_ARG, "plan launch order is not a permutation");
+    for (int64_t i = 0; i < n_items; ++i)
+      if (order[i] != i) return fail(KVQ_ERR_INVALID_ARG, "plan items are not a permutation");
   }
   kvq::DecodeInstance inst;
   rc = prepare_instance(cache->format, D, &inst);
@@ -404,7 +432,8 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
   p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
   p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
-  cudaError_t e = kvq::launch_decode(cache->format, D, tk, tv, p, total_splits * (cache->num_kv_heads / hg), st);
+  // one persistent CTA per plan bin
+  cudaError_t e = kvq::launch_decode(cache->format, D, tk, tv, p, num_ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (!(flags & KVQ_SKIP_MERGE) && total_splits > batch) {
     e = kvq::launch_merge(o_part, lse_part, plan, batch, num_q_heads, D, out, p.out_bf16, lse_out, st);

@@ -10,19 +10,23 @@
 // cache, faster first token", section "Lever two": one KV block is loaded once
 // for a whole group of query heads).
 //
-// Work item (one CTA, one per SM): one split (a range of whole pages) of one
-// sequence for a group of HG consecutive KV heads, HG = gcd(Hkv, CW) where CW is
-// the number of consumer warps (4 at D = 256, 8 at D = 128).  The pool keeps the
+// Work item: one split (a range of whole pages) of one sequence for a group of
+// HG consecutive KV heads, HG = gcd(Hkv, CW) where CW is the number of consumer
+// warps (8 at D = 256, 12 at D = 128).  CTAs are persistent, one per SM: the host
+// planner packs the items onto the CTAs (longest first, each to the least-loaded
+// CTA) and every CTA works through its list, so a batch of uneven sequences
+// runs in one wave.  The pool keeps the
 // KV heads of a page next to each other, so the HG heads' code blocks of a page
 // are one contiguous region and travel as ONE TMA box per tensor (16 KB at
 // D = 256 INT8 with 4 heads); a 1-D bulk copy brings their scales.  Few large
 // copies per page keep a single producer thread ahead of the consumers.
 //
-//   * warp CW (producer): lane 0 walks the split's pages through the block table
-//     (page ids staged in shared memory 32 at a time by the whole warp) and, per
-//     page, waits for the stage to be free, then issues the K and V boxes
-//     (128-byte swizzle) and the two scale copies, completing on the stage's
-//     mbarrier (expect-tx bytes).
+//   * warps CW.. (2 to 4 producers): producer i walks every NP-th page of the
+//     item through the block table (page ids staged in shared memory 32 at a
+//     time by its warp); its lane 0, per page, waits for the stage to be free,
+//     then issues the K and V boxes (128-byte swizzle) and the two scale copies,
+//     completing on the stage's mbarrier (expect-tx bytes).  Several producers
+//     are needed because one thread issues only about one copy per 300 ns.
 //   * warps 0..CW-1 (consumers): warp w owns KV head w % HG and, if CW / HG > 1,
 //     every (CW/HG)-th page.  Per page (16 tokens) a warp computes S = q K^T for
 //     its G <= 8 query heads with mma.m16n8k16 (heads are the M rows, tokens the N
@@ -74,16 +78,18 @@ struct DecodeTraits<KVQ_FMT_NVFP4, 256> {
   static constexpr int kScaleRow = 16;  // one E4M3 byte per 16 elements
 };
 
-// consumer warps per CTA: 4 (+1 producer = 5 warps, up to 255 registers) at D =
-// 256; 8 (+1 = 9 warps, <= 168 registers, enough at D = 128) at D = 128.
+// consumer warps per CTA: 8 at D = 256 (+1 producer = 9 warps: at most 3 per
+// SM sub-partition, so <= 168 registers a thread) and 12 at D = 128 (13 warps:
+// <= 128 registers, enough at D = 128).
 template <int D>
-constexpr int consumer_warps() { return 8; }
+constexpr int consumer_warps() { return D == 256 ? 8 : 12; }
 
 template <int FMT, int D>
 struct DecodeLayout {
   using T = DecodeTraits<FMT, D>;
   static constexpr int kCW = consumer_warps<D>();
-  static constexpr int kThreads = (kCW + 1) * 32;
+  static constexpr int kMaxProducers = 4;  // producer warps (a thread issues one copy per ~300 ns)
+  static constexpr int kThreads = (kCW + kMaxProducers) * 32;
   static constexpr int kHeadCode = kPage * T::kRow;        // one head's K (or V) code block of a page
   static constexpr int kHeadScale = kPage * T::kScaleRow;  // one head's K (or V) scale block of a page
   static constexpr int kKSteps = D / 16;
@@ -92,28 +98,66 @@ struct DecodeLayout {
   static constexpr int kQBytes = kKSteps * 2 * 128;
   // shared-memory stage ring: what is left of 227 KB after alignment slack, the
   // q tiles, the barriers and the page-id buffer
-  static constexpr int kRingBytes = (227 * 1024 - 1024 - kCW * kQBytes - 2 * kMaxStages * 8 - 2 * 32 * 4) / 1024 * 1024;
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kCW * kQBytes + 2 * kMaxStages * 8 + 2 * 32 * 4;
+  static constexpr int kIdBytes = kMaxProducers * 2 * 32 * 4;
+  static constexpr int kRingBytes = (227 * 1024 - 1024 - kCW * kQBytes - 2 * kMaxStages * 8 - kIdBytes) / 1024 * 1024;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kCW * kQBytes + 2 * kMaxStages * 8 + kIdBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  // epilogue reuses the code region: O[warp][8 heads][D] + m, l [warp][8]
-  static constexpr int kEpilogueBytes = kCW * 8 * D * 4 + 2 * kCW * 8 * 4;
+  // epilogue reuses the code region: O[warp][8 heads][D], m, l [warp][8], and
+  // the per-row merge weights [8 * kCW] + lse [8 * kCW]
+  static constexpr int kEpilogueBytes = kCW * 8 * D * 4 + 2 * kCW * 8 * 4 + 2 * 8 * kCW * 4;
 };
 
-// Stage count for a head group of `hg` heads: as many stages as fit the ring,
-// at most kMaxStages, and a multiple of the number of warps per head.  Page i goes
-// to stage i % stages and to the head's warp (i % warps-per-head); with the
-// stage count a multiple of warps-per-head every stage has a fixed set of
-// consumer warps, each of which consumed the stage's previous page itself before
-// waiting on the next one, so a parity wait can never be satisfied by a barrier
-// that is still two phases behind.
+// Producer warps and stage count for a head group of `hg` heads.  A single
+// thread issues about one copy per 300 ns whatever its size, so several producer
+// warps share the issuing: page i of an item is issued by producer i % NP and
+// consumed by the head's warp i % WPH (WPH = warps per head).  The stage count is
+// as large as the ring allows (at most kMaxStages) and a multiple of both, so
+// within an item every stage has a fixed producer and a fixed set of consumer
+// warps, each of which handled the stage's previous page itself before waiting on
+// the next one: a parity wait can never be satisfied by a barrier that is still
+// two phases behind.  (Between items the CTA synchronizes, so every stage is idle.)
+template <int FMT, int D>
+__host__ __device__ inline int decode_producers(int hg) {
+  const int wph = DecodeLayout<FMT, D>::kCW / hg;
+  return wph == 1 ? 2 : (wph <= 4 ? wph : (wph % 4 == 0 ? 4 : 3));
+}
+
+template <int FMT, int D>
+__host__ __device__ inline int decode_stage_unit(int hg) {
+  const int wph = DecodeLayout<FMT, D>::kCW / hg;
+  const int np = decode_producers<FMT, D>(hg);
+  return wph > np ? wph : np;  // wph and np divide each other
+}
+
 template <int FMT, int D>
 __host__ __device__ inline int decode_stages(int hg) {
   using Lo = DecodeLayout<FMT, D>;
-  const int wph = Lo::kCW / hg;
+  const int unit = decode_stage_unit<FMT, D>(hg);
   const int stage = 2 * hg * (Lo::kHeadCode + Lo::kHeadScale);
   int n = Lo::kRingBytes / stage;
   n = n < kMaxStages ? n : kMaxStages;
-  return n / wph * wph;
+  return n / unit * unit;  // 0 if fewer than `unit` stages fit: such a group is not used
+}
+
+// Largest head group (a divisor of gcd(Hkv, CW)) whose ring holds at least two
+// stages and one per producer / consumer group, and whose code region can hold
+// the epilogue's merge buffer.  0 if none does.
+template <int FMT, int D>
+inline int decode_head_group(int hkv) {
+  using Lo = DecodeLayout<FMT, D>;
+  int g = hkv, b = Lo::kCW;
+  while (b) {
+    const int t = g % b;
+    g = b;
+    b = t;
+  }
+  for (int hg = g; hg >= 1; --hg) {
+    if (g % hg) continue;
+    const int nst = decode_stages<FMT, D>(hg);
+    const int unit = decode_stage_unit<FMT, D>(hg);
+    if (nst >= 2 && nst >= unit && nst * 2 * hg * Lo::kHeadCode >= Lo::kEpilogueBytes) return hg;
+  }
+  return 0;
 }
 
 // byte address (shared window) of 16-byte chunk `chunk` (0..kRow/16-1) of token
@@ -140,8 +184,15 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   const int HG = p.heads_per_cta;
   const int WPH = CW / HG;
   const int NST = decode_stages<FMT, D>(HG);
+  if (HG < 1 || CW % HG != 0 || NST < 2 || NST < decode_stage_unit<FMT, D>(HG)) {  // host picks valid groups
+    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
+    return;
+  }
   const int stage_code = 2 * HG * Lo::kHeadCode;
   const int stage_scale = 2 * HG * Lo::kHeadScale;
+  const int Hkv = p.num_kv_heads;
+  const int NHG = Hkv / HG;
+  const int G = p.num_q_heads / Hkv;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -150,142 +201,71 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   uint8_t* qfrag = smem + Lo::kRingBytes;                  // CW x kQBytes
   uint64_t* full = reinterpret_cast<uint64_t*>(qfrag + CW * Lo::kQBytes);
   uint64_t* empty = full + kMaxStages;
-  int* pid_s = reinterpret_cast<int*>(empty + kMaxStages);  // [2][32] page ids
+  int* pid_s = reinterpret_cast<int*>(empty + kMaxStages);  // [producer][2][32] page ids
 
-  const int Hkv = p.num_kv_heads;
-  const int NHG = Hkv / HG;
-  const int order = blockIdx.x / NHG;
-  const int hg = blockIdx.x - order * NHG;
-  const int G = p.num_q_heads / Hkv;
+  // ---- plan: split offsets [batch + 1], CTA count C, CTA offsets [C + 1], items
   const int32_t* offs = p.plan;
+  const int C = p.plan[p.batch + 1];
+  const int32_t* cta_off = p.plan + p.batch + 2;
+  const int32_t* items = cta_off + C + 1;
+  if (static_cast<int>(blockIdx.x) >= C) return;
+  const int it_begin = cta_off[blockIdx.x];
+  const int it_end = cta_off[blockIdx.x + 1];
+  if (it_begin < 0 || it_end < it_begin || it_end > p.total_splits * NHG) {
+    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
+    return;
+  }
 
-  // ---- which split of which sequence
-  const int item = p.plan[p.batch + 1 + order];
-  if (item < 0 || item >= p.total_splits) {
-    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
-    return;
-  }
-  int lo = 0, hi = p.batch;  // largest b with offs[b] <= item
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (offs[mid] <= item) lo = mid; else hi = mid;
-  }
-  const int b = lo;
-  const int nsplit = offs[b + 1] - offs[b];
-  const int s = item - offs[b];
-  if (nsplit <= 0 || s < 0 || s >= nsplit) {
-    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
-    return;
-  }
-  int L = p.seq_lens[b];
-  if (L < 0 || L > p.max_pages * kPage) {
-    if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
-    L = L < 0 ? 0 : p.max_pages * kPage;
-  }
-  const int npages = (L + kPage - 1) / kPage;
-  const int page_begin = static_cast<int>((int64_t)s * npages / nsplit);
-  const int page_end = static_cast<int>((int64_t)(s + 1) * npages / nsplit);
-  const int n = page_end - page_begin;
+  // Item -> (sequence, split, head group, page range); identical in every thread.
+  struct Item {
+    int b, split, hg, L, page_begin, n;
+    bool direct;  // the sequence has a single split: write `out` directly
+  };
+  auto decode_item = [&](int it, Item& w) -> bool {
+    const int item = items[it];
+    if (item < 0 || item >= p.total_splits * NHG) return false;
+    w.split = item / NHG;
+    w.hg = item - w.split * NHG;
+    int lo = 0, hi = p.batch;  // largest b with offs[b] <= split
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (offs[mid] <= w.split) lo = mid; else hi = mid;
+    }
+    w.b = lo;
+    const int nsplit = offs[w.b + 1] - offs[w.b];
+    const int s = w.split - offs[w.b];
+    if (nsplit <= 0 || s < 0 || s >= nsplit) return false;
+    int L = p.seq_lens[w.b];
+    if (L < 0 || L > p.max_pages * kPage) {
+      if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
+      L = L < 0 ? 0 : p.max_pages * kPage;
+    }
+    w.L = L;
+    const int npages = (L + kPage - 1) / kPage;
+    w.page_begin = static_cast<int>((int64_t)s * npages / nsplit);
+    w.n = static_cast<int>((int64_t)(s + 1) * npages / nsplit) - w.page_begin;
+    w.direct = nsplit == 1;
+    return true;
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  __shared__ int abort_flag;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], HG);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == CW) {
-    // ================================================================ producer
-    const int32_t* bt = p.block_tables + (size_t)b * p.max_pages + page_begin;
-    auto page_id = [&](int j) -> int {  // validated page id of split page j (or -1)
-      int v = -1;
-      if (j < n) {
-        v = bt[j];
-        if (v < 0 || v >= p.num_pages) {
-          atomicOr(p.status, KVQ_DEV_BAD_PAGE);
-          v = -1;
-        }
-      }
-      return v;
-    };
-    pid_s[lane] = page_id(lane);
-    __syncwarp();
-    bool ok = true;
-    int issued = 0, st = 0, rnd = 0;  // next page's stage and ring round
-    const size_t head0 = (size_t)hg * HG;
-    for (int base = 0, buf = 0; base < n; base += 32, buf ^= 1) {
-      const int nxt = page_id(base + 32 + lane);  // prefetch the next 32 ids
-      if (lane == 0) {
-        const int cnt = min(32, n - base);
-        for (int k = 0; k < cnt; ++k) {
-          const int pg = pid_s[buf * 32 + k];
-          if (rnd > 0 && !mbar_wait(&empty[st], (rnd - 1) & 1, kWaitLimitNs)) {
-            atomicOr(p.status, KVQ_DEV_TIMEOUT);
-            ok = false;
-            break;
-          }
-          if (pg >= 0) {
-            uint8_t* kc = codes + st * stage_code;
-            mbar_arrive_expect_tx(&full[st], stage_code + stage_scale);
-            tma_load_5d(kc, &tm_k, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
-            tma_load_5d(kc + HG * Lo::kHeadCode, &tm_v, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
-            if constexpr (T::kScaleRow > 0) {
-              uint8_t* ks = scales + st * stage_scale;
-              const size_t off = ((size_t)pg * Hkv + head0) * Lo::kHeadScale;
-              bulk_load(ks, p.k_scales + off, HG * Lo::kHeadScale, &full[st]);
-              bulk_load(ks + HG * Lo::kHeadScale, p.v_scales + off, HG * Lo::kHeadScale, &full[st]);
-            }
-          } else {
-            mbar_arrive(&full[st]);  // nothing to load; the stage keeps stale bytes (status flagged)
-          }
-          ++issued;
-          if (++st == NST) {
-            st = 0;
-            ++rnd;
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-      if (!ok) break;
-      pid_s[(buf ^ 1) * 32 + lane] = nxt;
-      __syncwarp();
-    }
-    // Drain: before this warp (and so the CTA) can exit, every copy it issued has
-    // landed; normally the consumers already waited for all of them.
-    if (lane == 0) {  // only lane 0 counted `issued`
-      for (int idx = max(0, issued - NST); idx < issued; ++idx) {
-        if (!mbar_wait(&full[idx % NST], (idx / NST) & 1, kWaitLimitNs)) {
-          atomicOr(p.status, KVQ_DEV_TIMEOUT);
-          break;
-        }
-      }
-    }
-    return;
-  }
-
-  // ================================================================== consumers
+  // consumer identity (used only by consumer warps)
   const int hl = warp % HG;   // head within the group
   const int grp = warp / HG;  // page subset of this head's warps
-  const int h = hg * HG + hl;
   const int r = lane >> 2;    // head row of S / P, token group of V^T fragments
   const int c = lane & 3;
-  const int hq = h * G + r;
   const bool head_ok = r < G;
-  const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.num_q_heads + hq) * D;
-  uint8_t* myq = qfrag + warp * Lo::kQBytes;
 
-  // ---- q fragments (A operand rows = heads), staged once per warp in shared
-  // memory and read per page with ldmatrix.  Column (k) order per format,
-  // matching the K fragments below: k-step j pairs (2c, 2c+1) with d dA(j, c) +
-  // {0, 1} and (2c+8, 2c+9) with dB(j, c) + {0, 1}.
-  float qk_scale;
-  {
-    uint32_t raw[KS][2];
+  // q of an item, as raw bf16 pairs in fragment column order (see below); issued
+  // before the producer starts streaming so these loads are not queued behind it.
+  uint32_t qraw[KS][2];
+  auto load_q = [&](const Item& w) {
+    const int hq = (w.hg * HG + hl) * G + r;
+    const __nv_bfloat16* qrow =
+        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)w.b * p.num_q_heads + hq) * D;
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
       int dA, dB;
@@ -299,52 +279,122 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         dA = 32 * (j >> 1) + 8 * c + 4 * (j & 1);
         dB = dA + 2;
       }
-      raw[j][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + dA) : 0u;
-      raw[j][1] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + dB) : 0u;
+      qraw[j][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + dA) : 0u;
+      qraw[j][1] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + dB) : 0u;
     }
-    float qs = p.sm_scale_log2;
-    if constexpr (!T::kBf16Mma) {
-      // bf16 -> f16 exactly: scale the head's row by a power of two so that its
-      // largest |q| lands in [2^14, 2^15); every element within 2^28 of it is then
-      // exactly representable in f16.  The power of two is undone on the logits.
-      float amax = 0.f;
-#pragma unroll
-      for (int j = 0; j < KS; ++j) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
-          amax = fmaxf(amax, fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))));
-        }
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      int k = 0;
-      if (amax > 0.f) {
-        int e;
-        frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
-        k = min(126, max(-126, 15 - e));
-      }
-      const float up = pow2f(k);
-#pragma unroll
-      for (int j = 0; j < KS; ++j) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
-          raw[j][u] = h2_as_u32(__floats2half2_rn(__low2float(v) * up, __high2float(v) * up));
-        }
-      }
-      qs *= pow2f(-k);
-      if constexpr (FMT == KVQ_FMT_NVFP4) qs *= p.k_gs_inv;
+  };
+
+  Item first;
+  const bool first_ok = it_begin < it_end && decode_item(it_begin, first);
+  if (warp < CW && first_ok) load_q(first);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], HG);
     }
-#pragma unroll
-    for (int j = 0; j < KS; ++j) {
-      uint32_t* m0 = reinterpret_cast<uint32_t*>(myq + (2 * j) * 128 + r * 16 + c * 4);
-      m0[0] = raw[j][0];
-      m0[32] = raw[j][1];  // next matrix (dB part), +128 bytes
-    }
-    qk_scale = qs;
+    fence_mbar_init();
+    abort_flag = 0;
   }
-  __syncwarp();
+  __syncthreads();
+
+  const int NP = decode_producers<FMT, D>(HG);
+  const int sync_threads = (CW + NP) * 32;  // consumers + active producers (item boundaries)
+  if (warp >= CW) {
+    // ================================================================ producers
+    const int pi = warp - CW;
+    if (pi >= NP) return;
+    bool ok = true;
+    int gidx = 0;                 // pages of this CTA before the current item
+    int last_first = 0, last_n = 0;
+    for (int it = it_begin; it < it_end; ++it) {
+      Item w;
+      const bool valid = ok && decode_item(it, w);
+      if (valid) {
+        const int32_t* bt = p.block_tables + (size_t)w.b * p.max_pages + w.page_begin;
+        const int n = w.n;
+        const int mine = n > pi ? (n - pi + NP - 1) / NP : 0;  // this producer's pages: idx = pi + NP*j
+        auto page_id = [&](int j) -> int {  // validated page id of this producer's page j (or -1)
+          int v = -1;
+          if (j < mine) {
+            v = bt[pi + NP * j];
+            if (v < 0 || v >= p.num_pages) {
+              atomicOr(p.status, KVQ_DEV_BAD_PAGE);
+              v = -1;
+            }
+          }
+          return v;
+        };
+        last_first = gidx;  // drain bookkeeping, also right if this item is cut short
+        last_n = n;
+        int* ids = pid_s + pi * 64;
+        ids[lane] = page_id(lane);
+        __syncwarp();
+        const size_t head0 = (size_t)w.hg * HG;
+        int g = gidx + pi;  // global ring position of the next page
+        int st = g % NST, rnd = g / NST;
+        for (int base = 0, buf = 0; base < mine; base += 32, buf ^= 1) {
+          const int nxt = page_id(base + 32 + lane);  // prefetch the next 32 ids
+          if (lane == 0) {
+            const int cnt = min(32, mine - base);
+            for (int k = 0; k < cnt; ++k) {
+              const int pg = ids[buf * 32 + k];
+              if (rnd > 0 && !mbar_wait(&empty[st], (rnd - 1) & 1, kWaitLimitNs)) {
+                atomicOr(p.status, KVQ_DEV_TIMEOUT);
+                ok = false;
+                break;
+              }
+              if (pg >= 0) {
+                uint8_t* kc = codes + st * stage_code;
+                mbar_arrive_expect_tx(&full[st], stage_code + stage_scale);
+                tma_load_5d(kc, &tm_k, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
+                tma_load_5d(kc + HG * Lo::kHeadCode, &tm_v, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
+                if constexpr (T::kScaleRow > 0) {
+                  uint8_t* ks = scales + st * stage_scale;
+                  const size_t off = ((size_t)pg * Hkv + head0) * Lo::kHeadScale;
+                  bulk_load(ks, p.k_scales + off, HG * Lo::kHeadScale, &full[st]);
+                  bulk_load(ks + HG * Lo::kHeadScale, p.v_scales + off, HG * Lo::kHeadScale, &full[st]);
+                }
+              } else {
+                mbar_arrive(&full[st]);  // nothing to load; the stage keeps stale bytes (status flagged)
+              }
+              st += NP;
+              if (st >= NST) {
+                st -= NST;
+                ++rnd;
+              }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+          if (!ok) break;
+          ids[(buf ^ 1) * 32 + lane] = nxt;
+          __syncwarp();
+        }
+        gidx += n;
+      }
+      if (lane == 0 && !ok) abort_flag = 1;
+      // the consumers' epilogue of this item is done: the ring is free
+      asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
+      if (abort_flag || !valid) break;
+    }
+    // Drain: before this warp (and so the CTA) can exit, every copy it issued has
+    // landed.  Only the last item can have copies in flight: the consumers
+    // finished the earlier ones before the item boundary.
+    if (lane == 0) {
+      for (int idx = pi; idx < last_n; idx += NP) {
+        const int g = last_first + idx;
+        if (g + NST < last_first + last_n) continue;  // a later page of this stage was issued
+        if (!mbar_wait(&full[g % NST], (g / NST) & 1, kWaitLimitNs)) {
+          atomicOr(p.status, KVQ_DEV_TIMEOUT);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ================================================================== consumers
+  uint8_t* myq = qfrag + warp * Lo::kQBytes;
   const uint32_t qbase = smem_addr(myq) + ((lane >> 3) * 8 + (lane & 7)) * 16;
   // Per-lane byte offsets of the swizzled ldmatrix rows inside a head block,
   // one per value of (chunk & 7) of the iteration (the XOR with the row index
@@ -356,28 +406,99 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 #pragma unroll
     for (int v4 = 0; v4 < 4; ++v4) voff[v4] = (8 * (mm & 1) + rr) * 128 + (((2 * v4 + (mm >> 1)) ^ rr) << 4);
   }
+  float* red_o = reinterpret_cast<float*>(codes);  // epilogue: [CW][8][D]
+  float* red_m = red_o + CW * 8 * D;                // [CW][8]
+  float* red_l = red_m + CW * 8;                    // [CW][8]
+  float* row_w = red_l + CW * 8;                    // [8 * CW] merge weights (row, warp of the head)
+  float* row_lse = row_w + 8 * CW;                  // [8 * CW]
+  constexpr float kLn2 = 0.69314718055994530942f;
 
-  float oacc[Lo::kMTiles][4];
-#pragma unroll
-  for (int mt = 0; mt < Lo::kMTiles; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
-  float m_run = -INFINITY;  // running max (log2 domain) of head r
-  float l_run = 0.f;        // this lane's part of the running sum of head r
-
-  bool alive = true;
-  int st = grp, rnd = 0;  // stage and ring round of page `idx`
-  for (int idx = grp; idx < n; idx += WPH) {
-    const bool got = mbar_wait(&full[st], rnd & 1, kWaitLimitNs);
-    if (!__all_sync(0xffffffffu, got)) {
-      if (lane == 0) atomicOr(p.status, KVQ_DEV_TIMEOUT);
-      alive = false;
+  int gidx = 0;  // pages of this CTA before the current item (global ring position)
+  Item w = first, nw;
+  bool ok_item = first_ok, next_ok = false;
+  for (int it = it_begin; it < it_end; ++it) {
+    if (!ok_item) {  // a bad plan entry: every thread of the CTA stops here
+      if (threadIdx.x == 0) {
+        atomicOr(p.status, KVQ_DEV_BAD_PLAN);
+        abort_flag = 1;
+      }
+      asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
       break;
     }
-    const uint32_t kblk = smem_addr(codes + st * stage_code + hl * Lo::kHeadCode);
-    const uint32_t vblk = kblk + HG * Lo::kHeadCode;
-    const uint8_t* ksc = scales + st * stage_scale + hl * Lo::kHeadScale;
-    const uint8_t* vsc = ksc + HG * Lo::kHeadScale;
-    const int tok0 = (page_begin + idx) * kPage;
-    const int nvalid = min(kPage, L - tok0);
+    // ---- q fragments (A operand rows = heads) for this item, converted from
+    // the raw bf16 pairs loaded earlier.  Column (k) order per format, matching
+    // the K fragments below: k-step j pairs (2c, 2c+1) with d dA(j, c) + {0, 1}
+    // and (2c+8, 2c+9) with dB(j, c) + {0, 1}.
+    float qk_scale = p.sm_scale_log2;
+    {
+      if constexpr (!T::kBf16Mma) {
+        // bf16 -> f16 exactly: scale the head's row by a power of two so that its
+        // largest |q| lands in [2^14, 2^15); every element within 2^28 of it is
+        // then exactly representable in f16.  The power of two is undone on the
+        // logits.
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&qraw[j][u]);
+            amax = fmaxf(amax, fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))));
+          }
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int k = 0;
+        if (amax > 0.f) {
+          int e;
+          frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
+          k = min(126, max(-126, 15 - e));
+        }
+        const float up = pow2f(k);
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&qraw[j][u]);
+            qraw[j][u] = h2_as_u32(__floats2half2_rn(__low2float(v) * up, __high2float(v) * up));
+          }
+        }
+        qk_scale *= pow2f(-k);
+        if constexpr (FMT == KVQ_FMT_NVFP4) qk_scale *= p.k_gs_inv;
+      }
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        uint32_t* m0 = reinterpret_cast<uint32_t*>(myq + (2 * j) * 128 + r * 16 + c * 4);
+        m0[0] = qraw[j][0];
+        m0[32] = qraw[j][1];  // next matrix (dB part), +128 bytes
+      }
+    }
+    __syncwarp();
+
+    float oacc[Lo::kMTiles][4];
+#pragma unroll
+    for (int mt = 0; mt < Lo::kMTiles; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+    float m_run = -INFINITY;  // running max (log2 domain) of head r
+    float l_run = 0.f;        // this lane's part of the running sum of head r
+    const int n = w.n;
+    const int L = w.L;
+    const int page_begin = w.page_begin;
+
+    bool alive = true;
+    // this warp's pages: idx = grp, grp + WPH, ... ; global ring position gidx + idx
+    int st = (gidx + grp) % NST, rnd = (gidx + grp) / NST;
+    for (int idx = grp; idx < n; idx += WPH) {
+      const bool got = mbar_wait(&full[st], rnd & 1, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) atomicOr(p.status, KVQ_DEV_TIMEOUT);
+        alive = false;
+        break;
+      }
+      const uint32_t kblk = smem_addr(codes + st * stage_code + hl * Lo::kHeadCode);
+      const uint32_t vblk = kblk + HG * Lo::kHeadCode;
+      const uint8_t* ksc = scales + st * stage_scale + hl * Lo::kHeadScale;
+      const uint8_t* vsc = ksc + HG * Lo::kHeadScale;
+      const int tok0 = (page_begin + idx) * kPage;
+      const int nvalid = min(kPage, L - tok0);
 
     // ---------------------------------------------------------- S = q K^T
     float sacc[2][2][4];
@@ -600,104 +721,110 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       }
     }
     (void)partial;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    st += WPH;
-    if (st >= NST) {
-      st -= NST;
-      ++rnd;
-    }
-  }
-
-  // ================================================================== epilogue
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  if (!alive) {
-    m_run = -INFINITY;
-    l_run = 0.f;
-  }
-  // all consumer warps are past their last page, so every stage has landed and
-  // been read: the code region can be reused.
-  asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
-  float* red_o = reinterpret_cast<float*>(codes);  // [CW][8][D]
-  float* red_m = red_o + CW * 8 * D;                // [CW][8]
-  float* red_l = red_m + CW * 8;                    // [CW][8]
-  {
-    float* ow = red_o + warp * 8 * D;
-#pragma unroll
-    for (int mt = 0; mt < Lo::kMTiles; ++mt) {
-      int da, db;
-      if constexpr (FMT == KVQ_FMT_INT8) {
-        da = 16 * mt + 2 * r;
-        db = da + 1;
-      } else if constexpr (FMT == KVQ_FMT_BF16) {
-        da = 16 * mt + r;
-        db = da + 8;
-      } else {
-        da = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1);
-        db = da + 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      st += WPH;
+      if (st >= NST) {
+        st -= NST;
+        ++rnd;
       }
-      ow[(2 * c) * D + da] = oacc[mt][0];
-      ow[(2 * c + 1) * D + da] = oacc[mt][1];
-      ow[(2 * c) * D + db] = oacc[mt][2];
-      ow[(2 * c + 1) * D + db] = oacc[mt][3];
     }
-    if (c == 0) {
-      red_m[warp * 8 + r] = m_run;
-      red_l[warp * 8 + r] = l_run;
-    }
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+    gidx += n;
 
-  const int tid = threadIdx.x;  // 0 .. CW*32-1
-  const bool direct = nsplit == 1;
-  constexpr float kLn2 = 0.69314718055994530942f;
-  // outputs of the group: HG heads x G query heads x D/4 float4 columns
-  for (int e4 = tid; e4 < HG * G * (D / 4); e4 += CW * 32) {
-    const int hh = e4 / (G * (D / 4));
-    const int rem = e4 - hh * G * (D / 4);
-    const int g = rem / (D / 4);
-    const int d = (rem - g * (D / 4)) * 4;
-    float M = -INFINITY;
-    for (int j = 0; j < WPH; ++j) M = fmaxf(M, red_m[(hh + j * HG) * 8 + g]);
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
-    if (M != -INFINITY) {
+    // ================================================================ epilogue
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (!alive) {
+      m_run = -INFINITY;
+      l_run = 0.f;
+      if (lane == 0) abort_flag = 1;
+    }
+    // every consumer warp is past this item's last page: every stage has landed
+    // and been read, and the producer waits for this item's end, so the code
+    // region can be reused.
+    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+    {
+      float* ow = red_o + warp * 8 * D;
+#pragma unroll
+      for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+        int da, db;
+        if constexpr (FMT == KVQ_FMT_INT8) {
+          da = 16 * mt + 2 * r;
+          db = da + 1;
+        } else if constexpr (FMT == KVQ_FMT_BF16) {
+          da = 16 * mt + r;
+          db = da + 8;
+        } else {
+          da = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1);
+          db = da + 1;
+        }
+        ow[(2 * c) * D + da] = oacc[mt][0];
+        ow[(2 * c + 1) * D + da] = oacc[mt][1];
+        ow[(2 * c) * D + db] = oacc[mt][2];
+        ow[(2 * c + 1) * D + db] = oacc[mt][3];
+      }
+      if (c == 0) {
+        red_m[warp * 8 + r] = m_run;
+        red_l[warp * 8 + r] = l_run;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+    // prefetch the next item's q while the results are written
+    next_ok = it + 1 < it_end && decode_item(it + 1, nw);
+    if (next_ok) load_q(nw);
+    const int tid = threadIdx.x;  // 0 .. CW*32-1
+    const int rows = HG * G;      // query heads of the group
+    // merge weights of the warps of each head, once per (head, query head) row
+    if (tid < rows) {
+      const int hh = tid / G, g = tid - hh * G;
+      float M = -INFINITY;
+      for (int j = 0; j < WPH; ++j) M = fmaxf(M, red_m[(hh + j * HG) * 8 + g]);
       float Lsum = 0.f;
+      if (M != -INFINITY)
+        for (int j = 0; j < WPH; ++j) Lsum += red_l[(hh + j * HG) * 8 + g] * exp2f(red_m[(hh + j * HG) * 8 + g] - M);
+      const bool any = M != -INFINITY && Lsum > 0.f;
+      float inv = any ? 1.f / Lsum : 0.f;
+      if constexpr (FMT == KVQ_FMT_NVFP4) inv *= p.v_gs_inv;
+      for (int j = 0; j < WPH; ++j)
+        row_w[tid * WPH + j] = any ? exp2f(red_m[(hh + j * HG) * 8 + g] - M) * inv : 0.f;
+      row_lse[tid] = any ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+    for (int e4 = tid; e4 < rows * (D / 4); e4 += CW * 32) {
+      const int row = e4 / (D / 4);
+      const int d = (e4 - row * (D / 4)) * 4;
+      const int hh = row / G, g = row - hh * G;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j = 0; j < WPH; ++j) {
-        const int w = hh + j * HG;
-        const float wt = exp2f(red_m[w * 8 + g] - M);
-        Lsum += red_l[w * 8 + g] * wt;
-        const float4 ow = *reinterpret_cast<const float4*>(red_o + (w * 8 + g) * D + d);
+        const float wt = row_w[row * WPH + j];
+        const float4 ow = *reinterpret_cast<const float4*>(red_o + ((hh + j * HG) * 8 + g) * D + d);
         o.x += ow.x * wt;
         o.y += ow.y * wt;
         o.z += ow.z * wt;
         o.w += ow.w * wt;
       }
-      float inv = 1.f / Lsum;
-      if constexpr (FMT == KVQ_FMT_NVFP4) inv *= p.v_gs_inv;
-      o.x *= inv;
-      o.y *= inv;
-      o.z *= inv;
-      o.w *= inv;
-      lse = (M + log2f(Lsum)) * kLn2;
-    }
-    const int qh = (hg * HG + hh) * G + g;
-    if (direct) {
-      const size_t off = ((size_t)b * p.num_q_heads + qh) * D + d;
-      if (p.out_bf16) {
-        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off);
-        ob[0] = __floats2bfloat162_rn(o.x, o.y);
-        ob[1] = __floats2bfloat162_rn(o.z, o.w);
+      const int qh = (w.hg * HG + hh) * G + g;
+      if (w.direct) {
+        const size_t off = ((size_t)w.b * p.num_q_heads + qh) * D + d;
+        if (p.out_bf16) {
+          __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off);
+          ob[0] = __floats2bfloat162_rn(o.x, o.y);
+          ob[1] = __floats2bfloat162_rn(o.z, o.w);
+        } else {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + off) = o;
+        }
+        if (d == 0 && p.lse_out) p.lse_out[(size_t)w.b * p.num_q_heads + qh] = row_lse[row];
       } else {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + off) = o;
+        const size_t prow = (size_t)w.split * p.num_q_heads + qh;
+        *reinterpret_cast<float4*>(p.o_part + prow * D + d) = o;
+        if (d == 0) p.lse_part[prow] = row_lse[row];
       }
-      if (d == 0 && p.lse_out) p.lse_out[(size_t)b * p.num_q_heads + qh] = lse;
-    } else {
-      const size_t row = (size_t)item * p.num_q_heads + qh;
-      *reinterpret_cast<float4*>(p.o_part + row * D + d) = o;
-      if (d == 0) p.lse_part[row] = lse;
     }
+    // with the producers: the ring may be refilled for the next item
+    asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
+    if (abort_flag) break;
+    w = nw;
+    ok_item = next_ok;
   }
 }
 

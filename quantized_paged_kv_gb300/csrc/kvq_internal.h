@@ -51,8 +51,9 @@ struct DecodeInstance {
   const void* kernel;          // __global__ function
   int smem_bytes;
   int threads;
-  int consumer_warps;          // KV heads per work item = gcd(num_kv_heads, consumer_warps)
+  int consumer_warps;          // consumer warps per CTA
   int row_bytes;               // code bytes per token row
+  int (*head_group)(int hkv);  // KV heads per work item for num_kv_heads = hkv (0: none fits)
 };
 
 bool decode_instance(int format, int head_dim, DecodeInstance* out);

@@ -55,13 +55,17 @@ def _struct(kvq, fmt="int8", pages=4096, Hkv=4, D=256):
     return kvq._binding.KvqCacheStruct(None, None, None, None, pages, 16, Hkv, D, kvq._binding.FORMATS[fmt], 1.0, 1.0)
 
 
-def _check_plan(plan, seq_lens, total, override=None):
+def _check_plan(plan, seq_lens, total, nctas, nhg, override=None):
     B = len(seq_lens)
     offs = plan[:B + 1]
-    order = plan[B + 1:]
     assert offs[0] == 0 and offs[-1] == total
-    assert sorted(order.tolist()) == list(range(total))
-    sizes = {}
+    C = plan[B + 1]
+    assert C == nctas and 1 <= C <= total * nhg
+    co = plan[B + 2:B + 3 + C]
+    assert co[0] == 0 and co[-1] == total * nhg and all(co[i] <= co[i + 1] for i in range(C))
+    items = plan[B + 3 + C:B + 3 + C + total * nhg]
+    assert sorted(items.tolist()) == list(range(total * nhg))
+    size = {}
     for b, L in enumerate(seq_lens):
         n = -(-L // 16)
         S = offs[b + 1] - offs[b]
@@ -73,27 +77,37 @@ def _check_plan(plan, seq_lens, total, override=None):
         assert all(bounds[i][1] == bounds[i + 1][0] for i in range(S - 1))
         assert max(e - b_ for b_, e in bounds) - min(e - b_ for b_, e in bounds) <= 1
         for s, (b0, e0) in enumerate(bounds):
-            sizes[int(offs[b]) + s] = e0 - b0
-    got = [sizes[int(i)] for i in order]
-    assert got == sorted(got, reverse=True)  # longest work first
+            for g in range(nhg):
+                size[(int(offs[b]) + s) * nhg + g] = e0 - b0
+    # longest-first packing: within a CTA the items come in decreasing size, and no
+    # CTA carries more than the average load plus one item (LPT bound)
+    loads = []
+    for c in range(C):
+        its = [int(i) for i in items[co[c]:co[c + 1]]]
+        sz = [size[i] for i in its]
+        assert sz == sorted(sz, reverse=True)
+        loads.append(sum(x + 8 for x in sz))
+    biggest = max(size.values()) + 8
+    assert max(loads) <= sum(loads) / C + biggest
 
 
 def test_planner_override_and_auto(kvq):
-    s = _struct(kvq)
+    s = _struct(kvq)  # Hkv = 4, D = 256: the 4 heads form one group (nhg = 1)
     rng = np.random.default_rng(0)
     for seq_lens in ([32768], [512], [0], [1, 17, 300, 0, 64], rng.integers(512, 8193, 64).tolist()):
         for ov in (1, 2, 4, 64):
-            plan, total, mx = kvq.kvq_plan_splits(s, seq_lens, ov, 0)
-            _check_plan(plan.numpy(), seq_lens, total, ov)
-        plan, total, mx = kvq.kvq_plan_splits(s, seq_lens, 0, 152)
-        _check_plan(plan.numpy(), seq_lens, total)
-    plan, total, _ = kvq.kvq_plan_splits(s, [32768], 0, 152)
-    # 4 KV heads form one head group (4 consumer warps at D = 256): 2048 page units
-    # over 152 CTAs -> 14 pages per item -> 147 splits
-    assert total == 147
-    s8 = _struct(kvq, pages=4096, Hkv=8, D=128)
-    plan, total, _ = kvq.kvq_plan_splits(s8, [32768], 0, 152)
-    assert total == 147  # 8 heads = one group of the 8 consumer warps at D = 128
+            plan, total, nctas = kvq.kvq_plan_splits(s, seq_lens, ov, 152)
+            _check_plan(plan.numpy(), seq_lens, total, nctas, 1, ov)
+        plan, total, nctas = kvq.kvq_plan_splits(s, seq_lens, 0, 152)
+        _check_plan(plan.numpy(), seq_lens, total, nctas, 1)
+    plan, total, nctas = kvq.kvq_plan_splits(s, [32768], 0, 152)
+    # 2048 page units over 152 CTAs -> 14 pages per item -> 147 splits, one per CTA
+    assert total == 147 and nctas == 147
+    s8 = _struct(kvq, pages=4096, Hkv=8, D=128)  # 12 consumer warps at D = 128 -> groups of 4 heads
+    lens = rng.integers(512, 8193, 64).tolist()
+    plan, total, nctas = kvq.kvq_plan_splits(s8, lens, 0, 152)
+    _check_plan(plan.numpy(), lens, total, nctas, 2)
+    assert nctas == 152
 
 
 def test_workspace_layout(kvq):
@@ -119,12 +133,12 @@ def test_host_validation_errors(kvq):
     rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
     assert rc == 1
     s.k_global_scale = 1.0
-    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
-    assert rc == 3 and total.value == 1  # size query
+    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 152, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    assert rc == 3 and total.value == 1 and mx.value == 1  # size query: 1 split, 1 CTA
     # device calls refuse NULL / misaligned arguments before touching the GPU
     rc = L.kvq_quant_append(ctypes.byref(s), None, None, None, 4, None, 0, None)
     assert rc == 1
-    rc = L.kvq_paged_decode_attention(ctypes.byref(s), None, 1, 4, 0.1, None, 1, None, None, 1, None, 0, None, 0,
-                                      None, 0, None)
+    rc = L.kvq_paged_decode_attention(ctypes.byref(s), None, 1, 4, 0.1, None, 1, None, None, 1, 1, None, 0, None,
+                                      0, None, 0, None)
     assert rc == 1
     assert L.kvq_split_merge(None, None, None, 1, 1, 256, None, 0, None, None) == 1
