@@ -9,10 +9,10 @@ CUDA graph and replayed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
 
-Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica of
-the workload on its own GPU (the batch shards across ranks with no exchange in
-the data path: weak scaling); the only collective is the max-over-ranks of the
-timings.  --impl reference times the float64 CPU oracle on the host cores.
+Prints one JSON line (rank 0).  Under torchrun the job is one independent
+problem of the workload per rank (own seed, own pools), the sequences sharded
+across ranks with no exchange in the data path (weak scaling); the only
+collectives are barriers and the max-over-ranks of the timings.  --impl reference times the float64 CPU oracle on the host cores.
 """
 from __future__ import annotations
 
@@ -313,7 +313,13 @@ def run_ours(args, rank, world, barrier, allmax):
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     peaks, peak_kind = measured_peaks()
 
-    wl = W.make(WORKLOAD)
+    # the job at N ranks is N independent problems of the workload, sharded by
+    # sequence (one per rank here); problem 0 is the workload itself
+    from quantized_paged_kv_gb300.dist import problem_seed, shard_sequences
+
+    base = W.make(WORKLOAD)
+    mine = shard_sequences([base.total_tokens] * world, world)[rank]
+    wl = W.make(WORKLOAD, seed=problem_seed(base.seed, int(mine[0])))
     per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token("int8", wl.Hkv, wl.D)
     R = layers_for(per_layer, l2, floor=16)
     ls = LayerSet(wl, "int8", R, dev)
@@ -345,7 +351,7 @@ def run_ours(args, rank, world, barrier, allmax):
                    "split_plan": f"auto: {plan.total_splits} splits", "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer pools x {per_layer / 1e6:.1f} MB visited round-robin",
                    "timing": "CUDA graph of R consecutive calls (decode + merge), CUDA events",
-                   "parallelism": f"replicas x{world}", "kv_bytes_per_step": bytes_step,
+                   "parallelism": f"dp{world}: one independent problem per rank, no data-path collective", "kv_bytes_per_step": bytes_step,
                    "us_per_16_layer_step": round(16 * t_call * 1e6, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -487,30 +493,19 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
-    barrier = lambda: None  # noqa: E731
-    allmax = lambda x: x  # noqa: E731
+    from quantized_paged_kv_gb300.dist import RankGroup
+
     if world > 1:
         import torch
-        import torch.distributed as dist
 
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        dist.init_process_group("nccl")
-
-        def barrier():  # noqa: F811
-            dist.barrier()
-
-        def allmax(x):  # noqa: F811
-            t = torch.tensor([x], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-
-    line = run_ours(args, rank, world, barrier, allmax)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.destroy_process_group()
+    group = RankGroup.from_env("nccl")
+    try:
+        line = run_ours(args, rank, world, group.barrier, group.allmax)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        group.close()
 
 
 if __name__ == "__main__":
