@@ -6,6 +6,7 @@
  *   kvq_quant_append            quantize new K/V rows and scatter them into pool slots
  *   kvq_paged_decode_attention  split-KV (flash-decoding) GQA decode attention that
  *                               reads the quantized pages directly
+ *   kvq_paged_decode_attention_static  the same, with library-owned scratch
  *   kvq_split_merge             log-sum-exp combine of the per-split partial results
  *
  * plus host helpers (byte accounting, split planning, workspace sizing, errors).
@@ -236,6 +237,36 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
                                void* workspace, size_t workspace_bytes,
                                void* out, int32_t out_dtype, float* lse_out,
                                uint32_t flags, void* stream);
+
+/* ---- paged_decode_attention_static (no counterpart in the pages: an
+ *      allocation-free variant of kvq_paged_decode_attention) ----------------- */
+/* Bytes of the library's static decode scratch region on each device. */
+#define KVQ_STATIC_SCRATCH_BYTES (16u << 20)
+/*
+ * The same computation, arguments and results as kvq_paged_decode_attention,
+ * without the workspace: the status block and the partials live in a fixed
+ * KVQ_STATIC_SCRATCH_BYTES region of device memory owned by the library, so the
+ * call allocates nothing (for callers with no device allocator, or with device
+ * memory committed in full to the page pool).
+ *   - Returns KVQ_ERR_WORKSPACE, touching nothing, when
+ *     kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim) exceeds
+ *     KVQ_STATIC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the region's address there (with that
+ *     device current); make that first call before any stream capture.
+ *   - Each call clears the region's status block on `stream`, then runs the
+ *     decode (and merge) there; with KVQ_CHECKED the status is read and cleared
+ *     as in kvq_paged_decode_attention.
+ *   - All calls on a device share the region, which keeps the last call's
+ *     contents: calls whose kernels overlap on the GPU (other streams, other
+ *     threads) race on it and give undefined results.  Serialize them.
+ */
+int kvq_paged_decode_attention_static(const kvq_cache* cache, const void* q, int32_t batch,
+                                      int32_t num_q_heads, float sm_scale,
+                                      const int32_t* block_tables, int32_t max_pages_per_seq,
+                                      const int32_t* seq_lens, const int32_t* plan,
+                                      int32_t total_splits, int32_t num_ctas,
+                                      void* out, int32_t out_dtype, float* lse_out,
+                                      uint32_t flags, void* stream);
 
 /* ---- split_merge ([long-ctx]: merge with the normalisation terms; averaging
  *      the partial outputs would be wrong) ------------------------------------ */

@@ -21,13 +21,14 @@ KVQ_OUT_F32, KVQ_OUT_BF16 = 0, 1
 KVQ_CHECKED, KVQ_SKIP_MERGE = 1, 2
 KVQ_DEV_BAD_PAGE, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_BAD_PLAN = 1, 2, 4
 KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_SLOT, KVQ_DEV_NONFINITE = 8, 16, 32
+KVQ_STATIC_SCRATCH_BYTES = 16 << 20
 FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4}
 
 # every symbol include/kvq.h declares
 EXPORTS = (
     "kvq_bytes_per_token", "kvq_cache_array_bytes", "kvq_quant_append", "kvq_plan_splits",
     "kvq_decode_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
-    "kvq_split_merge", "kvq_read_status", "kvq_last_error",
+    "kvq_paged_decode_attention_static", "kvq_split_merge", "kvq_read_status", "kvq_last_error",
 )
 
 
@@ -68,6 +69,8 @@ def lib():
         "kvq_workspace_partials": (c_int32, [P, c_int32, c_int32, c_int32, POINTER(c_void_p), POINTER(c_void_p)]),
         "kvq_paged_decode_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P, c_int32,
                                                  P, P, c_int32, c_int32, P, c_size_t, P, c_int32, P, c_uint32, P]),
+        "kvq_paged_decode_attention_static": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P,
+                                                        c_int32, P, P, c_int32, c_int32, P, c_int32, P, c_uint32, P]),
         "kvq_split_merge": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P, c_int32, P, P]),
         "kvq_read_status": (c_int32, [P, P, POINTER(c_int32)]),
         "kvq_last_error": (ctypes.c_char_p, []),
@@ -186,6 +189,26 @@ def kvq_paged_decode_attention(cache_struct, q, sm_scale, block_tables, seq_lens
         _ptr(seq_lens), _ptr(plan), total_splits, num_ctas, _ptr(workspace), workspace.numel(), _ptr(out), od,
         _ptr(lse_out),
         flags, _stream(stream)), "kvq_paged_decode_attention")
+
+
+def kvq_paged_decode_attention_static(cache_struct, q, sm_scale, block_tables, seq_lens, plan, total_splits,
+                                      num_ctas, out, lse_out=None, flags=0, stream=None):
+    """kvq_paged_decode_attention with the library's static scratch region in place of a workspace."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(plan, torch.int32, "plan")
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    _need(out, out.dtype, "out")
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out")
+    B, Hq, _ = q.shape
+    od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
+    _check(lib().kvq_paged_decode_attention_static(
+        ctypes.byref(cache_struct), _ptr(q), B, Hq, float(sm_scale), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), _ptr(plan), total_splits, num_ctas, _ptr(out), od, _ptr(lse_out), flags, _stream(stream)),
+        "kvq_paged_decode_attention_static")
 
 
 def kvq_split_merge(o_part_ptr, lse_part_ptr, split_offsets, batch, num_q_heads, head_dim, out, lse_out=None,

@@ -157,6 +157,16 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
+int kvq::record_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return code;
+}
+
 extern "C" {
 
 int64_t kvq_bytes_per_token(int32_t format, int32_t num_kv_heads, int32_t head_dim) {

@@ -60,6 +60,8 @@ bool decode_instance(int format, int head_dim, DecodeInstance* out);
 cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaStream_t stream);
+// Record a printf-style message as the calling thread's last error; returns code.
+int record_error(int code, const char* fmt, ...);
 cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
                          int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
                          cudaStream_t stream);
