@@ -46,6 +46,12 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true", help="also measure the other workloads and the split sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler and its soak")
+    ap.add_argument("--ncu-case", default=None, metavar="WORKLOAD",
+                    help="profiling case: build the workload's pools (just over L2 in total), run --calls eager "
+                         "decode calls over them and exit (no timing)")
+    ap.add_argument("--fmt", default="int8", choices=["int8", "nvfp4", "bf16"])
+    ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args()
 
 
@@ -219,41 +225,61 @@ def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=
     return e0.elapsed_time(e1) * 1e-3 / (reps * ls.R), reps * ls.R, clocks
 
 
-def time_e2e(ls, plan, steps):
-    """Through the public API with host buffers: per step, copy q, block table and
-    seq_lens from pinned host memory, decode, copy the output back."""
+def time_e2e(ls, plan, steps, warmup=3):
+    """Through the public API with host buffers: every step copies q, the block
+    table and seq_lens (one packed buffer) from pinned host memory, decodes, and
+    copies the output back to pinned host memory.  R consecutive steps are
+    captured in one CUDA graph (copies included) and replayed, as the
+    device-side timing is."""
     import torch
 
     import quantized_paged_kv_gb300 as kvq
 
-    q_h = ls.q.cpu().pin_memory()
-    bt_h = ls.bt.cpu().pin_memory()
-    sl_h = ls.sl.cpu().pin_memory()
+    # the step's inputs travel as one packed host buffer (q | block table | seq_lens,
+    # each part 16-byte aligned) and arrive as views of one device buffer
+    parts = [ls.q, ls.bt, ls.sl]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = [0]
+    for n in sizes:
+        offs.append(offs[-1] + (n + 15) // 16 * 16)
+    stage_h = torch.zeros(offs[-1], dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(offs[-1], dtype=torch.uint8, device=ls.device)
+    views_d = []
+    for t, o, n in zip(parts, offs, sizes):
+        stage_h[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+        views_d.append(stage_d[o:o + n].view(t.dtype).view(t.shape))
+    q_d, bt_d, sl_d = views_d
     out_h = torch.empty(ls.out.shape, dtype=ls.out.dtype).pin_memory()
-    q_d, bt_d, sl_d = torch.empty_like(ls.q), torch.empty_like(ls.bt), torch.empty_like(ls.sl)
     stream = torch.cuda.Stream()
-    steps = max(ls.R, min(steps, 2000))
 
     def one(r):
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
+        stage_d.copy_(stage_h, non_blocking=True)
         kvq.decode(ls.caches[r], plan, q_d, bt_d, sl_d, ls.out, ls.wl.sm_scale)
         out_h.copy_(ls.out, non_blocking=True)
 
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for r in range(ls.R):
             one(r)
     stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for r in range(ls.R):
+            one(r)
+    reps = max(1, math.ceil(min(steps, 4000) / ls.R))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / ls.R))):
+            g.replay()
+    stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(steps):
-            one(i % ls.R)
+        for _ in range(reps):
+            g.replay()
         e1.record(stream)
     stream.synchronize()
-    t = e0.elapsed_time(e1) * 1e-3 / steps
-    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * ls.R)
+    h2d = stage_h.numel()
     d2h = out_h.numel() * out_h.element_size()
     return t, h2d, d2h
 
@@ -324,7 +350,7 @@ def run_ours(args, rank, world, barrier, allmax):
     R = layers_for(per_layer, l2, floor=16)
     ls = LayerSet(wl, "int8", R, dev)
     plan = ls.plan(0)
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     t_call, calls, clocks = time_graph(ls, plan, args.steps, args.warmup, barrier=barrier, sampler=sampler)
     t_call = allmax(t_call)
     if clocks is not None and clocks.get("samples", 0) < 3:  # timed region too short: extend by an untimed soak
@@ -333,7 +359,7 @@ def run_ours(args, rank, world, barrier, allmax):
         clocks = dict(c2 or clocks, window="timed region too short; sampled over a 1.5 s soak of the same step")
     t_dec, _, _ = time_graph(ls, plan, args.steps, args.warmup, skip_merge=True)
     t_dec = allmax(t_dec)
-    e2e_t, h2d, d2h = time_e2e(ls, plan, args.steps)
+    e2e_t, h2d, d2h = time_e2e(ls, plan, args.steps, args.warmup)
     e2e_t = allmax(e2e_t)
 
     bytes_step = ls.kv_bytes()
@@ -360,7 +386,9 @@ def run_ours(args, rank, world, barrier, allmax):
                      "traffic": (tr["dram_bytes_per_launch"] if tr else None),
                      "traffic_algorithmic_ratio": (round(tr["dram_bytes_per_launch"] / bytes_step, 4) if tr else None)},
         "e2e": {"value": round(world * bytes_step / e2e_t / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_t * 1e6, 3)},
+                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_t * 1e6, 3),
+                "how": "public API per step: q | block table | seq_lens as one packed copy from pinned host memory, decode, output "
+                       "back to pinned host memory; R steps in one CUDA graph, CUDA events"},
         "gpu_launches": calls * (2 if plan.total_splits > wl.B else 1),
         "clocks": clocks,
     }
@@ -485,8 +513,35 @@ def run_reference(args):
     }
 
 
+def run_ncu_case(args):
+    """A small, untimed case for ncu: pools of one workload just over the L2 size
+    in total, then `calls` decode calls (decode + merge) visiting them in turn."""
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+    from quantized_paged_kv_gb300 import workloads as W
+
+    kvq.lib()
+    wl = W.make(args.ncu_case)
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token(args.fmt, wl.Hkv, wl.D)
+    R = max(1, math.ceil(1.1 * l2 / max(per_layer, 1)))
+    ls = LayerSet(wl, args.fmt, R, "cuda")  # NVFP4 global scale 1 (it does not change the work)
+    plan = ls.plan(0)
+    for i in range(args.calls):
+        ls.call(i % R, plan)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": args.ncu_case, "fmt": args.fmt, "layers": R, "calls": args.calls,
+                      "total_splits": plan.total_splits, "num_ctas": plan.num_ctas,
+                      "kv_bytes_per_call": ls.kv_bytes()}), flush=True)
+
+
 def main():
     args = parse()
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -163,19 +163,28 @@ int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_ne
  *      overhead against parallelism) ----------------------------------------- */
 /*
  * Choose, on the host, how many splits each sequence gets and how the work is
- * spread over persistent CTAs, and write the plan:
- *   plan[0..batch]            split_offsets: sequence b owns splits (and partial
- *                             slots) [plan[b], plan[b+1]); plan[0] = 0, plan[batch] = total
- *   plan[batch+1]             C = *num_ctas, the number of persistent CTAs
- *   plan[batch+2 .. +C+1]     CTA offsets: CTA c works through item list entries
- *                             [off[c], off[c+1]), off[0] = 0, off[C] = total * NHG
- *   then total * NHG items    item = split * NHG + head group, NHG = Hkv / HG, where
- *                             HG = gcd(Hkv, consumer warps of the kernel: 8 at D = 256,
- *                             12 at D = 128) KV heads are handled together
- * Split s of a sequence with n pages and S splits covers pages
- * [floor(s*n/S), floor((s+1)*n/S)) — whole pages, sizes differing by at most one.
- * Items are packed onto the C CTAs longest first, each onto the CTA with the least
- * work so far, so an uneven batch runs in one wave.
+ * spread over persistent CTAs, and write the plan.  A work item is one split of
+ * one sequence for a group of HG KV heads, HG = gcd(Hkv, consumer warps of the
+ * kernel: 8 at D = 256, 12 at D = 128) (or a divisor of it when the shared-memory
+ * ring needs smaller groups); NHG = Hkv / HG groups, total * NHG items.  Layout
+ * (int32 entries; A = batch + 2 rounded up to a multiple of 4, R = A + 5C + 1
+ * rounded up to a multiple of 4):
+ *   plan[0..batch]          split_offsets: sequence b owns splits (and partial
+ *                           slots) [plan[b], plan[b+1]); plan[0] = 0, plan[batch] = total
+ *   plan[batch+1]           C = *num_ctas, the number of persistent CTAs
+ *   plan[A .. A+4C)         the first item of each CTA, one 4-entry descriptor each
+ *   plan[A+4C .. A+5C]      CTA c's further items are rest entries [o[c], o[c+1]),
+ *                           o[0] = 0, o[C] = total * NHG - C
+ *   plan[R ..]              the rest entries, one 4-entry descriptor each
+ * A descriptor is {b, split, first page, n | direct << 23 | group << 24}: sequence
+ * b's split `split` (a global split index) covers its pages [first page, first
+ * page + n) for KV heads [group * HG, (group + 1) * HG); direct = the sequence has
+ * a single split (the kernel writes `out` directly).  Split s of a sequence with
+ * n pages and S splits covers pages [floor(s*n/S), floor((s+1)*n/S)) — whole
+ * pages, sizes differing by at most one.  Items are packed onto the C CTAs longest
+ * first, each onto the CTA with the least work so far, so an uneven batch runs in
+ * one wave; a CTA's first item sits at a fixed place so that it can start loading
+ * pages without first reading an offset.
  *   seq_lens        host int32 [batch], each >= 0
  *   split_override  > 0: S_b = clamp(split_override, 1, max(n_pages_b, 1));
  *                   0: automatic — pages per split = max(4, ceil(NHG * total_pages / C))
@@ -184,9 +193,10 @@ int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_ne
  *                   C = min(target_ctas, total * NHG)
  *   plan            host int32 buffer of plan_capacity entries (nullable for a size query)
  *   total_splits, num_ctas  out (always written when the inputs are valid)
- * Returns KVQ_ERR_WORKSPACE if plan is NULL or shorter than
- * batch + 3 + C + total * NHG.  The plan must be copied to the device before
- * kvq_paged_decode_attention.
+ * Returns KVQ_ERR_WORKSPACE if plan is NULL or shorter than R + 4 * (total * NHG - C)
+ * (at most batch + 9 + C + 4 * total * num_kv_heads).  The plan must be copied to
+ * the device before kvq_paged_decode_attention, and plan, total_splits and
+ * num_ctas passed there must come from the same call.
  */
 int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch,
                     int32_t split_override, int32_t target_ctas,

@@ -132,8 +132,8 @@ def kvq_plan_splits(cache_struct, seq_lens, split_override=0, target_ctas=0):
                            split_override, target_ctas, None, 0, ctypes.byref(total), ctypes.byref(nctas))
     if rc not in (0, 3):  # 3 = KVQ_ERR_WORKSPACE (size query)
         _check(rc, "kvq_plan_splits")
-    # head groups per item <= num_kv_heads, so this bounds the plan length
-    plan = torch.zeros(B + 3 + nctas.value + total.value * cache_struct.num_kv_heads, dtype=torch.int32)
+    # head groups per split <= num_kv_heads, so this bounds the plan length
+    plan = torch.zeros(B + 9 + nctas.value + 4 * total.value * cache_struct.num_kv_heads, dtype=torch.int32)
     _check(L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
                              split_override, target_ctas, plan.numpy().ctypes.data_as(POINTER(c_int32)),
                              plan.numel(), ctypes.byref(total), ctypes.byref(nctas)), "kvq_plan_splits")

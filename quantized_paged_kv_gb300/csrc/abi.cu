@@ -127,6 +127,11 @@ int make_code_map(CUtensorMap* map, void* base, int64_t num_pages, int64_t hkv, 
 }
 
 // KV heads per decode work item for a cache (0 if no kernel exists for it).
+// Plan layout offsets (int32 entries): the first-item descriptors and the rest
+// list start on 16-byte boundaries so the kernel can load a descriptor at once.
+int64_t plan_first_at(int64_t batch) { return (batch + 2 + 3) / 4 * 4; }
+int64_t plan_rest_at(int64_t batch, int64_t C) { return (plan_first_at(batch) + 5 * C + 1 + 3) / 4 * 4; }
+
 int heads_per_cta(const kvq_cache* c) {
   kvq::DecodeInstance inst;
   if (!kvq::decode_instance(c->format, c->head_dim, &inst)) return 0;
@@ -294,43 +299,64 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
   const int64_t C = std::min<int64_t>(target, n_items);  // persistent CTAs
   *total_splits = static_cast<int32_t>(total);
   *num_ctas = static_cast<int32_t>(C);
-  const int64_t need = batch + 1 + 1 + (C + 1) + n_items;
+  if (nhg > 127) return fail(KVQ_ERR_UNSUPPORTED, "more than 127 KV-head groups");
+  const int64_t A = plan_first_at(batch);
+  const int64_t roff_at = A + 4 * C;
+  const int64_t rest_at = plan_rest_at(batch, C);
+  const int64_t need = rest_at + 4 * (n_items - C);
   if (!plan || plan_capacity < need)
     return fail(KVQ_ERR_WORKSPACE, "plan needs %lld int32 entries", (long long)need);
+  for (int b = 0; b < batch; ++b)
+    if (npages[b] >= (1 << 23)) return fail(KVQ_ERR_UNSUPPORTED, "sequence %d has too many pages", b);
   plan[0] = 0;
   for (int b = 0; b < batch; ++b) plan[b + 1] = plan[b] + splits[b];
-  // Items (split, head group) with their page counts; longest first, each onto the
+  plan[batch + 1] = static_cast<int32_t>(C);
+  for (int64_t i = batch + 2; i < A; ++i) plan[i] = 0;
+  // Items with their descriptors and page counts; longest first, each onto the
   // CTA with the least work so far (a page costs 1, an item's fixed prologue and
   // epilogue are counted as 8 pages).
-  std::vector<std::pair<int64_t, int32_t>> items;
+  struct Desc {
+    int64_t cost;
+    int32_t d[4];
+  };
+  std::vector<Desc> items;
   items.reserve(n_items);
   for (int b = 0; b < batch; ++b)
     for (int s = 0; s < splits[b]; ++s) {
       const int64_t pb = (int64_t)s * npages[b] / splits[b], pe = (int64_t)(s + 1) * npages[b] / splits[b];
-      for (int g = 0; g < nhg; ++g) items.emplace_back(pe - pb, (plan[b] + s) * nhg + g);
+      for (int g = 0; g < nhg; ++g) {
+        Desc it;
+        it.cost = pe - pb;
+        it.d[0] = b;
+        it.d[1] = plan[b] + s;
+        it.d[2] = static_cast<int32_t>(pb);
+        it.d[3] = static_cast<int32_t>((pe - pb) | ((splits[b] == 1 ? 1 : 0) << 23) | (g << 24));
+        items.push_back(it);
+      }
     }
-  std::stable_sort(items.begin(), items.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
-  std::vector<std::vector<int32_t>> bins(C);
+  std::stable_sort(items.begin(), items.end(), [](const Desc& a, const Desc& b) { return a.cost > b.cost; });
+  std::vector<std::vector<int64_t>> bins(C);
   std::vector<std::pair<int64_t, int32_t>> heap;  // (load, cta) min-heap
   heap.reserve(C);
   for (int32_t cta = 0; cta < C; ++cta) heap.emplace_back(0, cta);
   auto cmp = [](const auto& a, const auto& b) { return a.first > b.first || (a.first == b.first && a.second > b.second); };
   std::make_heap(heap.begin(), heap.end(), cmp);
-  for (const auto& it : items) {
+  for (int64_t i = 0; i < n_items; ++i) {
     std::pop_heap(heap.begin(), heap.end(), cmp);
     auto& top = heap.back();
-    bins[top.second].push_back(it.second);
-    top.first += it.first + 8;
+    bins[top.second].push_back(i);
+    top.first += items[i].cost + 8;
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
-  int32_t* hdr = plan + batch + 1;
-  hdr[0] = static_cast<int32_t>(C);
-  int32_t* cta_off = hdr + 1;
-  int32_t* out_items = cta_off + C + 1;
-  cta_off[0] = 0;
+  int32_t* roff = plan + roff_at;
+  for (int64_t i = roff_at + C + 1; i < rest_at; ++i) plan[i] = 0;
+  roff[0] = 0;
   for (int64_t cta = 0; cta < C; ++cta) {
-    cta_off[cta + 1] = cta_off[cta] + static_cast<int32_t>(bins[cta].size());
-    std::copy(bins[cta].begin(), bins[cta].end(), out_items + cta_off[cta]);
+    const auto& bin = bins[cta];  // never empty: the first C items go to distinct CTAs
+    std::copy(items[bin[0]].d, items[bin[0]].d + 4, plan + A + 4 * cta);
+    roff[cta + 1] = roff[cta] + static_cast<int32_t>(bin.size() - 1);
+    for (size_t k = 1; k < bin.size(); ++k)
+      std::copy(items[bin[k]].d, items[bin[k]].d + 4, plan + rest_at + 4 * (roff[cta] + k - 1));
   }
   return succeed();
 }
@@ -382,30 +408,50 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool checked = flags & KVQ_CHECKED;
   if (checked) {
-    // host-side validation of the plan (the kernel also checks every entry it uses)
+    // host-side validation of the plan against seq_lens (the kernel also checks
+    // every descriptor it uses)
     const int hgc = heads_per_cta(cache);
     if (hgc <= 0) return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this cache");
-    const int nhg_checked = cache->num_kv_heads / hgc;
-    if (num_ctas > (int64_t)total_splits * nhg_checked)
-      return fail(KVQ_ERR_INVALID_ARG, "num_ctas %d exceeds the number of work items", num_ctas);
-    std::vector<int32_t> h(batch + 1 + 1 + (num_ctas + 1) + (size_t)total_splits * nhg_checked);
+    const int64_t nhg_checked = cache->num_kv_heads / hgc;
+    const int64_t n_items = (int64_t)total_splits * nhg_checked;
+    if (num_ctas > n_items) return fail(KVQ_ERR_INVALID_ARG, "num_ctas %d exceeds the number of work items", num_ctas);
+    const int64_t A = plan_first_at(batch), roff_at = A + 4 * (int64_t)num_ctas;
+    const int64_t rest_at = plan_rest_at(batch, num_ctas);
+    std::vector<int32_t> h(rest_at + 4 * (n_items - num_ctas));
+    std::vector<int32_t> lens(batch);
     cudaError_t e = cudaMemcpyAsync(h.data(), plan, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(lens.data(), seq_lens, lens.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "reading plan");
     if (h[0] != 0 || h[batch] != total_splits) return fail(KVQ_ERR_INVALID_ARG, "plan offsets do not span total_splits");
     for (int b = 0; b < batch; ++b)
       if (h[b + 1] <= h[b]) return fail(KVQ_ERR_INVALID_ARG, "plan gives sequence %d no split", b);
-    const int64_t C = h[batch + 1];
-    const int64_t n_items = (int64_t)total_splits * nhg_checked;
-    if (C != num_ctas) return fail(KVQ_ERR_INVALID_ARG, "plan CTA count %lld != num_ctas %d", (long long)C, num_ctas);
-    const int32_t* co = h.data() + batch + 2;
-    if (co[0] != 0 || co[C] != n_items) return fail(KVQ_ERR_INVALID_ARG, "plan CTA offsets do not span the items");
-    for (int64_t i = 0; i < C; ++i)
-      if (co[i + 1] < co[i]) return fail(KVQ_ERR_INVALID_ARG, "plan CTA offsets decrease");
-    std::vector<int32_t> order(co + C + 1, co + C + 1 + n_items);
-    std::sort(order.begin(), order.end());
-    for (int64_t i = 0; i < n_items; ++i)
-      if (order[i] != i) return fail(KVQ_ERR_INVALID_ARG, "plan items are not a permutation");
+    if (h[batch + 1] != num_ctas)
+      return fail(KVQ_ERR_INVALID_ARG, "plan CTA count %d != num_ctas %d", h[batch + 1], num_ctas);
+    const int32_t* ro = h.data() + roff_at;
+    if (ro[0] != 0 || ro[num_ctas] != n_items - num_ctas)
+      return fail(KVQ_ERR_INVALID_ARG, "plan CTA offsets do not span the items");
+    for (int64_t i = 0; i < num_ctas; ++i)
+      if (ro[i + 1] < ro[i]) return fail(KVQ_ERR_INVALID_ARG, "plan CTA offsets decrease");
+    std::vector<uint8_t> seen(n_items, 0);
+    for (int64_t i = 0; i < n_items; ++i) {
+      const int32_t* d = i < num_ctas ? h.data() + A + 4 * i : h.data() + rest_at + 4 * (i - num_ctas);
+      const int b = d[0], split = d[1], pb = d[2];
+      const int n = d[3] & 0x7FFFFF, direct = (d[3] >> 23) & 1, g = (uint32_t)d[3] >> 24;
+      if (b < 0 || b >= batch || split < h[b] || split >= h[b + 1] || g >= nhg_checked)
+        return fail(KVQ_ERR_INVALID_ARG, "plan item %lld names a bad sequence / split / head group", (long long)i);
+      if (lens[b] < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_lens[%d] = %d < 0", b, lens[b]);
+      const int64_t S = h[b + 1] - h[b], sidx = split - h[b];
+      const int64_t np = (lens[b] + cache->page_size - 1) / cache->page_size;
+      if (pb != sidx * np / S || n != (sidx + 1) * np / S - pb || direct != (S == 1 ? 1 : 0))
+        return fail(KVQ_ERR_INVALID_ARG, "plan item %lld does not match seq_lens[%d] = %d", (long long)i, b, lens[b]);
+      if (pb + n > max_pages_per_seq)
+        return fail(KVQ_ERR_INVALID_ARG, "plan item %lld runs past the block table", (long long)i);
+      const int64_t key = (int64_t)split * nhg_checked + g;
+      if (seen[key]) return fail(KVQ_ERR_INVALID_ARG, "plan item (split %d, group %d) appears twice", split, g);
+      seen[key] = 1;
+    }
   }
   kvq::DecodeInstance inst;
   rc = prepare_instance(cache->format, D, &inst);

@@ -102,9 +102,11 @@ struct DecodeLayout {
   static constexpr int kRingBytes = (227 * 1024 - 1024 - kCW * kQBytes - 2 * kMaxStages * 8 - kIdBytes) / 1024 * 1024;
   static constexpr int kSmemBytes = 1024 + kRingBytes + kCW * kQBytes + 2 * kMaxStages * 8 + kIdBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  // epilogue reuses the code region: O[warp][8 heads][D], m, l [warp][8], and
-  // the per-row merge weights [8 * kCW] + lse [8 * kCW]
-  static constexpr int kEpilogueBytes = kCW * 8 * D * 4 + 2 * kCW * 8 * 4 + 2 * 8 * kCW * 4;
+  // epilogue exchange in the ring: each warp other than a head's first leaves its
+  // accumulators (one float4 per lane and m-tile) and (m, l) of 8 head rows
+  static constexpr int kPartOBytes = kMTiles * 32 * 16;
+  static constexpr int kExchangeBytes = (kCW - 1) * (kPartOBytes + 8 * 8);
+  static_assert(kExchangeBytes <= kRingBytes, "epilogue exchange must fit in the ring");
 };
 
 // Producer warps and stage count for a head group of `hg` heads.  A single
@@ -140,8 +142,7 @@ __host__ __device__ inline int decode_stages(int hg) {
 }
 
 // Largest head group (a divisor of gcd(Hkv, CW)) whose ring holds at least two
-// stages and one per producer / consumer group, and whose code region can hold
-// the epilogue's merge buffer.  0 if none does.
+// stages and one per producer / consumer group.  0 if none does.
 template <int FMT, int D>
 inline int decode_head_group(int hkv) {
   using Lo = DecodeLayout<FMT, D>;
@@ -155,7 +156,7 @@ inline int decode_head_group(int hkv) {
     if (g % hg) continue;
     const int nst = decode_stages<FMT, D>(hg);
     const int unit = decode_stage_unit<FMT, D>(hg);
-    if (nst >= 2 && nst >= unit && nst * 2 * hg * Lo::kHeadCode >= Lo::kEpilogueBytes) return hg;
+    if (nst >= 2 && nst >= unit) return hg;
   }
   return 0;
 }
@@ -203,54 +204,55 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   uint64_t* empty = full + kMaxStages;
   int* pid_s = reinterpret_cast<int*>(empty + kMaxStages);  // [producer][2][32] page ids
 
-  // ---- plan: split offsets [batch + 1], CTA count C, CTA offsets [C + 1], items
-  const int32_t* offs = p.plan;
-  const int C = p.plan[p.batch + 1];
-  const int32_t* cta_off = p.plan + p.batch + 2;
-  const int32_t* items = cta_off + C + 1;
-  if (static_cast<int>(blockIdx.x) >= C) return;
-  const int it_begin = cta_off[blockIdx.x];
-  const int it_end = cta_off[blockIdx.x + 1];
-  if (it_begin < 0 || it_end < it_begin || it_end > p.total_splits * NHG) {
+  // ---- plan: split offsets [batch + 1], C = gridDim.x, then (16-byte aligned) the
+  // first item descriptor of every CTA, the CTAs' offsets into the list of their
+  // further items, and that list.  A CTA reads its first descriptor at a fixed
+  // place, so its producers can ask for page ids after one dependent load.
+  const int C = static_cast<int>(gridDim.x);
+  const int A = (p.batch + 2 + 3) & ~3;
+  const int4* firsts = reinterpret_cast<const int4*>(p.plan + A);
+  const int32_t* roff = p.plan + A + 4 * C;
+  const int4* rest = reinterpret_cast<const int4*>(p.plan + ((A + 5 * C + 1 + 3) & ~3));
+  const int n_items = p.total_splits * NHG;
+  const int4 d0 = firsts[blockIdx.x];
+  const int r0 = roff[blockIdx.x];
+  const int r1 = roff[blockIdx.x + 1];
+  if (p.plan[p.batch + 1] != C || r0 < 0 || r1 < r0 || r1 > n_items - C) {
     if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_PLAN);
     return;
   }
+  const int cnt = 1 + (r1 - r0);  // items of this CTA: d0, then rest[r0 .. r1)
 
-  // Item -> (sequence, split, head group, page range); identical in every thread.
+  // Item = (sequence, split, head group, page range) of a descriptor
+  // {b, split, first page, n | direct << 23 | group << 24}; identical in every thread.
   struct Item {
     int b, split, hg, L, page_begin, n;
     bool direct;  // the sequence has a single split: write `out` directly
   };
-  auto decode_item = [&](int it, Item& w) -> bool {
-    const int item = items[it];
-    if (item < 0 || item >= p.total_splits * NHG) return false;
-    w.split = item / NHG;
-    w.hg = item - w.split * NHG;
-    int lo = 0, hi = p.batch;  // largest b with offs[b] <= split
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (offs[mid] <= w.split) lo = mid; else hi = mid;
-    }
-    w.b = lo;
-    const int nsplit = offs[w.b + 1] - offs[w.b];
-    const int s = w.split - offs[w.b];
-    if (nsplit <= 0 || s < 0 || s >= nsplit) return false;
-    int L = p.seq_lens[w.b];
+  auto unpack = [&](const int4 d, Item& w) -> bool {
+    w.b = d.x;
+    w.split = d.y;
+    w.page_begin = d.z;
+    w.n = d.w & 0x7FFFFF;
+    w.direct = ((d.w >> 23) & 1) != 0;
+    w.hg = static_cast<int>(static_cast<uint32_t>(d.w) >> 24);
+    w.L = 0;
+    return w.b >= 0 && w.b < p.batch && w.split >= 0 && w.split < p.total_splits && w.hg < NHG &&
+           w.page_begin >= 0 && w.page_begin <= p.max_pages - w.n;
+  };
+  auto seq_len = [&](int b) -> int {  // tokens of sequence b, clamped to its block table
+    int L = p.seq_lens[b];
     if (L < 0 || L > p.max_pages * kPage) {
       if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
       L = L < 0 ? 0 : p.max_pages * kPage;
     }
-    w.L = L;
-    const int npages = (L + kPage - 1) / kPage;
-    w.page_begin = static_cast<int>((int64_t)s * npages / nsplit);
-    w.n = static_cast<int>((int64_t)(s + 1) * npages / nsplit) - w.page_begin;
-    w.direct = nsplit == 1;
-    return true;
+    return L;
   };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   __shared__ int abort_flag;
+  __shared__ int4 next_desc;
 
   // consumer identity (used only by consumer warps)
   const int hl = warp % HG;   // head within the group
@@ -285,8 +287,11 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   };
 
   Item first;
-  const bool first_ok = it_begin < it_end && decode_item(it_begin, first);
-  if (warp < CW && first_ok) load_q(first);
+  const bool first_ok = unpack(d0, first);
+  if (warp < CW && first_ok) {
+    first.L = seq_len(first.b);
+    load_q(first);
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -307,38 +312,41 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     bool ok = true;
     int gidx = 0;                 // pages of this CTA before the current item
     int last_first = 0, last_n = 0;
-    for (int it = it_begin; it < it_end; ++it) {
-      Item w;
-      const bool valid = ok && decode_item(it, w);
+    int* ids = pid_s + pi * 64;
+    // this producer's pages of an item are idx = pi + NP*j; page_id(w, j) is the
+    // validated page id of its page j (or -1)
+    auto mine_of = [&](const Item& w) { return w.n > pi ? (w.n - pi + NP - 1) / NP : 0; };
+    auto page_id = [&](const Item& w, int j) -> int {
+      int v = -1;
+      if (j < mine_of(w)) {
+        v = p.block_tables[(size_t)w.b * p.max_pages + w.page_begin + pi + NP * j];
+        if (v < 0 || v >= p.num_pages) {
+          atomicOr(p.status, KVQ_DEV_BAD_PAGE);
+          v = -1;
+        }
+      }
+      return v;
+    };
+    Item w = first;
+    bool valid = first_ok;
+    int v0 = valid ? page_id(w, lane) : -1;  // ids of the item's first 32 pages of this producer
+    for (int k = 0; k < cnt; ++k) {
       if (valid) {
-        const int32_t* bt = p.block_tables + (size_t)w.b * p.max_pages + w.page_begin;
         const int n = w.n;
-        const int mine = n > pi ? (n - pi + NP - 1) / NP : 0;  // this producer's pages: idx = pi + NP*j
-        auto page_id = [&](int j) -> int {  // validated page id of this producer's page j (or -1)
-          int v = -1;
-          if (j < mine) {
-            v = bt[pi + NP * j];
-            if (v < 0 || v >= p.num_pages) {
-              atomicOr(p.status, KVQ_DEV_BAD_PAGE);
-              v = -1;
-            }
-          }
-          return v;
-        };
+        const int mine = mine_of(w);
         last_first = gidx;  // drain bookkeeping, also right if this item is cut short
         last_n = n;
-        int* ids = pid_s + pi * 64;
-        ids[lane] = page_id(lane);
+        ids[lane] = v0;
         __syncwarp();
         const size_t head0 = (size_t)w.hg * HG;
         int g = gidx + pi;  // global ring position of the next page
         int st = g % NST, rnd = g / NST;
         for (int base = 0, buf = 0; base < mine; base += 32, buf ^= 1) {
-          const int nxt = page_id(base + 32 + lane);  // prefetch the next 32 ids
+          const int nxt = page_id(w, base + 32 + lane);  // prefetch the next 32 ids
           if (lane == 0) {
-            const int cnt = min(32, mine - base);
-            for (int k = 0; k < cnt; ++k) {
-              const int pg = ids[buf * 32 + k];
+            const int cnt32 = min(32, mine - base);
+            for (int kk = 0; kk < cnt32; ++kk) {
+              const int pg = ids[buf * 32 + kk];
               if (rnd > 0 && !mbar_wait(&empty[st], (rnd - 1) & 1, kWaitLimitNs)) {
                 atomicOr(p.status, KVQ_DEV_TIMEOUT);
                 ok = false;
@@ -372,10 +380,22 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         }
         gidx += n;
       }
+      // the next item's descriptor and first page ids, fetched while the
+      // consumers finish this one
+      Item nw;
+      bool nvalid = false;
+      int nv0 = -1;
+      if (ok && valid && k + 1 < cnt) {
+        nvalid = unpack(rest[r0 + k], nw);
+        if (nvalid) nv0 = page_id(nw, lane);
+      }
       if (lane == 0 && !ok) abort_flag = 1;
       // the consumers' epilogue of this item is done: the ring is free
       asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
       if (abort_flag || !valid) break;
+      w = nw;
+      valid = nvalid;
+      v0 = nv0;
     }
     // Drain: before this warp (and so the CTA) can exit, every copy it issued has
     // landed.  Only the last item can have copies in flight: the consumers
@@ -406,17 +426,17 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 #pragma unroll
     for (int v4 = 0; v4 < 4; ++v4) voff[v4] = (8 * (mm & 1) + rr) * 128 + (((2 * v4 + (mm >> 1)) ^ rr) << 4);
   }
-  float* red_o = reinterpret_cast<float*>(codes);  // epilogue: [CW][8][D]
-  float* red_m = red_o + CW * 8 * D;                // [CW][8]
-  float* red_l = red_m + CW * 8;                    // [CW][8]
-  float* row_w = red_l + CW * 8;                    // [8 * CW] merge weights (row, warp of the head)
-  float* row_lse = row_w + 8 * CW;                  // [8 * CW]
+  // epilogue exchange in the (then idle) ring: the WPH-1 other warps of each head
+  // leave their accumulators in fragment order, [slot][m-tile][lane] float4, and
+  // their (m, l) per head row, [slot][8] float2; slot = head * (WPH-1) + warp - 1.
+  float4* part_o = reinterpret_cast<float4*>(codes);
+  float2* part_ml = reinterpret_cast<float2*>(codes + (CW - 1) * Lo::kPartOBytes);
   constexpr float kLn2 = 0.69314718055994530942f;
 
   int gidx = 0;  // pages of this CTA before the current item (global ring position)
   Item w = first, nw;
   bool ok_item = first_ok, next_ok = false;
-  for (int it = it_begin; it < it_end; ++it) {
+  for (int k = 0; k < cnt; ++k) {
     if (!ok_item) {  // a bad plan entry: every thread of the CTA stops here
       if (threadIdx.x == 0) {
         atomicOr(p.status, KVQ_DEV_BAD_PLAN);
@@ -425,6 +445,9 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
       break;
     }
+    // the next item's descriptor, fetched now and kept in shared memory (read in
+    // the epilogue, after the barrier that ends this item's pages)
+    if (threadIdx.x == 0) next_desc = k + 1 < cnt ? rest[r0 + k] : make_int4(-1, -1, -1, -1);
     // ---- q fragments (A operand rows = heads) for this item, converted from
     // the raw bf16 pairs loaded earlier.  Column (k) order per format, matching
     // the K fragments below: k-step j pairs (2c, 2c+1) with d dA(j, c) + {0, 1}
@@ -740,85 +763,112 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       if (lane == 0) abort_flag = 1;
     }
     // every consumer warp is past this item's last page: every stage has landed
-    // and been read, and the producer waits for this item's end, so the code
-    // region can be reused.
+    // and been read, and the producers wait for this item's end, so the ring can
+    // hold the exchange.
     asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
-    {
-      float* ow = red_o + warp * 8 * D;
+    next_ok = k + 1 < cnt && unpack(next_desc, nw);
+    if (next_ok) nw.L = seq_len(nw.b);
+    const int others = WPH - 1;
+    if (grp > 0) {
+      const int slot = hl * others + grp - 1;
 #pragma unroll
-      for (int mt = 0; mt < Lo::kMTiles; ++mt) {
-        int da, db;
-        if constexpr (FMT == KVQ_FMT_INT8) {
-          da = 16 * mt + 2 * r;
-          db = da + 1;
-        } else if constexpr (FMT == KVQ_FMT_BF16) {
-          da = 16 * mt + r;
-          db = da + 8;
-        } else {
-          da = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1);
-          db = da + 1;
-        }
-        ow[(2 * c) * D + da] = oacc[mt][0];
-        ow[(2 * c + 1) * D + da] = oacc[mt][1];
-        ow[(2 * c) * D + db] = oacc[mt][2];
-        ow[(2 * c + 1) * D + db] = oacc[mt][3];
-      }
-      if (c == 0) {
-        red_m[warp * 8 + r] = m_run;
-        red_l[warp * 8 + r] = l_run;
-      }
+      for (int mt = 0; mt < Lo::kMTiles; ++mt)
+        part_o[(slot * Lo::kMTiles + mt) * 32 + lane] = make_float4(oacc[mt][0], oacc[mt][1], oacc[mt][2], oacc[mt][3]);
+      if (c == 0) part_ml[slot * 8 + r] = make_float2(m_run, l_run);
+      if (next_ok) load_q(nw);  // the accumulators are in shared memory: registers are free
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
-    // prefetch the next item's q while the results are written
-    next_ok = it + 1 < it_end && decode_item(it + 1, nw);
-    if (next_ok) load_q(nw);
-    const int tid = threadIdx.x;  // 0 .. CW*32-1
-    const int rows = HG * G;      // query heads of the group
-    // merge weights of the warps of each head, once per (head, query head) row
-    if (tid < rows) {
-      const int hh = tid / G, g = tid - hh * G;
-      float M = -INFINITY;
-      for (int j = 0; j < WPH; ++j) M = fmaxf(M, red_m[(hh + j * HG) * 8 + g]);
-      float Lsum = 0.f;
-      if (M != -INFINITY)
-        for (int j = 0; j < WPH; ++j) Lsum += red_l[(hh + j * HG) * 8 + g] * exp2f(red_m[(hh + j * HG) * 8 + g] - M);
-      const bool any = M != -INFINITY && Lsum > 0.f;
+    if (others > 0) asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+    if (grp == 0) {
+      // combine the head's warps: weights per head row r (this lane's row of S)
+      float M = m_run;
+      for (int j = 0; j < others; ++j) M = fmaxf(M, part_ml[(hl * others + j) * 8 + r].x);
+      const bool live = M != -INFINITY;
+      float Lsum = live ? l_run * exp2f(m_run - M) : 0.f;
+      for (int j = 0; j < others; ++j) {
+        const float2 ml = part_ml[(hl * others + j) * 8 + r];
+        if (live) Lsum += ml.y * exp2f(ml.x - M);
+      }
+      const bool any = live && Lsum > 0.f;
       float inv = any ? 1.f / Lsum : 0.f;
+      const float lse = any ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
       if constexpr (FMT == KVQ_FMT_NVFP4) inv *= p.v_gs_inv;
-      for (int j = 0; j < WPH; ++j)
-        row_w[tid * WPH + j] = any ? exp2f(red_m[(hh + j * HG) * 8 + g] - M) * inv : 0.f;
-      row_lse[tid] = any ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
-    for (int e4 = tid; e4 < rows * (D / 4); e4 += CW * 32) {
-      const int row = e4 / (D / 4);
-      const int d = (e4 - row * (D / 4)) * 4;
-      const int hh = row / G, g = row - hh * G;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < WPH; ++j) {
-        const float wt = row_w[row * WPH + j];
-        const float4 ow = *reinterpret_cast<const float4*>(red_o + ((hh + j * HG) * 8 + g) * D + d);
-        o.x += ow.x * wt;
-        o.y += ow.y * wt;
-        o.z += ow.z * wt;
-        o.w += ow.w * wt;
-      }
-      const int qh = (w.hg * HG + hh) * G + g;
-      if (w.direct) {
-        const size_t off = ((size_t)w.b * p.num_q_heads + qh) * D + d;
-        if (p.out_bf16) {
-          __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off);
-          ob[0] = __floats2bfloat162_rn(o.x, o.y);
-          ob[1] = __floats2bfloat162_rn(o.z, o.w);
-        } else {
-          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + off) = o;
+      // accumulator columns are heads 2c and 2c+1: their weights live in lanes 8c and 8c+4
+      {
+        const float wr = any ? exp2f(m_run - M) * inv : 0.f;
+        const float w0 = __shfl_sync(0xffffffffu, wr, 8 * c);
+        const float w1 = __shfl_sync(0xffffffffu, wr, 8 * c + 4);
+#pragma unroll
+        for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+          oacc[mt][0] *= w0;
+          oacc[mt][1] *= w1;
+          oacc[mt][2] *= w0;
+          oacc[mt][3] *= w1;
         }
-        if (d == 0 && p.lse_out) p.lse_out[(size_t)w.b * p.num_q_heads + qh] = row_lse[row];
-      } else {
-        const size_t prow = (size_t)w.split * p.num_q_heads + qh;
-        *reinterpret_cast<float4*>(p.o_part + prow * D + d) = o;
-        if (d == 0) p.lse_part[prow] = row_lse[row];
       }
+      for (int j = 0; j < others; ++j) {
+        const int slot = hl * others + j;
+        const float wr = any ? exp2f(part_ml[slot * 8 + r].x - M) * inv : 0.f;
+        const float w0 = __shfl_sync(0xffffffffu, wr, 8 * c);
+        const float w1 = __shfl_sync(0xffffffffu, wr, 8 * c + 4);
+#pragma unroll
+        for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+          const float4 v = part_o[(slot * Lo::kMTiles + mt) * 32 + lane];
+          oacc[mt][0] += v.x * w0;
+          oacc[mt][1] += v.y * w1;
+          oacc[mt][2] += v.z * w0;
+          oacc[mt][3] += v.w * w1;
+        }
+      }
+      // write heads 2c, 2c+1 of this group straight from the accumulators
+      const int qh0 = (w.hg * HG + hl) * G;  // first query head of this KV head
+      const bool direct = w.direct;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hr = 2 * c + e;  // head row within the KV head's group
+        if (hr >= G) continue;
+        const size_t row = direct ? (size_t)w.b * p.num_q_heads + qh0 + hr
+                                  : (size_t)w.split * p.num_q_heads + qh0 + hr;
+#pragma unroll
+        for (int mt = 0; mt < Lo::kMTiles; ++mt) {
+          int da, db;
+          if constexpr (FMT == KVQ_FMT_INT8) {
+            da = 16 * mt + 2 * r;
+            db = da + 1;
+          } else if constexpr (FMT == KVQ_FMT_BF16) {
+            da = 16 * mt + r;
+            db = da + 8;
+          } else {
+            da = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1);
+            db = da + 1;
+          }
+          const float va = oacc[mt][e], vb = oacc[mt][2 + e];
+          if (direct && p.out_bf16) {
+            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D;
+            if (db == da + 1) {
+              *reinterpret_cast<__nv_bfloat162*>(ob + da) = __floats2bfloat162_rn(va, vb);
+            } else {
+              ob[da] = __float2bfloat16_rn(va);
+              ob[db] = __float2bfloat16_rn(vb);
+            }
+          } else {
+            float* of = (direct ? reinterpret_cast<float*>(p.out) : p.o_part) + row * D;
+            if (db == da + 1) {
+              *reinterpret_cast<float2*>(of + da) = make_float2(va, vb);
+            } else {
+              of[da] = va;
+              of[db] = vb;
+            }
+          }
+        }
+      }
+      if (c == 0 && r < G) {
+        if (direct) {
+          if (p.lse_out) p.lse_out[(size_t)w.b * p.num_q_heads + qh0 + r] = lse;
+        } else {
+          p.lse_part[(size_t)w.split * p.num_q_heads + qh0 + r] = lse;
+        }
+      }
+      if (next_ok) load_q(nw);
     }
     // with the producers: the ring may be refilled for the next item
     asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");

@@ -6,13 +6,23 @@
 //   M = max_s lse_s,  w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s,
 //   lse = M + log(sum_s w_s);  a split with lse = -inf (no tokens) has weight 0.
 //
-// A persistent grid (at most two CTAs per SM) walks the (sequence, query head,
-// 64-column slice of D) tuples; sequences with a single split are skipped at the
-// cost of one load.  A CTA's 256 threads are 16 float4 columns x 16 split lanes,
-// each split lane summing every 16th split with four partial rows in flight,
-// then a shared-memory reduction over the split lanes.  The kernel is launched as a programmatic dependent of the decode
-// kernel (it may start while the decode grid drains) and waits for the decode
-// grid's results with griddepcontrol.wait before reading any partial.
+// Work unit: a task = (sequence, query head, slice of D columns), merged by WPR
+// warps.  Within a warp, L = 32 / R lanes cover the slice (4 columns each, float4)
+// and the R lane phases take different splits, so one load instruction brings R
+// partial rows; each lane keeps eight loads in flight.  The shape is the same for
+// the whole launch and is chosen on the device from the largest split count of
+// the batch (every CTA scans the split offsets first):
+//   * at most 16 splits: R = 1 (128-column slices), WPR = 1 — one task per warp,
+//     eight tasks per CTA;
+//   * more: R = 4 (32-column slices) and WPR up to 8, so a long sequence's rows
+//     spread over many CTAs and each CTA still has many rows in flight.
+// Every warp of a task computes the same maximum lse itself, so all partial sums
+// of a task add directly (lane phases by shuffles, warps through shared memory).
+// Sequences with a single split are skipped (the decode kernel wrote them).  The
+// grid is persistent (at most two CTAs per SM) and walks groups of 8 / WPR tasks.
+// The kernel is launched as a programmatic dependent of the decode kernel (it
+// may start while the decode grid drains) and waits for the decode grid's
+// results with griddepcontrol.wait before reading any partial.
 #include <algorithm>
 
 #include "kvq_internal.h"
@@ -22,117 +32,153 @@ namespace kvq {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kCols = 16;                          // float4 columns per CTA (64 elements)
-constexpr int kLanes = kMergeThreads / kCols;      // split lanes
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMinSliceCols = 32;                // narrowest slice (R = 4)
+constexpr int kShortSplits = 16;                 // up to this many splits: R = 1, WPR = 1
+constexpr int kInFlight = 8;                     // loads in flight per lane
+
+template <int R>
+__device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                                            const int32_t* __restrict__ offs, int batch, int num_q_heads, int D,
+                                            void* out, int out_bf16, float* lse_out, int wpr,
+                                            float4 (*red_o)[32], float* red_w) {
+  constexpr int L = 32 / R;            // lanes per row
+  constexpr int kCols = 4 * L;         // columns per task
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int phase = lane / L, col = lane % L;
+  const int tasks_per_group = kMergeWarps / wpr;
+  const int sub = warp % wpr;
+  const int slot = warp / wpr;
+  const int slices = D / kCols;
+  const int64_t tasks = (int64_t)batch * num_q_heads * slices;
+  const int64_t groups = (tasks + tasks_per_group - 1) / tasks_per_group;
+  const size_t ostride = (size_t)num_q_heads * D;
+  const int row0 = sub * R + phase;     // first split of this lane
+  const int rstep = wpr * R;            // splits between this lane's rows
+  for (int64_t grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+    const int64_t t = grp * tasks_per_group + slot;
+    int S = 0, base = 0, b = 0, g = 0, slice = 0;
+    if (t < tasks) {
+      const int bg = static_cast<int>(t / slices);
+      slice = static_cast<int>(t - (int64_t)bg * slices);
+      b = bg / num_q_heads;
+      g = bg - b * num_q_heads;
+      base = offs[b];
+      S = offs[b + 1] - base;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f, M = -INFINITY;
+    const bool active = S > 1;  // uniform over the task's warps
+    if (active) {
+      const float* lrow = lse_part + (size_t)base * num_q_heads + g;  // stride num_q_heads
+      float m = -INFINITY;
+      for (int s = lane; s < S; s += 32) m = fmaxf(m, lrow[(size_t)s * num_q_heads]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      M = m;
+      if (M != -INFINITY) {
+        const float* orow = o_part + (size_t)base * ostride + (size_t)g * D + slice * kCols + col * 4;
+        for (int s0 = row0; s0 < S; s0 += kInFlight * rstep) {
+          float l[kInFlight];
+          float4 v[kInFlight];
+#pragma unroll
+          for (int u = 0; u < kInFlight; ++u) {
+            const int s = s0 + u * rstep;
+            l[u] = -INFINITY;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < S) {
+              l[u] = lrow[(size_t)s * num_q_heads];
+              v[u] = *reinterpret_cast<const float4*>(orow + (size_t)s * ostride);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kInFlight; ++u) {
+            const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - M);
+            wsum += w;
+            acc.x += w * v[u].x;
+            acc.y += w * v[u].y;
+            acc.z += w * v[u].z;
+            acc.w += w * v[u].w;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = L; o < 32; o <<= 1) {  // add the lane phases
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+        wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      }
+    }
+    if (wpr > 1) {  // add the partial sums of the task's warps (uniform branch)
+      red_o[warp][lane] = acc;
+      if (lane == 0) red_w[warp] = wsum;
+      __syncthreads();
+      if (sub == 0) {
+        for (int j = 1; j < wpr; ++j) {
+          const float4 v = red_o[warp + j][lane];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+          wsum += red_w[warp + j];
+        }
+      }
+      __syncthreads();  // the buffers are reused by the next group
+    }
+    if (active && sub == 0 && phase == 0) {
+      float lse = -INFINITY;
+      if (M != -INFINITY && wsum > 0.f) {
+        const float inv = 1.f / wsum;
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+        lse = M + logf(wsum);
+      } else {
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      const size_t off = ((size_t)b * num_q_heads + g) * D + slice * kCols + col * 4;
+      if (out_bf16) {
+        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + off);
+        ob[0] = __floats2bfloat162_rn(acc.x, acc.y);
+        ob[1] = __floats2bfloat162_rn(acc.z, acc.w);
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + off) = acc;
+      }
+      if (slice == 0 && col == 0 && lse_out) lse_out[(size_t)b * num_q_heads + g] = lse;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                  const int32_t* __restrict__ offs, int batch, int num_q_heads, int D, void* out, int out_bf16,
                  float* lse_out) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float red_m[kMergeThreads / 32];
-  __shared__ float4 red_o[kLanes][kCols];
-  __shared__ float red_w[kLanes];
-  const int tid = threadIdx.x;
-  const int col = tid % kCols;
-  const int lane = tid / kCols;
-  const int slices = D / (4 * kCols);
-  const int64_t tuples = (int64_t)batch * num_q_heads * slices;
-  for (int64_t t = blockIdx.x; t < tuples; t += gridDim.x) {
-    const int bg = static_cast<int>(t / slices);
-    const int slice = static_cast<int>(t - (int64_t)bg * slices);
-    const int b = bg / num_q_heads;
-    const int g = bg - b * num_q_heads;
-    const int base = offs[b];
-    const int S = offs[b + 1] - base;
-    if (S <= 1) continue;  // written directly by the decode kernel (uniform across the CTA)
-    const float* lrow = lse_part + (size_t)base * num_q_heads + g;  // stride num_q_heads
+  __shared__ float4 red_o[kMergeWarps][32];
+  __shared__ float red_w[kMergeWarps];
+  __shared__ int red_s[kMergeWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // max of the split lse values
-    float m = -INFINITY;
-    for (int s = tid; s < S; s += kMergeThreads) m = fmaxf(m, lrow[(size_t)s * num_q_heads]);
+  // largest split count of the batch -> task shape (uniform over the grid)
+  int smax = 0;
+  for (int b = tid; b < batch; b += kMergeThreads) smax = max(smax, offs[b + 1] - offs[b]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((tid & 31) == 0) red_m[tid >> 5] = m;
-    __syncthreads();
-    float M = -INFINITY;
+  for (int o = 16; o > 0; o >>= 1) smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+  if (lane == 0) red_s[warp] = smax;
+  __syncthreads();
+  smax = 0;
 #pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) M = fmaxf(M, red_m[w]);
-
-    const int d = slice * 4 * kCols + col * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (M != -INFINITY) {
-      const float* orow = o_part + (size_t)base * num_q_heads * D + (size_t)g * D + d;
-      const size_t ostride = (size_t)num_q_heads * D;
-      int s = lane;
-      for (; s + 3 * kLanes < S; s += 4 * kLanes) {  // four rows in flight
-        float l[4];
-        float4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          l[u] = lrow[(size_t)(s + u * kLanes) * num_q_heads];
-          v[u] = *reinterpret_cast<const float4*>(orow + (size_t)(s + u * kLanes) * ostride);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - M);
-          wsum += w;
-          acc.x += w * v[u].x;
-          acc.y += w * v[u].y;
-          acc.z += w * v[u].z;
-          acc.w += w * v[u].w;
-        }
-      }
-      for (; s < S; s += kLanes) {
-        const float l = lrow[(size_t)s * num_q_heads];
-        if (l == -INFINITY) continue;
-        const float w = expf(l - M);
-        const float4 v = *reinterpret_cast<const float4*>(orow + (size_t)s * ostride);
-        wsum += w;
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-      }
-    }
-    red_o[lane][col] = acc;
-    if (col == 0) red_w[lane] = wsum;
-    __syncthreads();
-    if (lane == 0) {
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      float W = 0.f;
-#pragma unroll
-      for (int j = 0; j < kLanes; ++j) {
-        const float4 v = red_o[j][col];
-        o.x += v.x;
-        o.y += v.y;
-        o.z += v.z;
-        o.w += v.w;
-        W += red_w[j];
-      }
-      float lse = -INFINITY;
-      if (M != -INFINITY && W > 0.f) {
-        const float inv = 1.f / W;
-        o.x *= inv;
-        o.y *= inv;
-        o.z *= inv;
-        o.w *= inv;
-        lse = M + logf(W);
-      } else {
-        o = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      const size_t off = ((size_t)b * num_q_heads + g) * D + d;
-      if (out_bf16) {
-        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + off);
-        ob[0] = __floats2bfloat162_rn(o.x, o.y);
-        ob[1] = __floats2bfloat162_rn(o.z, o.w);
-      } else {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + off) = o;
-      }
-      if (d == 0 && lse_out) lse_out[(size_t)b * num_q_heads + g] = lse;
-    }
-    __syncthreads();  // shared buffers are reused by the next tuple
+  for (int w = 0; w < kMergeWarps; ++w) smax = max(smax, red_s[w]);
+  if (smax <= 1) return;  // nothing to merge
+  if (smax <= kShortSplits) {
+    merge_tasks<1>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, 1, red_o, red_w);
+  } else {
+    int wpr = 1;  // 4 splits per warp-load, 8 loads in flight: 32 splits per warp per round
+    while (wpr < kMergeWarps && wpr * 4 * kInFlight < smax) wpr <<= 1;
+    merge_tasks<4>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, wpr, red_o, red_w);
   }
 }
 
@@ -153,9 +199,9 @@ int merge_grid_limit() {
 cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
                          int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
                          cudaStream_t stream) {
-  const int64_t tuples = (int64_t)batch * num_q_heads * (head_dim / (4 * kCols));
-  if (tuples <= 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>(tuples, merge_grid_limit());
+  const int64_t tasks = (int64_t)batch * num_q_heads * (head_dim / kMinSliceCols);  // most tasks of any shape
+  if (tasks <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>(tasks, merge_grid_limit());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kMergeThreads);

@@ -55,17 +55,26 @@ def _struct(kvq, fmt="int8", pages=4096, Hkv=4, D=256):
     return kvq._binding.KvqCacheStruct(None, None, None, None, pages, 16, Hkv, D, kvq._binding.FORMATS[fmt], 1.0, 1.0)
 
 
+def _descriptors(plan, B, C, n_items):
+    """(first-item descriptors [C, 4], CTA offsets [C+1], rest descriptors) of a plan."""
+    A = (B + 2 + 3) // 4 * 4
+    R = (A + 5 * C + 1 + 3) // 4 * 4
+    firsts = plan[A:A + 4 * C].reshape(C, 4)
+    ro = plan[A + 4 * C:A + 5 * C + 1]
+    rest = plan[R:R + 4 * (n_items - C)].reshape(-1, 4)
+    return firsts, ro, rest
+
+
 def _check_plan(plan, seq_lens, total, nctas, nhg, override=None):
     B = len(seq_lens)
     offs = plan[:B + 1]
     assert offs[0] == 0 and offs[-1] == total
     C = plan[B + 1]
     assert C == nctas and 1 <= C <= total * nhg
-    co = plan[B + 2:B + 3 + C]
-    assert co[0] == 0 and co[-1] == total * nhg and all(co[i] <= co[i + 1] for i in range(C))
-    items = plan[B + 3 + C:B + 3 + C + total * nhg]
-    assert sorted(items.tolist()) == list(range(total * nhg))
-    size = {}
+    n_items = total * nhg
+    firsts, ro, rest = _descriptors(plan, B, C, n_items)
+    assert ro[0] == 0 and ro[-1] == n_items - C and all(ro[i] <= ro[i + 1] for i in range(C))
+    expect = {}  # (split, group) -> (b, first page, n, direct)
     for b, L in enumerate(seq_lens):
         n = -(-L // 16)
         S = offs[b + 1] - offs[b]
@@ -78,16 +87,26 @@ def _check_plan(plan, seq_lens, total, nctas, nhg, override=None):
         assert max(e - b_ for b_, e in bounds) - min(e - b_ for b_, e in bounds) <= 1
         for s, (b0, e0) in enumerate(bounds):
             for g in range(nhg):
-                size[(int(offs[b]) + s) * nhg + g] = e0 - b0
-    # longest-first packing: within a CTA the items come in decreasing size, and no
-    # CTA carries more than the average load plus one item (LPT bound)
+                expect[(int(offs[b]) + s, g)] = (b, b0, e0 - b0, int(S == 1))
+    seen = set()
     loads = []
     for c in range(C):
-        its = [int(i) for i in items[co[c]:co[c + 1]]]
-        sz = [size[i] for i in its]
+        descs = [firsts[c]] + [rest[i] for i in range(ro[c], ro[c + 1])]
+        sz = []
+        for d in descs:
+            b, split, pb, w = (int(x) for x in d)
+            n, direct, g = w & 0x7FFFFF, (w >> 23) & 1, w >> 24
+            key = (split, g)
+            assert key in expect and key not in seen
+            seen.add(key)
+            assert expect[key] == (b, pb, n, direct)
+            sz.append(n)
+        # longest-first packing: within a CTA the items come in decreasing size
         assert sz == sorted(sz, reverse=True)
         loads.append(sum(x + 8 for x in sz))
-    biggest = max(size.values()) + 8
+    assert len(seen) == n_items
+    # and no CTA carries more than the average load plus one item (LPT bound)
+    biggest = max(v[2] for v in expect.values()) + 8
     assert max(loads) <= sum(loads) / C + biggest
 
 

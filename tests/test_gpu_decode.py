@@ -135,7 +135,7 @@ def test_skip_merge_then_split_merge_matches():
 
 
 def test_checked_mode_reports_bad_metadata():
-    from quantized_paged_kv_gb300 import DecodePlan, KvqError, decode
+    from quantized_paged_kv_gb300 import DecodePlan, KvqError, decode, kvq_read_status
 
     wl = W.make("tiny_int8", lens=("list", [64, 64]), seed=2)
     cache = H.gpu_cache(wl, "int8")
@@ -150,12 +150,24 @@ def test_checked_mode_reports_bad_metadata():
         decode(cache, plan, q, bad, sl, out, wl.sm_scale, checked=True)
     assert e.value.code == 5
     bad_len = sl.clone()
-    bad_len[0] = 10**6                    # longer than the block table
+    bad_len[0] = 10**6                    # longer than the block table: the plan no longer matches
     with pytest.raises(KvqError) as e:
         decode(cache, plan, q, bt, bad_len, out, wl.sm_scale, checked=True)
-    assert e.value.code == 5
-    bad_plan = plan.plan.clone()
-    bad_plan[wl.B + 1] = 99               # launch order is not a permutation
+    assert e.value.code == 1
+    # raw mode: the kernel clamps the length to the block table and flags it
+    decode(cache, plan, q, bt, bad_len, out, wl.sm_scale, checked=False)
+    rc, bits = kvq_read_status(plan.workspace)
+    assert rc == 5 and bits & 2  # KVQ_DEV_BAD_SEQLEN
+    good_plan = plan.plan
+    bad_plan = good_plan.clone()
+    bad_plan[wl.B + 1] = 99               # CTA count differs from num_ctas
+    plan.plan = bad_plan
+    with pytest.raises(KvqError) as e:
+        decode(cache, plan, q, bt, sl, out, wl.sm_scale, checked=True)
+    assert e.value.code == 1
+    bad_plan = good_plan.clone()
+    A = (wl.B + 2 + 3) // 4 * 4
+    bad_plan[A + 1] = plan.total_splits + 3  # first item of CTA 0 names a split that does not exist
     plan.plan = bad_plan
     with pytest.raises(KvqError) as e:
         decode(cache, plan, q, bt, sl, out, wl.sm_scale, checked=True)
