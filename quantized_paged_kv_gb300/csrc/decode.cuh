@@ -106,7 +106,10 @@ struct DecodeLayout {
   // accumulators (one float4 per lane and m-tile) and (m, l) of 8 head rows
   static constexpr int kPartOBytes = kMTiles * 32 * 16;
   static constexpr int kExchangeBytes = (kCW - 1) * (kPartOBytes + 8 * 8);
-  static_assert(kExchangeBytes <= kRingBytes, "epilogue exchange must fit in the ring");
+  // then one output staging block per head of the group: 8 rows of D fp32
+  static constexpr int kStageAt = (kExchangeBytes + 127) / 128 * 128;
+  static constexpr int kStageBytes = 8 * D * 4;
+  static_assert(kStageAt + kCW * kStageBytes <= kRingBytes, "epilogue exchange and staging must fit in the ring");
 };
 
 // Producer warps and stage count for a head group of `hg` heads.  A single
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   __shared__ int abort_flag;
   __shared__ int4 next_desc;
+  __shared__ int4 cur_desc;
 
   // consumer identity (used only by consumer warps)
   const int hl = warp % HG;   // head within the group
@@ -286,13 +290,6 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     }
   };
 
-  Item first;
-  const bool first_ok = unpack(d0, first);
-  if (warp < CW && first_ok) {
-    first.L = seq_len(first.b);
-    load_q(first);
-  }
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
@@ -301,7 +298,14 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     fence_mbar_init();
     abort_flag = 0;
   }
-  __syncthreads();
+  __syncthreads();  // before any load that depends on the descriptor: producers go on at once
+
+  Item first;
+  const bool first_ok = unpack(d0, first);
+  if (warp < CW && first_ok) {
+    first.L = seq_len(first.b);
+    load_q(first);
+  }
 
   const int NP = decode_producers<FMT, D>(HG);
   const int sync_threads = (CW + NP) * 32;  // consumers + active producers (item boundaries)
@@ -447,7 +451,13 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     }
     // the next item's descriptor, fetched now and kept in shared memory (read in
     // the epilogue, after the barrier that ends this item's pages)
-    if (threadIdx.x == 0) next_desc = k + 1 < cnt ? rest[r0 + k] : make_int4(-1, -1, -1, -1);
+    // this item's descriptor is kept there too: the epilogue reads its sequence,
+    // split and head group from shared memory, not from registers held through
+    // the page loop
+    if (threadIdx.x == 0) {
+      cur_desc = k == 0 ? d0 : next_desc;
+      next_desc = k + 1 < cnt ? rest[r0 + k] : make_int4(-1, -1, -1, -1);
+    }
     // ---- q fragments (A operand rows = heads) for this item, converted from
     // the raw bf16 pairs loaded earlier.  Column (k) order per format, matching
     // the K fragments below: k-step j pairs (2c, 2c+1) with d dA(j, c) + {0, 1}
@@ -766,8 +776,16 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     // and been read, and the producers wait for this item's end, so the ring can
     // hold the exchange.
     asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
-    next_ok = k + 1 < cnt && unpack(next_desc, nw);
-    if (next_ok) nw.L = seq_len(nw.b);
+    Item cw;
+    unpack(cur_desc, cw);
+    // the next item: q and length loads are issued once this warp's accumulators are written out
+    auto next_item = [&]() {
+      next_ok = k + 1 < cnt && unpack(next_desc, nw);
+      if (next_ok) {
+        load_q(nw);
+        nw.L = seq_len(nw.b);
+      }
+    };
     const int others = WPH - 1;
     if (grp > 0) {
       const int slot = hl * others + grp - 1;
@@ -775,7 +793,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       for (int mt = 0; mt < Lo::kMTiles; ++mt)
         part_o[(slot * Lo::kMTiles + mt) * 32 + lane] = make_float4(oacc[mt][0], oacc[mt][1], oacc[mt][2], oacc[mt][3]);
       if (c == 0) part_ml[slot * 8 + r] = make_float2(m_run, l_run);
-      if (next_ok) load_q(nw);  // the accumulators are in shared memory: registers are free
+      next_item();  // the accumulators are in shared memory: registers are free
     }
     if (others > 0) asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
     if (grp == 0) {
@@ -810,65 +828,81 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         const float wr = any ? exp2f(part_ml[slot * 8 + r].x - M) * inv : 0.f;
         const float w0 = __shfl_sync(0xffffffffu, wr, 8 * c);
         const float w1 = __shfl_sync(0xffffffffu, wr, 8 * c + 4);
+        const float4* src = part_o + slot * Lo::kMTiles * 32 + lane;
 #pragma unroll
-        for (int mt = 0; mt < Lo::kMTiles; ++mt) {
-          const float4 v = part_o[(slot * Lo::kMTiles + mt) * 32 + lane];
-          oacc[mt][0] += v.x * w0;
-          oacc[mt][1] += v.y * w1;
-          oacc[mt][2] += v.z * w0;
-          oacc[mt][3] += v.w * w1;
+        for (int mt0 = 0; mt0 < Lo::kMTiles; mt0 += 4) {  // four m-tiles of loads in flight
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[u] = src[(mt0 + u) * 32];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            oacc[mt0 + u][0] += v[u].x * w0;
+            oacc[mt0 + u][1] += v[u].y * w1;
+            oacc[mt0 + u][2] += v[u].z * w0;
+            oacc[mt0 + u][3] += v[u].w * w1;
+          }
         }
       }
-      // write heads 2c, 2c+1 of this group straight from the accumulators
-      const int qh0 = (w.hg * HG + hl) * G;  // first query head of this KV head
-      const bool direct = w.direct;
+      // Stage the head's G query rows (fp32, or bf16 for a direct bf16 output) in
+      // shared memory, row-major, and copy them out with one bulk copy: the G
+      // query heads of a KV head are consecutive rows of both `out` and the
+      // partials.  The copy runs asynchronously; the ring is reused only after
+      // its source reads are done.
+      const bool direct = cw.direct;
+      const bool to_bf16 = direct && p.out_bf16;
+      uint8_t* stage = codes + Lo::kStageAt + hl * Lo::kStageBytes;
+      const int row_bytes = to_bf16 ? 2 * D : 4 * D;
+      auto put = [&](int hr, int d, float v0, float v1, bool pair) {  // elements d (and d+1 if pair) of row hr
+        if (to_bf16) {
+          const int byte = 2 * d;
+          uint8_t* at = stage + hr * row_bytes + byte;
+          if (pair) *reinterpret_cast<__nv_bfloat162*>(at) = __floats2bfloat162_rn(v0, v1);
+          else *reinterpret_cast<__nv_bfloat16*>(at) = __float2bfloat16_rn(v0);
+        } else {
+          const int byte = 4 * d;
+          uint8_t* at = stage + hr * row_bytes + byte;
+          if (pair) *reinterpret_cast<float2*>(at) = make_float2(v0, v1);
+          else *reinterpret_cast<float*>(at) = v0;
+        }
+      };
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int hr = 2 * c + e;  // head row within the KV head's group
         if (hr >= G) continue;
-        const size_t row = direct ? (size_t)w.b * p.num_q_heads + qh0 + hr
-                                  : (size_t)w.split * p.num_q_heads + qh0 + hr;
 #pragma unroll
         for (int mt = 0; mt < Lo::kMTiles; ++mt) {
-          int da, db;
           if constexpr (FMT == KVQ_FMT_INT8) {
-            da = 16 * mt + 2 * r;
-            db = da + 1;
+            put(hr, 16 * mt + 2 * r, oacc[mt][e], oacc[mt][2 + e], true);
           } else if constexpr (FMT == KVQ_FMT_BF16) {
-            da = 16 * mt + r;
-            db = da + 8;
+            put(hr, 16 * mt + r, oacc[mt][e], 0.f, false);
+            put(hr, 16 * mt + 8 + r, oacc[mt][2 + e], 0.f, false);
           } else {
-            da = 32 * (mt >> 1) + 4 * r + 2 * (mt & 1);
-            db = da + 1;
-          }
-          const float va = oacc[mt][e], vb = oacc[mt][2 + e];
-          if (direct && p.out_bf16) {
-            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D;
-            if (db == da + 1) {
-              *reinterpret_cast<__nv_bfloat162*>(ob + da) = __floats2bfloat162_rn(va, vb);
-            } else {
-              ob[da] = __float2bfloat16_rn(va);
-              ob[db] = __float2bfloat16_rn(vb);
-            }
-          } else {
-            float* of = (direct ? reinterpret_cast<float*>(p.out) : p.o_part) + row * D;
-            if (db == da + 1) {
-              *reinterpret_cast<float2*>(of + da) = make_float2(va, vb);
-            } else {
-              of[da] = va;
-              of[db] = vb;
-            }
+            put(hr, 32 * (mt >> 1) + 4 * r + 2 * (mt & 1), oacc[mt][e], oacc[mt][2 + e], true);
           }
         }
+      }
+      __syncwarp();
+      const int qh0 = (cw.hg * HG + hl) * G;  // first query head of this KV head
+      {
+        const size_t row0 = direct ? (size_t)cw.b * p.num_q_heads + qh0 : (size_t)cw.split * p.num_q_heads + qh0;
+        uint8_t* dst = direct ? reinterpret_cast<uint8_t*>(p.out) + row0 * row_bytes
+                              : reinterpret_cast<uint8_t*>(p.o_part + row0 * D);
+        fence_proxy_async_smem();  // the staged rows, written by this warp, become visible to the copy
+        __syncwarp();
+        if (lane == 0) bulk_store(dst, stage, G * row_bytes);
       }
       if (c == 0 && r < G) {
         if (direct) {
-          if (p.lse_out) p.lse_out[(size_t)w.b * p.num_q_heads + qh0 + r] = lse;
+          if (p.lse_out) p.lse_out[(size_t)cw.b * p.num_q_heads + qh0 + r] = lse;
         } else {
-          p.lse_part[(size_t)w.split * p.num_q_heads + qh0 + r] = lse;
+          p.lse_part[(size_t)cw.split * p.num_q_heads + qh0 + r] = lse;
         }
       }
-      if (next_ok) load_q(nw);
+      next_item();
+    }
+    if (grp == 0 && lane == 0) {
+      if (k + 1 < cnt) bulk_wait_read();  // the ring may be overwritten once the copy has read it
+      else bulk_wait_all();               // last item: the rows are written before the CTA exits
     }
     // with the producers: the ring may be refilled for the next item
     asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
