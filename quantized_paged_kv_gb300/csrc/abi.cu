@@ -151,6 +151,14 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
   std::lock_guard<std::mutex> lock(mu);
   bool& d = done[dev][format][D == 256 ? 1 : 0];
   if (!d) {
+    // the kernel's warp roles split its launch registers (setmaxnreg): the split
+    // is only valid for the register count it was written for
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, inst->kernel);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(decode kernel)");
+    if (fa.numRegs != inst->launch_regs)
+      return fail(KVQ_ERR_UNSUPPORTED, "decode kernel built with %d registers a thread, its register split assumes %d",
+                  fa.numRegs, inst->launch_regs);
     e = cudaFuncSetAttribute(inst->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, inst->smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
     d = true;

@@ -90,6 +90,24 @@ struct DecodeLayout {
   static constexpr int kCW = consumer_warps<D>();
   static constexpr int kMaxProducers = 4;  // producer warps (a thread issues one copy per ~300 ns)
   static constexpr int kThreads = (kCW + kMaxProducers) * 32;
+  // Registers: the kernel launches with kLaunchRegs a thread (all of the SM's
+  // 64K registers); the producer warpgroup then gives registers back
+  // (setmaxnreg.dec to kProducerRegs) and the consumer warpgroups take them
+  // (setmaxnreg.inc to kConsumerRegs).  The split never asks for more than the
+  // launch allocation, and the host refuses to launch a build whose register
+  // count differs from kLaunchRegs.
+  // (NVFP4 keeps the launch allocation everywhere: its consumer code compiles
+  // better without the split.)
+  static constexpr bool kRegSplit = FMT != KVQ_FMT_NVFP4;
+  static constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;
+  static constexpr int kProducerRegs = kRegSplit ? (D == 256 ? 104 : 56) : kLaunchRegs;
+  static constexpr int kConsumerRegs =
+      ((kLaunchRegs * kThreads - kProducerRegs * kMaxProducers * 32) / (kCW * 32) / 8 * 8) > 256
+          ? 256
+          : ((kLaunchRegs * kThreads - kProducerRegs * kMaxProducers * 32) / (kCW * 32) / 8 * 8);
+  static_assert(kCW % 4 == 0 && kMaxProducers == 4, "warpgroup-aligned roles");
+  static_assert(kConsumerRegs * kCW * 32 + kProducerRegs * kMaxProducers * 32 <= kLaunchRegs * kThreads,
+                "register split exceeds the launch allocation");
   static constexpr int kHeadCode = kPage * T::kRow;        // one head's K (or V) code block of a page
   static constexpr int kHeadScale = kPage * T::kScaleRow;  // one head's K (or V) scale block of a page
   static constexpr int kKSteps = D / 16;
@@ -311,6 +329,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   const int sync_threads = (CW + NP) * 32;  // consumers + active producers (item boundaries)
   if (warp >= CW) {
     // ================================================================ producers
+    if constexpr (Lo::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Lo::kProducerRegs));
     const int pi = warp - CW;
     if (pi >= NP) return;
     bool ok = true;
@@ -418,6 +437,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   }
 
   // ================================================================== consumers
+  if constexpr (Lo::kRegSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Lo::kConsumerRegs));
   uint8_t* myq = qfrag + warp * Lo::kQBytes;
   const uint32_t qbase = smem_addr(myq) + ((lane >> 3) * 8 + (lane & 7)) * 16;
   // Per-lane byte offsets of the swizzled ldmatrix rows inside a head block,

@@ -8,7 +8,7 @@ template <int FMT, int D>
 DecodeInstance instance_of() {
   using Lo = DecodeLayout<FMT, D>;
   return DecodeInstance{reinterpret_cast<const void*>(&decode_kernel<FMT, D>), Lo::kSmemBytes, Lo::kThreads, Lo::kCW,
-                        DecodeTraits<FMT, D>::kRow, &decode_head_group<FMT, D>};
+                        DecodeTraits<FMT, D>::kRow, &decode_head_group<FMT, D>, Lo::kLaunchRegs};
 }
 
 template <int FMT, int D>

@@ -54,6 +54,7 @@ struct DecodeInstance {
   int consumer_warps;          // consumer warps per CTA
   int row_bytes;               // code bytes per token row
   int (*head_group)(int hkv);  // KV heads per work item for num_kv_heads = hkv (0: none fits)
+  int launch_regs;             // registers a thread the kernel's register split assumes at launch
 };
 
 bool decode_instance(int format, int head_dim, DecodeInstance* out);
