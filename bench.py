@@ -175,9 +175,12 @@ class LayerSet:
         return kvq.DecodePlan(self.caches[0], self.wl.seq_lens, self.wl.Hq, split_override=split, device=self.device)
 
     def call(self, r, plan, skip_merge=False):
+        # the plan and block tables are written once, before any timed call: the
+        # decode may read them while the previous call's kernels finish
         import quantized_paged_kv_gb300 as kvq
 
-        kvq.decode(self.caches[r], plan, self.q, self.bt, self.sl, self.out, self.wl.sm_scale, skip_merge=skip_merge)
+        kvq.decode(self.caches[r], plan, self.q, self.bt, self.sl, self.out, self.wl.sm_scale, skip_merge=skip_merge,
+                   early_start=True)
 
     def kv_bytes(self):
         import quantized_paged_kv_gb300 as kvq
@@ -254,7 +257,8 @@ def time_e2e(ls, plan, steps, warmup=3):
 
     def one(r):
         stage_d.copy_(stage_h, non_blocking=True)
-        kvq.decode(ls.caches[r], plan, q_d, bt_d, sl_d, ls.out, ls.wl.sm_scale)
+        # the block table arrives by copy, not from a kernel: early start stays valid
+        kvq.decode(ls.caches[r], plan, q_d, bt_d, sl_d, ls.out, ls.wl.sm_scale, early_start=True)
         out_h.copy_(ls.out, non_blocking=True)
 
     torch.cuda.synchronize()

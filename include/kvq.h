@@ -74,8 +74,16 @@ enum {
   KVQ_CHECKED = 1u,    /* validate metadata on the host, synchronize, read the device
                           status word; not graph-capturable ([nvfp4] "Testing the cache
                           without loading the model": the checked API syncs) */
-  KVQ_SKIP_MERGE = 2u  /* decode only: leave the split partials in the workspace and
+  KVQ_SKIP_MERGE = 2u, /* decode only: leave the split partials in the workspace and
                           do not launch the merge (the caller calls kvq_split_merge) */
+  KVQ_EARLY_START = 4u /* decode only: the plan and the block tables of this call are
+                          not written by the kernel just before it on the stream, so the
+                          decode may read them (and find its first pages) while that
+                          kernel is still running.  Every other input (q, the cache,
+                          seq_lens) and every output is touched only after that kernel
+                          has completed.  The decode kernel is always launched as a
+                          programmatic dependent of the preceding kernel; without this
+                          flag it waits for that kernel before reading anything. */
 };
 
 /* device status word bits (kvq_read_status) */

@@ -70,7 +70,10 @@ class DecodePlan:
 
 
 def decode(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, checked=False, skip_merge=False,
-           stream=None):
-    flags = (B.KVQ_CHECKED if checked else 0) | (B.KVQ_SKIP_MERGE if skip_merge else 0)
+           early_start=False, stream=None):
+    """early_start: the plan and block tables are not written by the kernel just before this call on the stream
+    (e.g. they were uploaded once for all layers of a step), so the decode may read them early."""
+    flags = ((B.KVQ_CHECKED if checked else 0) | (B.KVQ_SKIP_MERGE if skip_merge else 0)
+             | (B.KVQ_EARLY_START if early_start else 0))
     B.kvq_paged_decode_attention(cache.struct, q, sm_scale, block_tables, seq_lens, plan.plan, plan.total_splits,
                                  plan.num_ctas, plan.workspace, out, lse_out, flags, stream)

@@ -493,6 +493,7 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   p.total_splits = total_splits;
   p.heads_per_cta = hg;
   p.out_bf16 = out_dtype == KVQ_OUT_BF16;
+  p.early_start = (flags & KVQ_EARLY_START) ? 1 : 0;
   p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
   p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
   p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;

@@ -43,6 +43,9 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
 
 template <int FMT, int D>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
+  // a following decode (a programmatic dependent) may be scheduled now; it waits
+  // for this grid to complete before it reads the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int TPR = D / 8;
   constexpr int ROWS = kAppendThreads / TPR;
   const int64_t row = (int64_t)blockIdx.x * ROWS + threadIdx.x / TPR;

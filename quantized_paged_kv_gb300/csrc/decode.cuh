@@ -203,6 +203,12 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   // the merge kernel is launched as a programmatic dependent: let it be scheduled
   // (it waits for this grid's results before reading them)
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // This grid is itself launched as a programmatic dependent of the preceding
+  // kernel.  Unless the caller promised that the plan and block tables are not
+  // written by that kernel, wait for it before reading anything; otherwise the
+  // producers wait just before their first copy and the consumers before they
+  // read q and the sequence lengths.
+  if (!p.early_start) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int HG = p.heads_per_cta;
   const int WPH = CW / HG;
   const int NST = decode_stages<FMT, D>(HG);
@@ -320,6 +326,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 
   Item first;
   const bool first_ok = unpack(d0, first);
+  if (warp < CW && p.early_start) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp < CW && first_ok) {
     first.L = seq_len(first.b);
     load_q(first);
@@ -353,6 +360,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     Item w = first;
     bool valid = first_ok;
     int v0 = valid ? page_id(w, lane) : -1;  // ids of the item's first 32 pages of this producer
+    if (p.early_start) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int k = 0; k < cnt; ++k) {
       if (valid) {
         const int n = w.n;

@@ -15,8 +15,19 @@ template <int FMT, int D>
 cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                      cudaStream_t stream) {
   using Lo = DecodeLayout<FMT, D>;
-  decode_kernel<FMT, D><<<grid, Lo::kThreads, Lo::kSmemBytes, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  // programmatic dependent of the preceding kernel: the kernel waits for it
+  // (griddepcontrol.wait) before touching anything that kernel may write
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(Lo::kThreads);
+  cfg.dynamicSmemBytes = Lo::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<FMT, D>, tk, tv, p);
 }
 
 }  // namespace

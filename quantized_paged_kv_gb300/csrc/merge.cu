@@ -156,6 +156,9 @@ __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                  const int32_t* __restrict__ offs, int batch, int num_q_heads, int D, void* out, int out_bf16,
                  float* lse_out) {
+  // a following decode may be scheduled now (it waits for this grid before it
+  // writes anything this kernel reads)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float4 red_o[kMergeWarps][32];
   __shared__ float red_w[kMergeWarps];

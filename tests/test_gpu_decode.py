@@ -208,3 +208,42 @@ def test_long_nvfp4_full_size_sampled():
     order = np.argsort(wl.seq_lens)
     units = [(int(order[0]), 1), (int(order[-1]), 2)]
     _check(wl, "nvfp4", 0, units=units)
+
+
+def test_early_start_chain_in_a_graph_matches_plain_calls():
+    """Calls launched as programmatic dependents of each other (early start): a
+    CUDA graph of back-to-back calls on alternating queries and output buffers
+    gives exactly the plain calls' results."""
+    from quantized_paged_kv_gb300 import DecodePlan, decode
+
+    wl = W.make("tiny_int8", lens=("list", [700, 33, 4096]), seed=13)
+    cache = H.gpu_cache(wl, "int8")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=5)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    sl = torch.from_numpy(wl.seq_lens).cuda()
+    qs = [torch.from_numpy(wl.q()).to(torch.bfloat16).cuda()]
+    qs.append((qs[0].float() * -0.5 + 0.25).to(torch.bfloat16))
+    refs = []
+    for q in qs:
+        o = torch.empty((wl.B, wl.Hq, wl.D), device="cuda")
+        decode(cache, plan, q, bt, sl, o, wl.sm_scale)
+        refs.append(o)
+    outs = [torch.full((wl.B, wl.Hq, wl.D), float("nan"), device="cuda") for _ in range(4)]
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):  # warm-up outside capture
+        for i in range(4):
+            decode(cache, plan, qs[i % 2], bt, sl, outs[i], wl.sm_scale, early_start=True)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(4):
+            decode(cache, plan, qs[i % 2], bt, sl, outs[i], wl.sm_scale, early_start=True)
+    for o in outs:
+        o.fill_(float("nan"))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for i in range(4):
+        assert torch.equal(outs[i], refs[i % 2]), i
