@@ -16,8 +16,9 @@
 //     eight tasks per CTA;
 //   * more: R = 4 (32-column slices) and WPR up to 8, so a long sequence's rows
 //     spread over many CTAs and each CTA still has many rows in flight.
-// Every warp of a task computes the same maximum lse itself, so all partial sums
-// of a task add directly (lane phases by shuffles, warps through shared memory).
+// Each lane keeps a running maximum of the lse values it has seen and rescales
+// its sums when it grows (one pass over the partials); lane phases and warps are
+// then combined the same way (by shuffles, and through shared memory).
 // Sequences with a single split are skipped (the decode kernel wrote them).  The
 // grid is persistent (at most two CTAs per SM) and walks groups of 8 / WPR tasks.
 // The kernel is launched as a programmatic dependent of the decode kernel (it
@@ -41,7 +42,7 @@ template <int R>
 __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                                             const int32_t* __restrict__ offs, int batch, int num_q_heads, int D,
                                             void* out, int out_bf16, float* lse_out, int wpr,
-                                            float4 (*red_o)[32], float* red_w) {
+                                            float4 (*red_o)[32], float* red_w, float* red_m) {
   constexpr int L = 32 / R;            // lanes per row
   constexpr int kCols = 4 * L;         // columns per task
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -66,34 +67,41 @@ __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, co
       base = offs[b];
       S = offs[b + 1] - base;
     }
+    // one pass with an online rescale: (m, wsum, acc) = running max of the lse
+    // values seen, sum of exp(lse - m), and sum of exp(lse - m) * o
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f, M = -INFINITY;
+    float wsum = 0.f, m = -INFINITY;
     const bool active = S > 1;  // uniform over the task's warps
     if (active) {
       const float* lrow = lse_part + (size_t)base * num_q_heads + g;  // stride num_q_heads
-      float m = -INFINITY;
-      for (int s = lane; s < S; s += 32) m = fmaxf(m, lrow[(size_t)s * num_q_heads]);
+      const float* orow = o_part + (size_t)base * ostride + (size_t)g * D + slice * kCols + col * 4;
+      for (int s0 = row0; s0 < S; s0 += kInFlight * rstep) {
+        float l[kInFlight];
+        float4 v[kInFlight];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      M = m;
-      if (M != -INFINITY) {
-        const float* orow = o_part + (size_t)base * ostride + (size_t)g * D + slice * kCols + col * 4;
-        for (int s0 = row0; s0 < S; s0 += kInFlight * rstep) {
-          float l[kInFlight];
-          float4 v[kInFlight];
-#pragma unroll
-          for (int u = 0; u < kInFlight; ++u) {
-            const int s = s0 + u * rstep;
-            l[u] = -INFINITY;
-            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (s < S) {
-              l[u] = lrow[(size_t)s * num_q_heads];
-              v[u] = *reinterpret_cast<const float4*>(orow + (size_t)s * ostride);
-            }
+        for (int u = 0; u < kInFlight; ++u) {
+          const int s = s0 + u * rstep;
+          l[u] = -INFINITY;
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s < S) {
+            l[u] = lrow[(size_t)s * num_q_heads];
+            v[u] = *reinterpret_cast<const float4*>(orow + (size_t)s * ostride);
           }
+        }
+        float lm = m;
+#pragma unroll
+        for (int u = 0; u < kInFlight; ++u) lm = fmaxf(lm, l[u]);
+        if (lm != -INFINITY) {
+          const float sc = expf(m - lm);  // m = -inf: 0 (acc and wsum are 0 then)
+          wsum *= sc;
+          acc.x *= sc;
+          acc.y *= sc;
+          acc.z *= sc;
+          acc.w *= sc;
+          m = lm;
 #pragma unroll
           for (int u = 0; u < kInFlight; ++u) {
-            const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - M);
+            const float w = l[u] == -INFINITY ? 0.f : expf(l[u] - m);
             wsum += w;
             acc.x += w * v[u].x;
             acc.y += w * v[u].y;
@@ -103,39 +111,61 @@ __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, co
         }
       }
 #pragma unroll
-      for (int o = L; o < 32; o <<= 1) {  // add the lane phases
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
-        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
-        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
-        wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      for (int o = L; o < 32; o <<= 1) {  // combine the lane phases
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+        const float wo = __shfl_xor_sync(0xffffffffu, wsum, o);
+        const float ax = __shfl_xor_sync(0xffffffffu, acc.x, o);
+        const float ay = __shfl_xor_sync(0xffffffffu, acc.y, o);
+        const float az = __shfl_xor_sync(0xffffffffu, acc.z, o);
+        const float aw = __shfl_xor_sync(0xffffffffu, acc.w, o);
+        const float mn = fmaxf(m, mo);
+        const float s1 = mn == -INFINITY ? 0.f : expf(m - mn), s2 = mn == -INFINITY ? 0.f : expf(mo - mn);
+        wsum = wsum * s1 + wo * s2;
+        acc.x = acc.x * s1 + ax * s2;
+        acc.y = acc.y * s1 + ay * s2;
+        acc.z = acc.z * s1 + az * s2;
+        acc.w = acc.w * s1 + aw * s2;
+        m = mn;
       }
     }
-    if (wpr > 1) {  // add the partial sums of the task's warps (uniform branch)
+    if (wpr > 1) {  // combine the task's warps (uniform branch)
       red_o[warp][lane] = acc;
-      if (lane == 0) red_w[warp] = wsum;
+      if (lane == 0) {
+        red_w[warp] = wsum;
+        red_m[warp] = m;
+      }
       __syncthreads();
       if (sub == 0) {
+        float mn = m;
+        for (int j = 1; j < wpr; ++j) mn = fmaxf(mn, red_m[warp + j]);
+        const float s0 = mn == -INFINITY ? 0.f : expf(m - mn);
+        wsum *= s0;
+        acc.x *= s0;
+        acc.y *= s0;
+        acc.z *= s0;
+        acc.w *= s0;
         for (int j = 1; j < wpr; ++j) {
+          const float sj = mn == -INFINITY ? 0.f : expf(red_m[warp + j] - mn);
           const float4 v = red_o[warp + j][lane];
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-          wsum += red_w[warp + j];
+          acc.x += v.x * sj;
+          acc.y += v.y * sj;
+          acc.z += v.z * sj;
+          acc.w += v.w * sj;
+          wsum += red_w[warp + j] * sj;
         }
+        m = mn;
       }
       __syncthreads();  // the buffers are reused by the next group
     }
     if (active && sub == 0 && phase == 0) {
       float lse = -INFINITY;
-      if (M != -INFINITY && wsum > 0.f) {
+      if (m != -INFINITY && wsum > 0.f) {
         const float inv = 1.f / wsum;
         acc.x *= inv;
         acc.y *= inv;
         acc.z *= inv;
         acc.w *= inv;
-        lse = M + logf(wsum);
+        lse = m + logf(wsum);
       } else {
         acc = make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -162,6 +192,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float4 red_o[kMergeWarps][32];
   __shared__ float red_w[kMergeWarps];
+  __shared__ float red_m[kMergeWarps];
   __shared__ int red_s[kMergeWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -177,11 +208,11 @@ __global__ void __launch_bounds__(kMergeThreads)
   for (int w = 0; w < kMergeWarps; ++w) smax = max(smax, red_s[w]);
   if (smax <= 1) return;  // nothing to merge
   if (smax <= kShortSplits) {
-    merge_tasks<1>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, 1, red_o, red_w);
+    merge_tasks<1>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, 1, red_o, red_w, red_m);
   } else {
     int wpr = 1;  // 4 splits per warp-load, 8 loads in flight: 32 splits per warp per round
     while (wpr < kMergeWarps && wpr * 4 * kInFlight < smax) wpr <<= 1;
-    merge_tasks<4>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, wpr, red_o, red_w);
+    merge_tasks<4>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, wpr, red_o, red_w, red_m);
   }
 }
 
