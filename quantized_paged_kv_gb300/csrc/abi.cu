@@ -7,8 +7,10 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <functional>
 #include <mutex>
 #include <numeric>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -290,15 +292,57 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
     target = (int64_t)sms * std::max(per_sm, 1);
   }
   target = std::max<int64_t>(target, 1);
+  // Cost of a work item for the packing: its pages plus a fixed per-item cost
+  // (prologue, epilogue and merge share), in page units.
+  constexpr int64_t kItemCost = 8;
+  // Longest-first packing of the items of a split choice onto C = min(target,
+  // items) CTAs: returns the largest CTA load (the critical path).
+  auto makespan = [&](const std::vector<int32_t>& sp) -> int64_t {
+    std::vector<int64_t> sizes;
+    for (int b = 0; b < batch; ++b)
+      for (int s = 0; s < sp[b]; ++s) {
+        const int64_t sz = (int64_t)(s + 1) * npages[b] / sp[b] - (int64_t)s * npages[b] / sp[b];
+        for (int g = 0; g < nhg; ++g) sizes.push_back(sz + kItemCost);
+      }
+    std::sort(sizes.begin(), sizes.end(), std::greater<int64_t>());
+    const int64_t C = std::min<int64_t>(target, (int64_t)sizes.size());
+    std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> bins;
+    for (int64_t i = 0; i < C; ++i) bins.push(0);
+    int64_t worst = 0;
+    for (int64_t sz : sizes) {
+      const int64_t l = bins.top() + sz;
+      bins.pop();
+      bins.push(l);
+      worst = std::max(worst, l);
+    }
+    return worst;
+  };
   std::vector<int32_t> splits(batch, 1);
   if (split_override > 0) {
     for (int b = 0; b < batch; ++b)
       splits[b] = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(split_override, std::max<int64_t>(npages[b], 1))));
   } else {
+    // Pages per split x = units / (target * m) for a few oversubscription factors
+    // m (at least 4 pages): a sequence of n pages gets ceil(n / x) splits.  The
+    // choice with the shortest critical path wins (ties: fewer items).
     const int64_t units = total_pages * nhg;  // (page, head group) units
-    const int64_t chunk = std::max<int64_t>(4, (units + target - 1) / target);
-    for (int b = 0; b < batch; ++b)
-      splits[b] = static_cast<int32_t>(std::max<int64_t>(1, (npages[b] + chunk - 1) / chunk));
+    const double ms[] = {1.0, 1.25, 1.5, 2.0, 2.5, 3.0, 4.0, 6.0};
+    int64_t best = -1, best_items = 0;
+    for (double m : ms) {
+      const double x = std::max(4.0, (double)units / ((double)target * m));
+      std::vector<int32_t> sp(batch);
+      int64_t items = 0;
+      for (int b = 0; b < batch; ++b) {
+        sp[b] = static_cast<int32_t>(std::max<int64_t>(1, (int64_t)std::ceil((double)npages[b] / x - 1e-9)));
+        items += (int64_t)sp[b] * nhg;
+      }
+      const int64_t span = makespan(sp);
+      if (best < 0 || span < best || (span == best && items < best_items)) {
+        best = span;
+        best_items = items;
+        splits = sp;
+      }
+    }
   }
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) total += splits[b];
@@ -321,8 +365,7 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
   plan[batch + 1] = static_cast<int32_t>(C);
   for (int64_t i = batch + 2; i < A; ++i) plan[i] = 0;
   // Items with their descriptors and page counts; longest first, each onto the
-  // CTA with the least work so far (a page costs 1, an item's fixed prologue and
-  // epilogue are counted as 8 pages).
+  // CTA with the least work so far (a page costs 1, an item kItemCost more).
   struct Desc {
     int64_t cost;
     int32_t d[4];
@@ -353,7 +396,7 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
     std::pop_heap(heap.begin(), heap.end(), cmp);
     auto& top = heap.back();
     bins[top.second].push_back(i);
-    top.first += items[i].cost + 8;
+    top.first += items[i].cost + kItemCost;
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
   int32_t* roff = plan + roff_at;

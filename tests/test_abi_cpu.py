@@ -120,8 +120,23 @@ def test_planner_override_and_auto(kvq):
         plan, total, nctas = kvq.kvq_plan_splits(s, seq_lens, 0, 152)
         _check_plan(plan.numpy(), seq_lens, total, nctas, 1)
     plan, total, nctas = kvq.kvq_plan_splits(s, [32768], 0, 152)
-    # 2048 page units over 152 CTAs -> 14 pages per item -> 147 splits, one per CTA
-    assert total == 147 and nctas == 147
+    # 2048 page units over 152 CTAs: 152 splits of 13 or 14 pages, one per CTA
+    assert total == 152 and nctas == 152
+    # uneven lengths: a split granularity whose packing fills every CTA evenly
+    # wins over one split per CTA's worth of pages (which leaves some CTAs two items)
+    lens = [4096 * 16, 3000 * 16, 900 * 16, 333 * 16, 4100 * 16]
+    plan, total, nctas = kvq.kvq_plan_splits(s, lens, 0, 152)
+    _check_plan(plan.numpy(), lens, total, nctas, 1)
+    sizes = []
+    off = plan.numpy()[:len(lens) + 1]
+    for b, L in enumerate(lens):
+        n, S = -(-L // 16), off[b + 1] - off[b]
+        sizes += [(s_ + 1) * n // S - s_ * n // S for s_ in range(S)]
+    loads = sorted(sizes, reverse=True)
+    bins = [0] * nctas
+    for x in loads:
+        bins[bins.index(min(bins))] += x + 8
+    assert max(bins) <= 1.25 * (sum(loads) + 8 * len(loads)) / nctas
     s8 = _struct(kvq, pages=4096, Hkv=8, D=128)  # 12 consumer warps at D = 128 -> groups of 4 heads
     lens = rng.integers(512, 8193, 64).tolist()
     plan, total, nctas = kvq.kvq_plan_splits(s8, lens, 0, 152)
