@@ -544,7 +544,8 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   cudaError_t e = kvq::launch_decode(cache->format, D, tk, tv, p, num_ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (!(flags & KVQ_SKIP_MERGE) && total_splits > batch) {
-    e = kvq::launch_merge(o_part, lse_part, plan, batch, num_q_heads, D, out, p.out_bf16, lse_out, st);
+    // the split offsets come from the plan, which the decode kernel never writes
+    e = kvq::launch_merge(o_part, lse_part, plan, batch, num_q_heads, D, out, p.out_bf16, lse_out, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (checked) {
@@ -564,7 +565,7 @@ int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* s
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "bad out_dtype");
   if (!aligned16(o_part) || !aligned16(out)) return fail(KVQ_ERR_INVALID_ARG, "o_part / out must be 16-byte aligned");
   cudaError_t e = kvq::launch_merge(o_part, lse_part, split_offsets, batch, num_q_heads, head_dim, out,
-                                    out_dtype == KVQ_OUT_BF16, lse_out, reinterpret_cast<cudaStream_t>(stream));
+                                    out_dtype == KVQ_OUT_BF16, lse_out, false, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return succeed();
 }

@@ -928,10 +928,10 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       }
       next_item();
     }
-    if (grp == 0 && lane == 0) {
-      if (k + 1 < cnt) bulk_wait_read();  // the ring may be overwritten once the copy has read it
-      else bulk_wait_all();               // last item: the rows are written before the CTA exits
-    }
+    // the ring (or, after the last item, the CTA's shared memory) may be reused
+    // once the copy has read it; the copy's global writes complete on their own
+    // and are visible to the next kernel once this grid has completed
+    if (grp == 0 && lane == 0) bulk_wait_read();
     // with the producers: the ring may be refilled for the next item
     asm volatile("bar.sync 2, %0;" ::"r"(sync_threads) : "memory");
     if (abort_flag) break;

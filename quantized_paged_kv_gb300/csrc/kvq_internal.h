@@ -64,8 +64,10 @@ cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const
 cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaStream_t stream);
 // Record a printf-style message as the calling thread's last error; returns code.
 int record_error(int code, const char* fmt, ...);
+// offsets_ready: the offsets are not written by the preceding kernel on the
+// stream (read before waiting for it)
 cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
-                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
+                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out, bool offsets_ready,
                          cudaStream_t stream);
 
 }  // namespace kvq

@@ -185,11 +185,14 @@ __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, co
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                  const int32_t* __restrict__ offs, int batch, int num_q_heads, int D, void* out, int out_bf16,
-                 float* lse_out) {
+                 float* lse_out, int offs_ready) {
   // a following decode may be scheduled now (it waits for this grid before it
   // writes anything this kernel reads)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The split offsets may be read before the preceding kernel completes when the
+  // caller says so (they come from the plan, which the decode kernel never
+  // writes); the partials only after it.
+  if (!offs_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float4 red_o[kMergeWarps][32];
   __shared__ float red_w[kMergeWarps];
   __shared__ float red_m[kMergeWarps];
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) smax = max(smax, red_s[w]);
   if (smax <= 1) return;  // nothing to merge
+  if (offs_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (smax <= kShortSplits) {
     merge_tasks<1>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, 1, red_o, red_w, red_m);
   } else {
@@ -231,7 +235,7 @@ int merge_grid_limit() {
 }  // namespace
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
-                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
+                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out, bool offsets_ready,
                          cudaStream_t stream) {
   const int64_t tasks = (int64_t)batch * num_q_heads * (head_dim / kMinSliceCols);  // most tasks of any shape
   if (tasks <= 0) return cudaSuccess;
@@ -247,7 +251,7 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, merge_kernel, o_part, lse_part, offsets, batch, num_q_heads, head_dim, out,
-                            out_bf16, lse_out);
+                            out_bf16, lse_out, offsets_ready ? 1 : 0);
 }
 
 }  // namespace kvq
