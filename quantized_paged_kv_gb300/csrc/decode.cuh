@@ -223,7 +223,9 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   const int G = p.num_q_heads / Hkv;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (128-byte swizzle), derived from the shared array by
+  // pointer arithmetic so that every access through it stays a shared-memory one
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* codes = smem;                                   // NST x [K heads][V heads]
   uint8_t* scales = smem + NST * stage_code;               // NST x [K heads][V heads]
   uint8_t* qfrag = smem + Lo::kRingBytes;                  // CW x kQBytes
