@@ -537,6 +537,17 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     }
     __syncwarp();
 
+    // At D = 128 this item's q fragments (A operand, two k-steps per
+    // ldmatrix.x4) fit in registers for all of its pages; at D = 256 they are
+    // re-read from shared memory per page (the registers go to the accumulators).
+    constexpr bool kQInRegs = D == 128;
+    [[maybe_unused]] uint32_t qreg[kQInRegs ? KS : 1][2];
+    if constexpr (kQInRegs) {
+#pragma unroll
+      for (int jj = 0; jj < KS / 2; ++jj)
+        ldsm_x4(qbase + jj * 512, qreg[2 * jj][0], qreg[2 * jj][1], qreg[2 * jj + 1][0], qreg[2 * jj + 1][1]);
+    }
+
     float oacc[Lo::kMTiles][4];
 #pragma unroll
     for (int mt = 0; mt < Lo::kMTiles; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
@@ -585,10 +596,18 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 #pragma unroll
     for (int cg = 0; cg < NCG; ++cg) {
       uint32_t qa[QPG][2];
+      if constexpr (kQInRegs) {
 #pragma unroll
-      for (int jj = 0; jj < QPG / 2; ++jj)
-        ldsm_x4(qbase + (cg * (QPG / 2) + jj) * 512, qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj + 1][0],
-                qa[2 * jj + 1][1]);
+        for (int m = 0; m < QPG; ++m) {
+          qa[m][0] = qreg[cg * QPG + m][0];
+          qa[m][1] = qreg[cg * QPG + m][1];
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < QPG / 2; ++jj)
+          ldsm_x4(qbase + (cg * (QPG / 2) + jj) * 512, qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj + 1][0],
+                  qa[2 * jj + 1][1]);
+      }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         uint32_t w[4];
