@@ -53,6 +53,7 @@ namespace kvq {
 constexpr int kPage = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxStages = 32;
+constexpr int kMaxInflight = 160 * 1024;  // ring bytes a CTA keeps in flight
 
 template <int FMT, int D>
 struct DecodeTraits;
@@ -112,14 +113,19 @@ struct DecodeLayout {
   static constexpr int kHeadScale = kPage * T::kScaleRow;  // one head's K (or V) scale block of a page
   static constexpr int kKSteps = D / 16;
   static constexpr int kMTiles = D / 16;
-  // q fragments per consumer warp: [k-step][dA / dB part][8 head rows][8 halves]
+  // q fragments of one KV head (shared by that head's warps):
+  // [k-step][dA / dB part][8 head rows][8 halves]
   static constexpr int kQBytes = kKSteps * 2 * 128;
-  // shared-memory stage ring: what is left of 227 KB after alignment slack, the
-  // q tiles, the barriers and the page-id buffer
+  // Shared memory after the 1024-byte alignment slack: the stage ring and then
+  // one q tile per head of the group (kAvail bytes together; the ring gets what
+  // the group's hg tiles leave), then the barriers and the page-id buffer.
   static constexpr int kIdBytes = kMaxProducers * 2 * 32 * 4;
-  static constexpr int kRingBytes = (227 * 1024 - 1024 - kCW * kQBytes - 2 * kMaxStages * 8 - kIdBytes) / 1024 * 1024;
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kCW * kQBytes + 2 * kMaxStages * 8 + kIdBytes;
+  static constexpr int kAvail = (227 * 1024 - 1024 - 2 * kMaxStages * 8 - kIdBytes) / 1024 * 1024;
+  static constexpr int kSmemBytes = 1024 + kAvail + 2 * kMaxStages * 8 + kIdBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static __host__ __device__ constexpr int ring_bytes(int hg) { return (kAvail - hg * kQBytes) / 1024 * 1024; }
+  // the smallest ring (a group of kCW heads): the epilogue's buffers fit in any
+  static constexpr int kRingBytes = (kAvail - kCW * kQBytes) / 1024 * 1024;
   // epilogue exchange in the ring: each warp other than a head's first leaves its
   // accumulators (one float4 per lane and m-tile) and (m, l) of 8 head rows
   static constexpr int kPartOBytes = kMTiles * 32 * 16;
@@ -157,7 +163,11 @@ __host__ __device__ inline int decode_stages(int hg) {
   using Lo = DecodeLayout<FMT, D>;
   const int unit = decode_stage_unit<FMT, D>(hg);
   const int stage = 2 * hg * (Lo::kHeadCode + Lo::kHeadScale);
-  int n = Lo::kRingBytes / stage;
+  // at most kMaxInflight bytes a CTA: with every CTA asking for its whole ring at
+  // the start, a deeper ring only delays each CTA's first page (measured: 6
+  // stages of 33 KB took 1.6 us longer than 4 on the 32K batch-1 workload)
+  int n = Lo::ring_bytes(hg) / stage;
+  if (n > kMaxInflight / stage) n = kMaxInflight / stage;
   n = n < kMaxStages ? n : kMaxStages;
   return n / unit * unit;  // 0 if fewer than `unit` stages fit: such a group is not used
 }
@@ -228,8 +238,8 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* codes = smem;                                   // NST x [K heads][V heads]
   uint8_t* scales = smem + NST * stage_code;               // NST x [K heads][V heads]
-  uint8_t* qfrag = smem + Lo::kRingBytes;                  // CW x kQBytes
-  uint64_t* full = reinterpret_cast<uint64_t*>(qfrag + CW * Lo::kQBytes);
+  uint8_t* qfrag = smem + Lo::ring_bytes(HG);              // HG x kQBytes
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo::kAvail);
   uint64_t* empty = full + kMaxStages;
   int* pid_s = reinterpret_cast<int*>(empty + kMaxStages);  // [producer][2][32] page ids
 
@@ -448,7 +458,10 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 
   // ================================================================== consumers
   if constexpr (Lo::kRegSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Lo::kConsumerRegs));
-  uint8_t* myq = qfrag + warp * Lo::kQBytes;
+  // Every warp of a head writes the head's q tile itself, with the same bytes as
+  // the head's other warps, so its own writes already give it the whole tile;
+  // tiles are rewritten only after the item boundary barrier.
+  uint8_t* myq = qfrag + hl * Lo::kQBytes;
   const uint32_t qbase = smem_addr(myq) + ((lane >> 3) * 8 + (lane & 7)) * 16;
   // Per-lane byte offsets of the swizzled ldmatrix rows inside a head block,
   // one per value of (chunk & 7) of the iteration (the XOR with the row index
