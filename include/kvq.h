@@ -29,6 +29,11 @@
  *     (pools, workspace, outputs) and the stream; the library allocates nothing
  *     and, unless KVQ_CHECKED is given, never synchronizes, so raw calls can be
  *     captured into a CUDA graph.
+ *   - q, block_tables, seq_lens, out and lse_out of a decode call may instead be
+ *     pinned host memory (page-locked and known to CUDA, e.g. cudaHostAlloc): the
+ *     kernels then read and write it directly over the host link (NVLink-C2C on
+ *     Grace systems), with no separate copy.  Pageable host memory is refused.
+ *     Pools, plans and workspaces are device memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - Every call returns a kvq_status; on failure kvq_last_error() returns a
  *     message (thread-local).  No exception or abort crosses the ABI.

@@ -102,8 +102,8 @@ def _need(t, dtype, name, device=True):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if device and not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if device and not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
 
 
 # ----------------------------------------------------------------- host helpers

@@ -12,6 +12,7 @@
 #include <numeric>
 #include <queue>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "kvq_internal.h"
@@ -133,6 +134,19 @@ int make_code_map(CUtensorMap* map, void* base, int64_t num_pages, int64_t hkv, 
 // list start on 16-byte boundaries so the kernel can load a descriptor at once.
 int64_t plan_first_at(int64_t batch) { return (batch + 2 + 3) / 4 * 4; }
 int64_t plan_rest_at(int64_t batch, int64_t C) { return (plan_first_at(batch) + 5 * C + 1 + 3) / 4 * 4; }
+
+// Where a caller buffer lives: device (or managed) memory, or pinned host memory
+// the kernels reach over the host link (*host = 1).  Pageable host memory is
+// refused.
+int memory_kind(const void* ptr, const char* name, int32_t* host) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  if (a.type == cudaMemoryTypeUnregistered)
+    return fail(KVQ_ERR_INVALID_ARG, "%s is pageable host memory: pass device or pinned host memory", name);
+  if (host) *host = a.type == cudaMemoryTypeHost ? 1 : 0;
+  return KVQ_OK;
+}
 
 int heads_per_cta(const kvq_cache* c) {
   kvq::DecodeInstance inst;
@@ -459,6 +473,12 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool checked = flags & KVQ_CHECKED;
   if (checked) {
+    for (const auto& pr : {std::make_pair(q, "q"), std::make_pair(static_cast<const void*>(block_tables), "block_tables"),
+                           std::make_pair(static_cast<const void*>(seq_lens), "seq_lens"),
+                           std::make_pair(static_cast<const void*>(plan), "plan")}) {
+      rc = memory_kind(pr.first, pr.second, nullptr);
+      if (rc) return rc;
+    }
     // host-side validation of the plan against seq_lens (the kernel also checks
     // every descriptor it uses)
     const int hgc = heads_per_cta(cache);
@@ -537,6 +557,8 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   p.heads_per_cta = hg;
   p.out_bf16 = out_dtype == KVQ_OUT_BF16;
   p.early_start = (flags & KVQ_EARLY_START) ? 1 : 0;
+  rc = memory_kind(out, "out", &p.out_host);
+  if (rc) return rc;
   p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
   p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
   p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;

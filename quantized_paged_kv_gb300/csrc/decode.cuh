@@ -949,9 +949,15 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         const size_t row0 = direct ? (size_t)cw.b * p.num_q_heads + qh0 : (size_t)cw.split * p.num_q_heads + qh0;
         uint8_t* dst = direct ? reinterpret_cast<uint8_t*>(p.out) + row0 * row_bytes
                               : reinterpret_cast<uint8_t*>(p.o_part + row0 * D);
-        fence_proxy_async_smem();  // the staged rows, written by this warp, become visible to the copy
-        __syncwarp();
-        if (lane == 0) bulk_store(dst, stage, G * row_bytes);
+        if (direct && p.out_host) {  // host memory: plain 16-byte stores over the host link
+          __syncwarp();
+          for (int i = lane; i < G * row_bytes / 16; i += 32)
+            *reinterpret_cast<uint4*>(dst + (size_t)i * 16) = *reinterpret_cast<const uint4*>(stage + i * 16);
+        } else {
+          fence_proxy_async_smem();  // the staged rows, written by this warp, become visible to the copy
+          __syncwarp();
+          if (lane == 0) bulk_store(dst, stage, G * row_bytes);
+        }
       }
       if (c == 0 && r < G) {
         if (direct) {

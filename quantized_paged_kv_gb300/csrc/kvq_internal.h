@@ -27,6 +27,7 @@ struct DecodeParams {
   int32_t heads_per_cta;       // KV heads per work item (a divisor of num_kv_heads)
   int32_t out_bf16;
   int32_t early_start;         // read plan / block tables before waiting for the preceding kernel
+  int32_t out_host;            // out is pinned host memory: direct rows are written with plain stores
   float sm_scale_log2;         // sm_scale * log2(e)
   float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scale
 };

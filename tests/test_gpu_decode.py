@@ -247,3 +247,50 @@ def test_early_start_chain_in_a_graph_matches_plain_calls():
     torch.cuda.synchronize()
     for i in range(4):
         assert torch.equal(outs[i], refs[i % 2]), i
+
+
+@pytest.mark.parametrize("split", [1, 4])
+def test_pinned_host_buffers_give_the_device_result(split):
+    """q, block table, sequence lengths, out and lse_out in pinned host memory
+    (read and written by the kernels over the host link) give exactly the result
+    of device buffers, for direct (one split) and merged outputs."""
+    from quantized_paged_kv_gb300 import DecodePlan, decode
+
+    wl = W.make("tiny_int8", lens=("list", [700, 33, 4096]), seed=17)
+    cache = H.gpu_cache(wl, "int8")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=split)
+    q = torch.from_numpy(wl.q()).to(torch.bfloat16)
+    bt = torch.from_numpy(wl.block_tables)
+    sl = torch.from_numpy(wl.seq_lens)
+    for od in (torch.float32, torch.bfloat16):
+        o_d = torch.empty((wl.B, wl.Hq, wl.D), dtype=od, device="cuda")
+        l_d = torch.empty((wl.B, wl.Hq), device="cuda")
+        decode(cache, plan, q.cuda(), bt.cuda(), sl.cuda(), o_d, wl.sm_scale, lse_out=l_d, checked=True)
+        o_h = torch.full((wl.B, wl.Hq, wl.D), float("nan"), dtype=od).pin_memory()
+        l_h = torch.full((wl.B, wl.Hq), float("nan")).pin_memory()
+        decode(cache, plan, q.pin_memory(), bt.pin_memory(), sl.pin_memory(), o_h, wl.sm_scale, lse_out=l_h,
+               checked=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o_h, o_d.cpu())
+        assert torch.equal(l_h, l_d.cpu())
+
+
+def test_pageable_host_output_is_refused():
+    from quantized_paged_kv_gb300 import DecodePlan, KvqError, decode
+
+    wl = W.make("tiny_int8", lens=("list", [64]), seed=18)
+    cache = H.gpu_cache(wl, "int8")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq)
+    q = torch.from_numpy(wl.q()).to(torch.bfloat16).cuda()
+    out = torch.empty((wl.B, wl.Hq, wl.D))  # pageable
+    from quantized_paged_kv_gb300 import _binding as Bd
+    with pytest.raises(KvqError) as e:
+        Bd.lib()  # loaded
+        import ctypes
+        rc = Bd.lib().kvq_paged_decode_attention(
+            ctypes.byref(cache.struct), Bd._ptr(q), wl.B, wl.Hq, float(wl.sm_scale),
+            Bd._ptr(torch.from_numpy(wl.block_tables).cuda()), wl.block_tables.shape[1],
+            Bd._ptr(torch.from_numpy(wl.seq_lens).cuda()), Bd._ptr(plan.plan), plan.total_splits, plan.num_ctas,
+            Bd._ptr(plan.workspace), plan.workspace.numel(), Bd._ptr(out), Bd.KVQ_OUT_F32, None, 0, None)
+        Bd._check(rc, "kvq_paged_decode_attention")
+    assert e.value.code == 1 and "pageable" in str(e.value)
