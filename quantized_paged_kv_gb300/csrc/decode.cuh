@@ -148,7 +148,7 @@ struct DecodeLayout {
 template <int FMT, int D>
 __host__ __device__ inline int decode_producers(int hg) {
   const int wph = DecodeLayout<FMT, D>::kCW / hg;
-  return wph == 1 ? 2 : (wph <= 4 ? wph : (wph % 4 == 0 ? 4 : 3));
+  return wph == 1 ? 2 : (wph == 2 ? 4 : (wph <= 4 ? wph : (wph % 4 == 0 ? 4 : 3)));
 }
 
 template <int FMT, int D>
