@@ -26,6 +26,14 @@ uses those terms; averaging the partial outputs would be wrong.
           lse = M + log sum_s w_s;  a segment with no tokens has lse = -inf, weight 0.
 
 An empty context (L = 0) gives out = 0 and lse = -inf.
+
+Verification of several proposed tokens ("half-the-memory-int8-kv-cache", section
+"Read the compressed cache without copying it first": one program both generates
+a token and checks several proposed ones, 6 query tokens x 6 heads at a verify
+step): T query tokens of sequence b, whose K/V are already the last T entries of
+its cache (L_b tokens in all).  Reading: causal, as in any autoregressive check —
+query token i sits at position L_b - T + i and sees tokens 0 .. L_b - T + i, i.e.
+the decode above over the first max(0, L_b - T + i + 1) tokens.
 """
 from __future__ import annotations
 
@@ -132,6 +140,30 @@ def paged_decode(fmt, pools, q, block_tables, seq_lens, sm_scale, heads=None, pa
         o, s = attend(q[b, h * G:(h + 1) * G], k, v, sm_scale)
         out[b, h * G:(h + 1) * G] = o
         lse[b, h * G:(h + 1) * G] = s
+    return out, lse
+
+
+def paged_verify(fmt, pools, q, block_tables, seq_lens, sm_scale, units=None, page_size=16):
+    """Attention for T query tokens a sequence over a paged pool, causal (module
+    docstring).  q: [B, T, Hq, D].  units: optional list of (b, i, kv_head) to
+    compute (others stay NaN).  Returns (out [B, T, Hq, D], lse [B, T, Hq])."""
+    q = np.asarray(q, dtype=np.float64)
+    B, T, Hq, D = q.shape
+    Hkv = pools["k_codes"].shape[1]
+    G = Hq // Hkv
+    out = np.full((B, T, Hq, D), np.nan)
+    lse = np.full((B, T, Hq), np.nan)
+    gk = pools.get("k_global_scale", 1.0)
+    gv = pools.get("v_global_scale", 1.0)
+    todo = units if units is not None else [(b, i, h) for b in range(B) for i in range(T) for h in range(Hkv)]
+    for (b, i, h) in todo:
+        visible = max(0, int(seq_lens[b]) - T + i + 1)
+        slots = layout.token_slots(block_tables[b], visible, page_size)
+        k = cache_rows(fmt, pools["k_codes"], pools.get("k_scales"), slots, h, gk)
+        v = cache_rows(fmt, pools["v_codes"], pools.get("v_scales"), slots, h, gv)
+        o, s = attend(q[b, i, h * G:(h + 1) * G], k, v, sm_scale)
+        out[b, i, h * G:(h + 1) * G] = o
+        lse[b, i, h * G:(h + 1) * G] = s
     return out, lse
 
 

@@ -314,3 +314,49 @@ def check_attention_invariants(attend, probabilities, seed=8):
     kd[17] = q[0] * 1e3
     o, _ = attend(q[:1], kd, v, 1.0)
     assert np.max(np.abs(o[0] - v[17])) < 1e-12
+
+
+def check_verify(paged_verify, seed=9):
+    """Causal verification against pure-Python attention over each query token's
+    visible prefix (tiny pools, brute force), and its single-token case against
+    decode-style attention over the whole sequence."""
+    from oracle import brute
+    from oracle import layout as olay
+
+    rng = np.random.default_rng(seed)
+    P, Hkv, G, D = 4, 2, 3, 8
+    for (lens, T) in [([9, 5], 3), ([4], 4), ([2, 7], 3), ([6], 1)]:
+        B = len(lens)
+        npages = sum(-(-L // P) for L in lens)
+        perm = rng.permutation(npages)
+        bt = np.full((B, max(-(-L // P) for L in lens)), -1, dtype=np.int32)
+        o = 0
+        for b, L in enumerate(lens):
+            n = -(-L // P)
+            bt[b, :n] = perm[o:o + n]
+            o += n
+        # INT8 codes with per-row scales; the brute force dequantizes by c * s itself
+        kc = rng.integers(-127, 128, (npages, Hkv, P, D)).astype(np.int8)
+        vc = rng.integers(-127, 128, (npages, Hkv, P, D)).astype(np.int8)
+        ks = rng.uniform(0.001, 0.05, (npages, Hkv, P)).astype(np.float32)
+        vs = rng.uniform(0.001, 0.05, (npages, Hkv, P)).astype(np.float32)
+        kx = kc.astype(np.float64) * ks.astype(np.float64)[..., None]
+        vx = vc.astype(np.float64) * vs.astype(np.float64)[..., None]
+        pools = {"k_codes": kc.view(np.uint8), "v_codes": vc.view(np.uint8), "k_scales": ks, "v_scales": vs}
+        q = rng.standard_normal((B, T, G * Hkv, D))
+        sm = 1.0 / math.sqrt(D)
+        out, lse = paged_verify("int8", pools, q, bt, np.array(lens), sm, page_size=P)
+        for b, L in enumerate(lens):
+            for i in range(T):
+                vis = max(0, L - T + i + 1)
+                slots = olay.token_slots(bt[b], vis, P)
+                for h in range(Hkv):
+                    kr = [list(kx[s // P, h, s % P]) for s in slots]
+                    vr = [list(vx[s // P, h, s % P]) for s in slots]
+                    qs = q[b, i, h * G:(h + 1) * G].tolist()
+                    if vis == 0:
+                        assert np.all(out[b, i, h * G:(h + 1) * G] == 0) and np.all(np.isneginf(lse[b, i, h * G:(h + 1) * G]))
+                        continue
+                    ob, sb = brute.attend_brute(qs, kr, vr, sm)
+                    assert np.max(np.abs(out[b, i, h * G:(h + 1) * G] - np.array(ob))) < 1e-12
+                    assert np.max(np.abs(lse[b, i, h * G:(h + 1) * G] - np.array(sb))) < 1e-12

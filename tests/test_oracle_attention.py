@@ -78,3 +78,7 @@ def test_paged_decode_equals_dense_attend_over_dequantized_rows():
         v = attention.cache_rows("int8", pools["v_codes"], pools["v_scales"], slots, h)
         ob, sb = brute.attend_brute(q[0, h * G:(h + 1) * G].tolist(), k.tolist(), v.tolist(), 0.25)
         assert np.max(np.abs(o[0, h * G:(h + 1) * G] - np.array(ob))) < 1e-12
+
+
+def test_verify_matches_brute_force_over_each_visible_prefix():
+    pins.check_verify(attention.paged_verify)

@@ -94,6 +94,22 @@ def test_attention_mutants_are_caught():
         p = attention.probabilities(q, k, sm)
         return o, s - np.log(1.0 / p.max(axis=1)) * 0 + 0.5
 
+    def verify_off_by_one(fmt, pools, q, bt, lens, sm, page_size=16):
+        # each query token sees one token too few
+        return attention.paged_verify(fmt, pools, q, bt, np.asarray(lens) - 1, sm, page_size=page_size)
+
+    def verify_tokens_swapped(fmt, pools, q, bt, lens, sm, page_size=16):
+        # query token i paired with token T-1-i's visible prefix
+        return attention.paged_verify(fmt, pools, q[:, ::-1], bt, lens, sm, page_size=page_size)
+
+    def verify_sees_all(fmt, pools, q, bt, lens, sm, page_size=16):
+        B, T = q.shape[:2]
+        outs = [attention.paged_verify(fmt, pools, q[:, i:i + 1], bt, lens, sm, page_size=page_size) for i in range(T)]
+        return np.concatenate([o for o, _ in outs], axis=1), np.concatenate([s for _, s in outs], axis=1)
+
+    _fails(pins.check_verify, verify_off_by_one)
+    _fails(pins.check_verify, verify_tokens_swapped)
+    _fails(pins.check_verify, verify_sees_all)
     _fails(pins.check_attend_brute, no_scale, brute.attend_brute)
     _fails(pins.check_attend_brute, transposed_v, brute.attend_brute)
     _fails(pins.check_attend_brute, lse_without_log, brute.attend_brute)
