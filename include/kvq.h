@@ -6,7 +6,8 @@
  *   kvq_quant_append            quantize new K/V rows and scatter them into pool slots
  *   kvq_paged_decode_attention  split-KV (flash-decoding) GQA decode attention that
  *                               reads the quantized pages directly
- *   kvq_paged_decode_attention_static  the same, with library-owned scratch
+ *   kvq_paged_verify_attention  the same for several query tokens a sequence (causal)
+ *   kvq_paged_decode_attention_static  the decode with library-owned scratch
  *   kvq_split_merge             log-sum-exp combine of the per-split partial results
  *
  * plus host helpers (byte accounting, split planning, workspace sizing, errors).
@@ -253,6 +254,41 @@ int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_
  * Supported: num_q_heads % num_kv_heads == 0 and 1 <= num_q_heads/num_kv_heads <= 8.
  */
 int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t batch,
+                               int32_t num_q_heads, float sm_scale,
+                               const int32_t* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, const int32_t* plan,
+                               int32_t total_splits, int32_t num_ctas,
+                               void* workspace, size_t workspace_bytes,
+                               void* out, int32_t out_dtype, float* lse_out,
+                               uint32_t flags, void* stream);
+
+/* ---- paged_verify_attention ([int8-kv] "Read the compressed cache without
+ *      copying it first": one program both generates a token and checks several
+ *      proposed ones; a verify step reads the whole context with 6 query tokens,
+ *      36 query rows for 6 heads, and an MMA kernel of 8-row granularity avoids
+ *      padding them) --------------------------------------------------------- */
+/*
+ * Causal attention for q_len query tokens a sequence whose K/V are already the
+ * last q_len entries of its cache (seq_lens[b] tokens in all, appended by
+ * kvq_quant_append): query token i of sequence b sits at position
+ * seq_lens[b] - q_len + i and attends over tokens 0 .. seq_lens[b] - q_len + i
+ * (none when that is negative: out = 0, lse = -inf).  The same kernels as
+ * kvq_paged_decode_attention, run over batch * q_len virtual sequences — token i
+ * of sequence b is virtual sequence b * q_len + i, with b's block table — so every
+ * MMA tile holds the G query heads of one token (8-row granularity), and the
+ * q_len tokens' items cover the same pages at about the same time, so a page
+ * read for one token is mostly still in L2 for the others.
+ *   q              device bf16 [batch][q_len][num_q_heads][head_dim]
+ *   seq_lens       device int32 [batch]: tokens in the cache, the q_len new ones included
+ *   plan           kvq_plan_splits over the batch * q_len virtual lengths
+ *                  max(0, seq_lens[b] - q_len + 1 + i), in order b * q_len + i
+ *   workspace      >= kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim)
+ *   out            device [batch][q_len][num_q_heads][head_dim] float or bf16
+ *   lse_out        device float [batch][q_len][num_q_heads] (nullable)
+ * Everything else (flags included) as for kvq_paged_decode_attention; q_len = 1
+ * is exactly kvq_paged_decode_attention.
+ */
+int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t batch, int32_t q_len,
                                int32_t num_q_heads, float sm_scale,
                                const int32_t* block_tables, int32_t max_pages_per_seq,
                                const int32_t* seq_lens, const int32_t* plan,

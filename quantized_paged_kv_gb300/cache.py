@@ -77,3 +77,19 @@ def decode(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, 
              | (B.KVQ_EARLY_START if early_start else 0))
     B.kvq_paged_decode_attention(cache.struct, q, sm_scale, block_tables, seq_lens, plan.plan, plan.total_splits,
                                  plan.num_ctas, plan.workspace, out, lse_out, flags, stream)
+
+
+def verify_lengths(seq_lens, q_len):
+    """Visible tokens of the batch * q_len virtual sequences of a verify call, in
+    the order b * q_len + i: max(0, L_b - q_len + 1 + i)."""
+    return [max(0, int(L) - q_len + 1 + i) for L in seq_lens for i in range(q_len)]
+
+
+def verify(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, checked=False, skip_merge=False,
+           early_start=False, stream=None):
+    """Causal attention for q.shape[1] query tokens a sequence; plan: DecodePlan over
+    verify_lengths(seq_lens, q_len)."""
+    flags = ((B.KVQ_CHECKED if checked else 0) | (B.KVQ_SKIP_MERGE if skip_merge else 0)
+             | (B.KVQ_EARLY_START if early_start else 0))
+    B.kvq_paged_verify_attention(cache.struct, q, sm_scale, block_tables, seq_lens, plan.plan, plan.total_splits,
+                                 plan.num_ctas, plan.workspace, out, lse_out, flags, stream)

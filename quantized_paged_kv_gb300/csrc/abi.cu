@@ -443,14 +443,24 @@ int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_
   return succeed();
 }
 
-int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t batch, int32_t num_q_heads,
-                               float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq,
-                               const int32_t* seq_lens, const int32_t* plan, int32_t total_splits,
-                               int32_t num_ctas, void* workspace, size_t workspace_bytes, void* out,
-                               int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode (q_len = 1) or causal verification of q_len tokens a sequence: the
+// launch works on batch = nseq x q_len virtual sequences (query token i of cache
+// sequence b is virtual sequence b * q_len + i, with b's block table and
+// L_b - q_len + 1 + i visible tokens).
+int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_len, int32_t num_q_heads,
+                float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                const int32_t* plan, int32_t total_splits, int32_t num_ctas, void* workspace, size_t workspace_bytes,
+                void* out, int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
   int rc = check_cache(cache, true);
   if (rc) return rc;
-  if (batch < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", batch);
+  if (nseq < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", nseq);
+  if (q_len < 1) return fail(KVQ_ERR_INVALID_ARG, "q_len %d < 1", q_len);
+  if ((int64_t)nseq * q_len > 0x7FFFFFFF / 4) return fail(KVQ_ERR_UNSUPPORTED, "batch x q_len too large");
+  const int32_t batch = nseq * q_len;  // virtual sequences of the launch
   if (!q || !block_tables || !seq_lens || !plan || !workspace || !out)
     return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer argument");
   if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
@@ -489,12 +499,16 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
     const int64_t A = plan_first_at(batch), roff_at = A + 4 * (int64_t)num_ctas;
     const int64_t rest_at = plan_rest_at(batch, num_ctas);
     std::vector<int32_t> h(rest_at + 4 * (n_items - num_ctas));
-    std::vector<int32_t> lens(batch);
+    std::vector<int32_t> real(nseq), lens(batch);
     cudaError_t e = cudaMemcpyAsync(h.data(), plan, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(lens.data(), seq_lens, lens.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+      e = cudaMemcpyAsync(real.data(), seq_lens, real.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "reading plan");
+    for (int b = 0; b < nseq; ++b) {
+      if (real[b] < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_lens[%d] = %d < 0", b, real[b]);
+      for (int i = 0; i < q_len; ++i) lens[b * q_len + i] = std::max(0, real[b] - (q_len - 1 - i));
+    }
     if (h[0] != 0 || h[batch] != total_splits) return fail(KVQ_ERR_INVALID_ARG, "plan offsets do not span total_splits");
     for (int b = 0; b < batch; ++b)
       if (h[b + 1] <= h[b]) return fail(KVQ_ERR_INVALID_ARG, "plan gives sequence %d no split", b);
@@ -512,11 +526,11 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
       const int n = d[3] & 0x7FFFFF, direct = (d[3] >> 23) & 1, g = (uint32_t)d[3] >> 24;
       if (b < 0 || b >= batch || split < h[b] || split >= h[b + 1] || g >= nhg_checked)
         return fail(KVQ_ERR_INVALID_ARG, "plan item %lld names a bad sequence / split / head group", (long long)i);
-      if (lens[b] < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_lens[%d] = %d < 0", b, lens[b]);
       const int64_t S = h[b + 1] - h[b], sidx = split - h[b];
       const int64_t np = (lens[b] + cache->page_size - 1) / cache->page_size;
       if (pb != sidx * np / S || n != (sidx + 1) * np / S - pb || direct != (S == 1 ? 1 : 0))
-        return fail(KVQ_ERR_INVALID_ARG, "plan item %lld does not match seq_lens[%d] = %d", (long long)i, b, lens[b]);
+        return fail(KVQ_ERR_INVALID_ARG, "plan item %lld does not match sequence %d's %d visible tokens", (long long)i,
+                    b, lens[b]);
       if (pb + n > max_pages_per_seq)
         return fail(KVQ_ERR_INVALID_ARG, "plan item %lld runs past the block table", (long long)i);
       const int64_t key = (int64_t)split * nhg_checked + g;
@@ -557,6 +571,7 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
   p.heads_per_cta = hg;
   p.out_bf16 = out_dtype == KVQ_OUT_BF16;
   p.early_start = (flags & KVQ_EARLY_START) ? 1 : 0;
+  p.q_len = q_len;
   rc = memory_kind(out, "out", &p.out_host);
   if (rc) return rc;
   p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
@@ -576,6 +591,28 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
     if (rc) return rc;
   }
   return succeed();
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t batch, int32_t num_q_heads,
+                               float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, const int32_t* plan, int32_t total_splits,
+                               int32_t num_ctas, void* workspace, size_t workspace_bytes, void* out,
+                               int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
+  return decode_impl(cache, q, batch, 1, num_q_heads, sm_scale, block_tables, max_pages_per_seq, seq_lens, plan,
+                     total_splits, num_ctas, workspace, workspace_bytes, out, out_dtype, lse_out, flags, stream);
+}
+
+int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t batch, int32_t q_len,
+                               int32_t num_q_heads, float sm_scale, const int32_t* block_tables,
+                               int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* plan,
+                               int32_t total_splits, int32_t num_ctas, void* workspace, size_t workspace_bytes,
+                               void* out, int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
+  return decode_impl(cache, q, batch, q_len, num_q_heads, sm_scale, block_tables, max_pages_per_seq, seq_lens, plan,
+                     total_splits, num_ctas, workspace, workspace_bytes, out, out_dtype, lse_out, flags, stream);
 }
 
 int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* split_offsets, int32_t batch,

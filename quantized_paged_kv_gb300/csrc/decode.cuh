@@ -279,13 +279,19 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     return w.b >= 0 && w.b < p.batch && w.split >= 0 && w.split < p.total_splits && w.hg < NHG &&
            w.page_begin >= 0 && w.page_begin <= p.max_pages - w.n;
   };
-  auto seq_len = [&](int b) -> int {  // tokens of sequence b, clamped to its block table
-    int L = p.seq_lens[b];
+  // Sequence b of the launch is query token i = b % q_len of cache sequence
+  // b / q_len (one token a sequence when decoding).  Token i of T sits at position
+  // L - T + i of its sequence and sees tokens 0 .. L - T + i: causal verification
+  // of T proposed tokens whose K/V are the last T entries of the cache.
+  auto seq_len = [&](int b) -> int {  // visible tokens of launch sequence b, clamped to its block table
+    const int rb = b / p.q_len;
+    int L = p.seq_lens[rb];
     if (L < 0 || L > p.max_pages * kPage) {
       if (threadIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
       L = L < 0 ? 0 : p.max_pages * kPage;
     }
-    return L;
+    L -= p.q_len - 1 - (b - rb * p.q_len);
+    return L > 0 ? L : 0;
   };
 
   const int warp = threadIdx.x >> 5;
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     auto page_id = [&](const Item& w, int j) -> int {
       int v = -1;
       if (j < mine_of(w)) {
-        v = p.block_tables[(size_t)w.b * p.max_pages + w.page_begin + pi + NP * j];
+        v = p.block_tables[(size_t)(w.b / p.q_len) * p.max_pages + w.page_begin + pi + NP * j];
         if (v < 0 || v >= p.num_pages) {
           atomicOr(p.status, KVQ_DEV_BAD_PAGE);
           v = -1;

@@ -24,6 +24,7 @@ struct DecodeParams {
   float* lse_out;              // [B][Hq] or null
   int32_t* status;             // device status word
   int32_t batch, num_q_heads, num_kv_heads, max_pages, num_pages, total_splits;
+  int32_t q_len;               // query tokens a sequence: batch = sequences x q_len virtual sequences
   int32_t heads_per_cta;       // KV heads per work item (a divisor of num_kv_heads)
   int32_t out_bf16;
   int32_t early_start;         // read plan / block tables before waiting for the preceding kernel

@@ -22,6 +22,7 @@ Workload recipes (name -> what is drawn):
                 (8192 in all) are the "new" tokens written by one append call.
   long_nvfp4    B=12, Hq=24, Hkv=4, D=256, L_b = floor(exp(U(ln 4096, ln 131072)));
                 q, K, V ~ N(0,1); per-tensor NVFP4 global scale 448*6/amax(tensor).
+  (any)         q_tokens(T): T query tokens a sequence for a verify step, N(0,1).
 """
 from __future__ import annotations
 
@@ -79,6 +80,11 @@ class Workload:
     def q(self):
         g = _rng(self.seed, 1)
         return bf16_round(g.standard_normal((self.B, self.Hq, self.D), dtype=np.float32))
+
+    def q_tokens(self, T):
+        """Queries of T tokens a sequence (a verify step): bf16 values [B, T, Hq, D]."""
+        g = _rng(self.seed, 6, T)
+        return bf16_round(g.standard_normal((self.B, T, self.Hq, self.D), dtype=np.float32))
 
     def _outlier_channels(self, which):
         g = _rng(self.seed, 2, which)
