@@ -52,6 +52,7 @@ def parse():
                          "decode calls over them and exit (no timing)")
     ap.add_argument("--fmt", default="int8", choices=["int8", "nvfp4", "bf16"])
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--verify-tokens", type=int, default=0, help="profiling case: verify calls of this many tokens")
     return ap.parse_args()
 
 
@@ -226,6 +227,49 @@ def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=
     if barrier:
         barrier()
     return e0.elapsed_time(e1) * 1e-3 / (reps * ls.R), reps * ls.R, clocks
+
+
+def time_verify(ls, T, steps, warmup=16):
+    """Verify calls (T query tokens a sequence, causal) over the R layer pools in
+    one CUDA graph; KV GB/s counts each page once."""
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+
+    wl = ls.wl
+    plan = kvq.DecodePlan(ls.caches[0], kvq.verify_lengths(wl.seq_lens, T), wl.Hq, device=ls.device)
+    q = torch.from_numpy(wl.q_tokens(T)).to(torch.bfloat16).to(ls.device)
+    out = torch.empty((wl.B, T, wl.Hq, wl.D), dtype=ls.out.dtype, device=ls.device)
+    stream = torch.cuda.Stream()
+
+    def one(r):
+        kvq.verify(ls.caches[r], plan, q, ls.bt, ls.sl, out, wl.sm_scale, early_start=True)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for r in range(ls.R):
+            one(r)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for r in range(ls.R):
+            one(r)
+    reps = max(1, math.ceil(steps / ls.R))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / ls.R))):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * ls.R)
+    nbytes = ls.kv_bytes()
+    return {"us": round(t * 1e6, 3), "GBps": round(nbytes / t / 1e9, 1), "splits": plan.total_splits,
+            "query_rows": T * wl.Hq, "note": "KV bytes counted once per call"}
 
 
 def time_e2e(ls, plan, steps, warmup=3):
@@ -463,6 +507,16 @@ def sweep(args, dev, l2, peak):
     measure(wl, "nvfp4", (0,), gs, tag="long_nvfp4(gs=1)")
     measure(wl, "int8", (0,))
     measure(wl, "bf16", (0,))
+    # verify step: 6 query tokens a sequence over the 32K context (the pages' verify shape)
+    wl = W.make("long_int8")
+    per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token("int8", wl.Hkv, wl.D)
+    R = layers_for(per_layer, l2, floor=2)
+    ls = LayerSet(wl, "int8", R, dev)
+    for T in (2, 6):
+        res[f"verify_long_int8/T={T}"] = time_verify(ls, T, steps)
+    del ls
+    gc.collect()
+    torch.cuda.empty_cache()
     # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences)
     wl = W.make("append_int8")
     cache = kvq.KVCache("int8", wl.num_pages, wl.Hkv, wl.D, device=dev, fill=0)
@@ -553,8 +607,16 @@ def run_ncu_case(args):
     R = max(1, math.ceil(1.1 * l2 / max(per_layer, 1)))
     ls = LayerSet(wl, args.fmt, R, "cuda")  # NVFP4 global scale 1 (it does not change the work)
     plan = ls.plan(0)
-    for i in range(args.calls):
-        ls.call(i % R, plan)
+    if args.verify_tokens:
+        T = args.verify_tokens
+        plan = kvq.DecodePlan(ls.caches[0], kvq.verify_lengths(wl.seq_lens, T), wl.Hq)
+        q = torch.from_numpy(wl.q_tokens(T)).to(torch.bfloat16).cuda()
+        out = torch.empty((wl.B, T, wl.Hq, wl.D), dtype=ls.out.dtype, device="cuda")
+        for i in range(args.calls):
+            kvq.verify(ls.caches[i % R], plan, q, ls.bt, ls.sl, out, wl.sm_scale)
+    else:
+        for i in range(args.calls):
+            ls.call(i % R, plan)
     torch.cuda.synchronize()
     print(json.dumps({"ncu_case": args.ncu_case, "fmt": args.fmt, "layers": R, "calls": args.calls,
                       "total_splits": plan.total_splits, "num_ctas": plan.num_ctas,
