@@ -11,22 +11,26 @@
 // for a whole group of query heads).
 //
 // Work item: one split (a range of whole pages) of one sequence for a group of
-// HG consecutive KV heads, HG = gcd(Hkv, CW) where CW is the number of consumer
-// warps (8 at D = 256, 12 at D = 128).  CTAs are persistent, one per SM: the host
-// planner packs the items onto the CTAs (longest first, each to the least-loaded
-// CTA) and every CTA works through its list, so a batch of uneven sequences
-// runs in one wave.  The pool keeps the
-// KV heads of a page next to each other, so the HG heads' code blocks of a page
-// are one contiguous region and travel as ONE TMA box per tensor (16 KB at
-// D = 256 INT8 with 4 heads); a 1-D bulk copy brings their scales.  Few large
-// copies per page keep a single producer thread ahead of the consumers.
+// HG consecutive KV heads, HG = gcd(Hkv, CW) (or a divisor of it that leaves the
+// ring at least two stages), where CW is the number of consumer warps (8 at
+// D = 256, 12 at D = 128).  CTAs are persistent, one per SM: the host planner
+// packs the items onto the CTAs (longest first, each to the least-loaded CTA)
+// and every CTA works through its list, so a batch of uneven sequences runs in
+// one wave; each CTA's first item descriptor sits at a fixed place in the plan.
+// The pool keeps the KV heads of a page next to each other, so the HG heads'
+// code blocks of a page are one contiguous region and travel as ONE TMA box per
+// tensor (16 KB at D = 256 INT8 with 4 heads); a 1-D bulk copy brings their
+// scales.  Few large copies per page keep the producers ahead of the consumers.
+// A launch sequence may also be one query token of a verify call (several
+// query tokens a cache sequence, causal): see seq_len below.
 //
-//   * warps CW.. (2 to 4 producers): producer i walks every NP-th page of the
-//     item through the block table (page ids staged in shared memory 32 at a
-//     time by its warp); its lane 0, per page, waits for the stage to be free,
-//     then issues the K and V boxes (128-byte swizzle) and the two scale copies,
-//     completing on the stage's mbarrier (expect-tx bytes).  Several producers
-//     are needed because one thread issues only about one copy per 300 ns.
+//   * warps CW..CW+3 (2 or 4 of them produce): producer i walks every NP-th page
+//     of the item through the block table (page ids staged in shared memory 32
+//     at a time by its warp); its lane 0, per page, waits for the stage to be
+//     free, then issues the K and V boxes (128-byte swizzle) and the two scale
+//     copies, completing on the stage's mbarrier (expect-tx bytes).  Several
+//     producers share the issuing because one thread issues only about one copy
+//     per 300 ns.  The ring keeps at most kMaxInflight bytes in flight.
 //   * warps 0..CW-1 (consumers): warp w owns KV head w % HG and, if CW / HG > 1,
 //     every (CW/HG)-th page.  Per page (16 tokens) a warp computes S = q K^T for
 //     its G <= 8 query heads with mma.m16n8k16 (heads are the M rows, tokens the N
@@ -38,8 +42,15 @@
 //     into P (V); NVFP4 group scales multiply the operands (products of an E2M1
 //     and an E4M3 value are exact in f16).  P' is split into hi + lo halves of two
 //     MMAs, so P carries ~22 bits.
-//   * epilogue: the warps of a head merge (m, l, O) in shared memory; a sequence
-//     with one split writes `out` directly, otherwise (o, lse) partials.
+//   * registers: the producer warpgroup gives registers back (setmaxnreg) and
+//     the consumer warpgroups take them (INT8 / BF16; NVFP4 keeps the launch
+//     split).
+//   * epilogue: the other warps of a head leave their (m, l, O) in the idle ring
+//     and the head's first warp combines them; it stages the head's query rows
+//     and writes them with one bulk copy — `out` directly for a sequence with one
+//     split, otherwise the (o, lse) partials the merge kernel combines.
+//   * start-up: the kernel is a programmatic dependent of the preceding kernel;
+//     with KVQ_EARLY_START it reads the plan and page ids before waiting for it.
 //
 // All waits are bounded (%globaltimer); on timeout the kernel sets
 // KVQ_DEV_TIMEOUT in the status word and stops instead of spinning.
@@ -140,7 +151,8 @@ struct DecodeLayout {
 // thread issues about one copy per 300 ns whatever its size, so several producer
 // warps share the issuing: page i of an item is issued by producer i % NP and
 // consumed by the head's warp i % WPH (WPH = warps per head).  The stage count is
-// as large as the ring allows (at most kMaxStages) and a multiple of both, so
+// as large as the ring and kMaxInflight allow (at most kMaxStages) and a multiple
+// of both, so
 // within an item every stage has a fixed producer and a fixed set of consumer
 // warps, each of which handled the stage's previous page itself before waiting on
 // the next one: a parity wait can never be satisfied by a barrier that is still
