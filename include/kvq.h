@@ -7,6 +7,7 @@
  *   kvq_paged_decode_attention  split-KV (flash-decoding) GQA decode attention that
  *                               reads the quantized pages directly
  *   kvq_paged_verify_attention  the same for several query tokens a sequence (causal)
+ *   kvq_paged_prefill_attention causal attention of a prompt chunk over the cache
  *   kvq_paged_decode_attention_static  the decode with library-owned scratch
  *   kvq_split_merge             log-sum-exp combine of the per-split partial results
  *
@@ -296,6 +297,38 @@ int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t ba
                                void* workspace, size_t workspace_bytes,
                                void* out, int32_t out_dtype, float* lse_out,
                                uint32_t flags, void* stream);
+
+/* ---- paged_prefill_attention ([int8-kv] "Read the prompt using a small temporary
+ *      buffer": a chunk of prompt tokens reuses every key it reads many times, the
+ *      cached history is read in sections whose partial results are combined with
+ *      their attention weights, and each token sees only the tokens before it and
+ *      itself) ---------------------------------------------------------------- */
+/*
+ * Causal attention of a prompt chunk: q holds the last q_len of one sequence's
+ * seq_len tokens (their K/V already appended); chunk token i sits at position
+ * seq_len - q_len + i and attends over tokens 0 .. seq_len - q_len + i of the
+ * cache, read in place (no converted copy: codes enter the tensor cores as exact
+ * integers, as in the decode).  A work item is 128 query rows (token, query head)
+ * of one KV head against one of `splits` key ranges; with splits > 1 the
+ * partials are combined by the merge kernel on the same stream.  INT8 and BF16
+ * caches, head_dim 128 or 256, 1 <= num_q_heads / num_kv_heads <= 8.
+ *   q              device bf16 [q_len][num_q_heads][head_dim]
+ *   block_table    device int32 [max_pages]: the sequence's pages
+ *   seq_len        host: tokens of the sequence, the q_len new ones included
+ *   splits         1 .. 64 key ranges (kvq_prefill_splits gives a default)
+ *   workspace      device, >= kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, splits),
+ *                  256-byte aligned; its first word is the device status word
+ *   out            device [q_len][num_q_heads][head_dim] float or bf16
+ *   lse_out        device float [q_len][num_q_heads] (nullable)
+ *   flags          KVQ_CHECKED: synchronize and read the status word
+ */
+int32_t kvq_prefill_splits(const kvq_cache* cache, int32_t q_len, int32_t num_q_heads, int32_t seq_len,
+                           int32_t target_ctas);  /* >= 1, or minus a kvq_status */
+size_t kvq_prefill_workspace_bytes(int32_t q_len, int32_t num_q_heads, int32_t head_dim, int32_t splits);
+int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q_len, int32_t num_q_heads,
+                                float sm_scale, const int32_t* block_table, int32_t max_pages, int32_t seq_len,
+                                int32_t splits, void* workspace, size_t workspace_bytes, void* out,
+                                int32_t out_dtype, float* lse_out, uint32_t flags, void* stream);
 
 /* ---- paged_decode_attention_static (no counterpart in the pages: an
  *      allocation-free variant of kvq_paged_decode_attention) ----------------- */

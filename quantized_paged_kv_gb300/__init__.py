@@ -14,4 +14,4 @@ from ._binding import (  # noqa: F401
     kvq_paged_decode_attention_static, kvq_paged_verify_attention, kvq_read_status, kvq_split_merge,
     kvq_workspace_partials, lib,
 )
-from .cache import DecodePlan, KVCache, decode, verify, verify_lengths  # noqa: F401
+from .cache import DecodePlan, KVCache, decode, prefill, verify, verify_lengths  # noqa: F401

@@ -28,7 +28,8 @@ FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4}
 EXPORTS = (
     "kvq_bytes_per_token", "kvq_cache_array_bytes", "kvq_quant_append", "kvq_plan_splits",
     "kvq_decode_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
-    "kvq_paged_decode_attention_static", "kvq_paged_verify_attention", "kvq_split_merge", "kvq_read_status",
+    "kvq_paged_decode_attention_static", "kvq_paged_verify_attention", "kvq_prefill_splits",
+    "kvq_prefill_workspace_bytes", "kvq_paged_prefill_attention", "kvq_split_merge", "kvq_read_status",
     "kvq_last_error",
 )
 
@@ -75,6 +76,10 @@ def lib():
         "kvq_paged_verify_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_int32, c_float, P,
                                                  c_int32, P, P, c_int32, c_int32, P, c_size_t, P, c_int32, P,
                                                  c_uint32, P]),
+        "kvq_prefill_splits": (c_int32, [POINTER(KvqCacheStruct), c_int32, c_int32, c_int32, c_int32]),
+        "kvq_prefill_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),
+        "kvq_paged_prefill_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P, c_int32,
+                                                  c_int32, c_int32, P, c_size_t, P, c_int32, P, c_uint32, P]),
         "kvq_split_merge": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P, c_int32, P, P]),
         "kvq_read_status": (c_int32, [P, P, POINTER(c_int32)]),
         "kvq_last_error": (ctypes.c_char_p, []),
@@ -234,6 +239,36 @@ def kvq_paged_verify_attention(cache_struct, q, sm_scale, block_tables, seq_lens
         ctypes.byref(cache_struct), _ptr(q), B, T, Hq, float(sm_scale), _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), _ptr(plan), total_splits, num_ctas, _ptr(workspace), workspace.numel(), _ptr(out), od,
         _ptr(lse_out), flags, _stream(stream)), "kvq_paged_verify_attention")
+
+
+def kvq_prefill_splits(cache_struct, q_len, num_q_heads, seq_len, target_ctas=0):
+    n = int(lib().kvq_prefill_splits(ctypes.byref(cache_struct), q_len, num_q_heads, seq_len, target_ctas))
+    if n < 1:
+        _check(-n, "kvq_prefill_splits")
+    return n
+
+
+def kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, splits):
+    return int(lib().kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, splits))
+
+
+def kvq_paged_prefill_attention(cache_struct, q, sm_scale, block_table, seq_len, splits, workspace, out,
+                                lse_out=None, flags=0, stream=None):
+    """q: bf16 [T, Hq, D] (the last T tokens of the sequence); block_table: int32 [max_pages]."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(workspace, torch.uint8, "workspace")
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    _need(out, out.dtype, "out")
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out")
+    T, Hq, _ = q.shape
+    od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
+    _check(lib().kvq_paged_prefill_attention(
+        ctypes.byref(cache_struct), _ptr(q), T, Hq, float(sm_scale), _ptr(block_table), block_table.numel(),
+        int(seq_len), splits, _ptr(workspace), workspace.numel(), _ptr(out), od, _ptr(lse_out), flags,
+        _stream(stream)), "kvq_paged_prefill_attention")
 
 
 def kvq_split_merge(o_part_ptr, lse_part_ptr, split_offsets, batch, num_q_heads, head_dim, out, lse_out=None,

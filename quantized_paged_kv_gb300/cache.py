@@ -93,3 +93,19 @@ def verify(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, 
              | (B.KVQ_EARLY_START if early_start else 0))
     B.kvq_paged_verify_attention(cache.struct, q, sm_scale, block_tables, seq_lens, plan.plan, plan.total_splits,
                                  plan.num_ctas, plan.workspace, out, lse_out, flags, stream)
+
+
+def prefill(cache, q, block_table, seq_len, out, sm_scale, lse_out=None, splits=0, workspace=None, checked=False,
+            stream=None):
+    """Causal attention of a prompt chunk: q [T, Hq, D] holds the last T of the sequence's seq_len tokens (their
+    K/V already appended); block_table [max_pages] int32.  splits 0 = kvq_prefill_splits' choice.  Returns the
+    workspace used (reusable for the same T / splits)."""
+    T, Hq, D = q.shape
+    if splits == 0:
+        splits = B.kvq_prefill_splits(cache.struct, T, Hq, int(seq_len))
+    need = B.kvq_prefill_workspace_bytes(T, Hq, D, splits)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    B.kvq_paged_prefill_attention(cache.struct, q, sm_scale, block_table, seq_len, splits, workspace, out, lse_out,
+                                  B.KVQ_CHECKED if checked else 0, stream)
+    return workspace

@@ -582,7 +582,7 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (!(flags & KVQ_SKIP_MERGE) && total_splits > batch) {
     // the split offsets come from the plan, which the decode kernel never writes
-    e = kvq::launch_merge(o_part, lse_part, plan, batch, num_q_heads, D, out, p.out_bf16, lse_out, true, st);
+    e = kvq::launch_merge(o_part, lse_part, plan, 0, batch, num_q_heads, D, out, p.out_bf16, lse_out, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (checked) {
@@ -615,6 +615,132 @@ int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t ba
                      total_splits, num_ctas, workspace, workspace_bytes, out, out_dtype, lse_out, flags, stream);
 }
 
+int32_t kvq_prefill_splits(const kvq_cache* cache, int32_t q_len, int32_t num_q_heads, int32_t seq_len,
+                           int32_t target_ctas) {
+  int rc = check_cache(cache, false);
+  if (rc) return -rc;
+  if (q_len < 1 || seq_len < q_len || num_q_heads < 1 || num_q_heads % cache->num_kv_heads)
+    return -fail(KVQ_ERR_INVALID_ARG, "bad q_len %d / seq_len %d / num_q_heads %d", q_len, seq_len, num_q_heads);
+  kvq::PrefillInstance inst;
+  if (!kvq::prefill_instance(cache->format, cache->head_dim, &inst))
+    return -fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, cache->head_dim);
+  int64_t target = target_ctas;
+  if (target <= 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return -cuda_fail(e, "querying the SM count");
+    target = sms;
+  }
+  const int64_t G = num_q_heads / cache->num_kv_heads;
+  const int64_t items = (q_len * G + inst.rows - 1) / inst.rows * cache->num_kv_heads;
+  const int64_t pages = (seq_len + cache->page_size - 1) / cache->page_size;
+  // about two CTAs' worth of items per SM, at least 16 pages a split, at most 16 splits
+  int64_t S = (2 * target + items - 1) / items;
+  S = std::max<int64_t>(1, std::min<int64_t>({S, 16, std::max<int64_t>(1, pages / 16)}));
+  succeed();
+  return static_cast<int32_t>(S);
+}
+
+size_t kvq_prefill_workspace_bytes(int32_t q_len, int32_t num_q_heads, int32_t head_dim, int32_t splits) {
+  if (q_len < 0 || num_q_heads < 0 || head_dim < 0 || splits < 1) return 0;
+  const size_t rows = splits > 1 ? (size_t)q_len * splits * num_q_heads : 0;
+  return 256 + align256(rows * sizeof(float)) + rows * head_dim * sizeof(float);
+}
+
+int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q_len, int32_t num_q_heads,
+                                float sm_scale, const int32_t* block_table, int32_t max_pages, int32_t seq_len,
+                                int32_t splits, void* workspace, size_t workspace_bytes, void* out,
+                                int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
+  int rc = check_cache(cache, true);
+  if (rc) return rc;
+  if (!q || !block_table || !workspace || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer argument");
+  if (q_len < 1 || seq_len < q_len) return fail(KVQ_ERR_INVALID_ARG, "q_len %d must be in [1, seq_len %d]", q_len, seq_len);
+  if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                cache->num_kv_heads);
+  const int G = num_q_heads / cache->num_kv_heads;
+  if (G > 8) return fail(KVQ_ERR_UNSUPPORTED, "query heads per KV head %d > 8", G);
+  if ((int64_t)(seq_len + cache->page_size - 1) / cache->page_size > max_pages)
+    return fail(KVQ_ERR_INVALID_ARG, "seq_len %d needs more than max_pages %d pages", seq_len, max_pages);
+  if (splits < 1 || splits > 64) return fail(KVQ_ERR_INVALID_ARG, "splits %d not in [1, 64]", splits);
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "bad out_dtype");
+  if (!std::isfinite(sm_scale)) return fail(KVQ_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(KVQ_ERR_INVALID_ARG, "q / out must be 16-byte aligned and workspace 256-byte aligned");
+  const int D = cache->head_dim;
+  const size_t need = kvq_prefill_workspace_bytes(q_len, num_q_heads, D, splits);
+  if (workspace_bytes < need) return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  kvq::PrefillInstance inst;
+  if (!kvq::prefill_instance(cache->format, D, &inst))
+    return fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, D);
+  {
+    static std::mutex mu;
+    static bool done[64][3][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    bool& d = done[dev][cache->format][D == 256 ? 1 : 0];
+    if (!d) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, inst.kernel);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(prefill kernel)");
+      if (fa.numRegs != inst.launch_regs)
+        return fail(KVQ_ERR_UNSUPPORTED, "prefill kernel built with %d registers a thread, its register split assumes %d",
+                    fa.numRegs, inst.launch_regs);
+      e = cudaFuncSetAttribute(inst.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, inst.smem_bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+      d = true;
+    }
+  }
+  CUtensorMap tk, tv;
+  rc = make_code_map(&tk, cache->k_codes, cache->num_pages, cache->num_kv_heads, row_bytes(cache->format, D), 1);
+  if (rc) return rc;
+  rc = make_code_map(&tv, cache->v_codes, cache->num_pages, cache->num_kv_heads, row_bytes(cache->format, D), 1);
+  if (rc) return rc;
+  kvq::PrefillParams p{};
+  p.q = q;
+  p.block_table = block_table;
+  p.k_scales = static_cast<const uint8_t*>(cache->k_scales);
+  p.v_scales = static_cast<const uint8_t*>(cache->v_scales);
+  const size_t rows = splits > 1 ? (size_t)q_len * splits * num_q_heads : 0;
+  char* ws = static_cast<char*>(workspace);
+  p.status = reinterpret_cast<int32_t*>(ws);
+  p.lse_part = reinterpret_cast<float*>(ws + 256);
+  p.o_part = reinterpret_cast<float*>(ws + 256 + align256(rows * sizeof(float)));
+  p.out = out;
+  p.lse_out = lse_out;
+  p.q_len = q_len;
+  p.seq_len = seq_len;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.num_pages = cache->num_pages;
+  p.splits = splits;
+  p.row_blocks = (q_len * G + inst.rows - 1) / inst.rows;
+  p.out_bf16 = out_dtype == KVQ_OUT_BF16;
+  p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+  rc = memory_kind(out, "out", nullptr);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t grid = (int64_t)p.row_blocks * cache->num_kv_heads * splits;
+  if (grid > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
+  cudaError_t e = kvq::launch_prefill(cache->format, D, tk, tv, p, static_cast<int>(grid), st);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  if (splits > 1) {
+    e = kvq::launch_merge(p.o_part, p.lse_part, nullptr, splits, q_len, num_q_heads, D, out, p.out_bf16, lse_out,
+                          false, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  if (flags & KVQ_CHECKED) {
+    int32_t bits = 0;
+    rc = kvq_read_status(workspace, stream, &bits);
+    if (rc) return rc;
+  }
+  return succeed();
+}
+
 int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* split_offsets, int32_t batch,
                     int32_t num_q_heads, int32_t head_dim, void* out, int32_t out_dtype, float* lse_out,
                     void* stream) {
@@ -623,7 +749,7 @@ int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* s
   if (head_dim != 128 && head_dim != 256) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d", head_dim);
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "bad out_dtype");
   if (!aligned16(o_part) || !aligned16(out)) return fail(KVQ_ERR_INVALID_ARG, "o_part / out must be 16-byte aligned");
-  cudaError_t e = kvq::launch_merge(o_part, lse_part, split_offsets, batch, num_q_heads, head_dim, out,
+  cudaError_t e = kvq::launch_merge(o_part, lse_part, split_offsets, 0, batch, num_q_heads, head_dim, out,
                                     out_dtype == KVQ_OUT_BF16, lse_out, false, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return succeed();

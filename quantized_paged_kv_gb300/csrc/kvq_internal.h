@@ -33,6 +33,21 @@ struct DecodeParams {
   float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scale
 };
 
+struct PrefillParams {
+  const void* q;               // bf16 [q_len][Hq][D]
+  const int32_t* block_table;  // [max_pages] of the sequence
+  const uint8_t* k_scales;     // pool scale arrays (INT8)
+  const uint8_t* v_scales;
+  float* o_part;               // [q_len * splits][Hq][D] (splits > 1)
+  float* lse_part;             // [q_len * splits][Hq]
+  void* out;                   // [q_len][Hq][D] f32 or bf16 (splits == 1)
+  float* lse_out;              // [q_len][Hq] or null
+  int32_t* status;             // device status word
+  int32_t q_len, seq_len, num_q_heads, num_kv_heads, num_pages;
+  int32_t splits, row_blocks, out_bf16;
+  float sm_scale_log2;
+};
+
 struct AppendParams {
   const uint16_t* k_new;       // bf16 [N][Hkv][D]
   const uint16_t* v_new;
@@ -61,15 +76,28 @@ struct DecodeInstance {
 };
 
 bool decode_instance(int format, int head_dim, DecodeInstance* out);
+
+struct PrefillInstance {
+  const void* kernel;
+  int smem_bytes;
+  int threads;
+  int launch_regs;             // registers a thread the kernel's register split assumes at launch
+  int rows;                    // query rows of a work item
+};
+bool prefill_instance(int format, int head_dim, PrefillInstance* out);
+cudaError_t launch_prefill(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaStream_t stream);
 // Record a printf-style message as the calling thread's last error; returns code.
 int record_error(int code, const char* fmt, ...);
-// offsets_ready: the offsets are not written by the preceding kernel on the
-// stream (read before waiting for it)
-cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
-                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out, bool offsets_ready,
-                         cudaStream_t stream);
+// offsets: split offsets [batch + 1], or null when every sequence has
+// uniform_splits splits (rows b * uniform_splits ...).  offsets_ready: the
+// offsets are not written by the preceding kernel on the stream (read before
+// waiting for it).
+cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int uniform_splits,
+                         int batch, int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
+                         bool offsets_ready, cudaStream_t stream);
 
 }  // namespace kvq

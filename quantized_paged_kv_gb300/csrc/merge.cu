@@ -16,8 +16,8 @@ constexpr int kMergeWarps = kMergeThreads / 32;
 
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                 const int32_t* __restrict__ offs, int batch, int num_q_heads, int D, void* out, int out_bf16,
-                 float* lse_out, int offs_ready) {
+                 const int32_t* __restrict__ offs, int uniform, int batch, int num_q_heads, int D, void* out,
+                 int out_bf16, float* lse_out, int offs_ready) {
   // a following decode may be scheduled now (it waits for this grid before it
   // writes anything this kernel reads)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -30,10 +30,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ float red_m[kMergeWarps];
   __shared__ int red_s[kMergeWarps];
   auto sync = [] { __syncthreads(); };
-  const int smax = merge_max_splits<kMergeWarps>(offs, batch, red_s, sync);
+  const int smax = merge_max_splits<kMergeWarps>(offs, uniform, batch, red_s, sync);
   if (smax <= 1) return;  // nothing to merge
   if (offs_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
-  merge_all<kMergeWarps>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, smax, red_o, red_w,
+  merge_all<kMergeWarps>(o_part, lse_part, offs, uniform, batch, num_q_heads, D, out, out_bf16, lse_out, smax, red_o, red_w,
                          red_m, sync);
 }
 
@@ -51,9 +51,9 @@ int merge_grid_limit() {
 
 }  // namespace
 
-cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int batch,
-                         int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out, bool offsets_ready,
-                         cudaStream_t stream) {
+cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* offsets, int uniform_splits,
+                         int batch, int num_q_heads, int head_dim, void* out, int out_bf16, float* lse_out,
+                         bool offsets_ready, cudaStream_t stream) {
   const int64_t tasks = (int64_t)batch * num_q_heads * (head_dim / kMinSliceCols);  // most tasks of any shape
   if (tasks <= 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>(tasks, merge_grid_limit());
@@ -67,8 +67,8 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, o_part, lse_part, offsets, batch, num_q_heads, head_dim, out,
-                            out_bf16, lse_out, offsets_ready ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg, merge_kernel, o_part, lse_part, offsets, uniform_splits, batch, num_q_heads,
+                            head_dim, out, out_bf16, lse_out, offsets_ready ? 1 : 0);
 }
 
 }  // namespace kvq

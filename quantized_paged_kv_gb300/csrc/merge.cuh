@@ -21,7 +21,9 @@
 // Each lane keeps a running maximum of the lse values it has seen and rescales
 // its sums when it grows (one pass over the partials); lane phases and warps are
 // then combined the same way (by shuffles, and through shared memory).
-// Sequences with a single split are skipped (the decode kernel wrote them).  CTAs
+// Sequences with a single split are skipped (the decode kernel wrote them).
+// Split offsets come from the plan, or (offs = null) every sequence has
+// `uniform` splits at rows b * uniform ...  CTAs
 // walk groups of NW / WPR tasks, grid-stride.  Partials are read with L1 bypassed
 // (they were written by other SMs).
 #pragma once
@@ -37,7 +39,7 @@ constexpr int kInFlight = 8;       // loads in flight per lane
 
 template <int R, int NW, class Sync>
 __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                                            const int32_t* __restrict__ offs, int batch, int num_q_heads, int D,
+                                            const int32_t* __restrict__ offs, int uniform, int batch, int num_q_heads, int D,
                                             void* out, int out_bf16, float* lse_out, int wpr,
                                             float4 (*red_o)[32], float* red_w, float* red_m, Sync sync) {
   constexpr int L = 32 / R;            // lanes per row
@@ -61,8 +63,8 @@ __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, co
       slice = static_cast<int>(t - (int64_t)bg * slices);
       b = bg / num_q_heads;
       g = bg - b * num_q_heads;
-      base = offs[b];
-      S = offs[b + 1] - base;
+      base = offs ? offs[b] : b * uniform;
+      S = offs ? offs[b + 1] - base : uniform;
     }
     // one pass with an online rescale: (m, wsum, acc) = running max of the lse
     // values seen, sum of exp(lse - m), and sum of exp(lse - m) * o
@@ -182,9 +184,11 @@ __device__ __forceinline__ void merge_tasks(const float* __restrict__ o_part, co
 
 // Largest split count of the batch (every thread of the NW warps gets it).
 template <int NW, class Sync>
-__device__ __forceinline__ int merge_max_splits(const int32_t* __restrict__ offs, int batch, int* red_s, Sync sync) {
+__device__ __forceinline__ int merge_max_splits(const int32_t* __restrict__ offs, int uniform, int batch, int* red_s,
+                                                Sync sync) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int smax = 0;
+  if (!offs) return uniform;
   for (int b = tid; b < batch; b += NW * 32) smax = max(smax, offs[b + 1] - offs[b]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, o));
@@ -200,17 +204,17 @@ __device__ __forceinline__ int merge_max_splits(const int32_t* __restrict__ offs
 // 0 .. NW*32-1 of the CTA take part); smax = merge_max_splits(...).
 template <int NW, class Sync>
 __device__ __forceinline__ void merge_all(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                                          const int32_t* __restrict__ offs, int batch, int num_q_heads, int D,
+                                          const int32_t* __restrict__ offs, int uniform, int batch, int num_q_heads, int D,
                                           void* out, int out_bf16, float* lse_out, int smax,
                                           float4 (*red_o)[32], float* red_w, float* red_m, Sync sync) {
   if (smax <= 1) return;  // nothing to merge
   if (smax <= kShortSplits) {
-    merge_tasks<1, NW>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, 1, red_o, red_w, red_m,
+    merge_tasks<1, NW>(o_part, lse_part, offs, uniform, batch, num_q_heads, D, out, out_bf16, lse_out, 1, red_o, red_w, red_m,
                        sync);
   } else {
     int wpr = 1;  // 4 splits per warp-load, 8 loads in flight: 32 splits per warp per round
     while (wpr < NW && (NW % (2 * wpr)) == 0 && wpr * 4 * kInFlight < smax) wpr <<= 1;
-    merge_tasks<4, NW>(o_part, lse_part, offs, batch, num_q_heads, D, out, out_bf16, lse_out, wpr, red_o, red_w, red_m,
+    merge_tasks<4, NW>(o_part, lse_part, offs, uniform, batch, num_q_heads, D, out, out_bf16, lse_out, wpr, red_o, red_w, red_m,
                        sync);
   }
 }
