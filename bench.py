@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--fmt", default="int8", choices=["int8", "nvfp4", "bf16"])
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--verify-tokens", type=int, default=0, help="profiling case: verify calls of this many tokens")
+    ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling case: prefill calls of this many tokens")
     return ap.parse_args()
 
 
@@ -272,6 +273,51 @@ def time_verify(ls, T, steps, warmup=16):
             "query_rows": T * wl.Hq, "note": "KV bytes counted once per call"}
 
 
+def time_prefill(ls, T, peak_tf, reps=20):
+    """Prefill of the last T tokens of layer pools' sequence (causal), CUDA graph of
+    the R layers' calls; FLOPs = 4 * Hq * D * (visible keys summed over the T tokens)."""
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+
+    wl = ls.wl
+    L = int(wl.seq_lens[0])
+    q = torch.from_numpy(wl.q_tokens(T)[0]).to(torch.bfloat16).to(ls.device)
+    out = torch.empty((T, wl.Hq, wl.D), dtype=ls.out.dtype, device=ls.device)
+    bt = ls.bt[0].contiguous()
+    splits = kvq.kvq_prefill_splits(ls.caches[0].struct, T, wl.Hq, L)
+    ws = torch.zeros(kvq.kvq_prefill_workspace_bytes(T, wl.Hq, wl.D, splits), dtype=torch.uint8, device=ls.device)
+    stream = torch.cuda.Stream()
+
+    def one(r):
+        kvq.prefill(ls.caches[r], q, bt, L, out, wl.sm_scale, splits=splits, workspace=ws)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for r in range(ls.R):
+            one(r)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for r in range(ls.R):
+            one(r)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * ls.R)
+    visible = sum(L - T + i + 1 for i in range(T))
+    flops = 4.0 * wl.Hq * wl.D * visible
+    return {"us": round(t * 1e6, 2), "TFLOPs": round(flops / t / 1e12, 1), "frac_of_bf16_peak": round(flops / t / 1e12 / peak_tf, 4),
+            "splits": splits, "context": L, "note": "f16 mma.sync; peak = measured cuBLAS bf16 burst"}
+
+
 def time_e2e(ls, plan, steps, warmup=3):
     """Through the public API with host buffers: every step hands the C ABI
     pinned host memory for q, the block table and seq_lens (inputs) and for the
@@ -461,13 +507,13 @@ def run_ours(args, rank, world, barrier, allmax):
         "clocks": clocks,
     }
     if args.sweep and rank == 0:
-        line["sweep"] = sweep(args, dev, l2, peak)
+        line["sweep"] = sweep(args, dev, l2, peak, float(peaks.get("bf16_tflops", 1900.0)))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     return line
 
 
-def sweep(args, dev, l2, peak):
+def sweep(args, dev, l2, peak, peak_tf=1937.0):
     """Split sweep and the other workloads (per-call µs and KV GB/s)."""
     import gc
 
@@ -514,6 +560,14 @@ def sweep(args, dev, l2, peak):
     ls = LayerSet(wl, "int8", R, dev)
     for T in (2, 6):
         res[f"verify_long_int8/T={T}"] = time_verify(ls, T, steps)
+    del ls
+    gc.collect()
+    torch.cuda.empty_cache()
+    # prefill: a 2,048-token chunk at the end of the 32K context (and the first chunk)
+    wl = W.make("long_int8")
+    ls = LayerSet(wl, "int8", 2, dev)
+    for T in (512, 2048):
+        res[f"prefill_long_int8/T={T}"] = time_prefill(ls, T, peak_tf=peak_tf)
     del ls
     gc.collect()
     torch.cuda.empty_cache()
@@ -607,7 +661,15 @@ def run_ncu_case(args):
     R = max(1, math.ceil(1.1 * l2 / max(per_layer, 1)))
     ls = LayerSet(wl, args.fmt, R, "cuda")  # NVFP4 global scale 1 (it does not change the work)
     plan = ls.plan(0)
-    if args.verify_tokens:
+    if args.prefill_tokens:
+        T = args.prefill_tokens
+        L = int(wl.seq_lens[0])
+        q = torch.from_numpy(wl.q_tokens(T)[0]).to(torch.bfloat16).cuda()
+        out = torch.empty((T, wl.Hq, wl.D), dtype=ls.out.dtype, device="cuda")
+        ws = None
+        for i in range(args.calls):
+            ws = kvq.prefill(ls.caches[i % R], q, ls.bt[0].contiguous(), L, out, wl.sm_scale, workspace=ws)
+    elif args.verify_tokens:
         T = args.verify_tokens
         plan = kvq.DecodePlan(ls.caches[0], kvq.verify_lengths(wl.seq_lens, T), wl.Hq)
         q = torch.from_numpy(wl.q_tokens(T)).to(torch.bfloat16).cuda()

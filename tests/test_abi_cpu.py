@@ -176,3 +176,21 @@ def test_host_validation_errors(kvq):
                                       0, None, 0, None)
     assert rc == 1
     assert L.kvq_split_merge(None, None, None, 1, 1, 256, None, 0, None, None) == 1
+
+
+def test_prefill_split_choice_and_workspace(kvq):
+    s = _struct(kvq)  # INT8, Hkv = 4, D = 256
+    # 2048 tokens x 6 heads = 96 row blocks of 128 a KV head: enough work, one split
+    assert kvq.kvq_prefill_splits(s, 2048, 24, 32768, 152) == 1
+    # 6 tokens: one row block a head -> more splits (at most 16, at least 16 pages each)
+    assert kvq.kvq_prefill_splits(s, 6, 24, 32768, 152) == 16
+    assert kvq.kvq_prefill_splits(s, 6, 24, 100, 152) == 1
+    assert kvq.kvq_prefill_workspace_bytes(6, 24, 256, 1) == 256
+    n = kvq.kvq_prefill_workspace_bytes(6, 24, 256, 3)
+    rows = 6 * 3 * 24
+    assert n == 256 + (rows * 4 + 255) // 256 * 256 + rows * 256 * 4
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_prefill_splits(s, 10, 24, 5, 152)  # q_len > seq_len
+    nv = _struct(kvq, fmt="nvfp4")
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_prefill_splits(nv, 10, 24, 500, 152)  # no NVFP4 prefill kernel
