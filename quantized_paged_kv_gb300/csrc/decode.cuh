@@ -497,6 +497,10 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   float4* part_o = reinterpret_cast<float4*>(codes);
   float2* part_ml = reinterpret_cast<float2*>(codes + (CW - 1) * Lo::kPartOBytes);
   constexpr float kLn2 = 0.69314718055994530942f;
+  // P' is split into hi + lo f16 (bf16) terms for fp32 output; for bf16 output one
+  // term is enough: its rounding (at most 2^-11 relative, 2^-8 for the BF16
+  // cache's bf16 P) is not above the output's own rounding to bf16
+  const bool p_lo = !p.out_bf16;
 
   int gidx = 0;  // pages of this CTA before the current item (global ring position)
   Item w = first, nw;
@@ -768,7 +772,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           const uint32_t a0 = i8pair_to_h2<0x4240>(x0), a1 = i8pair_to_h2<0x4341>(x0);
           const uint32_t a2 = i8pair_to_h2<0x4240>(x1), a3 = i8pair_to_h2<0x4341>(x1);
           mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, phi[0], phi[1]);
-          mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, plo[0], plo[1]);
+          if (p_lo) mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, plo[0], plo[1]);
         }
       }
     } else if constexpr (FMT == KVQ_FMT_BF16) {
@@ -785,7 +789,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           w[0] &= m0; w[1] &= m0; w[2] &= m1; w[3] &= m1;
         }
         mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], phi[0], phi[1]);
-        mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
+        if (p_lo) mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
       }
     } else {
       // NVFP4: lane gets b16 (4 nibbles = d 32ch+4r..+3) of tokens t, t+1 (t = 8tb+2c);
@@ -827,9 +831,9 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           }
           // m-tile 2ch: rows r <- d 32ch+4r, r+8 <- +1; m-tile 2ch+1: +2, +3
           mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], phi[0], phi[1]);
-          mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], plo[0], plo[1]);
+          if (p_lo) mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], plo[0], plo[1]);
           mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], phi[0], phi[1]);
-          mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], plo[0], plo[1]);
+          if (p_lo) mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], plo[0], plo[1]);
         }
       }
     }

@@ -19,7 +19,8 @@
 //     a bulk copy each for their scales.
 //   * warps 0..7: consumers, each over every page of the range: S = Q K^T for its
 //     16 rows, the online softmax with a causal limit per row, O^T += V^T P'^T
-//     (two 8-row column tiles; P' split hi + lo as in the decode kernel).
+//     (two 8-row column tiles; P' split hi + lo for fp32 output, as in the decode
+//     kernel).
 //   * registers: the producer warpgroup gives registers back, the consumers take
 //     them (setmaxnreg), as in the decode kernel.
 // All waits are bounded (%globaltimer); a timeout sets KVQ_DEV_TIMEOUT and stops.
@@ -56,7 +57,7 @@ struct PrefillLayout {
 
 // position (byte offset) of element (row, k) of a warp's q tile: rows of D f16,
 // 16-byte chunks XOR-swizzled by the row; within a k-step (16 elements) the
-// elements are stored in the order the K fragments use (see kperm)
+// elements are stored in the order the K fragments use (see the q tile loop)
 __device__ __forceinline__ uint32_t qtile_off(int row, int chunk, int D) {
   return row * D * 2 + (((chunk ^ (row & 7))) << 4);
 }
@@ -239,6 +240,8 @@ __global__ void __launch_bounds__(PrefillLayout<FMT, D>::kThreads, 1)
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
+  // P' in hi + lo terms for fp32 output, one term for bf16 output (as in the decode kernel)
+  const bool p_lo = !p.out_bf16;
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
   bool alive = true;
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(PrefillLayout<FMT, D>::kThreads, 1)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             mma16816<false>(oacc[2 * cp + u][nt], a0, a1, a2, a3, phi[nt][0], phi[nt][1]);
-            mma16816<false>(oacc[2 * cp + u][nt], a0, a1, a2, a3, plo[nt][0], plo[nt][1]);
+            if (p_lo) mma16816<false>(oacc[2 * cp + u][nt], a0, a1, a2, a3, plo[nt][0], plo[nt][1]);
           }
         }
       }
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(PrefillLayout<FMT, D>::kThreads, 1)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           mma16816<true>(oacc[mt][nt], w[0], w[1], w[2], w[3], phi[nt][0], phi[nt][1]);
-          mma16816<true>(oacc[mt][nt], w[0], w[1], w[2], w[3], plo[nt][0], plo[nt][1]);
+          if (p_lo) mma16816<true>(oacc[mt][nt], w[0], w[1], w[2], w[3], plo[nt][0], plo[nt][1]);
         }
       }
     }
