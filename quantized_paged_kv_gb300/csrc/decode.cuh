@@ -680,11 +680,12 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
             const int ch = 4 * cg + m;
             const uint32_t bsel = 2 * (ch & 1) + (c >> 1);
             const __half2 sdh = u32_as_h2(e4m3x2_to_h2(prmt(ksw[i][ch >> 1], 0u, bsel | (bsel << 4))));
+            uint32_t f[4];
+            e2m1x8_to_h2x4(w[m], f);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[m] >> (16 * hh)) & 0xFFu)), sdh));
-              const uint32_t b1 =
-                  h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((w[m] >> (16 * hh + 8)) & 0xFFu)), sdh));
+              const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(f[2 * hh]), sdh));
+              const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(f[2 * hh + 1]), sdh));
               mma16816<false>(sacc[i][hh], qa[2 * m + hh][0], 0u, qa[2 * m + hh][1], 0u, b0, b1);
             }
           }
@@ -804,48 +805,52 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         if (p_lo) mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
       }
     } else {
-      // NVFP4: lane gets b16 (4 nibbles = d 32ch+4r..+3) of tokens t, t+1 (t = 8tb+2c);
-      // regroup nibbles into per-d token pairs; group scale of those d's = 2ch + r/4.
-      const uint4 sa0 = *reinterpret_cast<const uint4*>(vsc + (2 * c) * 16);
-      const uint4 sb0 = *reinterpret_cast<const uint4*>(vsc + (2 * c + 1) * 16);
-      const uint4 sa1 = *reinterpret_cast<const uint4*>(vsc + (8 + 2 * c) * 16);
-      const uint4 sb1 = *reinterpret_cast<const uint4*>(vsc + (9 + 2 * c) * 16);
-      const uint32_t swa[2][4] = {{sa0.x, sa0.y, sa0.z, sa0.w}, {sa1.x, sa1.y, sa1.z, sa1.w}};
-      const uint32_t swb[2][4] = {{sb0.x, sb0.y, sb0.z, sb0.w}, {sb1.x, sb1.y, sb1.z, sb1.w}};
-      const uint32_t vmask[2] = {
-          (2 * c < nvalid ? 0x0000FFFFu : 0u) | (2 * c + 1 < nvalid ? 0xFFFF0000u : 0u),
-          (8 + 2 * c < nvalid ? 0x0000FFFFu : 0u) | (9 + 2 * c < nvalid ? 0xFFFF0000u : 0u)};
+      // NVFP4: lane (r, c) reads 16-byte chunk r (d 32r..32r+31) of token rows
+      // 2c, 2c+1 (MMA k 2c, 2c+1) and 2c+8, 2c+9 (k 2c+8, 2c+9).  The words of a
+      // token pair at the same d merge into bytes that each hold one d for both
+      // tokens, first token in the low nibble (f[.][0]: even d, f[.][1]: odd d).
+      // m-tile 4j+k takes d = 32r+8j+2k (row r) and d+1 (row r+8), both in
+      // scale group 2r + j/2, so the group scale is one f16x2 per token pair.
+      uint4 vw[2][2];  // [token pair][first / second token]
 #pragma unroll
-      for (int cp = 0; cp < 4; ++cp) {
-        const int mm = lane >> 3;
-        const int trow = 8 * (mm & 1) + (lane & 7);
-        uint32_t w[4];
-        ldsm_x4_t(swz(vblk, trow, 2 * cp + (mm >> 1)), w[0], w[1], w[2], w[3]);
+      for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int ch = 2 * cp + u;
-          const uint32_t bsel = 2 * (ch & 1) + (r >> 2);
-          uint32_t a[2][4];  // [tb][d offset 0..3] f16x2 over the token pair
+        for (int e = 0; e < 2; ++e) {
+          const int t = 8 * tb + 2 * c + e;
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(vw[tb][e].x), "=r"(vw[tb][e].y), "=r"(vw[tb][e].z), "=r"(vw[tb][e].w)
+                       : "r"(swz(vblk, t, r)));
+        }
+      uint32_t svp[2][2];  // [token pair][group 2r, 2r+1]: f16x2 over the pair's tokens
 #pragma unroll
-          for (int tb = 0; tb < 2; ++tb) {
-            const uint32_t wd = w[2 * u + tb];
-            const uint32_t lo4 = wd & 0x0F0F0F0Fu;
-            const uint32_t hi4 = (wd >> 4) & 0x0F0F0F0Fu;
-            const uint32_t ev = lo4 | (lo4 >> 12);  // byte0: d0 pair, byte1: d2 pair
-            const uint32_t od = hi4 | (hi4 >> 12);  // byte0: d1 pair, byte1: d3 pair
-            uint32_t sv = e4m3x2_to_h2(prmt(swa[tb][ch >> 1], swb[tb][ch >> 1], bsel | ((bsel + 4) << 4)));
-            sv &= vmask[tb];  // unwritten slots may hold NaN scales
-            const __half2 svh = u32_as_h2(sv);
-            a[tb][0] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(ev & 0xFFu)), svh));
-            a[tb][1] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2(od & 0xFFu)), svh));
-            a[tb][2] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((ev >> 8) & 0xFFu)), svh));
-            a[tb][3] = h2_as_u32(__hmul2(u32_as_h2(e2m1x2_to_h2((od >> 8) & 0xFFu)), svh));
-          }
-          // m-tile 2ch: rows r <- d 32ch+4r, r+8 <- +1; m-tile 2ch+1: +2, +3
-          mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], phi[0], phi[1]);
-          if (p_lo) mma16816<false>(oacc[2 * ch], a[0][0], a[0][1], a[1][0], a[1][1], plo[0], plo[1]);
-          mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], phi[0], phi[1]);
-          if (p_lo) mma16816<false>(oacc[2 * ch + 1], a[0][2], a[0][3], a[1][2], a[1][3], plo[0], plo[1]);
+      for (int tb = 0; tb < 2; ++tb) {
+        const int t = 8 * tb + 2 * c;
+        const uint32_t s0 = *reinterpret_cast<const uint16_t*>(vsc + t * 16 + 2 * r);
+        const uint32_t s1 = *reinterpret_cast<const uint16_t*>(vsc + (t + 1) * 16 + 2 * r);
+        const uint32_t sw = s0 | (s1 << 16);  // bytes: (g0, t) (g1, t) (g0, t+1) (g1, t+1)
+        const uint32_t vm = (t < nvalid ? 0x0000FFFFu : 0u) | (t + 1 < nvalid ? 0xFFFF0000u : 0u);
+        svp[tb][0] = e4m3x2_to_h2(prmt(sw, 0u, 0x20u)) & vm;  // unwritten slots may hold NaN scales
+        svp[tb][1] = e4m3x2_to_h2(prmt(sw, 0u, 0x31u)) & vm;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t f[2][2][4];  // [token pair][even / odd d][byte k]
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb) {
+          const uint32_t w0 = j == 0 ? vw[tb][0].x : j == 1 ? vw[tb][0].y : j == 2 ? vw[tb][0].z : vw[tb][0].w;
+          const uint32_t w1 = j == 0 ? vw[tb][1].x : j == 1 ? vw[tb][1].y : j == 2 ? vw[tb][1].z : vw[tb][1].w;
+          e2m1x8_to_h2x4(bitsel(w0, w1 << 4, 0x0F0F0F0Fu), f[tb][0]);
+          e2m1x8_to_h2x4(bitsel(w0 >> 4, w1, 0x0F0F0F0Fu), f[tb][1]);
+        }
+        const __half2 sa = u32_as_h2(svp[0][j >> 1]), sb = u32_as_h2(svp[1][j >> 1]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t a0 = h2_as_u32(__hmul2(u32_as_h2(f[0][0][k]), sa));
+          const uint32_t a1 = h2_as_u32(__hmul2(u32_as_h2(f[0][1][k]), sa));
+          const uint32_t a2 = h2_as_u32(__hmul2(u32_as_h2(f[1][0][k]), sb));
+          const uint32_t a3 = h2_as_u32(__hmul2(u32_as_h2(f[1][1][k]), sb));
+          mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, phi[0], phi[1]);
+          if (p_lo) mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, plo[0], plo[1]);
         }
       }
     }
@@ -973,7 +978,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
             put(hr, 16 * mt + r, oacc[mt][e], 0.f, false);
             put(hr, 16 * mt + 8 + r, oacc[mt][2 + e], 0.f, false);
           } else {
-            put(hr, 32 * (mt >> 1) + 4 * r + 2 * (mt & 1), oacc[mt][e], oacc[mt][2 + e], true);
+            put(hr, 32 * r + 8 * (mt >> 2) + 2 * (mt & 3), oacc[mt][e], oacc[mt][2 + e], true);
           }
         }
       }

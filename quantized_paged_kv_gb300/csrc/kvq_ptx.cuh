@@ -175,6 +175,21 @@ __device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte_in_low_bits) {
   return d;
 }
 
+// The four bytes of a word (each an E2M1 pair as above) -> four f16x2, byte j -> o[j].
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+// Bitwise select: bits of a where m is set, bits of b elsewhere (one LOP3).
+__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t m) { return (a & m) | (b & ~m); }
+
 // Two E4M3 bytes (low byte -> low half) -> f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
   uint32_t d;
