@@ -169,14 +169,16 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
   if (!d) {
     // the kernel's warp roles split its launch registers (setmaxnreg): the split
     // is only valid for the register count it was written for
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, inst->kernel);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(decode kernel)");
-    if (fa.numRegs != inst->launch_regs)
-      return fail(KVQ_ERR_UNSUPPORTED, "decode kernel built with %d registers a thread, its register split assumes %d",
-                  fa.numRegs, inst->launch_regs);
-    e = cudaFuncSetAttribute(inst->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, inst->smem_bytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+    for (const void* kern : inst->kernels) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(decode kernel)");
+      if (fa.numRegs != inst->launch_regs)
+        return fail(KVQ_ERR_UNSUPPORTED, "decode kernel built with %d registers a thread, its register split assumes %d",
+                    fa.numRegs, inst->launch_regs);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, inst->smem_bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+    }
     d = true;
   }
   return KVQ_OK;
@@ -301,7 +303,7 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inst.kernel, inst.threads, inst.smem_bytes);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, inst.kernels[0], inst.threads, inst.smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "querying SM count / occupancy");
     target = (int64_t)sms * std::max(per_sm, 1);
   }

@@ -214,7 +214,9 @@ __device__ __forceinline__ uint32_t swz(uint32_t block, int t, int chunk) {
 
 __device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }  // k in [-126, 127]
 
-template <int FMT, int D>
+// PLO: the P' operand carries a lo term (fp32 output); the launcher picks the
+// instance from the output type, so the choice costs nothing inside the page loop.
+template <int FMT, int D, bool PLO>
 __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeParams p) {
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   // P' is split into hi + lo f16 (bf16) terms for fp32 output; for bf16 output one
   // term is enough: its rounding (at most 2^-11 relative, 2^-8 for the BF16
   // cache's bf16 P) is not above the output's own rounding to bf16
-  const bool p_lo = !p.out_bf16;
+  constexpr bool p_lo = PLO;
 
   int gidx = 0;  // pages of this CTA before the current item (global ring position)
   Item w = first, nw;
@@ -785,7 +787,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           const uint32_t a0 = i8pair_to_h2<0x4240>(x0), a1 = i8pair_to_h2<0x4341>(x0);
           const uint32_t a2 = i8pair_to_h2<0x4240>(x1), a3 = i8pair_to_h2<0x4341>(x1);
           mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, phi[0], phi[1]);
-          if (p_lo) mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, plo[0], plo[1]);
+          if constexpr (p_lo) mma16816<false>(oacc[2 * cp + u], a0, a1, a2, a3, plo[0], plo[1]);
         }
       }
     } else if constexpr (FMT == KVQ_FMT_BF16) {
@@ -802,7 +804,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           w[0] &= m0; w[1] &= m0; w[2] &= m1; w[3] &= m1;
         }
         mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], phi[0], phi[1]);
-        if (p_lo) mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
+        if constexpr (p_lo) mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
       }
     } else {
       // NVFP4: lane (r, c) reads 16-byte chunk r (d 32r..32r+31) of token rows
@@ -850,7 +852,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           const uint32_t a2 = h2_as_u32(__hmul2(u32_as_h2(f[1][0][k]), sb));
           const uint32_t a3 = h2_as_u32(__hmul2(u32_as_h2(f[1][1][k]), sb));
           mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, phi[0], phi[1]);
-          if (p_lo) mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, plo[0], plo[1]);
+          if constexpr (p_lo) mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, plo[0], plo[1]);
         }
       }
     }

@@ -1,4 +1,4 @@
-// decode_launch.cu — the decode kernel instances (format x head_dim) and their launchers.
+// decode_launch.cu — the decode kernel instances (format x head_dim x P' terms) and their launchers.
 #include "decode.cuh"
 
 namespace kvq {
@@ -7,8 +7,14 @@ namespace {
 template <int FMT, int D>
 DecodeInstance instance_of() {
   using Lo = DecodeLayout<FMT, D>;
-  return DecodeInstance{reinterpret_cast<const void*>(&decode_kernel<FMT, D>), Lo::kSmemBytes, Lo::kThreads, Lo::kCW,
-                        DecodeTraits<FMT, D>::kRow, &decode_head_group<FMT, D>, Lo::kLaunchRegs};
+  return DecodeInstance{{reinterpret_cast<const void*>(&decode_kernel<FMT, D, true>),
+                         reinterpret_cast<const void*>(&decode_kernel<FMT, D, false>)},
+                        Lo::kSmemBytes,
+                        Lo::kThreads,
+                        Lo::kCW,
+                        DecodeTraits<FMT, D>::kRow,
+                        &decode_head_group<FMT, D>,
+                        Lo::kLaunchRegs};
 }
 
 template <int FMT, int D>
@@ -27,7 +33,9 @@ cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<FMT, D>, tk, tv, p);
+  // fp32 output: P' = hi + lo terms; bf16 output: the hi term alone
+  return p.out_bf16 ? cudaLaunchKernelEx(&cfg, decode_kernel<FMT, D, false>, tk, tv, p)
+                    : cudaLaunchKernelEx(&cfg, decode_kernel<FMT, D, true>, tk, tv, p);
 }
 
 }  // namespace

@@ -66,7 +66,7 @@ struct AppendParams {
 
 // Per-(format, head_dim) decode instance description.
 struct DecodeInstance {
-  const void* kernel;          // __global__ function
+  const void* kernels[2];      // __global__ functions: [0] fp32 output (P' hi + lo), [1] bf16 output (hi)
   int smem_bytes;
   int threads;
   int consumer_warps;          // consumer warps per CTA
