@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler and its soak")
     ap.add_argument("--ncu-case", default=None, metavar="WORKLOAD",
                     help="profiling case: build the workload's pools (just over L2 in total), run --calls eager "
-                         "decode calls over them and exit (no timing)")
+                         "decode calls over them and exit (no timing); for append_int8, --calls appends")
     ap.add_argument("--fmt", default="int8", choices=["int8", "nvfp4", "bf16"])
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--verify-tokens", type=int, default=0, help="profiling case: verify calls of this many tokens")
@@ -228,6 +228,65 @@ def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=
     if barrier:
         barrier()
     return e0.elapsed_time(e1) * 1e-3 / (reps * ls.R), reps * ls.R, clocks
+
+
+def time_append(wl, fmt, dev, l2, steps, warmup=16):
+    """kvq_quant_append of the workload's new tokens (the last `append_tail` tokens
+    of every sequence), timed as a CUDA graph of R appends that cycle through R
+    input sets and R pools, so that inputs and written pages are not L2-resident."""
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+    from quantized_paged_kv_gb300 import workloads as W
+
+    ks, vs, ss = [], [], []
+    for b in range(wl.B):
+        k, v = W.device_kv(wl, b, device=dev)
+        ks.append(k[-wl.append_tail:])
+        vs.append(v[-wl.append_tail:])
+        ss.append(torch.from_numpy(wl.slots(b)[-wl.append_tail:]))
+    k0, v0, s0 = torch.cat(ks), torch.cat(vs), torch.cat(ss).to(dev)
+    n_tok = k0.shape[0]
+    gs = (448.0 * 6.0 / float(k0.abs().max()), 448.0 * 6.0 / float(v0.abs().max())) if fmt == "nvfp4" else (1.0, 1.0)
+    in_bytes = k0.numel() * 2 * 2
+    out_bytes = n_tok * kvq.kvq_bytes_per_token(fmt, wl.Hkv, wl.D)
+    R = max(2, math.ceil(2 * l2 / (in_bytes + out_bytes)))
+    sets = []
+    for r in range(R):  # distinct inputs (a permutation of the tokens' rows) and pools
+        perm = torch.randperm(n_tok, device=dev, generator=torch.Generator(device=dev).manual_seed(r))
+        cache = kvq.KVCache(fmt, wl.num_pages, wl.Hkv, wl.D, device=dev, k_global_scale=gs[0],
+                            v_global_scale=gs[1], fill=0)
+        sets.append((cache, k0[perm].contiguous(), v0[perm].contiguous(), s0))
+    del k0, v0
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for cache, k, v, s in sets:
+            cache.append(k, v, s)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for cache, k, v, s in sets:
+            cache.append(k, v, s)
+    reps = max(1, math.ceil(steps / R))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / R))):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * R)
+    nbytes = in_bytes + out_bytes
+    peak = measured_peaks()[0]["hbm_gbs"]
+    del sets, g
+    return {"us": round(t * 1e6, 3), "GBps": round(nbytes / t / 1e9, 1), "frac": round(nbytes / t / 1e9 / peak, 4),
+            "bytes": nbytes, "inputs": R,
+            "note": "CUDA graph of R appends over R input sets and R pools (inputs larger than L2)"}
 
 
 def time_verify(ls, T, steps, warmup=16):
@@ -571,30 +630,12 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     del ls
     gc.collect()
     torch.cuda.empty_cache()
-    # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences)
+    # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences), INT8 and NVFP4
     wl = W.make("append_int8")
-    cache = kvq.KVCache("int8", wl.num_pages, wl.Hkv, wl.D, device=dev, fill=0)
-    ks, vs, ss = [], [], []
-    for b in range(wl.B):
-        k, v = W.device_kv(wl, b, device=dev)
-        ks.append(k[-wl.append_tail:])
-        vs.append(v[-wl.append_tail:])
-        ss.append(torch.from_numpy(wl.slots(b)[-wl.append_tail:]))
-    k, v, s = torch.cat(ks), torch.cat(vs), torch.cat(ss).to(dev)
-    for _ in range(10):
-        cache.append(k, v, s)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    n = 200
-    for _ in range(n):
-        cache.append(k, v, s)
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) * 1e-3 / n
-    nbytes = k.numel() * 2 * 2 + wl.append_tail * wl.B * kvq.kvq_bytes_per_token("int8", wl.Hkv, wl.D)
-    res["append_int8/8192 tokens"] = {"us": round(t * 1e6, 3), "GBps": round(nbytes / t / 1e9, 1),
-                                      "note": "eager launches, L2-resident inputs (50 MB)"}
+    for fmt in ("int8", "nvfp4"):
+        res[f"append_{fmt}/8192 tokens"] = time_append(wl, fmt, dev, l2, steps)
+        gc.collect()
+        torch.cuda.empty_cache()
     return res
 
 
@@ -655,6 +696,21 @@ def run_ncu_case(args):
 
     kvq.lib()
     wl = W.make(args.ncu_case)
+    if wl.append_tail:  # the workload's append: `calls` appends of its new tokens into one pool
+        ks, vs, ss = [], [], []
+        for b in range(wl.B):
+            k, v = W.device_kv(wl, b, device="cuda")
+            ks.append(k[-wl.append_tail:])
+            vs.append(v[-wl.append_tail:])
+            ss.append(torch.from_numpy(wl.slots(b)[-wl.append_tail:]))
+        k, v, s = torch.cat(ks), torch.cat(vs), torch.cat(ss).cuda()
+        cache = kvq.KVCache(args.fmt, wl.num_pages, wl.Hkv, wl.D, device="cuda", fill=0)
+        for _ in range(args.calls):
+            cache.append(k, v, s)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": args.ncu_case, "fmt": args.fmt, "calls": args.calls,
+                          "tokens": int(k.shape[0])}), flush=True)
+        return
     props = torch.cuda.get_device_properties(0)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token(args.fmt, wl.Hkv, wl.D)

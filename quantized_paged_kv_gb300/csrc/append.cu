@@ -9,9 +9,10 @@
 // 16 elements, an E4M3 scale per group, E2M1 rounding, pairs packed low nibble
 // first; invalid (negative) slots do not write.
 //
-// One thread handles 8 consecutive elements of one row (16-byte loads); D/8
-// threads share a row and reduce its maxima with shuffles.  A row is one
-// (token, KV head, K-or-V) triple.  Coalesced stores: codes 8 (INT8) / 4 (NVFP4) /
+// One thread handles 8 consecutive elements of a row (16-byte loads); D/8
+// threads share a row and reduce its maxima with shuffles, and carry
+// kAppendRows rows whose loads go out together.  A row is one (token, KV head,
+// K-or-V) triple; a block's rows share the KV head and K-or-V.  Coalesced stores: codes 8 (INT8) / 4 (NVFP4) /
 // 16 (BF16) bytes per thread, contiguous across the row.
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
@@ -30,43 +31,17 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&x)[8]) {
   }
 }
 
-// E2M1 code (sign in bit 3) of y: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to
-// the even code, saturating at 6.  The thresholds are the midpoints between grid
-// neighbours; at a midpoint the comparison is strict where the lower neighbour
-// has the even code and inclusive where the upper one does.
-__device__ __forceinline__ uint32_t e2m1_code(float y) {
-  const float a = fabsf(y);
-  const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
-                     (a > 5.0f);
-  return m | ((__float_as_uint(y) >> 31) << 3);
-}
-
+// Quantize one row (D/8 threads, this thread's 8 elements in `raw`): token n,
+// KV head h, K (which = 0) or V (1); write it to `slot`.
 template <int FMT, int D>
-__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
-  // a following decode (a programmatic dependent) may be scheduled now; it waits
-  // for this grid to complete before it reads the cache
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  constexpr int TPR = D / 8;
-  constexpr int ROWS = kAppendThreads / TPR;
-  const int64_t row = (int64_t)blockIdx.x * ROWS + threadIdx.x / TPR;
-  const int t = threadIdx.x % TPR;
-  const int64_t nrows = p.n_tokens * p.num_kv_heads * 2;
-  const bool in_range = row < nrows;
-  const int64_t r = in_range ? row : 0;
-  const int which = static_cast<int>(r & 1);  // 0: K, 1: V
-  const int64_t nh = r >> 1;
+__device__ __forceinline__ void append_row(const AppendParams& p, int h, int which, bool in_range, int64_t slot,
+                                           const uint4& raw, int t) {
   const int Hkv = p.num_kv_heads;
-  const int64_t n = nh / Hkv;
-  const int h = static_cast<int>(nh - n * Hkv);
-  const int64_t slot = p.slots[n];
   bool write = in_range && slot >= 0;
   if (write && slot >= p.capacity) {
     if (t == 0 && which == 0 && p.status) atomicOr(p.status, KVQ_DEV_BAD_SLOT);
     write = false;
   }
-
-  const uint16_t* src = (which ? p.v_new : p.k_new) + nh * D + t * 8;
-  const uint4 raw = *reinterpret_cast<const uint4*>(src);
   float x[8];
   unpack_bf16x8(raw, x);
   if (p.check_finite && in_range) {
@@ -85,21 +60,49 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   if constexpr (FMT == KVQ_FMT_BF16) {
     if (write) *reinterpret_cast<uint4*>(codes + drow * (2 * D) + t * 16) = raw;
   } else if constexpr (FMT == KVQ_FMT_INT8) {
+    constexpr int TPR = D / 8;
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    if constexpr (TPR == 32) {  // one row a warp: the bit patterns of |x| order like the values
+      amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+    } else {
 #pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, 127.0f);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      int ci = 0;
-      if (s > 0.f) ci = min(127, max(-127, __float2int_rn(__fdiv_rn(x[i], s))));
-      const uint32_t byte = static_cast<uint32_t>(ci) & 0xFFu;
-      if (i < 4) lo |= byte << (8 * i);
-      else hi |= byte << (8 * (i - 4));
+      for (int o = 1; o < TPR; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     }
+    const float s = __fdiv_rn(amax, 127.0f);
+    // code = rne(fp32(x / s)).  Adding 1.5 * 2^23 rounds a float with |v| < 2^22
+    // to an integer (ties to even) and leaves that integer's two's-complement low
+    // byte in the low byte of the sum's bits.  For a normal, finite s, q = fp32(x
+    // * fp32(1 / s)) is within 2^-23 relative (1.6e-5 absolute, |x / s| <= 127.0001)
+    // of x / s and fp32(x / s) within 2^-18 of it, so both round to the same
+    // integer unless q lies within 2^-14 of a half-integer; then, as for a
+    // subnormal, zero or non-finite s, the row takes the exact quotients.
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    const bool fast = s >= 1.17549435e-38f && s <= 3.40282347e+38f;
+    float y[8];
+    bool exact = !fast;
+    if (fast) {
+      const float rs = __frcp_rn(s);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float q = x[i] * rs;
+        y[i] = q + kMagic;
+        exact |= fabsf(q - (y[i] - kMagic)) > 0.5f - 0x1p-14f;
+      }
+    }
+    if (__any_sync(0xffffffffu, exact)) {  // rare: the whole row (all lanes) takes the exact path
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float q = s > 0.f ? fminf(127.f, fmaxf(-127.f, __fdiv_rn(x[i], s))) : 0.f;
+        y[i] = q + kMagic;
+      }
+    }
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(y[i]);
+    const uint32_t lo = prmt(prmt(b[0], b[1], 0x0040u), prmt(b[2], b[3], 0x0040u), 0x5410u);
+    const uint32_t hi = prmt(prmt(b[4], b[5], 0x0040u), prmt(b[6], b[7], 0x0040u), 0x5410u);
     if (write) {
       *reinterpret_cast<uint2*>(codes + drow * D + t * 8) = make_uint2(lo, hi);
       if (t == 0) reinterpret_cast<float*>(scales)[drow] = s;
@@ -113,13 +116,29 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
     const float t2 = __fmul_rn(__fdiv_rn(amax, 6.0f), gs);
     const uint32_t sf = f32_to_e4m3_satfinite(t2);
     const float sd = __low2float(u32_as_h2(e4m3x2_to_h2(sf)));
-    uint32_t packed = 0;
+    // y = fp32(fp32(x * gs) / sd) is rounded to E2M1 (ties to even, saturating),
+    // whose rounding thresholds 0.25 .. 5 are integers in 4 y.  With r = fp32(1 /
+    // sd) (sd >= 2^-9 or 0), v = fp32(fp32(x * gs) * r) is within 2^-23 relative of
+    // x gs / sd and y within 2^-24; |4 y| <= 26, so unless 4 v lies within 2^-16
+    // of an integer both round to the same code.  Otherwise the row takes the
+    // exact quotients.
+    float xg[8], y[8];
+    bool exact = false;
+    const float r = sd > 0.f ? __frcp_rn(sd) : 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      uint32_t ci = 0;
-      if (sd > 0.f) ci = e2m1_code(__fdiv_rn(__fmul_rn(x[i], gs), sd));
-      packed |= ci << (4 * i);  // element 2j in the low nibble of byte j
+      xg[i] = __fmul_rn(x[i], gs);
+      y[i] = xg[i] * r;  // sd = 0: every code 0 (y = 0, or NaN for a non-finite input)
+      const float u = 4.0f * y[i];
+      exact |= sd > 0.f && fabsf(u - rintf(u)) < 0x1p-16f;
     }
+    if (__any_sync(0xffffffffu, exact)) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = sd > 0.f ? __fdiv_rn(xg[i], sd) : 0.f;
+    }
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) packed |= (sd > 0.f ? f32x2_to_e2m1x2(y[2 * j], y[2 * j + 1]) : 0u) << (8 * j);
     if (write) {
       *reinterpret_cast<uint32_t*>(codes + drow * (D / 2) + t * 4) = packed;
       if ((t & 1) == 0) scales[drow * (D / 16) + t / 2] = static_cast<uint8_t>(sf);
@@ -127,14 +146,50 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   }
 }
 
+// Rows a thread group carries: their loads (rows and slot ids) are all issued
+// before the first row is quantized, so each thread keeps kAppendRows 16-byte
+// loads in flight instead of one.
+constexpr int kAppendRows = 2;
+
+// Grid: x over token blocks, y over (KV head, K or V) = 2 h + which, so that no
+// index needs a division.
+template <int FMT, int D>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
+  // a following decode (a programmatic dependent) may be scheduled now; it waits
+  // for this grid to complete before it reads the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int TPR = D / 8;
+  constexpr int ROWS = kAppendThreads / TPR;  // tokens a block handles side by side
+  const int t = threadIdx.x % TPR;
+  const int which = blockIdx.y & 1;
+  const int h = blockIdx.y >> 1;
+  const int64_t n0 = (int64_t)blockIdx.x * ROWS * kAppendRows + threadIdx.x / TPR;
+  const uint16_t* src = (which ? p.v_new : p.k_new) + (int64_t)h * D + t * 8;
+  const int64_t stride = (int64_t)p.num_kv_heads * D;  // elements between tokens
+  uint4 raw[kAppendRows];
+  int64_t slot[kAppendRows];
+#pragma unroll
+  for (int u = 0; u < kAppendRows; ++u) {
+    const int64_t n = n0 + (int64_t)u * ROWS;
+    const int64_t nn = n < p.n_tokens ? n : 0;
+    raw[u] = *reinterpret_cast<const uint4*>(src + nn * stride);
+    slot[u] = p.slots[nn];
+  }
+#pragma unroll
+  for (int u = 0; u < kAppendRows; ++u) {
+    const int64_t n = n0 + (int64_t)u * ROWS;
+    append_row<FMT, D>(p, h, which, n < p.n_tokens, slot[u], raw[u], t);
+  }
+}
+
 template <int FMT, int D>
 cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
-  constexpr int ROWS = kAppendThreads / (D / 8);
-  const int64_t nrows = p.n_tokens * p.num_kv_heads * 2;
-  const int64_t blocks = (nrows + ROWS - 1) / ROWS;
+  constexpr int TOKENS = kAppendThreads / (D / 8) * kAppendRows;  // tokens a block covers
+  const int64_t blocks = (p.n_tokens + TOKENS - 1) / TOKENS;
   if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  append_kernel<FMT, D><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(p);
+  if (blocks > 0x7FFFFFFF || 2 * p.num_kv_heads > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(2 * p.num_kv_heads));
+  append_kernel<FMT, D><<<grid, kAppendThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -198,6 +198,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
   return d;
 }
 
+// Two fp32 -> one byte of E2M1 codes (lo in the low nibble, hi in the high
+// nibble), round to nearest even, saturating to +-6; the sign bit follows the
+// value's sign (so a negative value that rounds to zero gives 0x8).
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(d)
+      : "f"(hi), "f"(lo));
+  return d;
+}
+
 // fp32 -> E4M3 byte, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float x) {
   uint16_t d;

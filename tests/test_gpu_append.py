@@ -76,6 +76,14 @@ def test_nvfp4_append_bit_exact(kind, gs):
     _append_and_compare("nvfp4", 2, 256, kind, gs=gs)
 
 
+@pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("nvfp4", 256), ("bf16", 256)])
+@pytest.mark.parametrize("n", [1, 5, 33, 301])
+def test_append_ragged_token_counts(fmt, D, n):
+    # a block carries several rows a thread group: token counts that leave the
+    # last block partly empty, down to a single token
+    _append_and_compare(fmt, 3, D, "normal", n=n, seed=n)
+
+
 @pytest.mark.parametrize("D", [128, 256])
 def test_bf16_append_copies(D):
     _append_and_compare("bf16", 3, D, "normal")
@@ -107,6 +115,78 @@ def test_nvfp4_scale_rounding_sweep():
     c_exp, s_exp = ofmt.nvfp4_quantize(x[:, 0, :], 1.0)
     assert np.array_equal(ks[slots // 16, 0, slots % 16], s_exp)
     assert np.array_equal(kc[slots // 16, 0, slots % 16], c_exp)
+
+
+def _bf16_upto(a):
+    """Every bf16 value v with |v| <= a (both signs, zero once), as float32."""
+    bits = np.arange(0x7F80, dtype=np.uint32)          # all finite non-negative bf16 patterns
+    v = (bits << 16).view(np.float32)
+    v = v[v <= a]
+    return np.concatenate([v, -v[1:]])
+
+
+def _dense_maxima(rng, n):
+    """bf16 row / group maxima over many binades, with random mantissas plus the
+    all-ones and power-of-two mantissas."""
+    e = rng.integers(-40, 40, n)
+    m = rng.integers(0, 128, n)
+    m[::7] = 127
+    m[1::7] = 0
+    a = ((1.0 + m / 128.0) * np.exp2(e)).astype(np.float32)
+    return torch.from_numpy(a).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def _append_rows(fmt, x, gs=1.0):
+    from quantized_paged_kv_gb300 import KVCache
+
+    n = x.shape[0]
+    cache = KVCache(fmt, (n + 15) // 16, 1, x.shape[-1], k_global_scale=gs, v_global_scale=gs, fill=H.SENTINEL)
+    slots = np.arange(n, dtype=np.int64)
+    xt = torch.from_numpy(np.ascontiguousarray(x[:, None, :])).to(torch.bfloat16).cuda()
+    cache.append(xt, xt, torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    kc, _, ks, _ = H.gpu_views_numpy(cache)
+    return kc[slots // 16, 0, slots % 16], ks[slots // 16, 0, slots % 16]
+
+
+def test_int8_append_dense_quotients():
+    """Each row holds its maximum and then every bf16 value up to it: every
+    quotient x / scale the row can produce, the half-integer ties included,
+    over many binades of the scale."""
+    rng = np.random.default_rng(11)
+    rows = []
+    for a in _dense_maxima(rng, 24):
+        v = _bf16_upto(a)
+        v = np.concatenate([v, np.zeros((-len(v)) % 255, np.float32)])
+        r = v.reshape(-1, 255)
+        rows.append(np.concatenate([np.full((len(r), 1), a, np.float32), r], axis=1))
+    x = np.concatenate(rows)
+    got_c, got_s = _append_rows("int8", x)
+    c_exp, s_exp = oatt.quantize_rows("int8", x)
+    assert np.array_equal(got_s.view(np.uint32), s_exp.view(np.uint32))
+    bad = np.argwhere(got_c != c_exp)
+    assert len(bad) == 0, (len(bad), bad[:5], x[tuple(bad[0])] if len(bad) else None)
+
+
+@pytest.mark.parametrize("gs", [1.0, 0.37, 1234.5])
+def test_nvfp4_append_dense_quotients(gs):
+    """Groups of 16 holding their maximum and 15 bf16 values up to it, so that
+    every value up to each maximum meets the group's E4M3 scale."""
+    rng = np.random.default_rng(12)
+    groups = []
+    for a in _dense_maxima(rng, 16):
+        v = _bf16_upto(a)
+        v = np.concatenate([v, np.zeros((-len(v)) % 15, np.float32)])
+        g = v.reshape(-1, 15)
+        groups.append(np.concatenate([np.full((len(g), 1), a, np.float32), g], axis=1))
+    g = np.concatenate(groups)
+    g = np.concatenate([g, np.zeros(((-len(g)) % 16, 16), np.float32)])
+    x = g.reshape(-1, 256)
+    got_c, got_s = _append_rows("nvfp4", x, gs)
+    c_exp, s_exp = oatt.quantize_rows("nvfp4", x, gs)
+    assert np.array_equal(got_s, s_exp)
+    bad = np.argwhere(got_c != c_exp)
+    assert len(bad) == 0, (len(bad), bad[:5])
 
 
 def test_slot_overwrite():
