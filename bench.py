@@ -553,7 +553,7 @@ def run_ours(args, rank, world, barrier, allmax):
                    "us_per_16_layer_step": round(16 * t_call * 1e6, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "decode_kernel<INT8, 256>", "kernel_us": round(t_dec * 1e6, 3),
+                     "kernel": "decode_kernel<INT8, 256, P' hi+lo>", "kernel_us": round(t_dec * 1e6, 3),
                      "frac_of_8TBs_nominal": round(achieved / 8000.0, 4),
                      "traffic": (tr["dram_bytes_per_launch"] if tr else None),
                      "traffic_algorithmic_ratio": (round(tr["dram_bytes_per_launch"] / bytes_step, 4) if tr else None)},
@@ -607,6 +607,9 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     measure(wl, "bf16", (16, 38, 64, 0))
     wl = W.make("serving_int8")
     measure(wl, "int8", (0, 1))
+    # the decode that follows the append workload's append: B = 8, contexts 4K..16K
+    wl = W.make("append_int8")
+    measure(wl, "int8", (0,))
     wl = W.make("long_nvfp4")
     gs = (1.0, 1.0)
     measure(wl, "nvfp4", (0,), gs, tag="long_nvfp4(gs=1)")

@@ -203,6 +203,13 @@ def test_serving_int8_full_size_sampled():
     _check(wl, "int8", 0, units=units)
 
 
+def test_append_workload_decode_full_size_sampled():
+    # the B = 8 decode over contexts of 4K..16K with 1% spikes x 20 (bf16 output)
+    wl = W.make("append_int8")
+    order = np.argsort(wl.seq_lens)
+    _check(wl, "int8", 0, units=[(int(order[0]), 0), (int(order[-1]), 3)])
+
+
 def test_long_nvfp4_full_size_sampled():
     wl = W.make("long_nvfp4")
     order = np.argsort(wl.seq_lens)
