@@ -359,6 +359,34 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
         splits = sp;
       }
     }
+    // Whole waves: for k = 1..4, the fewest pages per split whose items fit in
+    // k x target (a batch of uneven sequences rarely lands just under a wave with
+    // the factors above).  Taken only when strictly shorter.
+    int64_t max_pages = 1;
+    for (int b = 0; b < batch; ++b) max_pages = std::max(max_pages, npages[b]);
+    auto items_at = [&](int64_t x) {
+      int64_t n = 0;
+      for (int b = 0; b < batch; ++b) n += std::max<int64_t>(1, (npages[b] + x - 1) / x) * nhg;
+      return n;
+    };
+    for (int k = 1; k <= 4; ++k) {
+      int64_t lo = 4, hi = std::max<int64_t>(4, max_pages);  // items_at is non-increasing in x
+      if (items_at(hi) > k * target) continue;
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        if (items_at(mid) <= k * target) hi = mid;
+        else lo = mid + 1;
+      }
+      std::vector<int32_t> sp(batch);
+      for (int b = 0; b < batch; ++b)
+        sp[b] = static_cast<int32_t>(std::max<int64_t>(1, (npages[b] + lo - 1) / lo));
+      const int64_t span = makespan(sp);
+      if (span < best) {
+        best = span;
+        best_items = items_at(lo);
+        splits = sp;
+      }
+    }
   }
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) total += splits[b];
