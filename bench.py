@@ -374,7 +374,7 @@ def time_prefill(ls, T, peak_tf, reps=20):
     visible = sum(L - T + i + 1 for i in range(T))
     flops = 4.0 * wl.Hq * wl.D * visible
     return {"us": round(t * 1e6, 2), "TFLOPs": round(flops / t / 1e12, 1), "frac_of_bf16_peak": round(flops / t / 1e12 / peak_tf, 4),
-            "splits": splits, "context": L, "note": "f16 mma.sync; peak = measured cuBLAS bf16 burst"}
+            "splits": splits, "context": L, "note": "tcgen05 kind::f16 (fp32 accumulate); peak = measured cuBLAS bf16 burst"}
 
 
 def time_e2e(ls, plan, steps, warmup=3):

@@ -652,7 +652,7 @@ int32_t kvq_prefill_splits(const kvq_cache* cache, int32_t q_len, int32_t num_q_
   if (q_len < 1 || seq_len < q_len || num_q_heads < 1 || num_q_heads % cache->num_kv_heads)
     return -fail(KVQ_ERR_INVALID_ARG, "bad q_len %d / seq_len %d / num_q_heads %d", q_len, seq_len, num_q_heads);
   kvq::PrefillInstance inst;
-  if (!kvq::prefill_instance(cache->format, cache->head_dim, &inst))
+  if (!kvq::prefill_tc_instance(cache->format, cache->head_dim, &inst))
     return -fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, cache->head_dim);
   int64_t target = target_ctas;
   if (target <= 0) {
@@ -702,7 +702,7 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
   const size_t need = kvq_prefill_workspace_bytes(q_len, num_q_heads, D, splits);
   if (workspace_bytes < need) return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   kvq::PrefillInstance inst;
-  if (!kvq::prefill_instance(cache->format, D, &inst))
+  if (!kvq::prefill_tc_instance(cache->format, D, &inst))
     return fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, D);
   {
     static std::mutex mu;
@@ -714,25 +714,25 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
     std::lock_guard<std::mutex> lock(mu);
     bool& d = done[dev][cache->format][D == 256 ? 1 : 0];
     if (!d) {
-      cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, inst.kernel);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(prefill kernel)");
-      if (fa.numRegs != inst.launch_regs)
-        return fail(KVQ_ERR_UNSUPPORTED, "prefill kernel built with %d registers a thread, its register split assumes %d",
-                    fa.numRegs, inst.launch_regs);
-      e = cudaFuncSetAttribute(inst.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, inst.smem_bytes);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+      for (const void* kern : inst.kernels) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(prefill kernel)");
+        if (inst.launch_regs > 0 && fa.numRegs != inst.launch_regs)
+          return fail(KVQ_ERR_UNSUPPORTED,
+                      "prefill kernel built with %d registers a thread, its register split assumes %d", fa.numRegs,
+                      inst.launch_regs);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, inst.smem_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+      }
       d = true;
     }
   }
-  CUtensorMap tk, tv;
-  rc = make_code_map(&tk, cache->k_codes, cache->num_pages, cache->num_kv_heads, row_bytes(cache->format, D), 1);
-  if (rc) return rc;
-  rc = make_code_map(&tv, cache->v_codes, cache->num_pages, cache->num_kv_heads, row_bytes(cache->format, D), 1);
-  if (rc) return rc;
   kvq::PrefillParams p{};
   p.q = q;
   p.block_table = block_table;
+  p.k_codes = static_cast<const uint8_t*>(cache->k_codes);
+  p.v_codes = static_cast<const uint8_t*>(cache->v_codes);
   p.k_scales = static_cast<const uint8_t*>(cache->k_scales);
   p.v_scales = static_cast<const uint8_t*>(cache->v_scales);
   const size_t rows = splits > 1 ? (size_t)q_len * splits * num_q_heads : 0;
@@ -756,7 +756,7 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t grid = (int64_t)p.row_blocks * cache->num_kv_heads * splits;
   if (grid > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
-  cudaError_t e = kvq::launch_prefill(cache->format, D, tk, tv, p, static_cast<int>(grid), st);
+  cudaError_t e = kvq::launch_prefill_tc(cache->format, D, p, static_cast<int>(grid), st);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   if (splits > 1) {
     e = kvq::launch_merge(p.o_part, p.lse_part, nullptr, splits, q_len, num_q_heads, D, out, p.out_bf16, lse_out,

@@ -36,6 +36,8 @@ struct DecodeParams {
 struct PrefillParams {
   const void* q;               // bf16 [q_len][Hq][D]
   const int32_t* block_table;  // [max_pages] of the sequence
+  const uint8_t* k_codes;      // pool code arrays [num_pages][Hkv][16][row bytes]
+  const uint8_t* v_codes;
   const uint8_t* k_scales;     // pool scale arrays (INT8)
   const uint8_t* v_scales;
   float* o_part;               // [q_len * splits][Hq][D] (splits > 1)
@@ -78,15 +80,15 @@ struct DecodeInstance {
 bool decode_instance(int format, int head_dim, DecodeInstance* out);
 
 struct PrefillInstance {
-  const void* kernel;
+  const void* kernels[2];      // [0] fp32 output (P' hi + lo), [1] bf16 output (hi)
   int smem_bytes;
   int threads;
-  int launch_regs;             // registers a thread the kernel's register split assumes at launch
+  int launch_regs;             // registers a thread the kernel's register split assumes (0: no split)
   int rows;                    // query rows of a work item
 };
-bool prefill_instance(int format, int head_dim, PrefillInstance* out);
-cudaError_t launch_prefill(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int grid, cudaStream_t stream);
+// the prefill kernel (tcgen05 tensor cores, accumulators in TMEM)
+bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out);
+cudaError_t launch_prefill_tc(int format, int head_dim, const PrefillParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaStream_t stream);

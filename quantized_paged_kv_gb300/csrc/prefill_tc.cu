@@ -1,0 +1,500 @@
+// prefill_tc.cu — causal attention of a prompt chunk over a paged INT8 / BF16
+// cache on the fifth-generation tensor cores (tcgen05.mma, accumulators in TMEM)
+// ("half-the-memory-int8-kv-cache", section "Read the prompt using a small
+// temporary buffer": a chunk of prompt tokens does enough work per key that each
+// key is converted once to fp16 and then used by many queries; the history is
+// read in key ranges whose partial results are combined with their log-sum-exp
+// weights, as for a generated token).
+//
+// The chunk's T tokens are the last T entries of one sequence's cache (L tokens
+// in all); query token i sits at position L - T + i and sees tokens 0 .. L-T+i.
+//
+// Work item (one CTA): 128 query rows (token, query head) of one KV head — the
+// MMA's M — against one key range (a split; splits are merged by the merge
+// kernel), in tiles of 64 keys (four pages).  Warp roles:
+//   * warps 4..7 (converters): per tile, K codes -> fp16 in the canonical K-major
+//     layout with the 128-byte swizzle (the B operand of S = Q K^T) and V codes
+//     -> fp16 in the MN-major layout (the B operand of O = P V, no transpose); the
+//     INT8 scales go to shared memory.  Keys past the range or the sequence are
+//     written as zeros.
+//   * warp 8, lane 0 (MMA): S(i) = Q K(i)^T into one of two TMEM buffers, then
+//     O += P(i-1) V(i-1); each group of MMAs is committed to an mbarrier.
+//   * warps 0..3 (softmax, one query row a thread): the q row (INT8: scaled by a
+//     power of two so that it is exact in fp16) into the A tile; per tile, S from
+//     TMEM (tcgen05.ld), the online softmax with the row's causal limit, and P'
+//     (INT8: the V scale of each key folded in) as the fp16 / bf16 A operand of
+//     the P V product, in hi + lo terms for fp32 output.  The running maximum is
+//     raised only when a row's new maximum exceeds it by more than 2^8 (then the
+//     row of O in TMEM is rescaled), so p <= 256.
+// Every wait is bounded (%globaltimer); a timeout sets KVQ_DEV_TIMEOUT, the CTA
+// waits for its issued MMAs, frees its TMEM and returns.
+#include "decode.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kTcRows = 128;               // query rows of an item (the MMA's M)
+constexpr int kTcKeys = 64;                // keys of a tile
+constexpr int kTcPages = kTcKeys / kPage;  // pages of a tile
+constexpr int kTcThreads = 9 * 32;
+constexpr float kTcRescale = 8.0f;  // log2 of the largest p a stale maximum may give
+
+template <int FMT, int D>
+struct TcLayout {
+  static constexpr int kAtoms = D / 64;                  // 128-byte swizzle atoms along D (fp16)
+  static constexpr int kQBytes = kTcRows * D * 2;        // [atom][128 rows][128 B]
+  static constexpr int kKBytes = kTcKeys * D * 2;        // [atom][64 keys][128 B]
+  static constexpr int kVBytes = kTcKeys * D * 2;        // [8-key group][d atom][8 keys][128 B]
+  static constexpr int kPBytes = kTcRows * kTcKeys * 2;  // [128 rows][128 B]
+  static constexpr int kQAt = 0;
+  static constexpr int kKAt = kQAt + kQBytes;
+  static constexpr int kVAt = kKAt + kKBytes;
+  static constexpr int kPAt = kVAt + kVBytes;
+  static constexpr int kPLoAt = kPAt + kPBytes;
+  static constexpr int kScAt = kPLoAt + kPBytes;  // float k scales [2][64], v scales [2][64]
+  static constexpr int kBarAt = kScAt + 4 * kTcKeys * 4;
+  static constexpr int kNumBars = 10;
+  static constexpr int kSlotAt = kBarAt + kNumBars * 8;
+  static constexpr int kSmemBytes = 1024 + kSlotAt + 16;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static constexpr uint32_t kTmemO = 0;          // O: D columns
+  static constexpr uint32_t kTmemS = D;          // S: two buffers of 64 columns
+  static constexpr uint32_t kTmemCols = D + 2 * kTcKeys <= 256 ? 256 : 512;
+  // MN-major V: byte offset between d atoms (leading) and between 8-key groups (strided)
+  static constexpr uint32_t kVLbo = 1024, kVSbo = kAtoms * 1024;
+};
+
+enum : int { kBarQ = 0, kBarKReady, kBarVReady, kBarPReady, kBarS0, kBarS1, kBarKFree, kBarODone, kBarFinal };
+
+// byte offset of the 16-byte chunk holding elements d0 .. d0+7 (d0 % 8 == 0) of
+// row r in a K-major tile of `rows` rows ([atom][rows][128 B], 128-byte swizzle)
+__device__ __forceinline__ uint32_t kmajor_off(int r, int d0, int rows) {
+  const int a = d0 >> 6, c = (d0 & 63) >> 3;
+  return (uint32_t)(a * rows * 128 + r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// byte offset of elements d0 .. d0+7 of key n in the MN-major V tile
+template <int D>
+__device__ __forceinline__ uint32_t vtile_off(int n, int d0) {
+  const int g = n >> 3, kr = n & 7, a = d0 >> 6, c = (d0 & 63) >> 3;
+  return (uint32_t)(g * (D / 64) * 1024 + a * 1024 + kr * 128 + ((c ^ kr) << 4));
+}
+
+template <int FMT, int D, bool PLO>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const PrefillParams p) {
+  using T = DecodeTraits<FMT, D>;
+  using Lo = TcLayout<FMT, D>;
+  constexpr bool kBf16 = T::kBf16Mma;
+  constexpr int KS = D / 16;  // k-steps of S
+  constexpr uint32_t kIdescS = umma_idesc_f16(kTcRows, kTcKeys, kBf16, false);
+  constexpr uint32_t kIdescPV = umma_idesc_f16(kTcRows, D, kBf16, true);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lo::kBarAt);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Lo::kSlotAt);  // [0] TMEM base, [1] abort flag
+  float* ksc = reinterpret_cast<float*>(smem + Lo::kScAt);            // [2][64]
+  float* vsc = ksc + 2 * kTcKeys;                                     // [2][64]
+  const uint32_t sbase = smem_addr(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int TG = p.q_len * G;
+  const int it = blockIdx.x;
+  const int s = it % p.splits;
+  const int rest = it / p.splits;
+  const int h = rest % p.num_kv_heads;
+  const int rb = p.row_blocks - 1 - rest / p.num_kv_heads;  // heaviest row blocks first
+  const int row0 = rb * kTcRows;
+  const int last_tok = min(p.q_len - 1, (row0 + kTcRows - 1) / G);
+  const int kmax = p.seq_len - p.q_len + last_tok + 1;  // keys the block's last row sees
+  const int np_all = (kmax + kPage - 1) / kPage;
+  const int pg0 = (int)((int64_t)s * np_all / p.splits);
+  const int npg = (int)((int64_t)(s + 1) * np_all / p.splits) - pg0;
+  const int nt = (npg + kTcPages - 1) / kTcPages;
+  const int key_end = min(p.seq_len, (pg0 + npg) * kPage);  // keys of this range (exclusive)
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[kBarQ], 4);
+    mbar_init(&bars[kBarKReady], 4);
+    mbar_init(&bars[kBarVReady], 4);
+    mbar_init(&bars[kBarPReady], 4);
+    mbar_init(&bars[kBarS0], 1);
+    mbar_init(&bars[kBarS1], 1);
+    mbar_init(&bars[kBarKFree], 1);
+    mbar_init(&bars[kBarODone], 1);
+    mbar_init(&bars[kBarFinal], 1);
+    slot[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(slot, Lo::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = slot[0];
+  volatile uint32_t* abort_flag = slot + 1;
+  auto wait = [&](int b, uint32_t parity) -> bool {  // one thread
+    if (*abort_flag) return false;
+    if (mbar_wait(&bars[b], parity, kWaitLimitNs)) return true;
+    atomicOr(p.status, KVQ_DEV_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+  };
+  auto wait_warp = [&](int b, uint32_t parity) -> bool {  // a whole warp, one answer for all its lanes
+    return __all_sync(0xffffffffu, wait(b, parity));
+  };
+
+  if (warp == 8) {
+    // ================================================================== MMA issue
+    if (lane == 0 && nt > 0) {
+      bool ok = wait(kBarQ, 0);
+      tc_fence_after();
+      auto issue_pv = [&](int j) -> bool {
+        if (!wait(kBarPReady, j & 1) || !wait(kBarVReady, j & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTcKeys / 16; ++k) {
+          const uint64_t ad = umma_desc_sw128(sbase + Lo::kPAt + 32 * k, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(sbase + Lo::kVAt + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
+          umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        if constexpr (PLO) {
+#pragma unroll
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint64_t ad = umma_desc_sw128(sbase + Lo::kPLoAt + 32 * k, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(sbase + Lo::kVAt + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
+            umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, 1u);
+          }
+        }
+        umma_commit(&bars[kBarODone]);
+        return true;
+      };
+      for (int i = 0; ok && i < nt; ++i) {
+        if (!wait(kBarKReady, i & 1)) break;
+        tc_fence_after();
+        const uint32_t ds = tmem + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          const int a = k >> 2, kk = k & 3;
+          const uint64_t ad = umma_desc_sw128(sbase + Lo::kQAt + a * kTcRows * 128 + 32 * kk, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(sbase + Lo::kKAt + a * kTcKeys * 128 + 32 * kk, 16, 1024);
+          umma_f16(ds, ad, bd, kIdescS, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars[(i & 1) ? kBarS1 : kBarS0]);
+        umma_commit(&bars[kBarKFree]);
+        if (i > 0 && !issue_pv(i - 1)) break;
+        if (i == nt - 1) issue_pv(i);
+      }
+      // every MMA this thread issued has completed before the TMEM is freed
+      umma_commit(&bars[kBarFinal]);
+      if (!mbar_wait(&bars[kBarFinal], 0, kWaitLimitNs)) atomicOr(p.status, KVQ_DEV_TIMEOUT);
+    }
+  } else if (warp >= 4) {
+    // ================================================================== converters
+    const int ct = threadIdx.x - 128;
+    const int n = ct >> 1, half = ct & 1;  // key of the tile, half of its row
+    constexpr int kRowBytes = T::kRow;     // code bytes of a key row
+    constexpr int kHalfBytes = kRowBytes / 2;
+    constexpr int kChunks = kHalfBytes / 16;  // 16-byte source chunks of a half row
+    uint8_t* ktile = smem + Lo::kKAt;
+    uint8_t* vtile = smem + Lo::kVAt;
+    for (int i = 0; i < nt; ++i) {
+      const int jp = i * kTcPages + (n >> 4);  // page of the range
+      const int tok = (pg0 + jp) * kPage + (n & 15);
+      int pg = -1;
+      if (jp < npg && tok < key_end) {
+        pg = p.block_table[pg0 + jp];
+        if (pg < 0 || pg >= p.num_pages) {
+          if (half == 0 && (n & 15) == 0) atomicOr(p.status, KVQ_DEV_BAD_PAGE);
+          pg = -1;
+        }
+      }
+      const size_t rowoff = pg >= 0 ? ((size_t)pg * p.num_kv_heads + h) * kPage + (n & 15) : 0;
+      for (int which = 0; which < 2; ++which) {
+        const uint8_t* src = (which ? p.v_codes : p.k_codes) + rowoff * kRowBytes + half * kHalfBytes;
+        uint4 raw[kChunks];
+#pragma unroll
+        for (int u = 0; u < kChunks; ++u)
+          raw[u] = pg >= 0 ? __ldg(reinterpret_cast<const uint4*>(src) + u) : make_uint4(0, 0, 0, 0);
+        // the buffer is free once the MMAs of the previous tile that read it are done
+        if (i > 0 && !wait_warp(which ? kBarODone : kBarKFree, (i - 1) & 1)) break;
+        if constexpr (FMT == KVQ_FMT_INT8) {
+          // both scales of the tile go out with K: the softmax reads them once S is done
+          if (which == 0 && half == 0) {
+            ksc[(i & 1) * kTcKeys + n] = pg >= 0 ? __ldg(reinterpret_cast<const float*>(p.k_scales) + rowoff) : 0.f;
+            vsc[(i & 1) * kTcKeys + n] = pg >= 0 ? __ldg(reinterpret_cast<const float*>(p.v_scales) + rowoff) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < kChunks; ++u) {
+            const uint32_t w[4] = {raw[u].x ^ 0x80808080u, raw[u].y ^ 0x80808080u, raw[u].z ^ 0x80808080u,
+                                   raw[u].w ^ 0x80808080u};
+            const uint4 lo = make_uint4(i8pair_to_h2<0x4140>(w[0]), i8pair_to_h2<0x4342>(w[0]),
+                                        i8pair_to_h2<0x4140>(w[1]), i8pair_to_h2<0x4342>(w[1]));
+            const uint4 hi = make_uint4(i8pair_to_h2<0x4140>(w[2]), i8pair_to_h2<0x4342>(w[2]),
+                                        i8pair_to_h2<0x4140>(w[3]), i8pair_to_h2<0x4342>(w[3]));
+            const int d0 = half * (D / 2) + 16 * u;
+            if (which == 0) {
+              *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = lo;
+              *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0 + 8, kTcKeys)) = hi;
+            } else {
+              *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = lo;
+              *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0 + 8)) = hi;
+            }
+          }
+        } else {  // BF16: 8 elements a chunk, copied as they are
+#pragma unroll
+          for (int u = 0; u < kChunks; ++u) {
+            const int d0 = half * (D / 2) + 8 * u;
+            if (which == 0) *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = raw[u];
+            else *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = raw[u];
+          }
+        }
+        fence_proxy_async_smem();  // the tile's fp16 bytes become visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[which ? kBarVReady : kBarKReady]);
+      }
+      if (*abort_flag) break;
+    }
+  } else {
+    // ================================================================== softmax
+    const int rl = threadIdx.x;  // row of the item (warp w: TMEM lanes 32w .. 32w+31)
+    const int row = row0 + rl;
+    const bool live = row < TG;
+    const int ti = live ? row / G : 0, g = live ? row - (row / G) * G : 0;
+    // ---- q row -> the A tile (INT8: scaled by 2^k so its largest |q| is in [2^14, 2^15))
+    float row_scale = 1.f;
+    {
+      const uint4* qrow =
+          reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                         ((size_t)ti * p.num_q_heads + h * G + g) * D);
+      float up = 1.f;
+      if constexpr (!kBf16) {
+        float amax = 0.f;
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+          const uint4 v = live ? __ldg(qrow + c8) : make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+        }
+        int k = 0;
+        if (amax > 0.f) {
+          int ex;
+          frexpf(amax, &ex);
+          k = min(126, max(-126, 15 - ex));
+        }
+        up = pow2f(k);
+        row_scale = pow2f(-k);
+      }
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        const uint4 v = live ? __ldg(qrow + c8) : make_uint4(0, 0, 0, 0);
+        uint4 o = v;
+        if constexpr (!kBf16) {
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t r4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            r4[e] = h2_as_u32(__floats2half2_rn(__uint_as_float(w[e] << 16) * up, __uint_as_float(w[e] & 0xFFFF0000u) * up));
+          o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+        }
+        *reinterpret_cast<uint4*>(smem + Lo::kQAt + kmajor_off(rl, 8 * c8, kTcRows)) = o;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarQ]);
+    }
+    const int lim = live ? p.seq_len - p.q_len + ti + 1 : 0;  // keys this row sees (exclusive)
+    const int kend = min(lim, key_end);
+    const float qk = p.sm_scale_log2 * row_scale;
+    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+    float m_run = -INFINITY, l_run = 0.f;
+    uint8_t* prow = smem + Lo::kPAt + rl * 128;
+    uint8_t* plrow = smem + Lo::kPLoAt + rl * 128;
+    int done = 0;  // tiles completed
+    for (int i = 0; i < nt; ++i) {
+      if (!wait_warp((i & 1) ? kBarS1 : kBarS0, (i >> 1) & 1)) break;
+      tc_fence_after();
+      uint32_t sv[2][32];
+      tmem_ld32(tq + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys, sv[0]);
+      tmem_ld32(tq + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys + 32, sv[1]);
+      tmem_ld_wait();
+      const int tok0 = (pg0 + i * kTcPages) * kPage;
+      const float* ks = ksc + (i & 1) * kTcKeys;
+      const float* vs = vsc + (i & 1) * kTcKeys;
+      float z[kTcKeys];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kTcKeys; ++t) {
+        const float sval = __uint_as_float(sv[t >> 5][t & 31]);
+        const float kscale = FMT == KVQ_FMT_INT8 ? ks[t] : 1.f;
+        z[t] = (tok0 + t < kend) ? sval * kscale * qk : -INFINITY;
+        mx = fmaxf(mx, z[t]);
+      }
+      // the previous tile's P V has completed: O and the P tile may be touched
+      if (i > 0) {
+        if (!wait_warp(kBarODone, (i - 1) & 1)) break;
+        tc_fence_after();
+      }
+      const bool resc = m_run != -INFINITY && mx > m_run + kTcRescale;
+      if (__any_sync(0xffffffffu, resc)) {
+        const float alpha = resc ? exp2f(m_run - mx) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tq + Lo::kTmemO + 32 * c, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(tq + Lo::kTmemO + 32 * c, ov);
+        }
+        tmem_st_wait();
+        if (resc) {
+          l_run *= alpha;
+          m_run = mx;
+        }
+      }
+      if (m_run == -INFINITY) m_run = mx;  // first visible keys (still -inf if none)
+      float psum = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pv[2];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int t = 8 * c8 + 2 * e + q2;
+            const float pr = z[t] == -INFINITY ? 0.f : exp2f(z[t] - m_run);
+            psum += pr;
+            pv[q2] = z[t] == -INFINITY ? 0.f : (FMT == KVQ_FMT_INT8 ? pr * vs[t] : pr);
+          }
+          if constexpr (kBf16) {
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(pv[0], pv[1]);
+            hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            if constexpr (PLO) {
+              const __nv_bfloat162 lv = __floats2bfloat162_rn(pv[0] - __low2float(hv), pv[1] - __high2float(hv));
+              lw[e] = *reinterpret_cast<const uint32_t*>(&lv);
+            }
+          } else {
+            const __half2 hv = __floats2half2_rn(pv[0], pv[1]);
+            hw[e] = h2_as_u32(hv);
+            if constexpr (PLO) lw[e] = h2_as_u32(__floats2half2_rn(pv[0] - __low2float(hv), pv[1] - __high2float(hv)));
+          }
+        }
+        const int off = (c8 ^ (rl & 7)) << 4;
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if constexpr (PLO) *reinterpret_cast<uint4*>(plrow + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      l_run += psum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarPReady]);
+      done = i + 1;
+    }
+    // ================================================================ epilogue
+    bool have_o = done == nt && nt > 0;
+    if (have_o) {
+      have_o = wait_warp(kBarODone, (nt - 1) & 1);
+      tc_fence_after();
+    }
+    if (done != nt) {  // aborted: this row's result is not valid
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+    constexpr float kLn2 = 0.69314718055994530942f;
+    const bool any = m_run != -INFINITY && l_run > 0.f;
+    const float inv = any ? 1.f / l_run : 0.f;
+    const float lse = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    const bool direct = p.splits == 1;
+    const size_t qh = (size_t)h * G + g;
+    const size_t orow = direct ? (size_t)ti * p.num_q_heads + qh : ((size_t)ti * p.splits + s) * p.num_q_heads + qh;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      if (__any_sync(0xffffffffu, have_o)) {
+        tmem_ld32(tq + Lo::kTmemO + 32 * c, ov);
+        tmem_ld_wait();
+      }
+      if (!live) continue;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(have_o ? __uint_as_float(ov[e]) * inv : 0.f);
+      if (direct && p.out_bf16) {
+        uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * D + 32 * c);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(ov[8 * v4 + 2 * e]),
+                                                            __uint_as_float(ov[8 * v4 + 2 * e + 1]));
+            w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          ob[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        uint4* of = reinterpret_cast<uint4*>((direct ? reinterpret_cast<float*>(p.out) : p.o_part) + orow * D + 32 * c);
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) of[v4] = make_uint4(ov[4 * v4], ov[4 * v4 + 1], ov[4 * v4 + 2], ov[4 * v4 + 3]);
+      }
+    }
+    if (live) {
+      if (direct) {
+        if (p.lse_out) p.lse_out[orow] = lse;
+      } else {
+        p.lse_part[orow] = lse;
+      }
+    }
+  }
+  // all TMEM reads and MMAs are complete: free the columns
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lo::kTmemCols);
+  }
+}
+
+template <int FMT, int D>
+cudaError_t launch_tc_t(const PrefillParams& p, int grid, cudaStream_t stream) {
+  using Lo = TcLayout<FMT, D>;
+  if (p.out_bf16) prefill_tc_kernel<FMT, D, false><<<grid, kTcThreads, Lo::kSmemBytes, stream>>>(p);
+  else prefill_tc_kernel<FMT, D, true><<<grid, kTcThreads, Lo::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int FMT, int D>
+PrefillInstance tc_instance_of() {
+  using Lo = TcLayout<FMT, D>;
+  return PrefillInstance{{reinterpret_cast<const void*>(&prefill_tc_kernel<FMT, D, true>),
+                          reinterpret_cast<const void*>(&prefill_tc_kernel<FMT, D, false>)},
+                         Lo::kSmemBytes,
+                         kTcThreads,
+                         0,
+                         kTcRows};
+}
+
+}  // namespace
+
+bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out) {
+  if (format == KVQ_FMT_INT8 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_INT8, 256>();
+  else if (format == KVQ_FMT_INT8 && head_dim == 128) *out = tc_instance_of<KVQ_FMT_INT8, 128>();
+  else if (format == KVQ_FMT_BF16 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_BF16, 256>();
+  else if (format == KVQ_FMT_BF16 && head_dim == 128) *out = tc_instance_of<KVQ_FMT_BF16, 128>();
+  else return false;
+  return true;
+}
+
+cudaError_t launch_prefill_tc(int format, int head_dim, const PrefillParams& p, int grid, cudaStream_t stream) {
+  if (format == KVQ_FMT_INT8 && head_dim == 256) return launch_tc_t<KVQ_FMT_INT8, 256>(p, grid, stream);
+  if (format == KVQ_FMT_INT8 && head_dim == 128) return launch_tc_t<KVQ_FMT_INT8, 128>(p, grid, stream);
+  if (format == KVQ_FMT_BF16 && head_dim == 256) return launch_tc_t<KVQ_FMT_BF16, 256>(p, grid, stream);
+  if (format == KVQ_FMT_BF16 && head_dim == 128) return launch_tc_t<KVQ_FMT_BF16, 128>(p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq
