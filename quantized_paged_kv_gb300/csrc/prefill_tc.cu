@@ -47,15 +47,16 @@ struct TcLayout {
   static constexpr int kVBytes = kTcKeys * D * 2;        // [8-key group][d atom][8 keys][128 B]
   static constexpr int kPBytes = kTcRows * kTcKeys * 2;  // [128 rows][128 B]
   static constexpr int kQAt = 0;
-  static constexpr int kKAt = kQAt + kQBytes;
-  static constexpr int kVAt = kKAt + kKBytes;
-  static constexpr int kPAt = kVAt + kVBytes;
-  static constexpr int kPLoAt = kPAt + kPBytes;
-  static constexpr int kScAt = kPLoAt + kPBytes;  // float k scales [2][64], v scales [2][64]
-  static constexpr int kBarAt = kScAt + 4 * kTcKeys * 4;
-  static constexpr int kNumBars = 10;
+  static constexpr int kKAt = kQAt + kQBytes;            // two K tiles
+  static constexpr int kVAt = kKAt + 2 * kKBytes;        // two V tiles
+  static constexpr int kPAt = kVAt + 2 * kVBytes;        // P hi, then P lo
+  static constexpr int kScRing = 3;                      // scale buffers (tiles in flight)
+  static constexpr int kScAt = kPAt + 2 * kPBytes;       // float k scales [3][64], v scales [3][64]
+  static constexpr int kBarAt = kScAt + 2 * kScRing * kTcKeys * 4;
+  static constexpr int kNumBars = 14;
   static constexpr int kSlotAt = kBarAt + kNumBars * 8;
   static constexpr int kSmemBytes = 1024 + kSlotAt + 16;
+  static_assert(kNumBars >= 13, "barriers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t kTmemO = 0;          // O: D columns
   static constexpr uint32_t kTmemS = D;          // S: two buffers of 64 columns
@@ -64,7 +65,24 @@ struct TcLayout {
   static constexpr uint32_t kVLbo = 1024, kVSbo = kAtoms * 1024;
 };
 
-enum : int { kBarQ = 0, kBarKReady, kBarVReady, kBarPReady, kBarS0, kBarS1, kBarKFree, kBarODone, kBarFinal };
+// Per-buffer barriers alternate with the tile's parity (tile i uses buffer i & 1),
+// so that no waiter can see a barrier two phases ahead of the one it waits for.
+enum : int {
+  kBarQ = 0,
+  kBarP,       // P(i) written (softmax warps)
+  kBarK0,      // K(i) converted, buffers 0 / 1 (converter warps)
+  kBarK1,
+  kBarV0,      // V(i) converted
+  kBarV1,
+  kBarS0,      // S(i) = Q K(i)^T done (commit)
+  kBarS1,
+  kBarKF0,     // S(i) done: K buffer i & 1 free (commit)
+  kBarKF1,
+  kBarO0,      // P(i) V(i) done (commit)
+  kBarO1,
+  kBarFinal,
+  kBarCount
+};
 
 // byte offset of the 16-byte chunk holding elements d0 .. d0+7 (d0 % 8 == 0) of
 // row r in a K-major tile of `rows` rows ([atom][rows][128 B], 128-byte swizzle)
@@ -94,8 +112,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lo::kBarAt);
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Lo::kSlotAt);  // [0] TMEM base, [1] abort flag
-  float* ksc = reinterpret_cast<float*>(smem + Lo::kScAt);            // [2][64]
-  float* vsc = ksc + 2 * kTcKeys;                                     // [2][64]
+  float* ksc = reinterpret_cast<float*>(smem + Lo::kScAt);            // [3][64]
+  float* vsc = ksc + Lo::kScRing * kTcKeys;                           // [3][64]
   const uint32_t sbase = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -116,15 +134,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int key_end = min(p.seq_len, (pg0 + npg) * kPage);  // keys of this range (exclusive)
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[kBarQ], 4);
-    mbar_init(&bars[kBarKReady], 4);
-    mbar_init(&bars[kBarVReady], 4);
-    mbar_init(&bars[kBarPReady], 4);
-    mbar_init(&bars[kBarS0], 1);
-    mbar_init(&bars[kBarS1], 1);
-    mbar_init(&bars[kBarKFree], 1);
-    mbar_init(&bars[kBarODone], 1);
-    mbar_init(&bars[kBarFinal], 1);
+    for (int b = 0; b < kBarCount; ++b) mbar_init(&bars[b], b <= kBarV1 ? 4 : 1);
     slot[1] = 0;
     fence_mbar_init();
   }
@@ -153,41 +163,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0 && nt > 0) {
       bool ok = wait(kBarQ, 0);
       tc_fence_after();
-      auto issue_pv = [&](int j) -> bool {
-        if (!wait(kBarPReady, j & 1) || !wait(kBarVReady, j & 1)) return false;
-        tc_fence_after();
+      // step i: S(i) (K(i) ready), then P(i-1) V(i-1); S runs one tile ahead
+      for (int i = 0; ok && i <= nt; ++i) {
+        if (i < nt) {
+          if (!wait(kBarK0 + (i & 1), (i >> 1) & 1)) break;
+          tc_fence_after();
+          const uint32_t ds = tmem + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys;
+          const uint32_t kb = sbase + Lo::kKAt + (uint32_t)(i & 1) * Lo::kKBytes;
 #pragma unroll
-        for (int k = 0; k < kTcKeys / 16; ++k) {
-          const uint64_t ad = umma_desc_sw128(sbase + Lo::kPAt + 32 * k, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(sbase + Lo::kVAt + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
-          umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < KS; ++k) {
+            const int a = k >> 2, kk = k & 3;
+            const uint64_t ad = umma_desc_sw128(sbase + Lo::kQAt + a * kTcRows * 128 + 32 * kk, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(kb + a * kTcKeys * 128 + 32 * kk, 16, 1024);
+            umma_f16(ds, ad, bd, kIdescS, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars[kBarS0 + (i & 1)]);
+          umma_commit(&bars[kBarKF0 + (i & 1)]);
         }
-        if constexpr (PLO) {
+        if (i > 0) {
+          const int j = i - 1;
+          if (!wait(kBarP, j & 1) || !wait(kBarV0 + (j & 1), (j >> 1) & 1)) break;
+          tc_fence_after();
+          const uint32_t vb = sbase + Lo::kVAt + (uint32_t)(j & 1) * Lo::kVBytes;
 #pragma unroll
           for (int k = 0; k < kTcKeys / 16; ++k) {
-            const uint64_t ad = umma_desc_sw128(sbase + Lo::kPLoAt + 32 * k, 16, 1024);
-            const uint64_t bd = umma_desc_sw128(sbase + Lo::kVAt + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
-            umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, 1u);
+            const uint64_t ad = umma_desc_sw128(sbase + Lo::kPAt + 32 * k, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(vb + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
+            umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
           }
-        }
-        umma_commit(&bars[kBarODone]);
-        return true;
-      };
-      for (int i = 0; ok && i < nt; ++i) {
-        if (!wait(kBarKReady, i & 1)) break;
-        tc_fence_after();
-        const uint32_t ds = tmem + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys;
+          if constexpr (PLO) {
 #pragma unroll
-        for (int k = 0; k < KS; ++k) {
-          const int a = k >> 2, kk = k & 3;
-          const uint64_t ad = umma_desc_sw128(sbase + Lo::kQAt + a * kTcRows * 128 + 32 * kk, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(sbase + Lo::kKAt + a * kTcKeys * 128 + 32 * kk, 16, 1024);
-          umma_f16(ds, ad, bd, kIdescS, k > 0 ? 1u : 0u);
+            for (int k = 0; k < kTcKeys / 16; ++k) {
+              const uint64_t ad = umma_desc_sw128(sbase + Lo::kPAt + Lo::kPBytes + 32 * k, 16, 1024);
+              const uint64_t bd = umma_desc_sw128(vb + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
+              umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, 1u);
+            }
+          }
+          umma_commit(&bars[kBarO0 + (j & 1)]);
         }
-        umma_commit(&bars[(i & 1) ? kBarS1 : kBarS0]);
-        umma_commit(&bars[kBarKFree]);
-        if (i > 0 && !issue_pv(i - 1)) break;
-        if (i == nt - 1) issue_pv(i);
       }
       // every MMA this thread issued has completed before the TMEM is freed
       umma_commit(&bars[kBarFinal]);
@@ -200,64 +213,94 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kRowBytes = T::kRow;     // code bytes of a key row
     constexpr int kHalfBytes = kRowBytes / 2;
     constexpr int kChunks = kHalfBytes / 16;  // 16-byte source chunks of a half row
-    uint8_t* ktile = smem + Lo::kKAt;
-    uint8_t* vtile = smem + Lo::kVAt;
-    for (int i = 0; i < nt; ++i) {
+    uint8_t* ktiles = smem + Lo::kKAt;
+    uint8_t* vtiles = smem + Lo::kVAt;
+    // pool row of key n of tile i (-1: a key past the range or the sequence, or a bad page id)
+    auto tile_row = [&](int i) -> int64_t {
       const int jp = i * kTcPages + (n >> 4);  // page of the range
       const int tok = (pg0 + jp) * kPage + (n & 15);
-      int pg = -1;
-      if (jp < npg && tok < key_end) {
-        pg = p.block_table[pg0 + jp];
-        if (pg < 0 || pg >= p.num_pages) {
-          if (half == 0 && (n & 15) == 0) atomicOr(p.status, KVQ_DEV_BAD_PAGE);
-          pg = -1;
-        }
+      if (jp >= npg || tok >= key_end) return -1;
+      const int pg = p.block_table[pg0 + jp];
+      if (pg < 0 || pg >= p.num_pages) {
+        if (half == 0 && (n & 15) == 0) atomicOr(p.status, KVQ_DEV_BAD_PAGE);
+        return -1;
       }
-      const size_t rowoff = pg >= 0 ? ((size_t)pg * p.num_kv_heads + h) * kPage + (n & 15) : 0;
-      for (int which = 0; which < 2; ++which) {
-        const uint8_t* src = (which ? p.v_codes : p.k_codes) + rowoff * kRowBytes + half * kHalfBytes;
-        uint4 raw[kChunks];
+      return ((int64_t)pg * p.num_kv_heads + h) * kPage + (n & 15);
+    };
+    auto load = [&](const uint8_t* base, int64_t ro, uint4 (&raw)[kChunks]) {
+      const uint4* src = reinterpret_cast<const uint4*>(base + (ro >= 0 ? ro : 0) * kRowBytes + half * kHalfBytes);
 #pragma unroll
-        for (int u = 0; u < kChunks; ++u)
-          raw[u] = pg >= 0 ? __ldg(reinterpret_cast<const uint4*>(src) + u) : make_uint4(0, 0, 0, 0);
-        // the buffer is free once the MMAs of the previous tile that read it are done
-        if (i > 0 && !wait_warp(which ? kBarODone : kBarKFree, (i - 1) & 1)) break;
-        if constexpr (FMT == KVQ_FMT_INT8) {
-          // both scales of the tile go out with K: the softmax reads them once S is done
-          if (which == 0 && half == 0) {
-            ksc[(i & 1) * kTcKeys + n] = pg >= 0 ? __ldg(reinterpret_cast<const float*>(p.k_scales) + rowoff) : 0.f;
-            vsc[(i & 1) * kTcKeys + n] = pg >= 0 ? __ldg(reinterpret_cast<const float*>(p.v_scales) + rowoff) : 0.f;
-          }
+      for (int u = 0; u < kChunks; ++u) raw[u] = ro >= 0 ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+    };
+    // write a half row (raw codes of key n) as fp16 / bf16 into K tile buffer b (which = 0) or V
+    auto put = [&](int which, int b, const uint4 (&raw)[kChunks]) {
+      uint8_t* ktile = ktiles + b * Lo::kKBytes;
+      uint8_t* vtile = vtiles + b * Lo::kVBytes;
+      if constexpr (FMT == KVQ_FMT_INT8) {
 #pragma unroll
-          for (int u = 0; u < kChunks; ++u) {
-            const uint32_t w[4] = {raw[u].x ^ 0x80808080u, raw[u].y ^ 0x80808080u, raw[u].z ^ 0x80808080u,
-                                   raw[u].w ^ 0x80808080u};
-            const uint4 lo = make_uint4(i8pair_to_h2<0x4140>(w[0]), i8pair_to_h2<0x4342>(w[0]),
-                                        i8pair_to_h2<0x4140>(w[1]), i8pair_to_h2<0x4342>(w[1]));
-            const uint4 hi = make_uint4(i8pair_to_h2<0x4140>(w[2]), i8pair_to_h2<0x4342>(w[2]),
-                                        i8pair_to_h2<0x4140>(w[3]), i8pair_to_h2<0x4342>(w[3]));
-            const int d0 = half * (D / 2) + 16 * u;
-            if (which == 0) {
-              *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = lo;
-              *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0 + 8, kTcKeys)) = hi;
-            } else {
-              *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = lo;
-              *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0 + 8)) = hi;
-            }
-          }
-        } else {  // BF16: 8 elements a chunk, copied as they are
-#pragma unroll
-          for (int u = 0; u < kChunks; ++u) {
-            const int d0 = half * (D / 2) + 8 * u;
-            if (which == 0) *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = raw[u];
-            else *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = raw[u];
+        for (int u = 0; u < kChunks; ++u) {
+          const uint32_t w[4] = {raw[u].x ^ 0x80808080u, raw[u].y ^ 0x80808080u, raw[u].z ^ 0x80808080u,
+                                 raw[u].w ^ 0x80808080u};
+          const uint4 lo = make_uint4(i8pair_to_h2<0x4140>(w[0]), i8pair_to_h2<0x4342>(w[0]),
+                                      i8pair_to_h2<0x4140>(w[1]), i8pair_to_h2<0x4342>(w[1]));
+          const uint4 hi = make_uint4(i8pair_to_h2<0x4140>(w[2]), i8pair_to_h2<0x4342>(w[2]),
+                                      i8pair_to_h2<0x4140>(w[3]), i8pair_to_h2<0x4342>(w[3]));
+          const int d0 = half * (D / 2) + 16 * u;
+          if (which == 0) {
+            *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = lo;
+            *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0 + 8, kTcKeys)) = hi;
+          } else {
+            *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = lo;
+            *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0 + 8)) = hi;
           }
         }
-        fence_proxy_async_smem();  // the tile's fp16 bytes become visible to the tensor cores
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[which ? kBarVReady : kBarKReady]);
+      } else {  // BF16: 8 elements a chunk, copied as they are
+#pragma unroll
+        for (int u = 0; u < kChunks; ++u) {
+          const int d0 = half * (D / 2) + 8 * u;
+          if (which == 0) *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = raw[u];
+          else *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = raw[u];
+        }
       }
-      if (*abort_flag) break;
+    };
+    // one tensor's loads are in flight while the other is written: K(i+1) while
+    // V(i) is written, V(i) while K(i) is written
+    uint4 rk[kChunks], rv[kChunks];
+    int64_t ro = nt > 0 ? tile_row(0) : -1;
+    if (nt > 0) load(p.k_codes, ro, rk);
+    for (int i = 0; i < nt; ++i) {
+      float ksv = 0.f, vsv = 0.f;
+      if constexpr (FMT == KVQ_FMT_INT8) {
+        if (ro >= 0 && half == 0) {
+          ksv = __ldg(reinterpret_cast<const float*>(p.k_scales) + ro);
+          vsv = __ldg(reinterpret_cast<const float*>(p.v_scales) + ro);
+        }
+      }
+      load(p.v_codes, ro, rv);
+      // K buffer i & 1 is free once S(i-2) is done
+      if (i > 1 && !wait_warp(kBarKF0 + (i & 1), ((i - 2) >> 1) & 1)) break;
+      if constexpr (FMT == KVQ_FMT_INT8) {
+        // both scales of the tile go out with K: the softmax reads them once S is
+        // done.  Ring of three: the last reader of this slot, the softmax of tile
+        // i-3, finished before P(i-3) V(i-3), which V(i-1) above waited for.
+        if (half == 0) {
+          ksc[(i % Lo::kScRing) * kTcKeys + n] = ksv;
+          vsc[(i % Lo::kScRing) * kTcKeys + n] = vsv;
+        }
+      }
+      put(0, i & 1, rk);
+      fence_proxy_async_smem();  // the tile's bytes become visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarK0 + (i & 1)]);
+      const int64_t ro_next = i + 1 < nt ? tile_row(i + 1) : -1;
+      if (i + 1 < nt) load(p.k_codes, ro_next, rk);
+      // V buffer i & 1 is free once P(i-2) V(i-2) is done
+      if (i > 1 && !wait_warp(kBarO0 + (i & 1), ((i - 2) >> 1) & 1)) break;
+      put(1, i & 1, rv);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarV0 + (i & 1)]);
+      ro = ro_next;
     }
   } else {
     // ================================================================== softmax
@@ -312,8 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float qk = p.sm_scale_log2 * row_scale;
     const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     float m_run = -INFINITY, l_run = 0.f;
-    uint8_t* prow = smem + Lo::kPAt + rl * 128;
-    uint8_t* plrow = smem + Lo::kPLoAt + rl * 128;
+
     int done = 0;  // tiles completed
     for (int i = 0; i < nt; ++i) {
       if (!wait_warp((i & 1) ? kBarS1 : kBarS0, (i >> 1) & 1)) break;
@@ -323,20 +365,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld32(tq + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys + 32, sv[1]);
       tmem_ld_wait();
       const int tok0 = (pg0 + i * kTcPages) * kPage;
-      const float* ks = ksc + (i & 1) * kTcKeys;
-      const float* vs = vsc + (i & 1) * kTcKeys;
+      const float* ks = ksc + (i % Lo::kScRing) * kTcKeys;
+      const float* vs = vsc + (i % Lo::kScRing) * kTcKeys;
+      // pass 1: logits (log2 units) in place of S, and the tile maximum (four
+      // independent chains); only a tile that crosses the row's limit is masked
       float z[kTcKeys];
-      float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < kTcKeys; ++t) {
-        const float sval = __uint_as_float(sv[t >> 5][t & 31]);
-        const float kscale = FMT == KVQ_FMT_INT8 ? ks[t] : 1.f;
-        z[t] = (tok0 + t < kend) ? sval * kscale * qk : -INFINITY;
-        mx = fmaxf(mx, z[t]);
+      for (int t = 0; t < kTcKeys; ++t) z[t] = __uint_as_float(sv[t >> 5][t & 31]);
+      float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const int nvis = kend - tok0;  // visible keys of this tile for this row
+#pragma unroll
+      for (int c4 = 0; c4 < kTcKeys / 4; ++c4) {
+        float4 k4 = make_float4(qk, qk, qk, qk);
+        if constexpr (FMT == KVQ_FMT_INT8) {
+          k4 = *reinterpret_cast<const float4*>(ks + 4 * c4);
+          k4.x *= qk; k4.y *= qk; k4.z *= qk; k4.w *= qk;
+        }
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * c4 + e;
+          float zz = z[t] * kk[e];
+          if (nvis < kTcKeys) zz = t < nvis ? zz : -INFINITY;
+          z[t] = zz;
+          mxs[e] = fmaxf(mxs[e], zz);
+        }
       }
-      // the previous tile's P V has completed: O and the P tile may be touched
+      const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
+      // the P tile and O may be touched once P(i-1) V(i-1) has completed
       if (i > 0) {
-        if (!wait_warp(kBarODone, (i - 1) & 1)) break;
+        if (!wait_warp(kBarO0 + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
         tc_fence_after();
       }
       const bool resc = m_run != -INFINITY && mx > m_run + kTcRescale;
@@ -358,19 +416,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (m_run == -INFINITY) m_run = mx;  // first visible keys (still -inf if none)
-      float psum = 0.f;
+      uint8_t* prow = smem + Lo::kPAt + rl * 128;
+      uint8_t* plrow = prow + Lo::kPBytes;
+      // pass 2: p = 2^(z - m) <= 2^8 (ex2.approx.ftz: results below 2^-126 are 0,
+      // a masked key's z = -inf gives exactly 0), P' = p v_scale, packed hi (+ lo)
+      float psums[4] = {0.f, 0.f, 0.f, 0.f};
+      const float msub = m_run == -INFINITY ? 0.f : m_run;  // a row with no visible key: every z is -inf
 #pragma unroll
       for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
         uint32_t hw[4], lw[4];
+        float v8[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if constexpr (FMT == KVQ_FMT_INT8) {
+          const float4 va = *reinterpret_cast<const float4*>(vs + 8 * c8);
+          const float4 vb = *reinterpret_cast<const float4*>(vs + 8 * c8 + 4);
+          v8[0] = va.x; v8[1] = va.y; v8[2] = va.z; v8[3] = va.w;
+          v8[4] = vb.x; v8[5] = vb.y; v8[6] = vb.z; v8[7] = vb.w;
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float pv[2];
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2) {
             const int t = 8 * c8 + 2 * e + q2;
-            const float pr = z[t] == -INFINITY ? 0.f : exp2f(z[t] - m_run);
-            psum += pr;
-            pv[q2] = z[t] == -INFINITY ? 0.f : (FMT == KVQ_FMT_INT8 ? pr * vs[t] : pr);
+            float pr;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pr) : "f"(z[t] - msub));
+            psums[q2 + 2 * (e & 1)] += pr;
+            // v_scale of an unwritten slot may be NaN: a masked key contributes exactly 0
+            pv[q2] = FMT == KVQ_FMT_INT8 ? (pr > 0.f ? pr * v8[2 * e + q2] : 0.f) : pr;
           }
           if constexpr (kBf16) {
             const __nv_bfloat162 hv = __floats2bfloat162_rn(pv[0], pv[1]);
@@ -389,17 +461,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         if constexpr (PLO) *reinterpret_cast<uint4*>(plrow + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
-      l_run += psum;
+      l_run += (psums[0] + psums[1]) + (psums[2] + psums[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarPReady]);
+      if (lane == 0) mbar_arrive(&bars[kBarP]);
       done = i + 1;
     }
     // ================================================================ epilogue
     bool have_o = done == nt && nt > 0;
     if (have_o) {
-      have_o = wait_warp(kBarODone, (nt - 1) & 1);
+      have_o = wait_warp(kBarO0 + ((nt - 1) & 1), ((nt - 1) >> 1) & 1);
       tc_fence_after();
     }
     if (done != nt) {  // aborted: this row's result is not valid
