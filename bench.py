@@ -627,12 +627,13 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     torch.cuda.empty_cache()
     # prefill: a 2,048-token chunk at the end of the 32K context (and the first chunk)
     wl = W.make("long_int8")
-    ls = LayerSet(wl, "int8", 2, dev)
-    for T in (512, 2048):
-        res[f"prefill_long_int8/T={T}"] = time_prefill(ls, T, peak_tf=peak_tf)
-    del ls
-    gc.collect()
-    torch.cuda.empty_cache()
+    for fmt, Ts in (("int8", (512, 2048)), ("nvfp4", (2048,))):
+        ls = LayerSet(wl, fmt, 2, dev)
+        for T in Ts:
+            res[f"prefill_long_{fmt}/T={T}"] = time_prefill(ls, T, peak_tf=peak_tf)
+        del ls
+        gc.collect()
+        torch.cuda.empty_cache()
     # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences), INT8 and NVFP4
     wl = W.make("append_int8")
     for fmt in ("int8", "nvfp4"):

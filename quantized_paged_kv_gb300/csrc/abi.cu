@@ -751,6 +751,8 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
   p.row_blocks = (q_len * G + inst.rows - 1) / inst.rows;
   p.out_bf16 = out_dtype == KVQ_OUT_BF16;
   p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+  p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
+  p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
   rc = memory_kind(out, "out", nullptr);
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

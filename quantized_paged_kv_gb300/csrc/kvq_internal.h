@@ -48,6 +48,7 @@ struct PrefillParams {
   int32_t q_len, seq_len, num_q_heads, num_kv_heads, num_pages;
   int32_t splits, row_blocks, out_bf16;
   float sm_scale_log2;
+  float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scales (1 otherwise)
 };
 
 struct AppendParams {

@@ -1,5 +1,5 @@
-// prefill_tc.cu — causal attention of a prompt chunk over a paged INT8 / BF16
-// cache on the fifth-generation tensor cores (tcgen05.mma, accumulators in TMEM)
+// prefill_tc.cu — causal attention of a prompt chunk over a paged INT8 / NVFP4 /
+// BF16 cache on the fifth-generation tensor cores (tcgen05.mma, accumulators in TMEM)
 // ("half-the-memory-int8-kv-cache", section "Read the prompt using a small
 // temporary buffer": a chunk of prompt tokens does enough work per key that each
 // key is converted once to fp16 and then used by many queries; the history is
@@ -12,7 +12,8 @@
 // Work item (one CTA): 128 query rows (token, query head) of one KV head — the
 // MMA's M — against one key range (a split; splits are merged by the merge
 // kernel), in tiles of 64 keys (four pages).  Warp roles:
-//   * warps 4..7 (converters): per tile, K codes -> fp16 in the canonical K-major
+//   * warps 4..7 (converters): per tile, K codes -> fp16 (NVFP4: codes x group
+//     scale, exact in fp16; INT8: the codes) in the canonical K-major
 //     layout with the 128-byte swizzle (the B operand of S = Q K^T) and V codes
 //     -> fp16 in the MN-major layout (the B operand of O = P V, no transpose); the
 //     INT8 scales go to shared memory.  Keys past the range or the sequence are
@@ -233,10 +234,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int u = 0; u < kChunks; ++u) raw[u] = ro >= 0 ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
     };
     // write a half row (raw codes of key n) as fp16 / bf16 into K tile buffer b (which = 0) or V
-    auto put = [&](int which, int b, const uint4 (&raw)[kChunks]) {
+    auto put = [&](int which, int b, const uint4 (&raw)[kChunks], uint2 gsc) {
       uint8_t* ktile = ktiles + b * Lo::kKBytes;
       uint8_t* vtile = vtiles + b * Lo::kVBytes;
-      if constexpr (FMT == KVQ_FMT_INT8) {
+      if constexpr (FMT == KVQ_FMT_NVFP4) {
+        // 16 bytes = 32 values = two scale groups; E2M1 x E4M3 is exact in fp16
+        // (at most 6 significant bits, magnitudes 2^-10 .. 2688)
+#pragma unroll
+        for (int u = 0; u < kChunks; ++u) {
+          const uint32_t sb = u < 2 ? gsc.x : gsc.y;  // group scale bytes 2u, 2u+1 of the half row
+          const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t bsel = 2 * (u & 1) + (j >> 1);  // byte of sb holding this word's group
+            const __half2 sdh = u32_as_h2(e4m3x2_to_h2(prmt(sb, 0u, bsel | (bsel << 4))));
+            uint32_t f[4];
+            e2m1x8_to_h2x4(w[j], f);
+            const uint4 o = make_uint4(h2_as_u32(__hmul2(u32_as_h2(f[0]), sdh)), h2_as_u32(__hmul2(u32_as_h2(f[1]), sdh)),
+                                       h2_as_u32(__hmul2(u32_as_h2(f[2]), sdh)), h2_as_u32(__hmul2(u32_as_h2(f[3]), sdh)));
+            const int d0 = half * (D / 2) + 32 * u + 8 * j;
+            if (which == 0) *reinterpret_cast<uint4*>(ktile + kmajor_off(n, d0, kTcKeys)) = o;
+            else *reinterpret_cast<uint4*>(vtile + vtile_off<D>(n, d0)) = o;
+          }
+        }
+      } else if constexpr (FMT == KVQ_FMT_INT8) {
 #pragma unroll
         for (int u = 0; u < kChunks; ++u) {
           const uint32_t w[4] = {raw[u].x ^ 0x80808080u, raw[u].y ^ 0x80808080u, raw[u].z ^ 0x80808080u,
@@ -270,6 +291,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (nt > 0) load(p.k_codes, ro, rk);
     for (int i = 0; i < nt; ++i) {
       float ksv = 0.f, vsv = 0.f;
+      uint2 kgs = make_uint2(0, 0), vgs = make_uint2(0, 0);  // NVFP4: this half row's group scale bytes
+      if constexpr (FMT == KVQ_FMT_NVFP4) {
+        if (ro >= 0) {
+          kgs = __ldg(reinterpret_cast<const uint2*>(p.k_scales + ro * 16 + half * 8));
+          vgs = __ldg(reinterpret_cast<const uint2*>(p.v_scales + ro * 16 + half * 8));
+        }
+      }
       if constexpr (FMT == KVQ_FMT_INT8) {
         if (ro >= 0 && half == 0) {
           ksv = __ldg(reinterpret_cast<const float*>(p.k_scales) + ro);
@@ -288,7 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           vsc[(i % Lo::kScRing) * kTcKeys + n] = vsv;
         }
       }
-      put(0, i & 1, rk);
+      put(0, i & 1, rk, kgs);
       fence_proxy_async_smem();  // the tile's bytes become visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarK0 + (i & 1)]);
@@ -296,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (i + 1 < nt) load(p.k_codes, ro_next, rk);
       // V buffer i & 1 is free once P(i-2) V(i-2) is done
       if (i > 1 && !wait_warp(kBarO0 + (i & 1), ((i - 2) >> 1) & 1)) break;
-      put(1, i & 1, rv);
+      put(1, i & 1, rv, vgs);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarV0 + (i & 1)]);
@@ -352,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const int lim = live ? p.seq_len - p.q_len + ti + 1 : 0;  // keys this row sees (exclusive)
     const int kend = min(lim, key_end);
-    const float qk = p.sm_scale_log2 * row_scale;
+    const float qk = p.sm_scale_log2 * row_scale * p.k_gs_inv;  // NVFP4: the tiles hold values x gs
     const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     float m_run = -INFINITY, l_run = 0.f;
 
@@ -480,7 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     constexpr float kLn2 = 0.69314718055994530942f;
     const bool any = m_run != -INFINITY && l_run > 0.f;
-    const float inv = any ? 1.f / l_run : 0.f;
+    const float inv = any ? p.v_gs_inv / l_run : 0.f;
     const float lse = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     const bool direct = p.splits == 1;
     const size_t qh = (size_t)h * G + g;
@@ -553,7 +581,8 @@ PrefillInstance tc_instance_of() {
 }  // namespace
 
 bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out) {
-  if (format == KVQ_FMT_INT8 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_INT8, 256>();
+  if (format == KVQ_FMT_NVFP4 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_NVFP4, 256>();
+  else if (format == KVQ_FMT_INT8 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_INT8, 256>();
   else if (format == KVQ_FMT_INT8 && head_dim == 128) *out = tc_instance_of<KVQ_FMT_INT8, 128>();
   else if (format == KVQ_FMT_BF16 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_BF16, 256>();
   else if (format == KVQ_FMT_BF16 && head_dim == 128) *out = tc_instance_of<KVQ_FMT_BF16, 128>();
@@ -562,6 +591,7 @@ bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out) {
 }
 
 cudaError_t launch_prefill_tc(int format, int head_dim, const PrefillParams& p, int grid, cudaStream_t stream) {
+  if (format == KVQ_FMT_NVFP4 && head_dim == 256) return launch_tc_t<KVQ_FMT_NVFP4, 256>(p, grid, stream);
   if (format == KVQ_FMT_INT8 && head_dim == 256) return launch_tc_t<KVQ_FMT_INT8, 256>(p, grid, stream);
   if (format == KVQ_FMT_INT8 && head_dim == 128) return launch_tc_t<KVQ_FMT_INT8, 128>(p, grid, stream);
   if (format == KVQ_FMT_BF16 && head_dim == 256) return launch_tc_t<KVQ_FMT_BF16, 256>(p, grid, stream);

@@ -18,11 +18,11 @@ def _lib():
     H.ensure_built()
 
 
-def _check(wl, fmt, T, splits=0, out_dtype="f32", units=None):
+def _check(wl, fmt, T, splits=0, out_dtype="f32", units=None, gs=(1.0, 1.0)):
     from quantized_paged_kv_gb300 import prefill
 
     assert wl.B == 1
-    cache = H.gpu_cache(wl, fmt)
+    cache = H.gpu_cache(wl, fmt, gs=gs)
     q = wl.q_tokens(T)  # [1, T, Hq, D]
     qt = torch.from_numpy(q[0]).to(torch.bfloat16).cuda()
     od = {"f32": torch.float32, "bf16": torch.bfloat16}[out_dtype]
@@ -31,18 +31,22 @@ def _check(wl, fmt, T, splits=0, out_dtype="f32", units=None):
     bt = torch.from_numpy(wl.block_tables[0]).cuda()
     prefill(cache, qt, bt, int(wl.seq_lens[0]), out, wl.sm_scale, lse_out=lse, splits=splits, checked=True)
     torch.cuda.synchronize()
-    pools = H.oracle_pools(wl, fmt)
+    pools = H.oracle_pools(wl, fmt, gs=gs)
     ref, ref_lse = oatt.paged_verify(fmt, pools, q, wl.block_tables, wl.seq_lens, wl.sm_scale, units=units)
     o = out.float().cpu().numpy()
     l = lse.cpu().numpy()
     sel = ~np.isnan(ref_lse[0])
     err = np.abs(o - ref[0])[sel]
     assert np.all(np.isfinite(o[sel])), (fmt, T, splits)
-    assert err.max() <= H.tol(out_dtype), (fmt, T, splits, err.max())
+    bound = H.tol(out_dtype)
+    if out_dtype == "bf16" and np.abs(ref[0][sel]).max() > 2.5:
+        # bf16 rounding alone is 2^-8 |out| for large outputs (the tolerance reading)
+        bound = np.maximum(bound, 2.0 ** -8 * np.abs(ref[0][sel]))
+    assert np.all(err <= bound), (fmt, T, splits, err.max())
     assert np.abs(l[sel] - ref_lse[0][sel]).max() < 1e-3
 
 
-@pytest.mark.parametrize("fmt", ["int8", "bf16"])
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
 @pytest.mark.parametrize("T", [1, 5, 37, 130])
 def test_prefill_d256_gqa6(fmt, T):
     wl = W.make("tiny_int8", lens=("list", [700]), seed=41)
@@ -55,6 +59,15 @@ def test_prefill_d128_gqa4_bf16_out(fmt):
     wl = W.make("serving_int8", lens=("list", [1500]), seed=42)
     _check(wl, fmt, 200, 0, "bf16")
     _check(wl, fmt, 200, 2, "bf16")
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_prefill_nvfp4_tensor_global_scales(out_dtype):
+    # the global scales of the NVFP4 page's standalone choice (448 * 6 / amax per tensor)
+    wl = W.make("tiny_int8", lens=("list", [900]), seed=44)
+    gs = H.global_scales(wl, "nvfp4")
+    _check(wl, "nvfp4", 70, 0, out_dtype, gs=gs)
+    _check(wl, "nvfp4", 70, 2, out_dtype, gs=gs)
 
 
 def test_prefill_whole_sequence_and_tail_page():
