@@ -192,5 +192,4 @@ def test_prefill_split_choice_and_workspace(kvq):
     with pytest.raises(kvq.KvqError):
         kvq.kvq_prefill_splits(s, 10, 24, 5, 152)  # q_len > seq_len
     nv = _struct(kvq, fmt="nvfp4")
-    with pytest.raises(kvq.KvqError):
-        kvq.kvq_prefill_splits(nv, 10, 24, 500, 152)  # no NVFP4 prefill kernel
+    assert kvq.kvq_prefill_splits(nv, 10, 24, 500, 152) == 2  # NVFP4 runs on the same prefill kernel
