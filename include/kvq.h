@@ -307,11 +307,14 @@ int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t ba
  * Causal attention of a prompt chunk: q holds the last q_len of one sequence's
  * seq_len tokens (their K/V already appended); chunk token i sits at position
  * seq_len - q_len + i and attends over tokens 0 .. seq_len - q_len + i of the
- * cache, read in place (no converted copy: codes enter the tensor cores as exact
- * integers, as in the decode).  A work item is 128 query rows (token, query head)
- * of one KV head against one of `splits` key ranges; with splits > 1 the
- * partials are combined by the merge kernel on the same stream.  INT8 and BF16
- * caches, head_dim 128 or 256, 1 <= num_q_heads / num_kv_heads <= 8.
+ * cache.  Each 64-key tile of the cache is converted once per work item into an
+ * fp16 (BF16 cache: bf16) copy in shared memory (INT8: the exact integer codes;
+ * NVFP4: E2M1 x E4M3 group scale, exact in fp16) and multiplied on the tensor
+ * cores (tcgen05.mma, fp32 accumulators in tensor memory).  A work item is 128
+ * query rows (token, query head) of one KV head against one of `splits` key
+ * ranges; with splits > 1 the partials are combined by the merge kernel on the
+ * same stream.  INT8 and BF16 caches at head_dim 128 or 256, NVFP4 at 256;
+ * 1 <= num_q_heads / num_kv_heads <= 8.
  *   q              device bf16 [q_len][num_q_heads][head_dim]
  *   block_table    device int32 [max_pages]: the sequence's pages
  *   seq_len        host: tokens of the sequence, the q_len new ones included
