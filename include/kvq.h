@@ -83,7 +83,7 @@ enum {
                           without loading the model": the checked API syncs) */
   KVQ_SKIP_MERGE = 2u, /* decode only: leave the split partials in the workspace and
                           do not launch the merge (the caller calls kvq_split_merge) */
-  KVQ_EARLY_START = 4u /* decode only: the plan and the block tables of this call are
+  KVQ_EARLY_START = 4u, /* decode only: the plan and the block tables of this call are
                           not written by the kernel just before it on the stream, so the
                           decode may read them (and find its first pages) while that
                           kernel is still running.  Every other input (q, the cache,
@@ -91,6 +91,11 @@ enum {
                           has completed.  The decode kernel is always launched as a
                           programmatic dependent of the preceding kernel; without this
                           flag it waits for that kernel before reading anything. */
+  KVQ_TEST_STALL = 1u << 30 /* decode only, for testing the failure path: the
+                          producers issue no page copies and every pipeline wait
+                          gives up after 2 ms, so the call ends with KVQ_DEV_TIMEOUT
+                          in the status word (KVQ_ERR_DEVICE_TIMEOUT in checked mode)
+                          and the context stays usable.  The outputs are undefined. */
 };
 
 /* device status word bits (kvq_read_status) */

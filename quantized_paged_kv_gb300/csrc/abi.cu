@@ -601,6 +601,8 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   p.heads_per_cta = hg;
   p.out_bf16 = out_dtype == KVQ_OUT_BF16;
   p.early_start = (flags & KVQ_EARLY_START) ? 1 : 0;
+  p.drop_copies = (flags & KVQ_TEST_STALL) ? 1 : 0;
+  p.wait_limit_ns = (flags & KVQ_TEST_STALL) ? 2000000ull : 2000000000ull;  // 2 ms / 2 s
   p.q_len = q_len;
   rc = memory_kind(out, "out", &p.out_host);
   if (rc) return rc;

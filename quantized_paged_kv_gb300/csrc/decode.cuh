@@ -422,12 +422,14 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
             const int cnt32 = min(32, mine - base);
             for (int kk = 0; kk < cnt32; ++kk) {
               const int pg = ids[buf * 32 + kk];
-              if (rnd > 0 && !mbar_wait(&empty[st], (rnd - 1) & 1, kWaitLimitNs)) {
+              if (rnd > 0 && !mbar_wait(&empty[st], (rnd - 1) & 1, p.wait_limit_ns)) {
                 atomicOr(p.status, KVQ_DEV_TIMEOUT);
                 ok = false;
                 break;
               }
-              if (pg >= 0) {
+              if (p.drop_copies) {
+                // failure-path test: the stage is never filled, so its consumers' wait runs out
+              } else if (pg >= 0) {
                 uint8_t* kc = codes + st * stage_code;
                 mbar_arrive_expect_tx(&full[st], stage_code + stage_scale);
                 tma_load_5d(kc, &tm_k, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       for (int idx = pi; idx < last_n; idx += NP) {
         const int g = last_first + idx;
         if (g + NST < last_first + last_n) continue;  // a later page of this stage was issued
-        if (!mbar_wait(&full[g % NST], (g / NST) & 1, kWaitLimitNs)) {
+        if (!mbar_wait(&full[g % NST], (g / NST) & 1, p.wait_limit_ns)) {
           atomicOr(p.status, KVQ_DEV_TIMEOUT);
           break;
         }
@@ -610,7 +612,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     // this warp's pages: idx = grp, grp + WPH, ... ; global ring position gidx + idx
     int st = (gidx + grp) % NST, rnd = (gidx + grp) / NST;
     for (int idx = grp; idx < n; idx += WPH) {
-      const bool got = mbar_wait(&full[st], rnd & 1, kWaitLimitNs);
+      const bool got = mbar_wait(&full[st], rnd & 1, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) atomicOr(p.status, KVQ_DEV_TIMEOUT);
         alive = false;

@@ -29,6 +29,8 @@ struct DecodeParams {
   int32_t out_bf16;
   int32_t early_start;         // read plan / block tables before waiting for the preceding kernel
   int32_t out_host;            // out is pinned host memory: direct rows are written with plain stores
+  int32_t drop_copies;         // failure-path test: producers issue no page copies
+  uint64_t wait_limit_ns;      // limit of every pipeline wait
   float sm_scale_log2;         // sm_scale * log2(e)
   float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scale
 };

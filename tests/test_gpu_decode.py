@@ -301,3 +301,29 @@ def test_pageable_host_output_is_refused():
             Bd._ptr(plan.workspace), plan.workspace.numel(), Bd._ptr(out), Bd.KVQ_OUT_F32, None, 0, None)
         Bd._check(rc, "kvq_paged_decode_attention")
     assert e.value.code == 1 and "pageable" in str(e.value)
+
+
+def test_stalled_pipeline_times_out_and_the_context_survives():
+    """Failure path without a fault: with KVQ_TEST_STALL the producers issue no
+    page copies, every bounded wait gives up after 2 ms, and checked mode reports
+    KVQ_ERR_DEVICE_TIMEOUT; the next call on the same plan and workspace (the
+    status word was read and cleared) gives the oracle's result."""
+    from quantized_paged_kv_gb300 import DecodePlan, KvqError, decode
+    from quantized_paged_kv_gb300 import _binding as B
+
+    wl = W.make("tiny_int8")
+    cache = H.gpu_cache(wl, "int8")
+    qt = torch.from_numpy(wl.q()).to(torch.bfloat16).cuda()
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    sl = torch.from_numpy(wl.seq_lens).cuda()
+    out = torch.full((wl.B, wl.Hq, wl.D), float("nan"), dtype=torch.float32, device="cuda")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=4)
+    with pytest.raises(KvqError) as e:
+        B.kvq_paged_decode_attention(cache.struct, qt, wl.sm_scale, bt, sl, plan.plan, plan.total_splits,
+                                     plan.num_ctas, plan.workspace, out, None, B.KVQ_CHECKED | B.KVQ_TEST_STALL)
+    assert e.value.code == 6 and "timed out" in str(e.value)
+    decode(cache, plan, qt, bt, sl, out, wl.sm_scale, checked=True)
+    torch.cuda.synchronize()
+    ref, _ = H.oracle_decode(wl, "int8", H.oracle_pools(wl, "int8"))
+    assert np.abs(out.cpu().numpy() - ref).max() <= H.tol("f32")
+
