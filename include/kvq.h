@@ -225,7 +225,9 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
 
 /* Workspace bytes for a decode call: a 256-byte status block, then
  * lse_part float[total_splits][num_q_heads] (padded to 256 bytes), then
- * o_part float[total_splits][num_q_heads][head_dim].  The status block must be
+ * o_part float[total_splits][num_q_heads][head_dim] (256-byte aligned), then room
+ * for a bf16 copy of q (a query block in pinned host memory is copied there once
+ * per call, so that the decode reads it from device memory).  The status block must be
  * zero before the first call (e.g. cudaMemset once); the library only ORs bits
  * into it and kvq_read_status clears it. */
 size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int32_t head_dim);

@@ -459,7 +459,8 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
 size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int32_t head_dim) {
   if (total_splits < 0 || num_q_heads < 0 || head_dim < 0) return 0;
   const size_t rows = (size_t)total_splits * num_q_heads;
-  return 256 + align256(rows * sizeof(float)) + rows * head_dim * sizeof(float);
+  // status, lse partials, o partials, and room for a bf16 copy of q (total_splits >= rows of q)
+  return 256 + align256(rows * sizeof(float)) + align256(rows * head_dim * sizeof(float)) + rows * head_dim * 2;
 }
 
 int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_heads, int32_t head_dim,
@@ -580,8 +581,20 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   if (rc) return rc;
   float *o_part = nullptr, *lse_part = nullptr;
   kvq_workspace_partials(workspace, total_splits, num_q_heads, D, &o_part, &lse_part);
+  // q in pinned host memory: one copy into the workspace, read by the decode
+  int32_t q_host = 0;
+  rc = memory_kind(q, "q", &q_host);
+  if (rc) return rc;
+  const void* q_dev = q;
+  if (q_host) {
+    const size_t rows = (size_t)total_splits * num_q_heads;
+    void* q_stage = reinterpret_cast<char*>(o_part) + align256(rows * D * sizeof(float));
+    const cudaError_t es = kvq::launch_q_stage(q, q_stage, (size_t)batch * num_q_heads * D * 2, st);
+    if (es != cudaSuccess) return cuda_fail(es, "q staging launch");
+    q_dev = q_stage;
+  }
   kvq::DecodeParams p{};
-  p.q = q;
+  p.q = q_dev;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.plan = plan;

@@ -89,6 +89,8 @@ struct PrefillInstance {
   int launch_regs;             // registers a thread the kernel's register split assumes (0: no split)
   int rows;                    // query rows of a work item
 };
+// copy of the query block from host memory into the workspace (programmatic dependent)
+cudaError_t launch_q_stage(const void* src, void* dst, size_t bytes, cudaStream_t stream);
 // the prefill kernel (tcgen05 tensor cores, accumulators in TMEM)
 bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out);
 cudaError_t launch_prefill_tc(int format, int head_dim, const PrefillParams& p, int grid, cudaStream_t stream);

@@ -146,7 +146,8 @@ def test_planner_override_and_auto(kvq):
 
 def test_workspace_layout(kvq):
     n = kvq.kvq_decode_workspace_bytes(38, 24, 256)
-    assert n == 256 + ((38 * 24 * 4 + 255) // 256) * 256 + 38 * 24 * 256 * 4
+    # status, lse partials (padded), o partials (padded), a bf16 copy of q
+    assert n == 256 + ((38 * 24 * 4 + 255) // 256) * 256 + 38 * 24 * 256 * 4 + 38 * 24 * 256 * 2
 
 
 def test_host_validation_errors(kvq):
