@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // done.  Ring of three: the last reader of this slot, the softmax of tile
         // i-3, finished before P(i-3) V(i-3), which V(i-1) above waited for.
         if (half == 0) {
-          ksc[(i % Lo::kScRing) * kTcKeys + n] = ksv;
+          ksc[(i % Lo::kScRing) * kTcKeys + n] = ksv * p.sm_scale_log2;  // the softmax's log2 factor folded in
           vsc[(i % Lo::kScRing) * kTcKeys + n] = vsv;
         }
       }
@@ -380,7 +380,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const int lim = live ? p.seq_len - p.q_len + ti + 1 : 0;  // keys this row sees (exclusive)
     const int kend = min(lim, key_end);
-    const float qk = p.sm_scale_log2 * row_scale * p.k_gs_inv;  // NVFP4: the tiles hold values x gs
+    // logit (log2 units) = S x kfac x rs with rs = the row's power of two (q was
+    // scaled by 1/rs to be exact in fp16; 1 for BF16): INT8 kfac = the key's scale
+    // x sm_scale x log2(e) (folded in by the converters), otherwise kfac =
+    // sm_scale x log2(e) (NVFP4: x 1 / gs_K, the tiles hold values x gs).  kfac
+    // carries the sign of sm_scale and rs > 0, so max(S x kfac) x rs is the
+    // maximum logit.
+    const float rs = row_scale;
+    const float kconst = p.sm_scale_log2 * p.k_gs_inv;  // kfac of the non-INT8 formats
     const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     float m_run = -INFINITY, l_run = 0.f;
 
@@ -395,8 +402,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int tok0 = (pg0 + i * kTcPages) * kPage;
       const float* ks = ksc + (i % Lo::kScRing) * kTcKeys;
       const float* vs = vsc + (i % Lo::kScRing) * kTcKeys;
-      // pass 1: logits (log2 units) in place of S, and the tile maximum (four
-      // independent chains); only a tile that crosses the row's limit is masked
+      // pass 1: z = S x kfac (the logit before the row factor rs > 0) and the tile
+      // maximum (four independent chains); only a tile that crosses the row's
+      // limit is masked
       float z[kTcKeys];
 #pragma unroll
       for (int t = 0; t < kTcKeys; ++t) z[t] = __uint_as_float(sv[t >> 5][t & 31]);
@@ -404,12 +412,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nvis = kend - tok0;  // visible keys of this tile for this row
 #pragma unroll
       for (int c4 = 0; c4 < kTcKeys / 4; ++c4) {
-        float4 k4 = make_float4(qk, qk, qk, qk);
+        float kk[4] = {kconst, kconst, kconst, kconst};
         if constexpr (FMT == KVQ_FMT_INT8) {
-          k4 = *reinterpret_cast<const float4*>(ks + 4 * c4);
-          k4.x *= qk; k4.y *= qk; k4.z *= qk; k4.w *= qk;
+          const float4 k4 = *reinterpret_cast<const float4*>(ks + 4 * c4);
+          kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
         }
-        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int t = 4 * c4 + e;
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mxs[e] = fmaxf(mxs[e], zz);
         }
       }
-      const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
+      const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * rs;  // log2 units
       // the P tile and O may be touched once P(i-1) V(i-1) has completed
       if (i > 0) {
         if (!wait_warp(kBarO0 + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
@@ -467,10 +474,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int q2 = 0; q2 < 2; ++q2) {
             const int t = 8 * c8 + 2 * e + q2;
             float pr;
-            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pr) : "f"(z[t] - msub));
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pr) : "f"(fmaf(z[t], rs, -msub)));
             psums[q2 + 2 * (e & 1)] += pr;
-            // v_scale of an unwritten slot may be NaN: a masked key contributes exactly 0
-            pv[q2] = FMT == KVQ_FMT_INT8 ? (pr > 0.f ? pr * v8[2 * e + q2] : 0.f) : pr;
+            // the converters wrote v scale 0 for every key past the range or the
+            // sequence, so every scale here is finite and a masked key gives 0
+            pv[q2] = FMT == KVQ_FMT_INT8 ? pr * v8[2 * e + q2] : pr;
           }
           if constexpr (kBf16) {
             const __nv_bfloat162 hv = __floats2bfloat162_rn(pv[0], pv[1]);
