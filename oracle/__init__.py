@@ -12,6 +12,8 @@ layout      reads the documented paged-pool layout (page, KV head, row).
 attention   float64 decode attention, split ranges, log-sum-exp merge.
 brute       pure-Python (math.fsum) attention for tiny inputs.
 accounting  byte accounting of the formats (per token, per page, per pool).
+rotation    the orthogonal rotation of K/V/q rows before quantization (Hadamard
+            with a fixed sign vector), its fp32 butterfly arithmetic.
 
 Parity status: every function here is pinned by the CPU tests under ``tests/``
 (``test_oracle_*.py``) against closed forms printed on the pages, a library

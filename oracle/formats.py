@@ -25,7 +25,7 @@ NVFP4  E2M1 element codes (sign + magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two pe
 BF16   Values stored as bfloat16 (the comparison format of the pages' BF16 FA2
        runs); "decoding" is widening.
 
-Readings where the pages leave a step open (each is also listed in the design doc):
+Readings where the pages leave a step open:
   * INT8 quotient: q = fp32(x / s) with IEEE fp32 division by the stored scale,
     then round half to even, then clamp to [-127, 127]; s == 0 gives all-zero codes.
   * NVFP4 encoder: t = fp32(amax_g / 6), t2 = fp32(t * gs), scale byte =
