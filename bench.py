@@ -289,6 +289,70 @@ def time_append(wl, fmt, dev, l2, steps, warmup=16):
             "note": "CUDA graph of R appends over R input sets and R pools (inputs larger than L2)"}
 
 
+def time_graph_fn(fn, R, reps=50):
+    """CUDA graph of fn(0) .. fn(R-1); seconds per fn call over `reps` replays."""
+    import torch
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            fn(r)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for r in range(R):
+            fn(r)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / (reps * R)
+
+
+def time_rotation(dev, l2, peak):
+    """kvq_rotate_rows over the append workload's new K/V rows (65,536 rows of 256
+    bf16, in place over inputs larger than L2 in total), and the cost it adds
+    around a 32K batch-1 decode call (q rotated before, the output rotated back)."""
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+    from quantized_paged_kv_gb300 import workloads as W
+
+    res = {}
+    rows, D = 8192 * 4 * 2, 256
+    nbytes = rows * D * 2
+    R = max(2, math.ceil(2 * l2 / (2 * nbytes)))
+    bufs = [torch.randn(rows, D, device=dev).to(torch.bfloat16) for _ in range(R)]
+    t = time_graph_fn(lambda r: kvq.kvq_rotate_rows(bufs[r], bufs[r]), R)
+    res["rotate_rows/65536x256 bf16"] = {"us": round(t * 1e6, 3), "GBps": round(2 * nbytes / t / 1e9, 1),
+                                         "frac": round(2 * nbytes / t / 1e9 / peak, 4), "inputs": R}
+    del bufs
+    wl = W.make("long_int8")
+    ls = LayerSet(wl, "int8", 16, dev)
+    plan = ls.plan(0)
+    qr = torch.empty_like(ls.q)
+
+    def rotated_call(r):
+        kvq.kvq_rotate_rows(ls.q, qr)
+        kvq.decode(ls.caches[r], plan, qr, ls.bt, ls.sl, ls.out, wl.sm_scale, early_start=True)
+        kvq.kvq_rotate_rows(ls.out, ls.out, inverse=True)
+
+    t_plain = time_graph_fn(lambda r: ls.call(r, plan), ls.R)
+    t_rot = time_graph_fn(rotated_call, ls.R)
+    res["rotated_decode/long_int8"] = {"us": round(t_rot * 1e6, 3), "plain_us": round(t_plain * 1e6, 3),
+                                       "note": "q rotated before the call, the output rotated back after it"}
+    del ls
+    return res
+
+
 def time_verify(ls, T, steps, warmup=16):
     """Verify calls (T query tokens a sequence, causal) over the R layer pools in
     one CUDA graph; KV GB/s counts each page once."""
@@ -634,6 +698,9 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
         del ls
         gc.collect()
         torch.cuda.empty_cache()
+    res.update(time_rotation(dev, l2, peak))
+    gc.collect()
+    torch.cuda.empty_cache()
     # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences), INT8 and NVFP4
     wl = W.make("append_int8")
     for fmt in ("int8", "nvfp4"):

@@ -8,6 +8,7 @@
  *                               reads the quantized pages directly
  *   kvq_paged_verify_attention  the same for several query tokens a sequence (causal)
  *   kvq_paged_prefill_attention causal attention of a prompt chunk over the cache
+ *   kvq_rotate_rows         the rotation of rows before quantization (and its inverse)
  *   kvq_paged_decode_attention_static  the decode with library-owned scratch
  *   kvq_split_merge             log-sum-exp combine of the per-split partial results
  *
@@ -383,6 +384,27 @@ int kvq_paged_decode_attention_static(const kvq_cache* cache, const void* q, int
 int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* split_offsets,
                     int32_t batch, int32_t num_q_heads, int32_t head_dim,
                     void* out, int32_t out_dtype, float* lse_out, void* stream);
+
+/* ---- rotate_rows ([capstone] "Lever one: 4-bit KV with TurboQuant": the K and V
+ *      vectors are rotated before they are quantized, so that outliers spread
+ *      over all dimensions) -------------------------------------------------- */
+/*
+ * out[r] = R(in[r]) (inverse != 0: R^-1) for n_rows rows of head_dim values, with
+ * R(x) = head_dim^(-1/2) H (s * x): H the Sylvester Hadamard matrix, s_i = -1 iff
+ * bit 31 of (i + 1) * 2654435761 mod 2^32 is set.  R is orthogonal: rotating q and
+ * the cached K leaves the attention scores unchanged, and attention over rotated
+ * V returns R(o), so a caller rotates new K/V rows before kvq_quant_append, rotates
+ * q before the decode and applies the inverse to its output.  Arithmetic (it
+ * fixes the bits): fp32 butterflies, stages h = 1, 2, ..., head_dim/2, pairs
+ * (a, b) -> (a + b, a - b); one multiply by fp32(head_dim^-1/2); rounding to
+ * the output type (bf16: nearest even).
+ *   in, out    device or pinned host [n_rows][head_dim], KVQ_OUT_F32 (fp32) or
+ *              KVQ_OUT_BF16 (bf16) each (in_dtype / out_dtype); out may equal in
+ *              when the types match
+ *   head_dim   128 or 256
+ */
+int kvq_rotate_rows(const void* in, int32_t in_dtype, void* out, int32_t out_dtype, int64_t n_rows,
+                    int32_t head_dim, int32_t inverse, void* stream);
 
 /* Synchronize `stream`, read and clear a device status word (the first int32 of a
  * decode workspace, or an append dev_status).  *bits receives the KVQ_DEV_* bits.

@@ -31,7 +31,7 @@ EXPORTS = (
     "kvq_decode_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
     "kvq_paged_decode_attention_static", "kvq_paged_verify_attention", "kvq_prefill_splits",
     "kvq_prefill_workspace_bytes", "kvq_paged_prefill_attention", "kvq_split_merge", "kvq_read_status",
-    "kvq_last_error",
+    "kvq_last_error", "kvq_rotate_rows",
 )
 
 
@@ -278,3 +278,23 @@ def kvq_split_merge(o_part_ptr, lse_part_ptr, split_offsets, batch, num_q_heads,
     _check(lib().kvq_split_merge(c_void_p(o_part_ptr), c_void_p(lse_part_ptr), _ptr(split_offsets), batch,
                                  num_q_heads, head_dim, _ptr(out), od, _ptr(lse_out), _stream(stream)),
            "kvq_split_merge")
+
+
+def kvq_rotate_rows(x, out=None, inverse=False, stream=None):
+    """out[..., :] = R(x[..., :]) (or R^-1) over the last axis (head_dim 128 / 256);
+    x and out float32 or bfloat16, device or pinned host; out defaults to a new
+    tensor of x's dtype on x's device (out may be x)."""
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    if out is None:
+        out = torch.empty_like(x)
+    if out.dtype not in (torch.float32, torch.bfloat16) or out.shape != x.shape:
+        raise TypeError("out must be float32 or bfloat16 with x's shape")
+    if not x.is_contiguous() or not out.is_contiguous():
+        raise ValueError("x and out must be contiguous")
+    D = x.shape[-1]
+    dt = lambda t: KVQ_OUT_BF16 if t.dtype == torch.bfloat16 else KVQ_OUT_F32
+    _check(lib().kvq_rotate_rows(_ptr(x), dt(x), _ptr(out), dt(out), ctypes.c_int64(x.numel() // max(D, 1)), D,
+                                 1 if inverse else 0, _stream(stream)), "kvq_rotate_rows")
+    return out
+

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(PKG, "_lib", "obj")
 LIB = os.path.join(LIBDIR, "libkvq.so")
-SOURCES = ["abi.cu", "append.cu", "merge.cu", "decode_launch.cu", "static_scratch.cu", "prefill_tc.cu", "stage.cu"]
+SOURCES = ["abi.cu", "append.cu", "merge.cu", "decode_launch.cu", "static_scratch.cu", "prefill_tc.cu", "stage.cu", "rotate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v", f"-I{INCLUDE}", f"-I{CSRC}"]
 

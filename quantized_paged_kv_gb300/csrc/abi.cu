@@ -802,6 +802,26 @@ int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* s
   return succeed();
 }
 
+int kvq_rotate_rows(const void* in, int32_t in_dtype, void* out, int32_t out_dtype, int64_t n_rows,
+                    int32_t head_dim, int32_t inverse, void* stream) {
+  if (n_rows < 0) return fail(KVQ_ERR_INVALID_ARG, "n_rows %lld < 0", (long long)n_rows);
+  if (n_rows == 0) return succeed();
+  if (!in || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL pointer argument");
+  if (head_dim != 128 && head_dim != 256) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d (128 or 256)", head_dim);
+  for (int32_t t : {in_dtype, out_dtype})
+    if (t != KVQ_OUT_F32 && t != KVQ_OUT_BF16) return fail(KVQ_ERR_INVALID_ARG, "dtype %d is not f32 / bf16", t);
+  if (in == out && in_dtype != out_dtype) return fail(KVQ_ERR_INVALID_ARG, "in place needs the same dtype");
+  if (!aligned16(in) || !aligned16(out)) return fail(KVQ_ERR_INVALID_ARG, "in / out must be 16-byte aligned");
+  int rc = memory_kind(in, "in", nullptr);
+  if (rc) return rc;
+  rc = memory_kind(out, "out", nullptr);
+  if (rc) return rc;
+  const cudaError_t e = kvq::launch_rotate(in, in_dtype == KVQ_OUT_BF16, out, out_dtype == KVQ_OUT_BF16, n_rows,
+                                           head_dim, inverse != 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rotate launch");
+  return succeed();
+}
+
 int kvq_read_status(void* dev_status, void* stream, int32_t* bits) {
   if (!dev_status) return fail(KVQ_ERR_INVALID_ARG, "dev_status is NULL");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -89,6 +89,9 @@ struct PrefillInstance {
   int launch_regs;             // registers a thread the kernel's register split assumes (0: no split)
   int rows;                    // query rows of a work item
 };
+// rotation of rows (rotate.cu)
+cudaError_t launch_rotate(const void* in, bool in_bf16, void* out, bool out_bf16, int64_t n_rows, int head_dim,
+                          bool inverse, cudaStream_t stream);
 // copy of the query block from host memory into the workspace (programmatic dependent)
 cudaError_t launch_q_stage(const void* src, void* dst, size_t bytes, cudaStream_t stream);
 // the prefill kernel (tcgen05 tensor cores, accumulators in TMEM)
