@@ -22,9 +22,10 @@
  *               workers a piece of the attention calculation".
  *   [nvfp4]     "Building an NVFP4 KV cache for a hybrid Qwen model", sections
  *               "How 2,048 bytes became 576" and "Writing and reading the packed cache".
- *   [capstone]  "Smaller KV cache, faster first token", section "Lever two:
- *               block-sparse attention with BLASST" (one KV block is loaded once
- *               for a whole GQA group).
+ *   [capstone]  "Smaller KV cache, faster first token", sections "Lever one:
+ *               4-bit KV with TurboQuant" (K and V rotated before quantization)
+ *               and "Lever two: block-sparse attention with BLASST" (one KV block
+ *               is loaded once for a whole GQA group).
  *
  * Conventions for every call
  *   - Pointers named "device" are CUDA device pointers on the current device;
