@@ -7,7 +7,8 @@ baseline / reference arm may import it; the product package never does.
 
 Modules
 -------
-formats     INT8 per-token-head codec, E4M3 / E2M1 / NVFP4 codecs, BF16 rounding.
+formats     INT8 per-token-head codec (and with one scale per 32 values),
+            E4M3 / E2M1 / NVFP4 codecs, BF16 rounding.
 layout      reads the documented paged-pool layout (page, KV head, row).
 attention   float64 decode attention, split ranges, log-sum-exp merge.
 brute       pure-Python (math.fsum) attention for tiny inputs.

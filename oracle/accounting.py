@@ -6,6 +6,8 @@ Closed forms the pages print and that the tests check:
   * INT8: D code bytes + one 4-byte scale per tensor ("An 8-bit cache was already
     available": 520 bytes per token per head at D = 256; "Read the compressed
     cache without copying it first": the next head starts at byte 260).
+  * INT8 with one scale per 32 values: D code bytes + D/32 four-byte scales per
+    tensor ("Is 8 bits enough?": one scale per 32 values instead of one per 256).
   * NVFP4: D/2 code bytes + D/16 E4M3 scale bytes per tensor ("Building an NVFP4
     KV cache for a hybrid Qwen model", section "How 2,048 bytes became 576").
   * FP8 (accounting only, one byte per element): the same section's 1,024-byte row.
@@ -22,6 +24,8 @@ def record_bytes(fmt, head_dim):
         return D
     if fmt == "int8":
         return D + 4
+    if fmt == "int8_g32":
+        return D + 4 * (D // 32)
     if fmt == "nvfp4":
         return D // 2 + D // 16
     raise ValueError(fmt)

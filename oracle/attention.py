@@ -101,6 +101,8 @@ def dequantize_rows(fmt, codes, scales, global_scale=1.0):
     """Rows of one format -> float64 values [n, D]."""
     if fmt == "int8":
         return formats.int8_dequantize(codes.view(np.int8), scales)
+    if fmt == "int8_g32":
+        return formats.int8_group_dequantize(codes.view(np.int8), scales)
     if fmt == "nvfp4":
         return formats.nvfp4_dequantize(codes, scales, global_scale)
     if fmt == "bf16":
@@ -172,6 +174,9 @@ def quantize_rows(fmt, x, global_scale=1.0):
     x = np.asarray(x, dtype=np.float32)
     if fmt == "int8":
         c, s = formats.int8_quantize(x)
+        return c.view(np.uint8), s
+    if fmt == "int8_g32":
+        c, s = formats.int8_group_quantize(x)
         return c.view(np.uint8), s
     if fmt == "nvfp4":
         return formats.nvfp4_quantize(x, global_scale)

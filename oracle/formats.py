@@ -22,6 +22,13 @@ NVFP4  E2M1 element codes (sign + magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two pe
        cache for a hybrid Qwen model" page, section "How 2,048 bytes became 576";
        the writer steps (group maxima -> FP8 scales -> E2M1 rounding -> pack
        pairs) are from its section "Writing and reading the packed cache".
+INT8/32  The same INT8 codec applied to each group of 32 consecutive elements of
+       a row instead of the whole row: one fp32 scale per 32 values, scale =
+       absmax of the group / 127.  Source: "half-the-memory-int8-kv-cache" page,
+       section "Is 8 bits enough?" (llama.cpp's Q8_0 KV format keeps one scale per
+       32 values; one per 256 is cheaper but more exposed to outlier channels).
+       The page does not give the scale's type or the rounding; the reading is
+       the per-token codec's (fp32 scale, fp32 quotient, ties to even).
 BF16   Values stored as bfloat16 (the comparison format of the pages' BF16 FA2
        runs); "decoding" is widening.
 
@@ -65,6 +72,35 @@ def int8_quantize(x):
 def int8_dequantize(codes, scale):
     """x_hat = code * scale, exact in float64."""
     return np.asarray(codes, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+# ---------------------------------------------------------------------------
+# INT8 with one scale per 32 values
+# ---------------------------------------------------------------------------
+INT8_GROUP = 32
+
+
+def int8_group_quantize(x, group=INT8_GROUP):
+    """Quantize rows of ``x`` ([..., D], D a multiple of ``group``) with one INT8
+    scale per ``group`` consecutive elements ("half-the-memory-int8-kv-cache",
+    section "Is 8 bits enough?").
+
+    Returns ``(codes int8 [..., D], scales float32 [..., D / group])``: each group
+    is coded exactly as ``int8_quantize`` codes a row.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    assert D % group == 0
+    codes, scales = int8_quantize(x.reshape(x.shape[:-1] + (D // group, group)))
+    return codes.reshape(x.shape), scales
+
+
+def int8_group_dequantize(codes, scales, group=INT8_GROUP):
+    """x_hat = code * scale of its group, exact in float64."""
+    c = np.asarray(codes, dtype=np.float64)
+    D = c.shape[-1]
+    g = c.reshape(c.shape[:-1] + (D // group, group)) * np.asarray(scales, dtype=np.float64)[..., None]
+    return g.reshape(c.shape)
 
 
 # ---------------------------------------------------------------------------

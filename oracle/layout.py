@@ -10,7 +10,10 @@ re-derives token positions from that written description alone.
   * Codes: array ``[num_pages, Hkv, P, row_bytes]`` (row_bytes = 2D for bf16, D
     for int8, D/2 for nvfp4), one contiguous row per (page, KV head, slot).
   * Scales: int8 ``[num_pages, Hkv, P]`` float32; nvfp4 ``[num_pages, Hkv, P,
-    D/16]`` E4M3 bytes; bf16 has none.
+    D/16]`` E4M3 bytes; bf16 has none.  int8 with one scale per 32 values stores
+    its scales group-major inside each (page, KV head) block, ``[num_pages, Hkv,
+    D/32, P]`` float32: ``group_major_scales`` turns that array into the
+    ``[num_pages, Hkv, P, D/32]`` form the functions below index.
   * Token ``t`` of sequence ``b`` sits in slot ``block_table[b, t // P] * P + t % P``.
 """
 from __future__ import annotations
@@ -38,3 +41,14 @@ def scatter_rows(pool, slots, head, rows):
     P = pool.shape[2]
     slots = np.asarray(slots, dtype=np.int64)
     pool[slots // P, head, slots % P] = rows
+
+
+def group_major_scales(pool):
+    """A ``[num_pages, Hkv, groups, P]`` scale array as ``[num_pages, Hkv, P, groups]``
+    (slot-major: one row of group scales per slot)."""
+    return np.ascontiguousarray(np.swapaxes(np.asarray(pool), 2, 3))
+
+
+def to_group_major_scales(rows_pool):
+    """Inverse of ``group_major_scales``: the device's storage order."""
+    return np.ascontiguousarray(np.swapaxes(np.asarray(rows_pool), 2, 3))

@@ -131,6 +131,66 @@ def check_int8_invariants(int8_quantize, int8_dequantize, seed=1):
 
 
 # ---------------------------------------------------------------------------
+# INT8 with one scale per 32 values
+# ---------------------------------------------------------------------------
+def check_int8_group_exact(int8_group_quantize, seed=10, rows=24, D=128):
+    """Each group of 32 consecutive elements against exact rational arithmetic:
+    groups of a row get magnitudes 2^-6 .. 2^6 apart, so a wrong grouping (a
+    stride, a transposed reshape, a shared scale) changes scales and codes."""
+    rng = np.random.default_rng(seed)
+    mags = 2.0 ** rng.integers(-6, 7, (rows, D // 32))
+    x = bf16_values(rng, (rows, D)) * np.repeat(mags, 32, axis=1)
+    x[::5, 9] *= 30.0  # an outlier in group 0
+    x = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
+    codes, scales = int8_group_quantize(x)
+    assert codes.shape == x.shape and scales.shape == (rows, D // 32)
+    for i in range(rows):
+        for g in range(D // 32):
+            ec, es = int8_expected_exact(x[i, 32 * g:32 * g + 32])
+            assert float(scales[i, g]) == es, (i, g, float(scales[i, g]), es)
+            assert [int(c) for c in codes[i, 32 * g:32 * g + 32]] == ec, (i, g)
+
+
+def check_int8_group_hand_example(int8_group_quantize, int8_group_dequantize):
+    """A 64-element row worked by hand: group 0 holds 127/8 and halves of 1/8
+    (scale exactly 1/8, ties to even), group 1 holds 254 and the integers
+    -31 .. -1 times 2 (scale exactly 2, codes -31 .. -1)."""
+    halves = [0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 125.5, 126.5, -126.5]
+    g0 = [127 / 8] + [h / 8 for h in halves] + [0.0] * 21
+    g1 = [254.0] + [2.0 * k for k in range(-31, 0)]
+    codes, scales = int8_group_quantize(np.array([g0 + g1], dtype=np.float32))
+    assert [float(v) for v in scales[0]] == [0.125, 2.0]
+    assert [int(c) for c in codes[0, :11]] == [127, 0, 2, 2, 4, 0, -2, -2, 126, 126, -126]
+    assert not codes[0, 11:32].any()
+    assert [int(c) for c in codes[0, 32:]] == [127] + list(range(-31, 0))
+    back = int8_group_dequantize(np.arange(64, dtype=np.int8).reshape(1, 64), np.array([[0.5, 4.0]]))
+    assert np.array_equal(back[0], np.concatenate([np.arange(32) * 0.5, np.arange(32, 64) * 4.0]))
+
+
+def check_int8_group_invariants(int8_group_quantize, int8_group_dequantize, int8_quantize, seed=11):
+    """Per-group error bound and maxima; an outlier channel moves only its own
+    group; a row of 32 is the per-token codec's row."""
+    rng = np.random.default_rng(seed)
+    x = bf16_values(rng, (100, 256))
+    codes, s = int8_group_quantize(x)
+    xh = int8_group_dequantize(codes, s)
+    err = np.abs(x.astype(np.float64) - xh)
+    bound = (0.5 + 127 * 2.0 ** -24) * np.repeat(s.astype(np.float64), 32, axis=1)
+    assert np.all(err <= bound)
+    g = np.abs(x).reshape(100, 8, 32).argmax(axis=2)
+    assert np.all(np.abs(codes.reshape(100, 8, 32)[np.arange(100)[:, None], np.arange(8)[None, :], g]) == 127)
+    y = x.copy()
+    y[:, 77] *= 50.0  # channel 77 is in group 2
+    cy, sy = int8_group_quantize(y)
+    keep = [k for k in range(8) if k != 2]
+    assert np.array_equal(sy[:, keep], s[:, keep])
+    assert np.array_equal(cy.reshape(100, 8, 32)[:, keep], codes.reshape(100, 8, 32)[:, keep])
+    c32, s32 = int8_quantize(x[:, :32])
+    c1, s1 = int8_group_quantize(x[:, :32])
+    assert np.array_equal(c1, c32) and np.array_equal(s1[:, 0], s32)
+
+
+# ---------------------------------------------------------------------------
 # E4M3 / E2M1 / NVFP4
 # ---------------------------------------------------------------------------
 def torch_e4m3_values():

@@ -31,3 +31,11 @@ def test_closed_forms():
     assert acc.conversion_scratch_bytes(131072, 4, 256) // MiB == cf["fp16_scratch_128k_mib"]
     assert acc.conversion_scratch_bytes(32768, 4, 256) // MiB == cf["fp16_scratch_32k_mib"]
     assert round(acc.attention_flops(64, 131072, 256, 4) / 1e9) == cf["verify_gflop_128k_64rows"]
+
+
+def test_per_32_scale_record():
+    # one fp32 scale per 32 values: 256 codes + 8 scales, 128 codes + 4 scales
+    assert acc.record_bytes("int8_g32", 256) == 256 + 8 * 4
+    assert acc.record_bytes("int8_g32", 128) == 128 + 4 * 4
+    # 28 bytes more than one scale per 256 values at D = 256
+    assert acc.record_bytes("int8_g32", 256) - acc.record_bytes("int8", 256) == 28

@@ -17,6 +17,19 @@ def test_int8_invariants():
     pins.check_int8_invariants(formats.int8_quantize, formats.int8_dequantize)
 
 
+def test_int8_group_matches_exact_rational_arithmetic():
+    pins.check_int8_group_exact(formats.int8_group_quantize)
+
+
+def test_int8_group_hand_example():
+    pins.check_int8_group_hand_example(formats.int8_group_quantize, formats.int8_group_dequantize)
+
+
+def test_int8_group_invariants():
+    pins.check_int8_group_invariants(formats.int8_group_quantize, formats.int8_group_dequantize,
+                                     formats.int8_quantize)
+
+
 def test_e4m3_decode_matches_torch_float8():
     pins.check_e4m3_decode(formats.e4m3_value)
 

@@ -41,6 +41,28 @@ def test_int8_mutants_are_caught():
     _fails(pins.check_int8_exact, scale128)
 
 
+def test_int8_group_mutants_are_caught():
+    def strided(x, group=32):  # group = every (D/32)-th element
+        x = np.asarray(x, np.float32)
+        D = x.shape[-1]
+        c, s = formats.int8_quantize(x.reshape(x.shape[:-1] + (group, D // group)).swapaxes(-1, -2))
+        return c.swapaxes(-1, -2).reshape(x.shape), s
+
+    def row_scale(x, group=32):  # one scale for the whole row, repeated
+        c, s = formats.int8_quantize(x)
+        return c, np.repeat(s[..., None], x.shape[-1] // group, axis=-1)
+
+    def deq_wrong_group(codes, scales, group=32):  # group index off by one
+        c = np.asarray(codes, np.float64)
+        sc = np.roll(np.asarray(scales, np.float64), 1, axis=-1)
+        return (c.reshape(c.shape[:-1] + (-1, group)) * sc[..., None]).reshape(c.shape)
+
+    _fails(pins.check_int8_group_exact, strided)
+    _fails(pins.check_int8_group_exact, row_scale)
+    _fails(pins.check_int8_group_hand_example, formats.int8_group_quantize, deq_wrong_group)
+    _fails(pins.check_int8_group_invariants, formats.int8_group_quantize, deq_wrong_group, formats.int8_quantize)
+
+
 def test_fp8_fp4_mutants_are_caught():
     def bias8(b):
         return formats.e4m3_value(b) / 2.0
