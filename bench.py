@@ -669,8 +669,10 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     wl = W.make("long_int8")
     measure(wl, "int8", (1, 2, 4, 8, 16, 32, 38, 64, 0))
     measure(wl, "bf16", (16, 38, 64, 0))
+    measure(wl, "int8_g32", (0,))  # INT8 with one scale per 32 values
     wl = W.make("serving_int8")
     measure(wl, "int8", (0, 1))
+    measure(wl, "int8_g32", (0,))
     # the decode that follows the append workload's append: B = 8, contexts 4K..16K
     wl = W.make("append_int8")
     measure(wl, "int8", (0,))
@@ -701,9 +703,10 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     res.update(time_rotation(dev, l2, peak))
     gc.collect()
     torch.cuda.empty_cache()
-    # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences), INT8 and NVFP4
+    # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences), INT8 (per row
+    # and per 32 values) and NVFP4
     wl = W.make("append_int8")
-    for fmt in ("int8", "nvfp4"):
+    for fmt in ("int8", "int8_g32", "nvfp4"):
         res[f"append_{fmt}/8192 tokens"] = time_append(wl, fmt, dev, l2, steps)
         gc.collect()
         torch.cuda.empty_cache()

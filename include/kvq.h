@@ -71,8 +71,11 @@ typedef enum kvq_status {
 enum {
   KVQ_FMT_BF16 = 0,  /* bf16 values, no scales (comparison format) */
   KVQ_FMT_INT8 = 1,  /* int8 codes + one fp32 scale per (token, KV head), scale = absmax/127 */
-  KVQ_FMT_NVFP4 = 2  /* E2M1 codes, 2 per byte (element 2j low nibble), one E4M3 scale per
+  KVQ_FMT_NVFP4 = 2, /* E2M1 codes, 2 per byte (element 2j low nibble), one E4M3 scale per
                         16 elements, one fp32 global scale per tensor; x = fp4*scale/global */
+  KVQ_FMT_INT8_G32 = 3 /* int8 codes + one fp32 scale per 32 consecutive elements of a row,
+                        scale = absmax of the 32 / 127 ([int8-kv] "Is 8 bits enough?": one
+                        scale per 32 values instead of one per 256); decode and verify only */
 };
 
 /* ---- output dtypes ------------------------------------------------------ */
@@ -116,8 +119,11 @@ enum {
  *
  * Layout (all arrays dense, row-major, device memory, base 256-byte aligned):
  *   k_codes, v_codes   [num_pages][num_kv_heads][page_size][row_bytes]
- *                      row_bytes = 2*head_dim (BF16), head_dim (INT8), head_dim/2 (NVFP4)
+ *                      row_bytes = 2*head_dim (BF16), head_dim (INT8, INT8_G32), head_dim/2 (NVFP4)
  *   k_scales, v_scales INT8:  [num_pages][num_kv_heads][page_size] float
+ *                      INT8_G32: [num_pages][num_kv_heads][head_dim/32][page_size] float
+ *                             (group-major inside each (page, KV head) block: the scale of
+ *                             elements 32g .. 32g+31 of slot row i is at [.][.][g][i])
  *                      NVFP4: [num_pages][num_kv_heads][page_size][head_dim/16] E4M3 bytes
  *                      BF16:  unused (NULL)
  * Slot s is row (s % page_size) of page (s / page_size).  Each (page, KV head)
@@ -147,7 +153,8 @@ typedef struct kvq_cache {
 /* ---- host helpers: byte accounting ([int8-kv], [nvfp4]) ----------------- */
 
 /* K+V bytes one token occupies in one layer (codes + scales, all KV heads):
- * BF16 4*D*Hkv, INT8 2*(D+4)*Hkv (520 per head at D=256), NVFP4 2*(D/2+D/16)*Hkv
+ * BF16 4*D*Hkv, INT8 2*(D+4)*Hkv (520 per head at D=256), INT8_G32 2*(D+D/8)*Hkv
+ * (576 per head at D=256), NVFP4 2*(D/2+D/16)*Hkv
  * (576 per token per layer at 2 heads, D=256).  Returns -1 for an unknown format
  * or a non-positive size.  Host only; no GPU needed. */
 int64_t kvq_bytes_per_token(int32_t format, int32_t num_kv_heads, int32_t head_dim);
@@ -323,7 +330,9 @@ int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t ba
  * query rows (token, query head) of one KV head against one of `splits` key
  * ranges; with splits > 1 the partials are combined by the merge kernel on the
  * same stream.  INT8 and BF16 caches at head_dim 128 or 256, NVFP4 at 256;
- * 1 <= num_q_heads / num_kv_heads <= 8.
+ * 1 <= num_q_heads / num_kv_heads <= 8.  INT8_G32 caches are refused with
+ * KVQ_ERR_UNSUPPORTED (a per-32 scale cannot be folded into the logits or P,
+ * and the scaled values are not exact in fp16).
  *   q              device bf16 [q_len][num_q_heads][head_dim]
  *   block_table    device int32 [max_pages]: the sequence's pages
  *   seq_len        host: tokens of the sequence, the q_len new ones included

@@ -16,14 +16,14 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkvq.so")
 
-KVQ_FMT_BF16, KVQ_FMT_INT8, KVQ_FMT_NVFP4 = 0, 1, 2
+KVQ_FMT_BF16, KVQ_FMT_INT8, KVQ_FMT_NVFP4, KVQ_FMT_INT8_G32 = 0, 1, 2, 3
 KVQ_OUT_F32, KVQ_OUT_BF16 = 0, 1
 KVQ_CHECKED, KVQ_SKIP_MERGE, KVQ_EARLY_START = 1, 2, 4
 KVQ_TEST_STALL = 1 << 30  # failure-path test: no page copies, every device wait gives up after 2 ms
 KVQ_DEV_BAD_PAGE, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_BAD_PLAN = 1, 2, 4
 KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_SLOT, KVQ_DEV_NONFINITE = 8, 16, 32
 KVQ_STATIC_SCRATCH_BYTES = 16 << 20
-FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4}
+FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4, "int8_g32": KVQ_FMT_INT8_G32}
 
 # every symbol include/kvq.h declares
 EXPORTS = (

@@ -31,7 +31,8 @@ class KVCache:
 
     @property
     def row_bytes(self):
-        return {"bf16": 2 * self.head_dim, "int8": self.head_dim, "nvfp4": self.head_dim // 2}[self.fmt]
+        return {"bf16": 2 * self.head_dim, "int8": self.head_dim, "int8_g32": self.head_dim,
+                "nvfp4": self.head_dim // 2}[self.fmt]
 
     def views(self):
         """(k_codes, v_codes, k_scales, v_scales) reshaped to [num_pages, Hkv, P, ...]."""
@@ -42,6 +43,9 @@ class KVCache:
             return kc, vc, None, None
         if self.fmt == "int8":
             return kc, vc, self.k_scales.view(torch.float32).view(*shp), self.v_scales.view(torch.float32).view(*shp)
+        if self.fmt == "int8_g32":  # group-major: [num_pages, Hkv, D/32, P]
+            gshp = (self.num_pages, self.num_kv_heads, self.head_dim // 32, self.page_size)
+            return kc, vc, self.k_scales.view(torch.float32).view(*gshp), self.v_scales.view(torch.float32).view(*gshp)
         return kc, vc, self.k_scales.view(*shp, self.head_dim // 16), self.v_scales.view(*shp, self.head_dim // 16)
 
     def append(self, k_new, v_new, slot_mapping, dev_status=None, checked=False, stream=None):

@@ -44,6 +44,7 @@ int64_t row_bytes(int format, int D) {
   switch (format) {
     case KVQ_FMT_BF16: return 2LL * D;
     case KVQ_FMT_INT8: return D;
+    case KVQ_FMT_INT8_G32: return D;
     case KVQ_FMT_NVFP4: return D / 2;
     default: return -1;
   }
@@ -53,6 +54,7 @@ int64_t scale_row_bytes(int format, int D) {
   switch (format) {
     case KVQ_FMT_BF16: return 0;
     case KVQ_FMT_INT8: return 4;
+    case KVQ_FMT_INT8_G32: return 4LL * (D / 32);
     case KVQ_FMT_NVFP4: return D / 16;
     default: return -1;
   }
@@ -63,7 +65,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Validates the shape (and, if `pointers`, the device arrays) of a cache.
 int check_cache(const kvq_cache* c, bool pointers) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
-  if (c->format != KVQ_FMT_BF16 && c->format != KVQ_FMT_INT8 && c->format != KVQ_FMT_NVFP4)
+  if (c->format != KVQ_FMT_BF16 && c->format != KVQ_FMT_INT8 && c->format != KVQ_FMT_NVFP4 &&
+      c->format != KVQ_FMT_INT8_G32)
     return fail(KVQ_ERR_INVALID_ARG, "unknown cache format %d", c->format);
   if (c->page_size != 16) return fail(KVQ_ERR_UNSUPPORTED, "page_size %d: only 16 is implemented", c->page_size);
   if (c->head_dim != 128 && c->head_dim != 256)
@@ -159,7 +162,7 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
   if (!kvq::decode_instance(format, D, inst))
     return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for format %d head_dim %d", format, D);
   static std::mutex mu;
-  static bool done[64][3][2] = {};
+  static bool done[64][4][2] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -721,7 +724,7 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
     return fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, D);
   {
     static std::mutex mu;
-    static bool done[64][3][2] = {};
+    static bool done[64][4][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");

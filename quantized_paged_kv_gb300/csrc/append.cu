@@ -8,6 +8,9 @@
 // bytes became 576" and "Writing and reading the packed cache"): group maxima over
 // 16 elements, an E4M3 scale per group, E2M1 rounding, pairs packed low nibble
 // first; invalid (negative) slots do not write.
+// INT8 with one scale per 32 values (the same page, section "Is 8 bits
+// enough?"): the INT8 codec applied to each group of 32 consecutive elements; the
+// scales are stored group-major in each (page, KV head) block, [D/32][16].
 //
 // One thread handles 8 consecutive elements of a row (16-byte loads); D/8
 // threads share a row and reduce its maxima with shuffles, and carry
@@ -59,16 +62,17 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
 
   if constexpr (FMT == KVQ_FMT_BF16) {
     if (write) *reinterpret_cast<uint4*>(codes + drow * (2 * D) + t * 16) = raw;
-  } else if constexpr (FMT == KVQ_FMT_INT8) {
-    constexpr int TPR = D / 8;
+  } else if constexpr (FMT == KVQ_FMT_INT8 || FMT == KVQ_FMT_INT8_G32) {
+    // threads sharing one scale: the row, or a group of 32 elements (4 threads)
+    constexpr int TPG = FMT == KVQ_FMT_INT8 ? D / 8 : 4;
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    if constexpr (TPR == 32) {  // one row a warp: the bit patterns of |x| order like the values
+    if constexpr (TPG == 32) {  // one row a warp: the bit patterns of |x| order like the values
       amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
     } else {
 #pragma unroll
-      for (int o = 1; o < TPR; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int o = 1; o < TPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     }
     const float s = __fdiv_rn(amax, 127.0f);
     // code = rne(fp32(x / s)).  Adding 1.5 * 2^23 rounds a float with |v| < 2^22
@@ -105,7 +109,11 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
     const uint32_t hi = prmt(prmt(b[4], b[5], 0x0040u), prmt(b[6], b[7], 0x0040u), 0x5410u);
     if (write) {
       *reinterpret_cast<uint2*>(codes + drow * D + t * 8) = make_uint2(lo, hi);
-      if (t == 0) reinterpret_cast<float*>(scales)[drow] = s;
+      if constexpr (FMT == KVQ_FMT_INT8) {
+        if (t == 0) reinterpret_cast<float*>(scales)[drow] = s;
+      } else if ((t & 3) == 0) {  // group t / 4 of the row: [page][head][group][16 rows]
+        reinterpret_cast<float*>(scales)[((page * Hkv + h) * (D / 32) + t / 4) * 16 + prow] = s;
+      }
     }
   } else {  // NVFP4: a group of 16 elements = threads (2k, 2k+1)
     const float gs = which ? p.v_gs : p.k_gs;
@@ -200,6 +208,9 @@ cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaS
     case KVQ_FMT_INT8:
       return head_dim == 256 ? launch_append_t<KVQ_FMT_INT8, 256>(p, stream)
                              : launch_append_t<KVQ_FMT_INT8, 128>(p, stream);
+    case KVQ_FMT_INT8_G32:
+      return head_dim == 256 ? launch_append_t<KVQ_FMT_INT8_G32, 256>(p, stream)
+                             : launch_append_t<KVQ_FMT_INT8_G32, 128>(p, stream);
     case KVQ_FMT_BF16:
       return head_dim == 256 ? launch_append_t<KVQ_FMT_BF16, 256>(p, stream)
                              : launch_append_t<KVQ_FMT_BF16, 128>(p, stream);

@@ -78,6 +78,17 @@ struct DecodeTraits<KVQ_FMT_INT8, D> {
 };
 
 template <int D>
+struct DecodeTraits<KVQ_FMT_INT8_G32, D> {
+  static constexpr bool kBf16Mma = false;
+  static constexpr int kRow = D;
+  static constexpr int kScaleRow = 4 * (D / 32);  // one fp32 per 32 elements (group-major in the block)
+};
+
+// INT8 codes (one scale per row or per 32 elements): the same code paths
+template <int FMT>
+__host__ __device__ constexpr bool int8_codes() { return FMT == KVQ_FMT_INT8 || FMT == KVQ_FMT_INT8_G32; }
+
+template <int D>
 struct DecodeTraits<KVQ_FMT_BF16, D> {
   static constexpr bool kBf16Mma = true;
   static constexpr int kRow = 2 * D;
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
       int dA, dB;
-      if constexpr (FMT == KVQ_FMT_INT8) {
+      if constexpr (int8_codes<FMT>()) {
         dA = 16 * j + 4 * c;
         dB = dA + 2;
       } else if constexpr (FMT == KVQ_FMT_BF16) {
@@ -502,7 +513,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   // only touches the low three chunk bits; see swz()).  V (INT8, transposed):
   // matrix m = lane/8 is token block m%2, chunk 2 cp + m/2.
   [[maybe_unused]] uint32_t voff[4];
-  if constexpr (FMT == KVQ_FMT_INT8) {
+  if constexpr (int8_codes<FMT>()) {
     const int mm = lane >> 3, rr = lane & 7;
 #pragma unroll
     for (int v4 = 0; v4 < 4; ++v4) voff[v4] = (8 * (mm & 1) + rr) * 128 + (((2 * v4 + (mm >> 1)) ^ rr) << 4);
@@ -634,8 +645,12 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 
     // chunk groups of 4 x 16-byte chunks; q fragments of the group's k-steps are
     // fetched from shared memory (two k-steps per ldmatrix.x4).
-    constexpr int QPG = FMT == KVQ_FMT_INT8 ? 4 : (FMT == KVQ_FMT_BF16 ? 2 : 8);  // k-steps per group
+    constexpr int QPG = int8_codes<FMT>() ? 4 : (FMT == KVQ_FMT_BF16 ? 2 : 8);  // k-steps per group
     constexpr int NCG = KS / QPG;
+    // INT8 with one scale per 32 elements: each group's two k-steps go to a
+    // fresh accumulator, which is scaled by the group's per-token K scale and
+    // added to zg[n-tile][token] (the scales are [group][16 tokens] fp32)
+    [[maybe_unused]] float zg[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     [[maybe_unused]] uint32_t ksw[2][4];
     if constexpr (FMT == KVQ_FMT_NVFP4) {
 #pragma unroll
@@ -672,6 +687,21 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
             mma16816<false>(sacc[i][m & 1], qa[m][0], 0u, qa[m][1], 0u, i8pair_to_h2<0x4140>(x),
                             i8pair_to_h2<0x4342>(x));
           }
+        } else if constexpr (FMT == KVQ_FMT_INT8_G32) {
+          // chunks 4cg .. 4cg+3 are groups 2cg (m = 0, 1) and 2cg+1 (m = 2, 3)
+#pragma unroll
+          for (int gg = 0; gg < 2; ++gg) {
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int mm = 0; mm < 2; ++mm) {
+              const uint32_t x = w[2 * gg + mm] ^ 0x80808080u;
+              mma16816<false>(t, qa[2 * gg + mm][0], 0u, qa[2 * gg + mm][1], 0u, i8pair_to_h2<0x4140>(x),
+                              i8pair_to_h2<0x4342>(x));
+            }
+            const float2 sc = *reinterpret_cast<const float2*>(ksc + ((2 * cg + gg) * kPage + 8 * i + 2 * c) * 4);
+            zg[i][0] = fmaf(t[0], sc.x, zg[i][0]);
+            zg[i][1] = fmaf(t[1], sc.y, zg[i][1]);
+          }
         } else if constexpr (FMT == KVQ_FMT_BF16) {
           // chunk = 8 d's; k-step uses chunks 2j (k 2c..) and 2j+1 (k 2c+8..).
           mma16816<true>(sacc[i][0], qa[0][0], 0u, qa[0][1], 0u, w[0], w[1]);
@@ -701,10 +731,17 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     // lane holds head r, tokens 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c (n-tile 1).
     const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
     float z[4];
-    z[0] = sacc[0][0][0] + sacc[0][1][0];
-    z[1] = sacc[0][0][1] + sacc[0][1][1];
-    z[2] = sacc[1][0][0] + sacc[1][1][0];
-    z[3] = sacc[1][0][1] + sacc[1][1][1];
+    if constexpr (FMT == KVQ_FMT_INT8_G32) {  // K scales already applied per group
+      z[0] = zg[0][0];
+      z[1] = zg[0][1];
+      z[2] = zg[1][0];
+      z[3] = zg[1][1];
+    } else {
+      z[0] = sacc[0][0][0] + sacc[0][1][0];
+      z[1] = sacc[0][0][1] + sacc[0][1][1];
+      z[2] = sacc[1][0][0] + sacc[1][1][0];
+      z[3] = sacc[1][0][1] + sacc[1][1][1];
+    }
     float ks4[4] = {1.f, 1.f, 1.f, 1.f};
     if constexpr (FMT == KVQ_FMT_INT8) {
       const float2 a = *reinterpret_cast<const float2*>(ksc + 8 * c);
@@ -749,6 +786,9 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       const float vs4[4] = {a.x, a.y, bb.x, bb.y};
 #pragma unroll
       for (int u = 0; u < 4; ++u) pv[u] = (tk[u] < nvalid) ? pr[u] * vs4[u] : 0.f;
+    } else if constexpr (FMT == KVQ_FMT_INT8_G32) {  // the V scale depends on d: folded in per group below
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pv[u] = (tk[u] < nvalid) ? pr[u] : 0.f;
     } else {
 #pragma unroll
       for (int u = 0; u < 4; ++u) pv[u] = pr[u];
@@ -772,7 +812,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 
     // ---------------------------------------------------------- O^T += V^T P'^T
     const bool partial = nvalid < kPage;
-    if constexpr (FMT == KVQ_FMT_INT8) {
+    if constexpr (int8_codes<FMT>()) {
       // ldmatrix.trans of int8 pairs: lane gets [V[t][de], V[t][do], V[t+1][de], V[t+1][do]]
       // with t = 8tb+2c, de = 16ch+2r, do = de+1 -> m-tile ch rows r (de) and r+8 (do).
       uint32_t vb[4];
@@ -782,6 +822,22 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       for (int cp = 0; cp < Lo::kMTiles / 2; ++cp) {
         uint32_t w[4];
         ldsm_x4_t(vb[cp & 3] + (cp >> 2) * (kPage * 128), w[0], w[1], w[2], w[3]);
+        if constexpr (FMT == KVQ_FMT_INT8_G32) {
+          // m-tiles 2cp, 2cp+1 are d 32cp .. 32cp+31: group cp.  P' = P x that
+          // group's V scale of each token ([group][16 tokens] fp32).
+          const float2 a = *reinterpret_cast<const float2*>(vsc + (cp * kPage + 2 * c) * 4);
+          const float2 bb = *reinterpret_cast<const float2*>(vsc + (cp * kPage + 8 + 2 * c) * 4);
+          const float g4[4] = {pv[0] * a.x, pv[1] * a.y, pv[2] * bb.x, pv[3] * bb.y};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            // a masked token (pv = 0) may meet a NaN scale in an unwritten slot
+            const float e0 = pv[2 * u] != 0.f ? g4[2 * u] : 0.f;
+            const float e1 = pv[2 * u + 1] != 0.f ? g4[2 * u + 1] : 0.f;
+            const __half2 hh = __floats2half2_rn(e0, e1);
+            phi[u] = h2_as_u32(hh);
+            if constexpr (p_lo) plo[u] = h2_as_u32(__floats2half2_rn(e0 - __low2float(hh), e1 - __high2float(hh)));
+          }
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const uint32_t x0 = w[2 * u] ^ 0x80808080u;
@@ -976,7 +1032,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         if (hr >= G) continue;
 #pragma unroll
         for (int mt = 0; mt < Lo::kMTiles; ++mt) {
-          if constexpr (FMT == KVQ_FMT_INT8) {
+          if constexpr (int8_codes<FMT>()) {
             put(hr, 16 * mt + 2 * r, oacc[mt][e], oacc[mt][2 + e], true);
           } else if constexpr (FMT == KVQ_FMT_BF16) {
             put(hr, 16 * mt + r, oacc[mt][e], 0.f, false);

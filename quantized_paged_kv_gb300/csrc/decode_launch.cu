@@ -43,6 +43,8 @@ cudaError_t launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
 bool decode_instance(int format, int head_dim, DecodeInstance* out) {
   if (format == KVQ_FMT_INT8 && head_dim == 256) *out = instance_of<KVQ_FMT_INT8, 256>();
   else if (format == KVQ_FMT_INT8 && head_dim == 128) *out = instance_of<KVQ_FMT_INT8, 128>();
+  else if (format == KVQ_FMT_INT8_G32 && head_dim == 256) *out = instance_of<KVQ_FMT_INT8_G32, 256>();
+  else if (format == KVQ_FMT_INT8_G32 && head_dim == 128) *out = instance_of<KVQ_FMT_INT8_G32, 128>();
   else if (format == KVQ_FMT_BF16 && head_dim == 256) *out = instance_of<KVQ_FMT_BF16, 256>();
   else if (format == KVQ_FMT_BF16 && head_dim == 128) *out = instance_of<KVQ_FMT_BF16, 128>();
   else if (format == KVQ_FMT_NVFP4 && head_dim == 256) *out = instance_of<KVQ_FMT_NVFP4, 256>();
@@ -54,6 +56,8 @@ cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const
                           const DecodeParams& p, int grid, cudaStream_t stream) {
   if (format == KVQ_FMT_INT8 && head_dim == 256) return launch_t<KVQ_FMT_INT8, 256>(tk, tv, p, grid, stream);
   if (format == KVQ_FMT_INT8 && head_dim == 128) return launch_t<KVQ_FMT_INT8, 128>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_INT8_G32 && head_dim == 256) return launch_t<KVQ_FMT_INT8_G32, 256>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_INT8_G32 && head_dim == 128) return launch_t<KVQ_FMT_INT8_G32, 128>(tk, tv, p, grid, stream);
   if (format == KVQ_FMT_BF16 && head_dim == 256) return launch_t<KVQ_FMT_BF16, 256>(tk, tv, p, grid, stream);
   if (format == KVQ_FMT_BF16 && head_dim == 128) return launch_t<KVQ_FMT_BF16, 128>(tk, tv, p, grid, stream);
   if (format == KVQ_FMT_NVFP4 && head_dim == 256) return launch_t<KVQ_FMT_NVFP4, 256>(tk, tv, p, grid, stream);

@@ -54,13 +54,16 @@ def gpu_cache(wl, fmt, gs=(1.0, 1.0), seqs=None, device="cuda", fill=SENTINEL, e
 def oracle_pools(wl, fmt, gs=(1.0, 1.0), seqs=None, heads=None):
     """The same pools built by the oracle's codecs and layout (numpy)."""
     P = 16
-    row = {"bf16": 2 * wl.D, "int8": wl.D, "nvfp4": wl.D // 2}[fmt]
+    row = {"bf16": 2 * wl.D, "int8": wl.D, "int8_g32": wl.D, "nvfp4": wl.D // 2}[fmt]
     shp = (wl.num_pages, wl.Hkv, P)
     pools = {"k_codes": np.full(shp + (row,), SENTINEL, np.uint8), "v_codes": np.full(shp + (row,), SENTINEL, np.uint8),
              "k_global_scale": gs[0], "v_global_scale": gs[1]}
     if fmt == "int8":
         pools["k_scales"] = np.full(shp, np.nan, np.float32)
         pools["v_scales"] = np.full(shp, np.nan, np.float32)
+    elif fmt == "int8_g32":  # the oracle's slot-major form [pages, Hkv, P, D/32]
+        pools["k_scales"] = np.full(shp + (wl.D // 32,), np.nan, np.float32)
+        pools["v_scales"] = np.full(shp + (wl.D // 32,), np.nan, np.float32)
     elif fmt == "nvfp4":
         pools["k_scales"] = np.full(shp + (wl.D // 16,), SENTINEL, np.uint8)
         pools["v_scales"] = np.full(shp + (wl.D // 16,), SENTINEL, np.uint8)
@@ -81,9 +84,14 @@ def oracle_pools(wl, fmt, gs=(1.0, 1.0), seqs=None, heads=None):
 
 
 def gpu_views_numpy(cache):
+    """Codes and scales as numpy, scales in the oracle's slot-major form
+    ([pages, Hkv, P, ...]; the per-32 format's device order is group-major)."""
     kc, vc, ks, vs = cache.views()
     f = lambda t: None if t is None else t.cpu().numpy()
-    return f(kc), f(vc), f(ks), f(vs)
+    ks, vs = f(ks), f(vs)
+    if cache.fmt == "int8_g32":
+        ks, vs = olay.group_major_scales(ks), olay.group_major_scales(vs)
+    return f(kc), f(vc), ks, vs
 
 
 def run_decode(cache, wl, split=0, q=None, out_dtype=None, target_ctas=0, checked=True, lse=True, device="cuda"):

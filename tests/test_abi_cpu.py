@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from tests import harness as H
+from oracle import accounting as acc
 from tests import oracle_pins as pins
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -49,6 +50,11 @@ def test_bytes_per_token_matches_the_pages(kvq):
     assert (cb, sb) == (10 * 2 * 16 * 128, 10 * 2 * 16 * 16)
     cb, sb = kvq.kvq_cache_array_bytes("int8", 3, 16, 4, 256)
     assert (cb, sb) == (3 * 4 * 16 * 256, 3 * 4 * 16 * 4)
+    # one fp32 scale per 32 values
+    assert kvq.kvq_bytes_per_token("int8_g32", 1, 256) == 2 * acc.record_bytes("int8_g32", 256)
+    assert kvq.kvq_bytes_per_token("int8_g32", 8, 128) == 8 * 2 * acc.record_bytes("int8_g32", 128)
+    cb, sb = kvq.kvq_cache_array_bytes("int8_g32", 3, 16, 4, 256)
+    assert (cb, sb) == (3 * 4 * 16 * 256, 3 * 4 * 16 * 8 * 4)
 
 
 def _struct(kvq, fmt="int8", pages=4096, Hkv=4, D=256):
@@ -122,6 +128,11 @@ def test_planner_override_and_auto(kvq):
     plan, total, nctas = kvq.kvq_plan_splits(s, [32768], 0, 152)
     # 2048 page units over 152 CTAs: 152 splits of 13 or 14 pages, one per CTA
     assert total == 152 and nctas == 152
+    # the per-32 format plans with the same head groups (its stage holds 4 pages)
+    g = _struct(kvq, fmt="int8_g32")
+    for seq_lens in ([32768], [1, 17, 300, 0, 64]):
+        plan, total, nctas = kvq.kvq_plan_splits(g, seq_lens, 0, 152)
+        _check_plan(plan.numpy(), seq_lens, total, nctas, 1)
     # uneven lengths: a split granularity whose packing fills every CTA evenly
     # wins over one split per CTA's worth of pages (which leaves some CTAs two items)
     lens = [4096 * 16, 3000 * 16, 900 * 16, 333 * 16, 4100 * 16]
@@ -194,3 +205,6 @@ def test_prefill_split_choice_and_workspace(kvq):
         kvq.kvq_prefill_splits(s, 10, 24, 5, 152)  # q_len > seq_len
     nv = _struct(kvq, fmt="nvfp4")
     assert kvq.kvq_prefill_splits(nv, 10, 24, 500, 152) == 2  # NVFP4 runs on the same prefill kernel
+    g32 = _struct(kvq, fmt="int8_g32")
+    with pytest.raises(kvq.KvqError, match="no prefill kernel"):  # per-32 scales: decode and verify only
+        kvq.kvq_prefill_splits(g32, 10, 24, 500, 152)

@@ -70,13 +70,20 @@ def test_int8_append_bit_exact(D, kind):
     _append_and_compare("int8", 4, D, kind)
 
 
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("kind", ["normal", "outliers", "spikes", "edge"])
+def test_int8_g32_append_bit_exact(D, kind):
+    _append_and_compare("int8_g32", 4, D, kind)
+
+
 @pytest.mark.parametrize("kind", ["normal", "outliers", "spikes", "edge"])
 @pytest.mark.parametrize("gs", [(1.0, 1.0), "tensor", (0.37, 1234.5)])
 def test_nvfp4_append_bit_exact(kind, gs):
     _append_and_compare("nvfp4", 2, 256, kind, gs=gs)
 
 
-@pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("nvfp4", 256), ("bf16", 256)])
+@pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("int8_g32", 128), ("int8_g32", 256), ("nvfp4", 256),
+                                   ("bf16", 256)])
 @pytest.mark.parametrize("n", [1, 5, 33, 301])
 def test_append_ragged_token_counts(fmt, D, n):
     # a block carries several rows a thread group: token counts that leave the
@@ -166,6 +173,27 @@ def test_int8_append_dense_quotients():
     assert np.array_equal(got_s.view(np.uint32), s_exp.view(np.uint32))
     bad = np.argwhere(got_c != c_exp)
     assert len(bad) == 0, (len(bad), bad[:5], x[tuple(bad[0])] if len(bad) else None)
+
+
+def test_int8_g32_append_dense_quotients():
+    """Groups of 32 holding their maximum and 31 bf16 values up to it: every
+    quotient each group's scale can produce, ties included."""
+    rng = np.random.default_rng(13)
+    groups = []
+    for a in _dense_maxima(rng, 16):
+        v = _bf16_upto(a)
+        v = np.concatenate([v, np.zeros((-len(v)) % 31, np.float32)])
+        g = v.reshape(-1, 31)
+        groups.append(np.concatenate([np.full((len(g), 1), a, np.float32), g], axis=1))
+    g = np.concatenate(groups)
+    g = g[rng.permutation(len(g))]  # neighbouring groups of a row from different maxima
+    g = np.concatenate([g, np.zeros(((-len(g)) % 8, 32), np.float32)])
+    x = g.reshape(-1, 256)
+    got_c, got_s = _append_rows("int8_g32", x)
+    c_exp, s_exp = oatt.quantize_rows("int8_g32", x)
+    assert np.array_equal(got_s.view(np.uint32), s_exp.view(np.uint32))
+    bad = np.argwhere(got_c != c_exp)
+    assert len(bad) == 0, (len(bad), bad[:5])
 
 
 @pytest.mark.parametrize("gs", [1.0, 0.37, 1234.5])

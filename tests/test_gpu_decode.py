@@ -58,7 +58,7 @@ def test_tiny_int8(split):
         assert plan.total_splits == split
 
 
-@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
+@pytest.mark.parametrize("fmt", ["int8", "int8_g32", "nvfp4", "bf16"])
 @pytest.mark.parametrize("D,Hq,Hkv", [(256, 24, 4), (128, 32, 8), (256, 8, 8), (128, 16, 2)])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 def test_ragged_batch(fmt, D, Hq, Hkv, out_dtype):
@@ -178,7 +178,7 @@ def test_checked_mode_reports_bad_metadata():
 
 
 def test_nan_sentinels_in_unwritten_tail_slots_do_not_leak():
-    for fmt in ("int8", "nvfp4", "bf16"):
+    for fmt in ("int8", "int8_g32", "nvfp4", "bf16"):
         wl = W.make("tiny_int8", lens=("list", [33, 5, 47]), seed=6)
         _check(wl, fmt, 2)
 
@@ -208,6 +208,31 @@ def test_append_workload_decode_full_size_sampled():
     wl = W.make("append_int8")
     order = np.argsort(wl.seq_lens)
     _check(wl, "int8", 0, units=[(int(order[0]), 0), (int(order[-1]), 3)])
+
+
+def test_long_int8_g32_full_size_sampled():
+    wl = W.make("long_int8")
+    _check(wl, "int8_g32", 0, units=[(0, 2)])
+
+
+def test_serving_int8_g32_full_size_sampled():
+    wl = W.make("serving_int8")
+    order = np.argsort(wl.seq_lens)
+    _check(wl, "int8_g32", 0, units=[(int(order[-1]), 5)])
+
+
+def test_per_32_scales_bring_int8_closer_to_exact_attention():
+    # outlier channels x8: one scale per 32 values keeps the groups without an
+    # outlier fine-grained, so the output is closer (RMS over all elements) to
+    # attention over the bf16 K/V.  The largest error stays in the outlier
+    # channels, whose group scale equals the row scale.
+    wl = W.make("tiny_int8", lens=("list", [700]), seed=23)
+    exact, _ = H.oracle_decode(wl, "bf16", H.oracle_pools(wl, "bf16"))
+    errs = {}
+    for fmt in ("int8", "int8_g32"):
+        out, _, _ = H.run_decode(H.gpu_cache(wl, fmt), wl, out_dtype="f32")
+        errs[fmt] = np.sqrt(((out - exact) ** 2).mean())
+    assert errs["int8_g32"] < 0.7 * errs["int8"], errs
 
 
 def test_long_nvfp4_full_size_sampled():

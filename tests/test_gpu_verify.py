@@ -48,7 +48,7 @@ def _compare(wl, fmt, T, split=0, out_dtype="f32", gs=(1.0, 1.0), units=None):
     return plan
 
 
-@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
+@pytest.mark.parametrize("fmt", ["int8", "int8_g32", "nvfp4", "bf16"])
 @pytest.mark.parametrize("T", [1, 2, 4, 6])
 def test_verify_matches_the_oracle(fmt, T):
     # lengths include ones shorter than T: early query tokens then see nothing
