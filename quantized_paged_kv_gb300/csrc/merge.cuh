@@ -1,5 +1,5 @@
-// merge.cuh — the log-sum-exp combine of split partials as device code shared
-// by the merge kernel and the decode kernel's fused merge phase
+// merge.cuh — the log-sum-exp combine of split partials: the task code of the
+// merge kernel (its warp count and CTA barrier are parameters)
 // ("long-context-attention-and-lessons", section "Give more GPU workers a piece
 // of the attention calculation": each piece produces a weighted value sum and the
 // information needed to normalise it; averaging the partial outputs would be
