@@ -230,10 +230,13 @@ def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=
     return e0.elapsed_time(e1) * 1e-3 / (reps * ls.R), reps * ls.R, clocks
 
 
-def time_append(wl, fmt, dev, l2, steps, warmup=16):
+def time_append(wl, fmt, dev, l2, steps, warmup=16, rotate=None):
     """kvq_quant_append of the workload's new tokens (the last `append_tail` tokens
     of every sequence), timed as a CUDA graph of R appends that cycle through R
-    input sets and R pools, so that inputs and written pages are not L2-resident."""
+    input sets and R pools, so that inputs and written pages are not L2-resident.
+    rotate="fused": the append rotates each row itself (KVQ_ROTATE); "two_call":
+    kvq_rotate_rows of K and V into scratch rows, then the plain append.  Bytes and
+    GB/s count the append's own input and output either way."""
     import torch
 
     import quantized_paged_kv_gb300 as kvq
@@ -258,16 +261,27 @@ def time_append(wl, fmt, dev, l2, steps, warmup=16):
                             v_global_scale=gs[1], fill=0)
         sets.append((cache, k0[perm].contiguous(), v0[perm].contiguous(), s0))
     del k0, v0
+    if rotate == "two_call":
+        rk, rv = torch.empty_like(sets[0][1]), torch.empty_like(sets[0][2])
+
+    def one(cache, k, v, s):
+        if rotate == "two_call":
+            kvq.kvq_rotate_rows(k.view(-1, wl.D), rk.view(-1, wl.D))
+            kvq.kvq_rotate_rows(v.view(-1, wl.D), rv.view(-1, wl.D))
+            cache.append(rk, rv, s)
+        else:
+            cache.append(k, v, s, rotate=rotate == "fused")
+
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for cache, k, v, s in sets:
-            cache.append(k, v, s)
+            one(cache, k, v, s)
     stream.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for cache, k, v, s in sets:
-            cache.append(k, v, s)
+            one(cache, k, v, s)
     reps = max(1, math.ceil(steps / R))
     with torch.cuda.stream(stream):
         for _ in range(max(1, math.ceil(warmup / R))):
@@ -710,6 +724,12 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
         res[f"append_{fmt}/8192 tokens"] = time_append(wl, fmt, dev, l2, steps)
         gc.collect()
         torch.cuda.empty_cache()
+    # the same appends with the rows rotated first: in the append, or by a separate call
+    for fmt in ("int8", "nvfp4"):
+        for mode in ("fused", "two_call"):
+            res[f"append_{fmt}_rotated_{mode}/8192 tokens"] = time_append(wl, fmt, dev, l2, steps, rotate=mode)
+            gc.collect()
+            torch.cuda.empty_cache()
     return res
 
 

@@ -96,6 +96,14 @@ enum {
                           has completed.  The decode kernel is always launched as a
                           programmatic dependent of the preceding kernel; without this
                           flag it waits for that kernel before reading anything. */
+  KVQ_ROTATE = 8u,     /* append only: each new K and V row x is replaced by bf16(R(x)),
+                          the rotation of kvq_rotate_rows, before it is quantized
+                          ([capstone] "Lever one: 4-bit KV with TurboQuant": K and V
+                          are rotated before they are quantized).  The stored codes
+                          and scales are bit-identical to those of kvq_rotate_rows
+                          (bf16 in and out) followed by a plain kvq_quant_append; the
+                          rotated rows never go through memory.  The caller still
+                          rotates q (and applies R^-1 to the decode's output). */
   KVQ_TEST_STALL = 1u << 30 /* decode only, for testing the failure path: the
                           producers issue no page copies and every pipeline wait
                           gives up after 2 ms, so the call ends with KVQ_DEV_TIMEOUT
@@ -182,6 +190,7 @@ int kvq_cache_array_bytes(int32_t format, int32_t num_pages, int32_t page_size,
  *       code = E2M1_rne_satfinite(fp32(fp32(x*gs)/scale)) with the sign of x, zero
  *       codes when the scale is 0; element 2j in the low nibble.
  * BF16: the rows are copied.
+ * flags: KVQ_CHECKED; KVQ_ROTATE (rotate each row before quantizing it, see above).
  * Overwriting a slot that holds older data is allowed.
  */
 int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_new,

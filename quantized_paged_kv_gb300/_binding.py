@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "lib
 KVQ_FMT_BF16, KVQ_FMT_INT8, KVQ_FMT_NVFP4, KVQ_FMT_INT8_G32 = 0, 1, 2, 3
 KVQ_OUT_F32, KVQ_OUT_BF16 = 0, 1
 KVQ_CHECKED, KVQ_SKIP_MERGE, KVQ_EARLY_START = 1, 2, 4
+KVQ_ROTATE = 8  # append: rotate each new K/V row (bf16(R(x))) before quantizing it
 KVQ_TEST_STALL = 1 << 30  # failure-path test: no page copies, every device wait gives up after 2 ms
 KVQ_DEV_BAD_PAGE, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_BAD_PLAN = 1, 2, 4
 KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_SLOT, KVQ_DEV_NONFINITE = 8, 16, 32

@@ -48,9 +48,9 @@ class KVCache:
             return kc, vc, self.k_scales.view(torch.float32).view(*gshp), self.v_scales.view(torch.float32).view(*gshp)
         return kc, vc, self.k_scales.view(*shp, self.head_dim // 16), self.v_scales.view(*shp, self.head_dim // 16)
 
-    def append(self, k_new, v_new, slot_mapping, dev_status=None, checked=False, stream=None):
-        B.kvq_quant_append(self.struct, k_new, v_new, slot_mapping, dev_status,
-                           B.KVQ_CHECKED if checked else 0, stream)
+    def append(self, k_new, v_new, slot_mapping, dev_status=None, checked=False, rotate=False, stream=None):
+        flags = (B.KVQ_CHECKED if checked else 0) | (B.KVQ_ROTATE if rotate else 0)
+        B.kvq_quant_append(self.struct, k_new, v_new, slot_mapping, dev_status, flags, stream)
 
 
 class DecodePlan:

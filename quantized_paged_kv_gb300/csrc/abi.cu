@@ -266,6 +266,7 @@ int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_ne
   p.capacity = capacity;
   p.num_kv_heads = cache->num_kv_heads;
   p.check_finite = checked ? 1 : 0;
+  p.rotate = (flags & KVQ_ROTATE) ? 1 : 0;
   p.k_gs = cache->k_global_scale;
   p.v_gs = cache->v_global_scale;
   cudaError_t e = kvq::launch_append(cache->format, cache->head_dim, p, st);

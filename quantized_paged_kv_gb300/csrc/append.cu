@@ -12,6 +12,14 @@
 // enough?"): the INT8 codec applied to each group of 32 consecutive elements; the
 // scales are stored group-major in each (page, KV head) block, [D/32][16].
 //
+// With rotation ("Smaller KV cache, faster first token", section "Lever one:
+// 4-bit KV with TurboQuant": K and V are rotated before they are quantized), each
+// row is first replaced by R(x) = D^(-1/2) H_D (s * x) rounded to bf16, with the
+// same fp32 butterfly arithmetic as the rotation kernel (stages h = 1 .. D/2,
+// pairs (a, b) -> (a + b, a - b), one multiply by fp32(D^(-1/2)), nearest-even
+// bf16), so the stored codes equal those of a rotation pass followed by a plain
+// append, without the rotated rows' round trip through memory.
+//
 // One thread handles 8 consecutive elements of a row (16-byte loads); D/8
 // threads share a row and reduce its maxima with shuffles, and carry
 // kAppendRows rows whose loads go out together.  A row is one (token, KV head,
@@ -34,25 +42,78 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&x)[8]) {
   }
 }
 
+// Sign flips of the rotation for this thread's 8 elements 8 t .. 8 t + 7, as XOR
+// masks on the four bf16x2 words of its 16-byte piece: s_i = -1 iff bit 31 of
+// (i + 1) * 2654435761 mod 2^32 is set (Knuth's multiplicative hash).
+__device__ __forceinline__ uint4 rot_sign_masks(int t) {
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t i = static_cast<uint32_t>(8 * t + 2 * j);
+    const uint32_t lo = ((i + 1u) * 2654435761u) >> 31, hi = ((i + 2u) * 2654435761u) >> 31;
+    w[j] = (lo << 15) | (hi << 31);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// raw (this thread's 8 bf16 elements 8 t .. 8 t + 7 of a row spread over D/8
+// consecutive lanes, signs already applied) <- bf16(R(x)).  fp32 butterflies in
+// stage order; across lanes, fma(x, -1, w) = w - x and fma(x, 1, w) = x + w with
+// one rounding, as the plain sums.  Every lane of the warp takes part (shuffles).
+template <int D>
+__device__ __forceinline__ uint4 rotate_row_bf16(const uint4& raw, int t) {
+  float x[8];
+  unpack_bf16x8(raw, x);
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {  // butterflies inside the lane
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e & h) continue;
+      const float a = x[e], b = x[e + h];
+      x[e] = a + b;
+      x[e + h] = a - b;
+    }
+  }
+#pragma unroll
+  for (int h = 8; h < D; h <<= 1) {  // across the row's lanes: lane t pairs with t ^ (h / 8)
+    const int m = h / 8;
+    const float sg = (t & m) ? -1.f : 1.f;  // upper lane: w - x; lower lane: x + w
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = fmaf(x[e], sg, __shfl_xor_sync(0xffffffffu, x[e], m));
+  }
+  const float norm = D == 256 ? __uint_as_float(0x3d800000u) : __uint_as_float(0x3db504f3u);  // fp32(D^-1/2)
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * j] * norm, x[2 * j + 1] * norm);
+    w[j] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Quantize one row (D/8 threads, this thread's 8 elements in `raw`): token n,
-// KV head h, K (which = 0) or V (1); write it to `slot`.
-template <int FMT, int D>
+// KV head h, K (which = 0) or V (1); write it to `slot`.  ROT: rotate it first
+// (sgn: rot_sign_masks(t)).
+template <int FMT, int D, bool ROT>
 __device__ __forceinline__ void append_row(const AppendParams& p, int h, int which, bool in_range, int64_t slot,
-                                           const uint4& raw, int t) {
+                                           uint4 raw, int t, const uint4& sgn) {
   const int Hkv = p.num_kv_heads;
   bool write = in_range && slot >= 0;
   if (write && slot >= p.capacity) {
     if (t == 0 && which == 0 && p.status) atomicOr(p.status, KVQ_DEV_BAD_SLOT);
     write = false;
   }
-  float x[8];
-  unpack_bf16x8(raw, x);
   if (p.check_finite && in_range) {
+    float x[8];
+    unpack_bf16x8(raw, x);
     bool fin = true;
 #pragma unroll
     for (int i = 0; i < 8; ++i) fin &= isfinite(x[i]);
     if (!fin && p.status) atomicOr(p.status, KVQ_DEV_NONFINITE);
   }
+  if constexpr (ROT) raw = rotate_row_bf16<D>(make_uint4(raw.x ^ sgn.x, raw.y ^ sgn.y, raw.z ^ sgn.z, raw.w ^ sgn.w), t);
+  float x[8];
+  unpack_bf16x8(raw, x);
 
   const int64_t page = write ? slot / 16 : 0;
   const int prow = write ? static_cast<int>(slot % 16) : 0;
@@ -161,7 +222,7 @@ constexpr int kAppendRows = 2;
 
 // Grid: x over token blocks, y over (KV head, K or V) = 2 h + which, so that no
 // index needs a division.
-template <int FMT, int D>
+template <int FMT, int D, bool ROT>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
   // a following decode (a programmatic dependent) may be scheduled now; it waits
   // for this grid to complete before it reads the cache
@@ -183,10 +244,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
     raw[u] = *reinterpret_cast<const uint4*>(src + nn * stride);
     slot[u] = p.slots[nn];
   }
+  const uint4 sgn = ROT ? rot_sign_masks(t) : make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int u = 0; u < kAppendRows; ++u) {
     const int64_t n = n0 + (int64_t)u * ROWS;
-    append_row<FMT, D>(p, h, which, n < p.n_tokens, slot[u], raw[u], t);
+    append_row<FMT, D, ROT>(p, h, which, n < p.n_tokens, slot[u], raw[u], t, sgn);
   }
 }
 
@@ -197,7 +259,10 @@ cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF || 2 * p.num_kv_heads > 65535) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(2 * p.num_kv_heads));
-  append_kernel<FMT, D><<<grid, kAppendThreads, 0, stream>>>(p);
+  if (p.rotate)
+    append_kernel<FMT, D, true><<<grid, kAppendThreads, 0, stream>>>(p);
+  else
+    append_kernel<FMT, D, false><<<grid, kAppendThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,7 @@ struct AppendParams {
   int64_t capacity;            // num_pages * page_size
   int32_t num_kv_heads;
   int32_t check_finite;
+  int32_t rotate;              // rotate each row (bf16(R(x))) before quantizing it
   float k_gs, v_gs;            // NVFP4 global scales
 };
 

@@ -123,3 +123,79 @@ def test_rotation_brings_int8_closer_to_exact_attention():
     err_plain = np.abs(out - exact).max()
     err_rot = np.abs(rotated - exact).max()
     assert err_rot < 0.7 * err_plain, (err_rot, err_plain)
+
+
+def _fused_rows(rng, n, Hkv, D):
+    """bf16-valued K/V rows with a spread of magnitudes, outlier channels, an
+    all-zero row, a tiny row and a huge row."""
+    x = rng.standard_normal((n, Hkv, D)) * np.exp(rng.uniform(-3, 3, (n, Hkv, 1)))
+    x[:, :, [2, D // 5, D - 3]] *= 8.0
+    x[0] = 0.0
+    x[1] *= 1e-30
+    x[2] *= 3e4
+    return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+@pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("int8_g32", 128), ("int8_g32", 256),
+                                   ("nvfp4", 256), ("bf16", 128), ("bf16", 256)])
+@pytest.mark.parametrize("n", [5, 301])
+def test_fused_rotated_append_bit_exact(fmt, D, n):
+    # KVQ_ROTATE on the append: codes and scales equal the oracle's quantization of
+    # its rotated bf16 rows, and the two-call GPU path (rotate, then append)
+    from quantized_paged_kv_gb300 import KVCache, kvq_rotate_rows
+
+    Hkv, num_pages = 4, 40
+    rng = np.random.default_rng(1000 * D + n)
+    k, v = _fused_rows(rng, n, Hkv, D), _fused_rows(rng, n, Hkv, D)
+    gs = (0.37, 1234.5) if fmt == "nvfp4" else (1.0, 1.0)
+    slots = rng.permutation(num_pages * 16)[:n].astype(np.int64)
+    slots[1::7] = -1                                   # padding tokens: not written
+    dev = lambda a: torch.from_numpy(a).cuda()
+    kb, vb, sl = dev(k).to(torch.bfloat16), dev(v).to(torch.bfloat16), dev(slots)
+    fused = KVCache(fmt, num_pages, Hkv, D, k_global_scale=gs[0], v_global_scale=gs[1], fill=H.SENTINEL)
+    fused.append(kb, vb, sl, rotate=True)
+    two = KVCache(fmt, num_pages, Hkv, D, k_global_scale=gs[0], v_global_scale=gs[1], fill=H.SENTINEL)
+    rk = kvq_rotate_rows(kb.reshape(-1, D)).reshape(kb.shape)
+    rv = kvq_rotate_rows(vb.reshape(-1, D)).reshape(vb.shape)
+    two.append(rk, rv, sl)
+    torch.cuda.synchronize()
+    got, ref_gpu = H.gpu_views_numpy(fused), H.gpu_views_numpy(two)
+    for a, b in zip(got, ref_gpu):
+        if a is not None:
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    valid = slots >= 0
+    sv = slots[valid]
+    for x, codes, scales, g in ((k, got[0], got[2], gs[0]), (v, got[1], got[3], gs[1])):
+        xr = orot.rotate_fp32(x, out="bf16")
+        for h in range(Hkv):
+            c_exp, s_exp = oatt.quantize_rows(fmt, xr[valid, h, :], g)
+            got_c = codes[sv // 16, h, sv % 16]
+            assert np.array_equal(got_c, c_exp), (fmt, h, np.argwhere(got_c != c_exp)[:5])
+            if s_exp is not None:
+                got_s = scales[sv // 16, h, sv % 16]
+                assert np.array_equal(got_s.view(np.uint8), np.asarray(s_exp).view(np.uint8)), (fmt, h)
+    # unwritten slots keep the sentinel
+    written = np.zeros(num_pages * 16, bool)
+    written[sv] = True
+    kc = got[0]
+    assert np.all(kc.transpose(0, 2, 1, 3).reshape(num_pages * 16, Hkv, -1)[~written] == H.SENTINEL)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_rotated_decode_with_fused_append_matches_the_oracle(fmt):
+    from quantized_paged_kv_gb300 import DecodePlan, KVCache, decode, kvq_rotate_rows
+
+    wl = W.make("tiny_int8", lens=("list", [700, 45]), seed=21)
+    cache = KVCache(fmt, wl.num_pages, wl.Hkv, wl.D, fill=H.SENTINEL)
+    for b in range(wl.B):
+        k, v = wl.kv(b)
+        cache.append(torch.from_numpy(k).to(torch.bfloat16).cuda(), torch.from_numpy(v).to(torch.bfloat16).cuda(),
+                     torch.from_numpy(wl.slots(b)).cuda(), rotate=True)
+    qt = kvq_rotate_rows(torch.from_numpy(wl.q()).to(torch.bfloat16).cuda())
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq)
+    decode(cache, plan, qt, torch.from_numpy(wl.block_tables).cuda(), torch.from_numpy(wl.seq_lens).cuda(), out,
+           wl.sm_scale, checked=True)
+    kvq_rotate_rows(out, out, inverse=True)
+    torch.cuda.synchronize()
+    assert np.abs(out.cpu().numpy() - _oracle_rotated(wl, fmt)).max() <= H.tol("f32")
