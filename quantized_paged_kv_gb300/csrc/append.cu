@@ -20,11 +20,13 @@
 // bf16), so the stored codes equal those of a rotation pass followed by a plain
 // append, without the rotated rows' round trip through memory.
 //
-// One thread handles 8 consecutive elements of a row (16-byte loads); D/8
-// threads share a row and reduce its maxima with shuffles, and carry
-// kAppendRows rows whose loads go out together.  A row is one (token, KV head,
-// K-or-V) triple; a block's rows share the KV head and K-or-V.  Coalesced stores: codes 8 (INT8) / 4 (NVFP4) /
-// 16 (BF16) bytes per thread, contiguous across the row.
+// A thread handles EPT consecutive elements of a row (one or two 16-byte loads):
+// 16 for NVFP4 (a thread holds one whole scale group), 8 for the other formats;
+// D/EPT threads share a row and reduce its maxima with shuffles, and each thread
+// carries kAppendRows rows whose loads go out together.  A row is one (token, KV
+// head, K-or-V) triple; a block's rows share the KV head and K-or-V.  Coalesced
+// stores: codes EPT (INT8) / EPT/2 (NVFP4) / 2 EPT (BF16) bytes per thread,
+// contiguous across the row.
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
 
@@ -33,41 +35,91 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&x)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Elements a thread, per format.  Measured on 8,192 tokens (D = 256), 8 against
+// 16: INT8 14.7 / 14.7 us, INT8 per 32 values 19.1 / 22.1, BF16 12.7 / 12.9,
+// NVFP4 20.9 / 19.7.
+template <int FMT>
+__host__ __device__ constexpr int append_ept() {
+  return FMT == KVQ_FMT_NVFP4 ? 16 : 8;
+}
+
+template <int EPT>
+struct Piece {  // a thread's EPT bf16 elements
+  uint4 q[EPT / 8];
+};
+
+template <int EPT>
+__device__ __forceinline__ void unpack_piece(const Piece<EPT>& v, float (&x)[EPT]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  for (int k = 0; k < EPT / 8; ++k) {
+    const uint32_t w[4] = {v.q[k].x, v.q[k].y, v.q[k].z, v.q[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[8 * k + 2 * i] = __uint_as_float(w[i] << 16);
+      x[8 * k + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
   }
 }
 
-// Sign flips of the rotation for this thread's 8 elements 8 t .. 8 t + 7, as XOR
-// masks on the four bf16x2 words of its 16-byte piece: s_i = -1 iff bit 31 of
-// (i + 1) * 2654435761 mod 2^32 is set (Knuth's multiplicative hash).
-__device__ __forceinline__ uint4 rot_sign_masks(int t) {
-  uint32_t w[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t i = static_cast<uint32_t>(8 * t + 2 * j);
-    const uint32_t lo = ((i + 1u) * 2654435761u) >> 31, hi = ((i + 2u) * 2654435761u) >> 31;
-    w[j] = (lo << 15) | (hi << 31);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+// Packed fp32 pairs (add/sub/mul .rn.f32x2: two IEEE round-to-nearest operations
+// in one instruction, the same results as the scalar ones).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
-// raw (this thread's 8 bf16 elements 8 t .. 8 t + 7 of a row spread over D/8
-// consecutive lanes, signs already applied) <- bf16(R(x)).  fp32 butterflies in
-// stage order; across lanes, fma(x, -1, w) = w - x and fma(x, 1, w) = x + w with
-// one rounding, as the plain sums.  Every lane of the warp takes part (shuffles).
-template <int D>
-__device__ __forceinline__ uint4 rotate_row_bf16(const uint4& raw, int t) {
-  float x[8];
-  unpack_bf16x8(raw, x);
+// Sign flips of the rotation for this thread's elements EPT t .. EPT t + EPT - 1,
+// as XOR masks on the bf16x2 words of its piece: s_i = -1 iff bit 31 of (i + 1) *
+// 2654435761 mod 2^32 is set (Knuth's multiplicative hash).
+template <int EPT>
+__device__ __forceinline__ Piece<EPT> rot_sign_masks(int t) {
+  Piece<EPT> m;
 #pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {  // butterflies inside the lane
+  for (int k = 0; k < EPT / 8; ++k) {
+    uint32_t w[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t i = static_cast<uint32_t>(EPT * t + 8 * k + 2 * j);
+      const uint32_t lo = ((i + 1u) * 2654435761u) >> 31, hi = ((i + 2u) * 2654435761u) >> 31;
+      w[j] = (lo << 15) | (hi << 31);
+    }
+    m.q[k] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return m;
+}
+
+// raw (this thread's EPT bf16 elements EPT t .. EPT t + EPT - 1 of a row spread
+// over D/EPT consecutive lanes, signs already applied) <- bf16(R(x)).  fp32
+// butterflies in stage order; across lanes, fma(x, -1, w) = w - x and fma(x, 1, w)
+// = x + w with one rounding, as the plain sums.  Every lane of the warp takes part
+// (shuffles).
+template <int D, int EPT>
+__device__ __forceinline__ Piece<EPT> rotate_piece_bf16(const Piece<EPT>& raw, int t) {
+  float x[EPT];
+  unpack_piece<EPT>(raw, x);
+#pragma unroll
+  for (int h = 1; h < EPT; h <<= 1) {  // butterflies inside the lane
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
       if (e & h) continue;
       const float a = x[e], b = x[e + h];
       x[e] = a + b;
@@ -75,28 +127,33 @@ __device__ __forceinline__ uint4 rotate_row_bf16(const uint4& raw, int t) {
     }
   }
 #pragma unroll
-  for (int h = 8; h < D; h <<= 1) {  // across the row's lanes: lane t pairs with t ^ (h / 8)
-    const int m = h / 8;
+  for (int h = EPT; h < D; h <<= 1) {  // across the row's lanes: lane t pairs with t ^ (h / EPT)
+    const int m = h / EPT;
     const float sg = (t & m) ? -1.f : 1.f;  // upper lane: w - x; lower lane: x + w
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = fmaf(x[e], sg, __shfl_xor_sync(0xffffffffu, x[e], m));
+    for (int e = 0; e < EPT; ++e) x[e] = fmaf(x[e], sg, __shfl_xor_sync(0xffffffffu, x[e], m));
   }
   const float norm = D == 256 ? __uint_as_float(0x3d800000u) : __uint_as_float(0x3db504f3u);  // fp32(D^-1/2)
-  uint32_t w[4];
+  Piece<EPT> out;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * j] * norm, x[2 * j + 1] * norm);
-    w[j] = *reinterpret_cast<const uint32_t*>(&b);
+  for (int k = 0; k < EPT / 8; ++k) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(x[8 * k + 2 * j] * norm, x[8 * k + 2 * j + 1] * norm);
+      w[j] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    out.q[k] = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  return out;
 }
 
-// Quantize one row (D/8 threads, this thread's 8 elements in `raw`): token n,
+// Quantize one row (D/EPT threads, this thread's EPT elements in `raw`): token n,
 // KV head h, K (which = 0) or V (1); write it to `slot`.  ROT: rotate it first
 // (sgn: rot_sign_masks(t)).
-template <int FMT, int D, bool ROT>
+template <int FMT, int D, bool ROT, int EPT = append_ept<FMT>()>
 __device__ __forceinline__ void append_row(const AppendParams& p, int h, int which, bool in_range, int64_t slot,
-                                           uint4 raw, int t, const uint4& sgn) {
+                                           Piece<EPT> raw, int t, const Piece<EPT>& sgn) {
   const int Hkv = p.num_kv_heads;
   bool write = in_range && slot >= 0;
   if (write && slot >= p.capacity) {
@@ -104,16 +161,22 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
     write = false;
   }
   if (p.check_finite && in_range) {
-    float x[8];
-    unpack_bf16x8(raw, x);
+    float x[EPT];
+    unpack_piece<EPT>(raw, x);
     bool fin = true;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) fin &= isfinite(x[i]);
+    for (int i = 0; i < EPT; ++i) fin &= isfinite(x[i]);
     if (!fin && p.status) atomicOr(p.status, KVQ_DEV_NONFINITE);
   }
-  if constexpr (ROT) raw = rotate_row_bf16<D>(make_uint4(raw.x ^ sgn.x, raw.y ^ sgn.y, raw.z ^ sgn.z, raw.w ^ sgn.w), t);
-  float x[8];
-  unpack_bf16x8(raw, x);
+  if constexpr (ROT) {
+#pragma unroll
+    for (int k = 0; k < EPT / 8; ++k)
+      raw.q[k] = make_uint4(raw.q[k].x ^ sgn.q[k].x, raw.q[k].y ^ sgn.q[k].y, raw.q[k].z ^ sgn.q[k].z,
+                            raw.q[k].w ^ sgn.q[k].w);
+    raw = rotate_piece_bf16<D, EPT>(raw, t);
+  }
+  float x[EPT];
+  unpack_piece<EPT>(raw, x);
 
   const int64_t page = write ? slot / 16 : 0;
   const int prow = write ? static_cast<int>(slot % 16) : 0;
@@ -122,13 +185,17 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
   uint8_t* scales = which ? p.v_scales : p.k_scales;
 
   if constexpr (FMT == KVQ_FMT_BF16) {
-    if (write) *reinterpret_cast<uint4*>(codes + drow * (2 * D) + t * 16) = raw;
+    if (write) {
+      uint4* dst = reinterpret_cast<uint4*>(codes + drow * (2 * D) + t * (2 * EPT));
+#pragma unroll
+      for (int k = 0; k < EPT / 8; ++k) dst[k] = raw.q[k];
+    }
   } else if constexpr (FMT == KVQ_FMT_INT8 || FMT == KVQ_FMT_INT8_G32) {
-    // threads sharing one scale: the row, or a group of 32 elements (4 threads)
-    constexpr int TPG = FMT == KVQ_FMT_INT8 ? D / 8 : 4;
+    // threads sharing one scale: the row, or a group of 32 elements
+    constexpr int TPG = FMT == KVQ_FMT_INT8 ? D / EPT : 32 / EPT;
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    for (int i = 0; i < EPT; ++i) amax = fmaxf(amax, fabsf(x[i]));
     if constexpr (TPG == 32) {  // one row a warp: the bit patterns of |x| order like the values
       amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
     } else {
@@ -145,43 +212,52 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
     // subnormal, zero or non-finite s, the row takes the exact quotients.
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
     const bool fast = s >= 1.17549435e-38f && s <= 3.40282347e+38f;
-    float y[8];
+    float y[EPT];
     bool exact = !fast;
     if (fast) {
       const float rs = __frcp_rn(s);
+      const uint64_t rs2 = f2(rs, rs), mg2 = f2(kMagic, kMagic);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float q = x[i] * rs;
-        y[i] = q + kMagic;
-        exact |= fabsf(q - (y[i] - kMagic)) > 0.5f - 0x1p-14f;
+      for (int i = 0; i < EPT; i += 2) {  // q, q + magic, q - rne(q) for two elements at once
+        const uint64_t q2 = mul2(f2(x[i], x[i + 1]), rs2);
+        const uint64_t y2 = add2(q2, mg2);
+        float d0, d1;
+        f2_split(sub2(q2, sub2(y2, mg2)), d0, d1);
+        f2_split(y2, y[i], y[i + 1]);
+        exact |= fmaxf(fabsf(d0), fabsf(d1)) > 0.5f - 0x1p-14f;
       }
     }
-    if (__any_sync(0xffffffffu, exact)) {  // rare: the whole row (all lanes) takes the exact path
+    if (__any_sync(0xffffffffu, exact)) {  // rare: the warp's rows (all lanes) take the exact path
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < EPT; ++i) {
         const float q = s > 0.f ? fminf(127.f, fmaxf(-127.f, __fdiv_rn(x[i], s))) : 0.f;
         y[i] = q + kMagic;
       }
     }
-    uint32_t b[8];
+    uint32_t b[EPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(y[i]);
-    const uint32_t lo = prmt(prmt(b[0], b[1], 0x0040u), prmt(b[2], b[3], 0x0040u), 0x5410u);
-    const uint32_t hi = prmt(prmt(b[4], b[5], 0x0040u), prmt(b[6], b[7], 0x0040u), 0x5410u);
+    for (int i = 0; i < EPT; ++i) b[i] = __float_as_uint(y[i]);
+    uint32_t c[EPT / 4];
+#pragma unroll
+    for (int j = 0; j < EPT / 4; ++j)
+      c[j] = prmt(prmt(b[4 * j], b[4 * j + 1], 0x0040u), prmt(b[4 * j + 2], b[4 * j + 3], 0x0040u), 0x5410u);
     if (write) {
-      *reinterpret_cast<uint2*>(codes + drow * D + t * 8) = make_uint2(lo, hi);
+      if constexpr (EPT == 16)
+        *reinterpret_cast<uint4*>(codes + drow * D + t * EPT) = make_uint4(c[0], c[1], c[2], c[3]);
+      else
+        *reinterpret_cast<uint2*>(codes + drow * D + t * EPT) = make_uint2(c[0], c[1]);
       if constexpr (FMT == KVQ_FMT_INT8) {
         if (t == 0) reinterpret_cast<float*>(scales)[drow] = s;
-      } else if ((t & 3) == 0) {  // group t / 4 of the row: [page][head][group][16 rows]
-        reinterpret_cast<float*>(scales)[((page * Hkv + h) * (D / 32) + t / 4) * 16 + prow] = s;
+      } else if (t % TPG == 0) {  // group t / TPG of the row: [page][head][group][16 rows]
+        reinterpret_cast<float*>(scales)[((page * Hkv + h) * (D / 32) + t / TPG) * 16 + prow] = s;
       }
     }
-  } else {  // NVFP4: a group of 16 elements = threads (2k, 2k+1)
+  } else {  // NVFP4: a group of 16 elements = one thread
+    static_assert(FMT != KVQ_FMT_NVFP4 || EPT == 16, "an NVFP4 thread holds one scale group");
     const float gs = which ? p.v_gs : p.k_gs;
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    for (int i = 0; i < EPT; ++i) amax = fmaxf(amax, fabsf(x[i]));
     const float t2 = __fmul_rn(__fdiv_rn(amax, 6.0f), gs);
     const uint32_t sf = f32_to_e4m3_satfinite(t2);
     const float sd = __low2float(u32_as_h2(e4m3x2_to_h2(sf)));
@@ -191,11 +267,11 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
     // x gs / sd and y within 2^-24; |4 y| <= 26, so unless 4 v lies within 2^-16
     // of an integer both round to the same code.  Otherwise the row takes the
     // exact quotients.
-    float xg[8], y[8];
+    float xg[EPT], y[EPT];
     bool exact = false;
     const float r = sd > 0.f ? __frcp_rn(sd) : 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < EPT; ++i) {
       xg[i] = __fmul_rn(x[i], gs);
       y[i] = xg[i] * r;  // sd = 0: every code 0 (y = 0, or NaN for a non-finite input)
       const float u = 4.0f * y[i];
@@ -203,21 +279,24 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
     }
     if (__any_sync(0xffffffffu, exact)) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = sd > 0.f ? __fdiv_rn(xg[i], sd) : 0.f;
+      for (int i = 0; i < EPT; ++i) y[i] = sd > 0.f ? __fdiv_rn(xg[i], sd) : 0.f;
     }
-    uint32_t packed = 0;
+    uint32_t packed[2] = {0u, 0u};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) packed |= (sd > 0.f ? f32x2_to_e2m1x2(y[2 * j], y[2 * j + 1]) : 0u) << (8 * j);
+    for (int j = 0; j < 8; ++j)
+      packed[j / 4] |= (sd > 0.f ? f32x2_to_e2m1x2(y[2 * j], y[2 * j + 1]) : 0u) << (8 * (j % 4));
     if (write) {
-      *reinterpret_cast<uint32_t*>(codes + drow * (D / 2) + t * 4) = packed;
-      if ((t & 1) == 0) scales[drow * (D / 16) + t / 2] = static_cast<uint8_t>(sf);
+      *reinterpret_cast<uint2*>(codes + drow * (D / 2) + t * 8) = make_uint2(packed[0], packed[1]);
+      scales[drow * (D / 16) + t] = static_cast<uint8_t>(sf);
     }
   }
 }
 
 // Rows a thread group carries: their loads (rows and slot ids) are all issued
-// before the first row is quantized, so each thread keeps kAppendRows 16-byte
-// loads in flight instead of one.
+// before the first row is quantized, so each thread keeps EPT/8 kAppendRows
+// 16-byte loads in flight.  Measured on 8,192 tokens (D = 256,
+// 16 elements a thread): 2 rows 14.7 us (INT8), 3 rows 15.8, 4 rows 16.7 (fewer
+// resident blocks).
 constexpr int kAppendRows = 2;
 
 // Grid: x over token blocks, y over (KV head, K or V) = 2 h + which, so that no
@@ -227,24 +306,28 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   // a following decode (a programmatic dependent) may be scheduled now; it waits
   // for this grid to complete before it reads the cache
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  constexpr int TPR = D / 8;
+  constexpr int EPT = append_ept<FMT>();
+  constexpr int TPR = D / EPT;
   constexpr int ROWS = kAppendThreads / TPR;  // tokens a block handles side by side
   const int t = threadIdx.x % TPR;
   const int which = blockIdx.y & 1;
   const int h = blockIdx.y >> 1;
   const int64_t n0 = (int64_t)blockIdx.x * ROWS * kAppendRows + threadIdx.x / TPR;
-  const uint16_t* src = (which ? p.v_new : p.k_new) + (int64_t)h * D + t * 8;
+  const uint16_t* src = (which ? p.v_new : p.k_new) + (int64_t)h * D + t * EPT;
   const int64_t stride = (int64_t)p.num_kv_heads * D;  // elements between tokens
-  uint4 raw[kAppendRows];
+  Piece<EPT> raw[kAppendRows];
   int64_t slot[kAppendRows];
 #pragma unroll
   for (int u = 0; u < kAppendRows; ++u) {
     const int64_t n = n0 + (int64_t)u * ROWS;
     const int64_t nn = n < p.n_tokens ? n : 0;
-    raw[u] = *reinterpret_cast<const uint4*>(src + nn * stride);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + nn * stride);
+#pragma unroll
+    for (int k = 0; k < EPT / 8; ++k) raw[u].q[k] = s4[k];
     slot[u] = p.slots[nn];
   }
-  const uint4 sgn = ROT ? rot_sign_masks(t) : make_uint4(0, 0, 0, 0);
+  Piece<EPT> sgn{};
+  if constexpr (ROT) sgn = rot_sign_masks<EPT>(t);
 #pragma unroll
   for (int u = 0; u < kAppendRows; ++u) {
     const int64_t n = n0 + (int64_t)u * ROWS;
@@ -254,7 +337,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 
 template <int FMT, int D>
 cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
-  constexpr int TOKENS = kAppendThreads / (D / 8) * kAppendRows;  // tokens a block covers
+  constexpr int TOKENS = kAppendThreads / (D / append_ept<FMT>()) * kAppendRows;  // tokens a block covers
   const int64_t blocks = (p.n_tokens + TOKENS - 1) / TOKENS;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF || 2 * p.num_kv_heads > 65535) return cudaErrorInvalidValue;
