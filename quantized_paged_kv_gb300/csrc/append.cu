@@ -267,16 +267,25 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
     // x gs / sd and y within 2^-24; |4 y| <= 26, so unless 4 v lies within 2^-16
     // of an integer both round to the same code.  Otherwise the row takes the
     // exact quotients.
+    // On packed pairs: xg = x gs, y = xg r, u = 4 y (exact) and u - rne(u), with
+    // rne(u) = (u + 1.5 * 2^23) - 1.5 * 2^23 for |u| < 2^22 (a larger |u| means a
+    // saturated code either way).
     float xg[EPT], y[EPT];
-    bool exact = false;
+    bool near = false;
     const float r = sd > 0.f ? __frcp_rn(sd) : 0.f;
+    const uint64_t gs2 = f2(gs, gs), r2 = f2(r, r), four2 = f2(4.f, 4.f), mg2 = f2(12582912.0f, 12582912.0f);
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-      xg[i] = __fmul_rn(x[i], gs);
-      y[i] = xg[i] * r;  // sd = 0: every code 0 (y = 0, or NaN for a non-finite input)
-      const float u = 4.0f * y[i];
-      exact |= sd > 0.f && fabsf(u - rintf(u)) < 0x1p-16f;
+    for (int i = 0; i < EPT; i += 2) {
+      const uint64_t xg2 = mul2(f2(x[i], x[i + 1]), gs2);
+      const uint64_t y2 = mul2(xg2, r2);  // sd = 0: every code 0 (y = 0, or NaN for a non-finite input)
+      const uint64_t u2 = mul2(y2, four2);
+      float d0, d1;
+      f2_split(sub2(u2, sub2(add2(u2, mg2), mg2)), d0, d1);
+      f2_split(xg2, xg[i], xg[i + 1]);
+      f2_split(y2, y[i], y[i + 1]);
+      near |= fminf(fabsf(d0), fabsf(d1)) < 0x1p-16f;
     }
+    const bool exact = sd > 0.f && near;
     if (__any_sync(0xffffffffu, exact)) {
 #pragma unroll
       for (int i = 0; i < EPT; ++i) y[i] = sd > 0.f ? __fdiv_rn(xg[i], sd) : 0.f;

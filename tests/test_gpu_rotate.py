@@ -1,11 +1,16 @@
-"""kvq_rotate_rows on the GPU: bit-exact against the oracle's fp32 butterfly, and
-the rotated decode pipeline (rotate K/V before the append, rotate q, decode,
-rotate the output back) against the oracle."""
+"""kvq_rotate_rows on the GPU: bit-exact against the oracle's fp32 butterfly; the
+rotation inside the append (KVQ_ROTATE) bit-exact against the oracle and the
+two-call path, also on the full 8,192-token append workload; and the rotated
+decode pipeline (rotate K/V before the append, rotate q, decode, rotate the
+output back) against the oracle."""
+import functools
+
 import numpy as np
 import pytest
 import torch
 
 from oracle import attention as oatt
+from oracle import formats as ofmt
 from oracle import layout as olay
 from oracle import rotation as orot
 from quantized_paged_kv_gb300 import workloads as W
@@ -199,3 +204,42 @@ def test_rotated_decode_with_fused_append_matches_the_oracle(fmt):
     kvq_rotate_rows(out, out, inverse=True)
     torch.cuda.synchronize()
     assert np.abs(out.cpu().numpy() - _oracle_rotated(wl, fmt)).max() <= H.tol("f32")
+
+
+@functools.lru_cache(maxsize=1)
+def _append_workload_rows():
+    """The append workload's 8,192 new tokens (the last 1,024 of each of its 8
+    sequences): K, V [8192, 4, 256] bf16-valued float32 and their slots."""
+    wl = W.make("append_int8")
+    ks, vs, ss = [], [], []
+    for b in range(wl.B):
+        k, v = wl.kv(b)
+        ks.append(k[-wl.append_tail:])
+        vs.append(v[-wl.append_tail:])
+        ss.append(wl.slots(b)[-wl.append_tail:])
+    return wl, np.concatenate(ks), np.concatenate(vs), np.concatenate(ss)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_append_workload_full_size_bit_exact(fmt, rotate):
+    # every code and scale of the 8,192-token append (as timed), plain and with the
+    # rotation inside the append, against the oracle's quantization
+    from quantized_paged_kv_gb300 import KVCache
+
+    wl, k, v, slots = _append_workload_rows()
+    kr = orot.rotate_fp32(k, out="bf16") if rotate else k
+    vr = orot.rotate_fp32(v, out="bf16") if rotate else v
+    gs = (float(ofmt.nvfp4_tensor_global_scale(kr)), float(ofmt.nvfp4_tensor_global_scale(vr))) \
+        if fmt == "nvfp4" else (1.0, 1.0)
+    cache = KVCache(fmt, wl.num_pages, wl.Hkv, wl.D, k_global_scale=gs[0], v_global_scale=gs[1], fill=H.SENTINEL)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    cache.append(dev(k).to(torch.bfloat16), dev(v).to(torch.bfloat16), dev(slots), rotate=rotate)
+    torch.cuda.synchronize()
+    kc, vc, ks, vs = H.gpu_views_numpy(cache)
+    for x, codes, scales, g in ((kr, kc, ks, gs[0]), (vr, vc, vs, gs[1])):
+        for h in range(wl.Hkv):
+            c_exp, s_exp = oatt.quantize_rows(fmt, x[:, h, :], g)
+            assert np.array_equal(codes[slots // 16, h, slots % 16], c_exp), (fmt, rotate, h)
+            got_s = scales[slots // 16, h, slots % 16]
+            assert np.array_equal(got_s.view(np.uint8), np.asarray(s_exp).view(np.uint8)), (fmt, rotate, h)
