@@ -37,6 +37,31 @@ def test_library_exports_every_header_symbol(kvq):
     assert sorted(kvq._binding.EXPORTS) == syms
 
 
+def header_constants():
+    """Every KVQ_* enumerator of include/kvq.h with its value."""
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for body in re.findall(r"enum\s*\w*\s*\{(.*?)\}", text, flags=re.S):
+        for name, expr in re.findall(r"\b(KVQ_[A-Z0-9_]+)\s*=\s*([^,]+)", body):
+            out[name] = int(eval(expr.strip().replace("u", "")))  # integer literals and shifts only
+    return out
+
+
+def test_binding_constants_match_the_header(kvq):
+    consts = header_constants()
+    assert len(consts) >= 20
+    shared = [n for n in consts if hasattr(kvq._binding, n)]
+    for n in shared:
+        assert getattr(kvq._binding, n) == consts[n], n
+    # the flags and format codes a caller passes must all be there
+    for n in ("KVQ_CHECKED", "KVQ_SKIP_MERGE", "KVQ_EARLY_START", "KVQ_ROTATE", "KVQ_TEST_STALL", "KVQ_FMT_BF16",
+              "KVQ_FMT_INT8", "KVQ_FMT_NVFP4", "KVQ_FMT_INT8_G32", "KVQ_OUT_F32", "KVQ_OUT_BF16"):
+        assert n in shared, n
+    flags = [consts[n] for n in ("KVQ_CHECKED", "KVQ_SKIP_MERGE", "KVQ_EARLY_START", "KVQ_ROTATE", "KVQ_TEST_STALL")]
+    assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)  # distinct single bits
+
+
 def test_bytes_per_token_matches_the_pages(kvq):
     cf = pins.closed_forms()
     assert kvq.kvq_bytes_per_token("int8", 1, 256) == cf["int8_bytes_per_token_head_D256"]
