@@ -650,6 +650,102 @@ def run_ours(args, rank, world, barrier, allmax):
     return line
 
 
+def time_protocol(dev, l2, peak):
+    """The timing protocol's controls on the 32K batch-1 workload: a read-only
+    stream reference (torch's sum over 4 GiB, the read side of the copy peak),
+    the distribution of single graph replays (median and min per call), an
+    A-vs-A noise control (two identical graphs timed in alternation), INT8 and
+    BF16 caches timed in alternating order, and eager (ungraphed) calls."""
+    import statistics
+
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+    from quantized_paged_kv_gb300 import workloads as W
+
+    res = {}
+    buf = torch.ones(2**30, dtype=torch.float32, device=dev)  # 4 GiB, far above L2
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        buf.sum()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    res["read_only_stream"] = {"GBps": round(buf.numel() * 4 / best / 1e9, 1), "how": "torch sum over 4 GiB fp32, best of 10"}
+    del buf
+    torch.cuda.empty_cache()
+
+    wl = W.make("long_int8")
+    per_layer = {f: int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token(f, wl.Hkv, wl.D) for f in ("int8", "bf16")}
+    sets = {f: LayerSet(wl, f, layers_for(per_layer[f], l2, floor=2), dev) for f in ("int8", "bf16")}
+    stream = torch.cuda.Stream()
+
+    def graph_of(ls):
+        plan = ls.plan(0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for r in range(ls.R):
+                ls.call(r, plan)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(ls.R):
+                ls.call(r, plan)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        stream.synchronize()
+        return g, plan
+
+    def replay_us(g, R):  # one replay, microseconds per call
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / R
+
+    ls = sets["int8"]
+    ga, plan = graph_of(ls)
+    gb, _ = graph_of(ls)
+    a, b = [], []
+    for _ in range(30):  # A and A' alternate
+        a.append(replay_us(ga, ls.R))
+        b.append(replay_us(gb, ls.R))
+    res["replays_long_int8"] = {"median_us": round(statistics.median(a), 3), "min_us": round(min(a), 3),
+                                "max_us": round(max(a), 3), "replays": len(a), "calls_per_replay": ls.R}
+    res["a_vs_a_long_int8"] = {"median_us_a": round(statistics.median(a), 3), "median_us_a2": round(statistics.median(b), 3),
+                               "rel_diff": round(statistics.median(b) / statistics.median(a) - 1, 4)}
+    gf = {"int8": ga, "bf16": graph_of(sets["bf16"])[0]}
+    t = {"int8": [], "bf16": []}
+    for i in range(20):  # alternating format order: int8, bf16, bf16, int8, ...
+        order = ("int8", "bf16") if i % 2 == 0 else ("bf16", "int8")
+        for f in order:
+            t[f].append(replay_us(gf[f], sets[f].R))
+    res["paired_formats_long"] = {f: {"median_us": round(statistics.median(v), 3),
+                                      "GBps": round(per_layer[f] / (statistics.median(v) * 1e-6) / 1e9, 1)}
+                                  for f, v in t.items()}
+    torch.cuda.synchronize()  # eager calls: one launch sequence per call, no graph
+    with torch.cuda.stream(stream):
+        for r in range(ls.R):
+            ls.call(r, plan)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = 0
+        for _ in range(5):
+            for r in range(ls.R):
+                ls.call(r, plan)
+                n += 1
+        e1.record(stream)
+    stream.synchronize()
+    res["eager_long_int8"] = {"us": round(e0.elapsed_time(e1) * 1e3 / n, 3), "calls": n}
+    del sets, ga, gb, gf
+    return res
+
+
 def sweep(args, dev, l2, peak, peak_tf=1937.0):
     """Split sweep and the other workloads (per-call µs and KV GB/s)."""
     import gc
@@ -715,6 +811,9 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
         gc.collect()
         torch.cuda.empty_cache()
     res.update(time_rotation(dev, l2, peak))
+    gc.collect()
+    torch.cuda.empty_cache()
+    res.update(time_protocol(dev, l2, peak))
     gc.collect()
     torch.cuda.empty_cache()
     # quantize-and-append of 8192 tokens (the last 1024 of 8 sequences), INT8 (per row
