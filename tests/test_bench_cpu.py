@@ -1,0 +1,56 @@
+"""bench.py's host-side contract on a machine without a GPU: the reference arm
+(the oracle timed on the host cores) prints one JSON line with the contract's
+keys, the layer count keeps the timed pools above L2, and the committed DRAM
+traffic record is used only while the decode kernel's sources are unchanged."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 1
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_layers_keep_the_timed_pools_above_l2():
+    l2 = 126 * 2**20
+    for per_layer in (1 << 20, 68_157_440, 588_000_000, 2 * 10**9):
+        R = bench.layers_for(per_layer, l2, floor=2)
+        assert R >= 2 and (R * per_layer >= 4 * l2 or R == 2)
+        assert bench.layers_for(per_layer, l2) >= 8  # default floor
+
+
+def test_traffic_record_only_for_the_current_decode_source(tmp_path, monkeypatch):
+    rec = bench.traffic_record("long_int8")
+    assert rec is not None, "the committed record must match the current decode sources"
+    assert rec["kernel_sha"] == bench.kernel_sha()
+    assert 0.99 < rec["dram_bytes_per_launch"] / rec["algorithmic_bytes_per_launch"] < 1.2
+    # a record taken on other sources is ignored
+    fake = tmp_path / "profiles"
+    fake.mkdir()
+    stale = dict(rec, kernel_sha="0" * 16)
+    (fake / "traffic.json").write_text(json.dumps({"long_int8": stale}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    csrc = tmp_path / "quantized_paged_kv_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("decode.cuh", "kvq_ptx.cuh", "decode_launch.cu"):
+        (csrc / f).write_bytes(open(os.path.join(ROOT, "quantized_paged_kv_gb300", "csrc", f), "rb").read())
+    assert bench.traffic_record("long_int8") is None
