@@ -97,6 +97,75 @@ def check_int8_exact(int8_quantize, seed=0, rows=64, D=16):
         assert [int(c) for c in codes[i]] == ec, (i, codes[i], ec)
 
 
+def all_finite_bf16_upto(m):
+    """Every finite bf16 value v with |v| <= m (both signs, both zeros), as float32."""
+    v = (np.arange(1 << 16, dtype=np.uint32) << 16).view(np.float32)
+    return v[np.isfinite(v) & (np.abs(v) <= m)]
+
+
+def check_int8_exhaustive_bf16(int8_quantize, maxima=(1.0, 15.875, 29952.0, 1.0005e-30)):
+    """Every finite bf16 value up to a row maximum m, at several m (so several fixed
+    scales fp32(m/127), one of them near the bottom of the fp32 normal range): the
+    oracle's code of each value against exact rational arithmetic."""
+    for m in maxima:
+        m = float(torch.tensor([m]).to(torch.bfloat16).to(torch.float32)[0])
+        vals = all_finite_bf16_upto(m)
+        D = 32
+        n = -(-len(vals) // (D - 1))
+        body = np.zeros(n * (D - 1), np.float32)
+        body[:len(vals)] = vals
+        rows = np.empty((n, D), np.float32)
+        rows[:, 0] = m  # every row's maximum, so every row has the scale fp32(m / 127)
+        rows[:, 1:] = body.reshape(n, D - 1)
+        codes, scales = int8_quantize(rows)
+        s = rn_f32(Fraction(m) / 127)
+        assert np.all(scales.astype(np.float64) == float(s)), m
+        expect = {}
+        for v in np.unique(vals):
+            q = rn_f32(Fraction(float(v)) / s)
+            expect[float(v)] = max(-127, min(127, round(q)))
+        got = np.asarray(codes).astype(np.int64)[:, 1:].reshape(-1)[:len(vals)]
+        want = np.array([expect[float(v)] for v in vals], dtype=np.int64)
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, (m, vals[bad[:5]], got[bad[:5]], want[bad[:5]])
+
+
+def check_nvfp4_exhaustive_bf16(nvfp4_quantize, unpack_nibbles, cases=((1.0, 1.0), (3.0, 0.37), (448.0, 13.5))):
+    """Every finite bf16 value up to a group maximum m, under global scale gs: the
+    oracle's E4M3 scale of the group and E2M1 code of each value against exact
+    rational arithmetic (fp32 steps by rn_f32, the E4M3 step by torch's cast, the
+    E2M1 step by the nearest grid value with ties to the even code)."""
+    grid = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+    for m, gs in cases:
+        m = float(torch.tensor([m]).to(torch.bfloat16).to(torch.float32)[0])
+        gsf = Fraction(float(np.float32(gs)))
+        vals = all_finite_bf16_upto(m)
+        n = -(-len(vals) // 15)
+        body = np.zeros(n * 15, np.float32)
+        body[:len(vals)] = vals
+        rows = np.empty((n, 16), np.float32)
+        rows[:, 0] = m  # every group's maximum
+        rows[:, 1:] = body.reshape(n, 15)
+        codes, scales = nvfp4_quantize(rows, gs)
+        t2 = rn_f32(rn_f32(Fraction(m) / 6) * gsf)
+        sf = int(torch.tensor([float(t2)], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+        if float(t2) > 448:
+            sf = 0x7E
+        sd = Fraction(float(torch.tensor([sf], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32)[0]))
+        assert np.all(np.asarray(scales).reshape(-1) == sf), (m, gs)
+        assert sd > 0
+        expect = {}
+        for v in np.unique(vals):
+            y = rn_f32(rn_f32(Fraction(float(v)) * gsf) / sd)
+            a = abs(y)
+            best = min(range(8), key=lambda i: (abs(a - grid[i]), i % 2))
+            expect[float(v)] = best
+        c = np.asarray(unpack_nibbles(codes)).astype(np.int64)[:, 1:].reshape(-1)[:len(vals)]
+        want = np.array([expect[float(v)] | (8 if np.signbit(v) else 0) for v in vals], dtype=np.int64)
+        bad = np.nonzero(c != want)[0]
+        assert bad.size == 0, (m, gs, vals[bad[:5]], c[bad[:5]], want[bad[:5]])
+
+
 def check_int8_ties(int8_quantize):
     """Rows whose scale is exactly 1/8 (amax = 127/8), so x/s = k + 1/2 exactly."""
     s = 0.125

@@ -9,6 +9,14 @@ def test_int8_matches_exact_rational_arithmetic():
     pins.check_int8_exact(formats.int8_quantize)
 
 
+def test_int8_every_bf16_value_at_fixed_scales():
+    pins.check_int8_exhaustive_bf16(formats.int8_quantize)
+
+
+def test_nvfp4_every_bf16_value_at_fixed_group_scales():
+    pins.check_nvfp4_exhaustive_bf16(formats.nvfp4_quantize, formats.unpack_nibbles)
+
+
 def test_int8_ties_round_half_to_even():
     pins.check_int8_ties(formats.int8_quantize)
 
