@@ -82,3 +82,24 @@ def test_paged_decode_equals_dense_attend_over_dequantized_rows():
 
 def test_verify_matches_brute_force_over_each_visible_prefix():
     pins.check_verify(attention.paged_verify)
+
+
+def test_hand_worked_two_key_softmax():
+    # logits 0 and ln 2 (q . k scaled): p = (1/3, 2/3); V rows e0, e1 -> out = (1/3, 2/3);
+    # lse = log(1 + 2) = ln 3
+    q = np.array([[1.0, 0.0]])
+    k = np.array([[0.0, 0.0], [np.log(2.0), 0.0]])
+    v = np.array([[1.0, 0.0], [0.0, 1.0]])
+    o, lse = attention.attend(q, k, v, 1.0)
+    assert np.allclose(o[0], [1.0 / 3.0, 2.0 / 3.0], rtol=0, atol=1e-15)
+    assert abs(float(np.ravel(lse)[0]) - np.log(3.0)) < 1e-15
+
+
+def test_hand_worked_merge():
+    # two splits with lse 0 and ln 3 (weights 1 : 3), outputs e0 and e1:
+    # out = (1/4, 3/4), lse = ln 4
+    o = np.array([[[1.0, 0.0]], [[0.0, 1.0]]])  # [split][row][D]
+    s = np.array([[0.0], [np.log(3.0)]])        # [split][row]
+    om, sm = attention.merge(o, s)
+    assert np.allclose(om[0], [0.25, 0.75], rtol=0, atol=1e-15)
+    assert abs(float(sm[0]) - np.log(4.0)) < 1e-15
