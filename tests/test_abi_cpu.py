@@ -44,7 +44,9 @@ def header_constants():
     out = {}
     for body in re.findall(r"enum\s*\w*\s*\{(.*?)\}", text, flags=re.S):
         for name, expr in re.findall(r"\b(KVQ_[A-Z0-9_]+)\s*=\s*([^,]+)", body):
-            out[name] = int(eval(expr.strip().replace("u", "")))  # integer literals and shifts only
+            m = re.fullmatch(r"(\d+)u?(?:\s*<<\s*(\d+))?", expr.strip())  # N, Nu or Nu << K
+            assert m, (name, expr)
+            out[name] = int(m.group(1)) << int(m.group(2) or 0)
     return out
 
 
