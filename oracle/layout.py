@@ -15,6 +15,10 @@ re-derives token positions from that written description alone.
     D/32, P]`` float32: ``group_major_scales`` turns that array into the
     ``[num_pages, Hkv, P, D/32]`` form the functions below index.
   * Token ``t`` of sequence ``b`` sits in slot ``block_table[b, t // P] * P + t % P``.
+
+Pinned by hand-worked slot lists (tests/golden/page_mapping.txt), pools whose
+cells hold their own coordinates, and decode / verify checks over pools that the
+tests fill token by token without these functions.
 """
 from __future__ import annotations
 

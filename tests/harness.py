@@ -117,3 +117,13 @@ def oracle_decode(wl, fmt, pools, units=None, q=None):
 
 def tol(out_dtype):
     return 2e-3 if out_dtype == "f32" else 1e-2
+
+
+def bound(out_dtype, ref):
+    """Per-element max-abs bound for outputs compared with the reference values
+    ``ref``: 2e-3 for fp32 output; for bf16 output max(1e-2, 2^-8 |ref|), because
+    rounding the exact result to bf16 alone moves it by up to 2^-8 |ref| (half a
+    bf16 ulp), which exceeds 1e-2 once |ref| > 2.56."""
+    if out_dtype == "f32":
+        return np.full(np.shape(ref), 2e-3)
+    return np.maximum(1e-2, 2.0 ** -8 * np.abs(ref))

@@ -445,18 +445,29 @@ def check_attention_invariants(attend, probabilities, seed=8):
     assert np.max(np.abs(o[0] - v[17])) < 1e-12
 
 
+def place_logical_rows(pool, block_table_row, rows, page_size):
+    """Write a sequence's logical rows into a [num_pages, Hkv, P, ...] pool by
+    the page mapping itself, token by token: token t goes to page
+    block_table_row[t // P], row t % P (the test's own restatement; the oracle's
+    layout functions are not used)."""
+    for t in range(len(rows)):
+        pool[int(block_table_row[t // page_size]), :, t % page_size] = rows[t]
+
+
 def check_verify(paged_verify, seed=9):
     """Causal verification against pure-Python attention over each query token's
     visible prefix (tiny pools, brute force), and its single-token case against
-    decode-style attention over the whole sequence."""
+    decode-style attention over the whole sequence.  The pools are filled with
+    random bytes and then each sequence's logical rows are placed page by page;
+    the brute force reads the logical rows, so a slip in the oracle's page
+    mapping (page and row swapped, a wrong block-table index) fails here."""
     from oracle import brute
-    from oracle import layout as olay
 
     rng = np.random.default_rng(seed)
     P, Hkv, G, D = 4, 2, 3, 8
-    for (lens, T) in [([9, 5], 3), ([4], 4), ([2, 7], 3), ([6], 1)]:
+    for (lens, T) in [([9, 5], 3), ([4], 4), ([2, 7], 3), ([6], 1), ([13], 2)]:
         B = len(lens)
-        npages = sum(-(-L // P) for L in lens)
+        npages = sum(-(-L // P) for L in lens) + 2  # two pages no sequence uses
         perm = rng.permutation(npages)
         bt = np.full((B, max(-(-L // P) for L in lens)), -1, dtype=np.int32)
         o = 0
@@ -469,19 +480,27 @@ def check_verify(paged_verify, seed=9):
         vc = rng.integers(-127, 128, (npages, Hkv, P, D)).astype(np.int8)
         ks = rng.uniform(0.001, 0.05, (npages, Hkv, P)).astype(np.float32)
         vs = rng.uniform(0.001, 0.05, (npages, Hkv, P)).astype(np.float32)
-        kx = kc.astype(np.float64) * ks.astype(np.float64)[..., None]
-        vx = vc.astype(np.float64) * vs.astype(np.float64)[..., None]
+        logical = []
+        for b, L in enumerate(lens):
+            lk = rng.integers(-127, 128, (L, Hkv, D)).astype(np.int8)
+            lv = rng.integers(-127, 128, (L, Hkv, D)).astype(np.int8)
+            lks = rng.uniform(0.001, 0.05, (L, Hkv)).astype(np.float32)
+            lvs = rng.uniform(0.001, 0.05, (L, Hkv)).astype(np.float32)
+            for pool, rows in ((kc, lk), (vc, lv), (ks, lks), (vs, lvs)):
+                place_logical_rows(pool, bt[b], rows, P)
+            logical.append((lk.astype(np.float64) * lks.astype(np.float64)[..., None],
+                            lv.astype(np.float64) * lvs.astype(np.float64)[..., None]))
         pools = {"k_codes": kc.view(np.uint8), "v_codes": vc.view(np.uint8), "k_scales": ks, "v_scales": vs}
         q = rng.standard_normal((B, T, G * Hkv, D))
         sm = 1.0 / math.sqrt(D)
         out, lse = paged_verify("int8", pools, q, bt, np.array(lens), sm, page_size=P)
         for b, L in enumerate(lens):
+            kx, vx = logical[b]
             for i in range(T):
                 vis = max(0, L - T + i + 1)
-                slots = olay.token_slots(bt[b], vis, P)
                 for h in range(Hkv):
-                    kr = [list(kx[s // P, h, s % P]) for s in slots]
-                    vr = [list(vx[s // P, h, s % P]) for s in slots]
+                    kr = [list(kx[t, h]) for t in range(vis)]
+                    vr = [list(vx[t, h]) for t in range(vis)]
                     qs = q[b, i, h * G:(h + 1) * G].tolist()
                     if vis == 0:
                         assert np.all(out[b, i, h * G:(h + 1) * G] == 0) and np.all(np.isneginf(lse[b, i, h * G:(h + 1) * G]))
@@ -489,3 +508,147 @@ def check_verify(paged_verify, seed=9):
                     ob, sb = brute.attend_brute(qs, kr, vr, sm)
                     assert np.max(np.abs(out[b, i, h * G:(h + 1) * G] - np.array(ob))) < 1e-12
                     assert np.max(np.abs(lse[b, i, h * G:(h + 1) * G] - np.array(sb))) < 1e-12
+
+
+def check_paged_decode(paged_decode, seed=13):
+    """Decode over hand-placed pools (INT8 per-row scales, NVFP4 with a global
+    scale, BF16) against pure-Python attention over the logical rows, each
+    dequantized by its format's definition written out here: c * s; e2m1(c) *
+    e4m3(sf) / gs with the E2M1 grid and the E4M3 value read from the golden grid
+    and torch's float8_e4m3fn; the bf16 bits widened."""
+    from oracle import brute
+
+    rng = np.random.default_rng(seed)
+    P, Hkv, G, D = 4, 2, 2, 32
+    lens = [11, 3, 0, 8]
+    B = len(lens)
+    npages = sum(-(-L // P) for L in lens) + 1
+    perm = rng.permutation(npages)
+    bt = np.zeros((B, max(1, max(-(-L // P) for L in lens))), dtype=np.int32)
+    o = 0
+    for b, L in enumerate(lens):
+        n = -(-L // P)
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    grid = [float(x) for x in read_golden("e2m1_grid.txt")]
+    e4 = torch_e4m3_values()
+    q = rng.standard_normal((B, G * Hkv, D))
+    sm = 1.0 / math.sqrt(D)
+    for fmt in ("int8", "nvfp4", "bf16"):
+        rb = {"int8": D, "nvfp4": D // 2, "bf16": 2 * D}[fmt]
+        pools = {}
+        logical = [[None, None] for _ in lens]
+        for which, name in enumerate(("k", "v")):
+            codes = rng.integers(0, 256, (npages, Hkv, P, rb)).astype(np.uint8)
+            if fmt == "int8":
+                scales = rng.uniform(0.001, 0.05, (npages, Hkv, P)).astype(np.float32)
+            elif fmt == "nvfp4":
+                scales = rng.integers(0, 0x7F, (npages, Hkv, P, D // 16)).astype(np.uint8)
+            else:
+                scales = None
+            for b, L in enumerate(lens):
+                lc = rng.integers(0, 256, (L, Hkv, rb)).astype(np.uint8)
+                if fmt == "bf16":  # finite bf16 values: exponent field kept below all-ones
+                    lc[..., 1::2] &= 0xBF
+                place_logical_rows(codes, bt[b], lc, P)
+                x = np.zeros((L, Hkv, D))
+                if fmt == "int8":
+                    ls = rng.uniform(0.001, 0.05, (L, Hkv)).astype(np.float32)
+                    place_logical_rows(scales, bt[b], ls, P)
+                    x = lc.view(np.int8).astype(np.float64) * ls.astype(np.float64)[..., None]
+                elif fmt == "nvfp4":
+                    ls = rng.integers(0, 0x7F, (L, Hkv, D // 16)).astype(np.uint8)
+                    place_logical_rows(scales, bt[b], ls, P)
+                    for t in range(L):
+                        for h in range(Hkv):
+                            for d in range(D):
+                                nib = (int(lc[t, h, d // 2]) >> (4 * (d % 2))) & 0xF
+                                val = (-1.0 if nib & 8 else 1.0) * grid[nib & 7]
+                                x[t, h, d] = val * float(e4[int(ls[t, h, d // 16])]) / 3.5
+                else:
+                    x = (lc.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+                logical[b][which] = x
+            pools[name + "_codes"], pools[name + "_scales"] = codes, scales
+        if fmt == "nvfp4":
+            pools["k_global_scale"] = pools["v_global_scale"] = 3.5
+        out, lse = paged_decode(fmt, pools, q, bt, np.array(lens), sm, page_size=P)
+        for b, L in enumerate(lens):
+            kx, vx = logical[b]
+            for h in range(Hkv):
+                rows = slice(h * G, (h + 1) * G)
+                if L == 0:
+                    assert np.all(out[b, rows] == 0) and np.all(np.isneginf(lse[b, rows]))
+                    continue
+                ob, sb = brute.attend_brute(q[b, rows].tolist(), kx[:, h].tolist(), vx[:, h].tolist(), sm)
+                assert np.max(np.abs(out[b, rows] - np.array(ob))) < 1e-9 * max(1.0, np.max(np.abs(ob))), (fmt, b, h)
+                assert np.max(np.abs(lse[b, rows] - np.array(sb))) < 1e-9 * max(1.0, np.max(np.abs(sb))), (fmt, b, h)
+
+
+# ---------------------------------------------------------------------------
+# pool layout (the page mapping)
+# ---------------------------------------------------------------------------
+def _expand_ranges(tokens):
+    out = []
+    for tok in tokens:
+        if ".." in tok:
+            a, b = tok.split("..")
+            out.extend(range(int(a), int(b) + 1))
+        else:
+            out.append(int(tok))
+    return out
+
+
+def check_token_slots(token_slots):
+    """Slot lists worked by hand (tests/golden/page_mapping.txt)."""
+    rows = read_golden("page_mapping.txt")
+    assert len(rows) >= 6
+    for row in rows:
+        lhs, rhs = row.split("->")
+        P, bt, L = [s.strip() for s in lhs.split("|")]
+        table = np.array([int(x) for x in bt.split()], dtype=np.int32)
+        got = [int(s) for s in token_slots(table, int(L), int(P))]
+        assert got == _expand_ranges(rhs.split()), (row, got)
+
+
+def coordinate_pool(num_pages, hkv, P):
+    """A pool whose cell (page, head, row) holds the triple (page, head, row)."""
+    pool = np.zeros((num_pages, hkv, P, 3), np.int64)
+    for p in range(num_pages):
+        for h in range(hkv):
+            for r in range(P):
+                pool[p, h, r] = (p, h, r)
+    return pool
+
+
+def check_gather_scatter(gather_rows, scatter_rows):
+    """Row gather / scatter on pools whose cells name their own coordinates; the
+    expected cells are worked by hand from slot = page * P + row."""
+    pool = coordinate_pool(20, 3, 16)
+    # slot 37 = page 2 row 5; 2 = page 0 row 2; 16 = page 1 row 0; 63 = page 3 row 15; 305 = page 19 row 1
+    got = gather_rows(pool, np.array([37, 2, 16, 63, 305]), 1)
+    assert np.array_equal(got, [[2, 1, 5], [0, 1, 2], [1, 1, 0], [3, 1, 15], [19, 1, 1]]), got
+    dst = np.full((20, 3, 16, 2), -1, np.int64)
+    scatter_rows(dst, np.array([37, 2]), 2, np.array([[10, 11], [20, 21]]))
+    assert dst[2, 2, 5].tolist() == [10, 11] and dst[0, 2, 2].tolist() == [20, 21]
+    assert int((dst != -1).sum()) == 4
+    # a scale pool [pages, heads, P] with P = 4: slot 5 = page 1 row 1, slot 11 = page 2 row 3
+    sp = np.zeros((6, 2, 4))
+    scatter_rows(sp, np.array([5, 11]), 0, np.array([1.5, 2.5]))
+    assert sp[1, 0, 1] == 1.5 and sp[2, 0, 3] == 2.5 and np.count_nonzero(sp) == 2
+    assert gather_rows(sp, np.array([11, 5, 0]), 0).tolist() == [2.5, 1.5, 0.0]
+
+
+def check_group_major(group_major_scales):
+    """The device's group-major per-32 scales [pages, heads, groups, P] read as
+    [pages, heads, P, groups]: cells worked by hand on a 2 x 2 x 3 x 16 array
+    whose cell (p, h, g, r) holds p*10000 + h*1000 + g*100 + r."""
+    a = np.zeros((2, 2, 3, 16))
+    for p in range(2):
+        for h in range(2):
+            for g in range(3):
+                for r in range(16):
+                    a[p, h, g, r] = p * 10000 + h * 1000 + g * 100 + r
+    out = group_major_scales(a)
+    assert out.shape == (2, 2, 16, 3)
+    assert out[1, 0, 7, 2] == 10207 and out[0, 1, 15, 0] == 1015 and out[1, 1, 0, 1] == 11100
+    assert out[0, 0, 3].tolist() == [3, 103, 203]  # one slot row: its three group scales

@@ -41,7 +41,7 @@ def _compare(wl, fmt, T, split=0, out_dtype="f32", gs=(1.0, 1.0), units=None):
     sel = ~np.isnan(ref_lse)
     rows = sel[..., None].repeat(wl.D, -1)
     assert np.all(np.isfinite(out[rows]))
-    assert np.abs(out - ref)[rows].max() <= H.tol(out_dtype), (fmt, T, split)
+    assert np.all(np.abs(out - ref)[rows] <= H.bound(out_dtype, ref[rows])), (fmt, T, split)
     fin = sel & np.isfinite(ref_lse)
     assert np.abs(lse[fin] - ref_lse[fin]).max() < 1e-3
     assert np.all(np.isneginf(lse[sel & ~np.isfinite(ref_lse)]))

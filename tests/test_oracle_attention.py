@@ -30,23 +30,27 @@ def test_merge_skips_empty_segments():
 
 
 def _paged_pool(rng, fmt, L, D, Hkv, perm):
+    """Quantized pools with the sequence's rows placed page by page (the test's
+    own placement, not the oracle's layout functions); also returns the logical
+    (codes, scales) of K and V."""
     P = 16
     npages = -(-L // P)
     k = pins.bf16_values(rng, (L, Hkv, D))
     v = pins.bf16_values(rng, (L, Hkv, D))
-    pools = {}
+    pools, logical = {}, {}
     for name, x in (("k", k), ("v", v)):
         c, s = attention.quantize_rows(fmt, x.reshape(-1, D))
         c = c.reshape(L, Hkv, -1)
         cp = np.zeros((npages, Hkv, P, c.shape[-1]), np.uint8)
-        sp = None if s is None else np.full((npages, Hkv, P) + s.shape[1:], 0, s.dtype)
-        slots = layout.token_slots(perm, L, P)
-        for h in range(Hkv):
-            layout.scatter_rows(cp, slots, h, c[:, h])
-            if sp is not None:
-                layout.scatter_rows(sp, slots, h, s.reshape(L, Hkv, *s.shape[1:])[:, h])
+        pins.place_logical_rows(cp, perm, c, P)
+        sp = None
+        if s is not None:
+            s = s.reshape(L, Hkv, *s.shape[1:])
+            sp = np.zeros((npages, Hkv, P) + s.shape[2:], s.dtype)
+            pins.place_logical_rows(sp, perm, s, P)
         pools[name + "_codes"], pools[name + "_scales"] = cp, sp
-    return pools
+        logical[name] = (c, s)
+    return pools, logical
 
 
 def test_block_table_permutation_does_not_change_the_result():
@@ -59,7 +63,7 @@ def test_block_table_permutation_does_not_change_the_result():
         outs = []
         for perm in (np.arange(npages), rng.permutation(npages)):
             rng.bit_generator.state = state
-            pools = _paged_pool(np.random.default_rng(5), fmt, L, D, Hkv, perm)
+            pools, _ = _paged_pool(np.random.default_rng(5), fmt, L, D, Hkv, perm)
             o, s = attention.paged_decode(fmt, pools, q, perm[None, :], [L], 0.25)
             outs.append((o, s))
         assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
@@ -69,19 +73,39 @@ def test_paged_decode_equals_dense_attend_over_dequantized_rows():
     rng = np.random.default_rng(12)
     L, D, Hkv, G = 45, 16, 2, 2
     perm = rng.permutation(3)
-    pools = _paged_pool(rng, "int8", L, D, Hkv, perm)
+    pools, logical = _paged_pool(rng, "int8", L, D, Hkv, perm)
     q = pins.bf16_values(rng, (1, Hkv * G, D))
     o, s = attention.paged_decode("int8", pools, q, perm[None, :], [L], 0.25)
-    slots = layout.token_slots(perm, L, 16)
+    (kc, ks), (vc, vs) = logical["k"], logical["v"]
     for h in range(Hkv):
-        k = attention.cache_rows("int8", pools["k_codes"], pools["k_scales"], slots, h)
-        v = attention.cache_rows("int8", pools["v_codes"], pools["v_scales"], slots, h)
+        # logical rows dequantized by their definition c * s
+        k = kc[:, h].view(np.int8).astype(np.float64) * ks[:, h].astype(np.float64)[:, None]
+        v = vc[:, h].view(np.int8).astype(np.float64) * vs[:, h].astype(np.float64)[:, None]
         ob, sb = brute.attend_brute(q[0, h * G:(h + 1) * G].tolist(), k.tolist(), v.tolist(), 0.25)
         assert np.max(np.abs(o[0, h * G:(h + 1) * G] - np.array(ob))) < 1e-12
 
 
 def test_verify_matches_brute_force_over_each_visible_prefix():
     pins.check_verify(attention.paged_verify)
+
+
+def test_paged_decode_over_hand_placed_pools_of_each_format():
+    pins.check_paged_decode(attention.paged_decode)
+
+
+def test_token_slots_hand_worked():
+    pins.check_token_slots(layout.token_slots)
+
+
+def test_gather_and_scatter_rows_on_coordinate_pools():
+    pins.check_gather_scatter(layout.gather_rows, layout.scatter_rows)
+
+
+def test_group_major_scales_hand_worked():
+    pins.check_group_major(layout.group_major_scales)
+    # the inverse restores the device order
+    a = np.arange(2 * 2 * 3 * 16, dtype=np.float64).reshape(2, 2, 3, 16)
+    assert np.array_equal(layout.to_group_major_scales(layout.group_major_scales(a)), a)
 
 
 def test_hand_worked_two_key_softmax():

@@ -8,7 +8,7 @@ be pinning anything.
 import numpy as np
 import pytest
 
-from oracle import attention, formats
+from oracle import attention, formats, layout
 from tests import oracle_pins as pins
 
 
@@ -137,3 +137,65 @@ def test_attention_mutants_are_caught():
     _fails(pins.check_attend_brute, lse_without_log, brute.attend_brute)
     _fails(pins.check_split_merge, attention.attend, split_with_average)
     _fails(pins.check_merge_not_average, attention.attend, averaged)
+
+
+def test_layout_mutants_are_caught(monkeypatch):
+    def slots_page_row_swapped(bt, L, P):  # page from t % P, row from t // P (table index kept in range)
+        t = np.arange(int(L), dtype=np.int64)
+        bt = np.asarray(bt, np.int64)
+        return bt[(t % P) % len(bt)] * P + t // P
+
+    def slots_table_mod(bt, L, P):  # block_table[t % P] instead of block_table[t // P]
+        t = np.arange(int(L), dtype=np.int64)
+        bt = np.asarray(bt, np.int64)
+        return bt[(t % P) % len(bt)] * P + t % P
+
+    def slots_identity_pages(bt, L, P):  # block table ignored
+        return np.arange(int(L), dtype=np.int64)
+
+    def gather_page_row_swapped(pool, slots, head):
+        pool = np.asarray(pool)
+        P = pool.shape[2]
+        slots = np.asarray(slots, np.int64)
+        return pool[slots % P, head, slots // P]
+
+    def gather_head_page_swapped(pool, slots, head):
+        pool = np.asarray(pool)
+        P = pool.shape[2]
+        slots = np.asarray(slots, np.int64)
+        return pool[head, slots // P, slots % P] if pool.shape[0] > head else pool[slots // P, head, slots % P]
+
+    def scatter_page_row_swapped(pool, slots, head, rows):
+        P = pool.shape[2]
+        slots = np.asarray(slots, np.int64)
+        pool[slots % P, head, slots // P] = rows
+
+    def group_major_reshaped(a):  # reshape instead of a transpose
+        a = np.asarray(a)
+        return a.reshape(a.shape[0], a.shape[1], a.shape[3], a.shape[2])
+
+    def group_major_wrong_axes(a):
+        return np.ascontiguousarray(np.swapaxes(np.asarray(a), 1, 2))
+
+    def fails_or_raises(check, *args):  # an out-of-range index is as much a catch as a wrong value
+        with pytest.raises((AssertionError, IndexError)):
+            check(*args)
+
+    for m in (slots_page_row_swapped, slots_table_mod, slots_identity_pages):
+        _fails(pins.check_token_slots, m)
+    fails_or_raises(pins.check_gather_scatter, gather_page_row_swapped, layout.scatter_rows)
+    fails_or_raises(pins.check_gather_scatter, gather_head_page_swapped, layout.scatter_rows)
+    fails_or_raises(pins.check_gather_scatter, layout.gather_rows, scatter_page_row_swapped)
+    _fails(pins.check_group_major, group_major_reshaped)
+    with pytest.raises((AssertionError, ValueError)):
+        pins.check_group_major(group_major_wrong_axes)
+    # the same slips inside the oracle's decode and verify are caught by the
+    # pins of those functions (hand-placed pools, brute force over logical rows)
+    for m in (slots_page_row_swapped, slots_table_mod):
+        with monkeypatch.context() as mp:
+            mp.setattr(layout, "token_slots", m)
+            _fails(pins.check_verify, attention.paged_verify)
+            _fails(pins.check_paged_decode, attention.paged_decode)
+    with monkeypatch.context() as mp:
+        mp.setattr(layout, "gather_rows", gather_page_row_swapped)
+        fails_or_raises(pins.check_paged_decode, attention.paged_decode)
