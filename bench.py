@@ -375,7 +375,7 @@ def time_verify(ls, T, steps, warmup=16):
     import quantized_paged_kv_gb300 as kvq
 
     wl = ls.wl
-    plan = kvq.DecodePlan(ls.caches[0], kvq.verify_lengths(wl.seq_lens, T), wl.Hq, device=ls.device)
+    plan = kvq.DecodePlan(ls.caches[0], wl.seq_lens, wl.Hq, device=ls.device, q_len=T)
     q = torch.from_numpy(wl.q_tokens(T)).to(torch.bfloat16).to(ls.device)
     out = torch.empty((wl.B, T, wl.Hq, wl.D), dtype=ls.out.dtype, device=ls.device)
     stream = torch.cuda.Stream()
@@ -920,7 +920,7 @@ def run_ncu_case(args):
             ws = kvq.prefill(ls.caches[i % R], q, ls.bt[0].contiguous(), L, out, wl.sm_scale, workspace=ws)
     elif args.verify_tokens:
         T = args.verify_tokens
-        plan = kvq.DecodePlan(ls.caches[0], kvq.verify_lengths(wl.seq_lens, T), wl.Hq)
+        plan = kvq.DecodePlan(ls.caches[0], wl.seq_lens, wl.Hq, q_len=T)
         q = torch.from_numpy(wl.q_tokens(T)).to(torch.bfloat16).cuda()
         out = torch.empty((wl.B, T, wl.Hq, wl.D), dtype=ls.out.dtype, device="cuda")
         for i in range(args.calls):

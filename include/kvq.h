@@ -140,7 +140,7 @@ enum {
  * (the pages' vLLM layout put a 4-byte scale after each 256-byte row, which
  * blocked wide loads: [int8-kv] "Read the compressed cache without copying it first").
  *
- * Supported: page_size 16; head_dim 128 or 256 (NVFP4: 256); any num_kv_heads >= 1.
+ * Supported: page_size 16; head_dim 128 or 256 (every format); any num_kv_heads >= 1.
  * NVFP4 global scales must be finite and > 0 and must stay fixed while entries
  * are live ([nvfp4] "How 2,048 bytes became 576").
  */
@@ -225,7 +225,14 @@ int kvq_quant_append(const kvq_cache* cache, const void* k_new, const void* v_ne
  * pages without first reading an offset.
  *   seq_lens        host int32 [batch], each >= 0
  *   split_override  > 0: S_b = clamp(split_override, 1, max(n_pages_b, 1));
- *                   0: automatic — pages per split = max(4, ceil(NHG * total_pages / C))
+ *                   0: automatic.  Candidate split sizes x (pages a split, at
+ *                   least 4; S_b = ceil(n_pages_b / x)): x = NHG * total_pages /
+ *                   (C * m) for m in {1, 1.25, 1.5, 2, 2.5, 3, 4, 6}, and for k =
+ *                   1..4 the smallest x whose items fit in k * C (whole waves).
+ *                   Each candidate's items are packed as below and its critical
+ *                   path (the largest CTA load, a page costing 1 and an item 8
+ *                   more) is computed; the shortest wins (ties: fewer items;
+ *                   a whole-wave candidate only when strictly shorter).
  *   target_ctas     CTAs to plan for; 0 = measured on the current device (SM count
  *                   x resident decode CTAs per SM for this format/head_dim);
  *                   C = min(target_ctas, total * NHG)
@@ -240,6 +247,18 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
                     int32_t split_override, int32_t target_ctas,
                     int32_t* plan, int64_t plan_capacity,
                     int32_t* total_splits, int32_t* num_ctas);
+
+/* kvq_plan_splits for a verify call (kvq_paged_verify_attention) of q_len query
+ * tokens a sequence: the plan covers the batch * q_len virtual sequences, in
+ * order b * q_len + i, whose visible lengths max(0, seq_lens[b] - q_len + 1 + i)
+ * this call computes (causal: query token i sits at position seq_lens[b] -
+ * q_len + i).  seq_lens: host int32 [batch], the q_len new tokens included.
+ * Every other argument, the plan layout and the return codes are those of
+ * kvq_plan_splits (with batch * q_len in place of batch); KVQ_ERR_INVALID_ARG
+ * for q_len < 1. */
+int kvq_plan_verify_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                           int32_t split_override, int32_t target_ctas, int32_t* plan, int64_t plan_capacity,
+                           int32_t* total_splits, int32_t* num_ctas);
 
 /* Workspace bytes for a decode call: a 256-byte status block, then
  * lse_part float[total_splits][num_q_heads] (padded to 256 bytes), then
@@ -306,8 +325,9 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
  * read for one token is mostly still in L2 for the others.
  *   q              device bf16 [batch][q_len][num_q_heads][head_dim]
  *   seq_lens       device int32 [batch]: tokens in the cache, the q_len new ones included
- *   plan           kvq_plan_splits over the batch * q_len virtual lengths
- *                  max(0, seq_lens[b] - q_len + 1 + i), in order b * q_len + i
+ *   plan           kvq_plan_verify_splits(seq_lens, batch, q_len, ...): the plan
+ *                  over the batch * q_len virtual lengths max(0, seq_lens[b] -
+ *                  q_len + 1 + i), in order b * q_len + i
  *   workspace      >= kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim)
  *   out            device [batch][q_len][num_q_heads][head_dim] float or bf16
  *   lse_out        device float [batch][q_len][num_q_heads] (nullable)
@@ -338,7 +358,7 @@ int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t ba
  * cores (tcgen05.mma, fp32 accumulators in tensor memory).  A work item is 128
  * query rows (token, query head) of one KV head against one of `splits` key
  * ranges; with splits > 1 the partials are combined by the merge kernel on the
- * same stream.  INT8 and BF16 caches at head_dim 128 or 256, NVFP4 at 256;
+ * same stream.  INT8, NVFP4 and BF16 caches at head_dim 128 or 256;
  * 1 <= num_q_heads / num_kv_heads <= 8.  INT8_G32 caches are refused with
  * KVQ_ERR_UNSUPPORTED (a per-32 scale cannot be folded into the logits or P,
  * and the scaled values are not exact in fp16).

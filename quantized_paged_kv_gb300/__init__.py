@@ -12,9 +12,10 @@ call does, and raises if it has not been built.
 from . import _binding
 from ._binding import (  # noqa: F401
     FORMATS, KVQ_CHECKED, KVQ_EARLY_START, KVQ_ROTATE, KVQ_SKIP_MERGE, KvqError, kvq_bytes_per_token, kvq_cache_array_bytes,
-    kvq_decode_workspace_bytes, kvq_last_error, kvq_paged_decode_attention, kvq_plan_splits, kvq_quant_append,
+    kvq_decode_workspace_bytes, kvq_last_error, kvq_paged_decode_attention, kvq_plan_splits, kvq_plan_verify_splits,
+    kvq_quant_append,
     kvq_paged_decode_attention_static, kvq_paged_prefill_attention, kvq_paged_verify_attention,
     kvq_prefill_splits, kvq_prefill_workspace_bytes, kvq_read_status, kvq_rotate_rows, kvq_split_merge,
     kvq_workspace_partials, lib,
 )
-from .cache import DecodePlan, KVCache, decode, prefill, verify, verify_lengths  # noqa: F401
+from .cache import DecodePlan, KVCache, decode, prefill, verify  # noqa: F401

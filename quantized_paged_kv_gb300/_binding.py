@@ -28,7 +28,7 @@ FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4, "
 
 # every symbol include/kvq.h declares
 EXPORTS = (
-    "kvq_bytes_per_token", "kvq_cache_array_bytes", "kvq_quant_append", "kvq_plan_splits",
+    "kvq_bytes_per_token", "kvq_cache_array_bytes", "kvq_quant_append", "kvq_plan_splits", "kvq_plan_verify_splits",
     "kvq_decode_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
     "kvq_paged_decode_attention_static", "kvq_paged_verify_attention", "kvq_prefill_splits",
     "kvq_prefill_workspace_bytes", "kvq_paged_prefill_attention", "kvq_split_merge", "kvq_read_status",
@@ -69,6 +69,8 @@ def lib():
         "kvq_quant_append": (c_int32, [POINTER(KvqCacheStruct), P, P, P, c_int64, P, c_uint32, P]),
         "kvq_plan_splits": (c_int32, [POINTER(KvqCacheStruct), POINTER(c_int32), c_int32, c_int32, c_int32,
                                       POINTER(c_int32), c_int64, POINTER(c_int32), POINTER(c_int32)]),
+        "kvq_plan_verify_splits": (c_int32, [POINTER(KvqCacheStruct), POINTER(c_int32), c_int32, c_int32, c_int32,
+                                             c_int32, POINTER(c_int32), c_int64, POINTER(c_int32), POINTER(c_int32)]),
         "kvq_decode_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
         "kvq_workspace_partials": (c_int32, [P, c_int32, c_int32, c_int32, POINTER(c_void_p), POINTER(c_void_p)]),
         "kvq_paged_decode_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P, c_int32,
@@ -133,22 +135,38 @@ def kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim):
     return int(lib().kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim))
 
 
+def _plan(call, name, cache_struct, seq_lens, lead, split_override, target_ctas, virtual_batch):
+    """A size query, then the plan itself; ``lead`` = the arguments between
+    seq_lens and split_override (the batch, and q_len for a verify plan)."""
+    sl = torch.as_tensor(list(seq_lens), dtype=torch.int32)
+    total, nctas = c_int32(), c_int32()
+    slp = sl.numpy().ctypes.data_as(POINTER(c_int32))
+    rc = call(ctypes.byref(cache_struct), slp, *lead, split_override, target_ctas, None, 0, ctypes.byref(total),
+              ctypes.byref(nctas))
+    if rc not in (0, 3):  # 3 = KVQ_ERR_WORKSPACE (size query)
+        _check(rc, name)
+    # head groups per split <= num_kv_heads, so this bounds the plan length
+    plan = torch.zeros(virtual_batch + 9 + nctas.value + 4 * total.value * cache_struct.num_kv_heads,
+                       dtype=torch.int32)
+    _check(call(ctypes.byref(cache_struct), slp, *lead, split_override, target_ctas,
+                plan.numpy().ctypes.data_as(POINTER(c_int32)), plan.numel(), ctypes.byref(total),
+                ctypes.byref(nctas)), name)
+    return plan, total.value, nctas.value
+
+
 def kvq_plan_splits(cache_struct, seq_lens, split_override=0, target_ctas=0):
     """seq_lens: host int sequence.  Returns (plan int32 CPU tensor, total_splits, num_ctas)."""
-    sl = torch.as_tensor(list(seq_lens), dtype=torch.int32)
-    B = sl.numel()
-    total, nctas = c_int32(), c_int32()
-    L = lib()
-    rc = L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
-                           split_override, target_ctas, None, 0, ctypes.byref(total), ctypes.byref(nctas))
-    if rc not in (0, 3):  # 3 = KVQ_ERR_WORKSPACE (size query)
-        _check(rc, "kvq_plan_splits")
-    # head groups per split <= num_kv_heads, so this bounds the plan length
-    plan = torch.zeros(B + 9 + nctas.value + 4 * total.value * cache_struct.num_kv_heads, dtype=torch.int32)
-    _check(L.kvq_plan_splits(ctypes.byref(cache_struct), sl.numpy().ctypes.data_as(POINTER(c_int32)), B,
-                             split_override, target_ctas, plan.numpy().ctypes.data_as(POINTER(c_int32)),
-                             plan.numel(), ctypes.byref(total), ctypes.byref(nctas)), "kvq_plan_splits")
-    return plan, total.value, nctas.value
+    B = len(seq_lens)
+    return _plan(lib().kvq_plan_splits, "kvq_plan_splits", cache_struct, seq_lens, (B,), split_override,
+                 target_ctas, B)
+
+
+def kvq_plan_verify_splits(cache_struct, seq_lens, q_len, split_override=0, target_ctas=0):
+    """The plan of a verify call over q_len query tokens a sequence (the causal
+    visible lengths are computed by the library)."""
+    B = len(seq_lens)
+    return _plan(lib().kvq_plan_verify_splits, "kvq_plan_verify_splits", cache_struct, seq_lens, (B, q_len),
+                 split_override, target_ctas, B * q_len)
 
 
 def kvq_workspace_partials(workspace, total_splits, num_q_heads, head_dim):

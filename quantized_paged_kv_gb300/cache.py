@@ -55,14 +55,20 @@ class KVCache:
 
 class DecodePlan:
     """Host split plan for one batch composition, copied to the device, plus the
-    workspace it needs (status word zeroed once)."""
+    workspace it needs (status word zeroed once).  q_len > 1: the plan of a
+    verify call over q_len query tokens a sequence."""
 
-    def __init__(self, cache, seq_lens, num_q_heads, split_override=0, target_ctas=0, device="cuda"):
-        plan, self.total_splits, self.num_ctas = B.kvq_plan_splits(
-            cache.struct, [int(x) for x in seq_lens], split_override, target_ctas)
+    def __init__(self, cache, seq_lens, num_q_heads, split_override=0, target_ctas=0, device="cuda", q_len=1):
+        lens = [int(x) for x in seq_lens]
+        if q_len == 1:
+            plan, self.total_splits, self.num_ctas = B.kvq_plan_splits(cache.struct, lens, split_override, target_ctas)
+        else:
+            plan, self.total_splits, self.num_ctas = B.kvq_plan_verify_splits(cache.struct, lens, q_len,
+                                                                              split_override, target_ctas)
         self.plan_host = plan
         self.plan = plan.to(device)
-        self.batch = len(seq_lens)
+        self.q_len = q_len
+        self.batch = len(seq_lens) * q_len
         self.num_q_heads = num_q_heads
         self.head_dim = cache.head_dim
         self.workspace = torch.zeros(B.kvq_decode_workspace_bytes(self.total_splits, num_q_heads, cache.head_dim),
@@ -83,16 +89,11 @@ def decode(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, 
                                  plan.num_ctas, plan.workspace, out, lse_out, flags, stream)
 
 
-def verify_lengths(seq_lens, q_len):
-    """Visible tokens of the batch * q_len virtual sequences of a verify call, in
-    the order b * q_len + i: max(0, L_b - q_len + 1 + i)."""
-    return [max(0, int(L) - q_len + 1 + i) for L in seq_lens for i in range(q_len)]
-
-
 def verify(cache, plan, q, block_tables, seq_lens, out, sm_scale, lse_out=None, checked=False, skip_merge=False,
            early_start=False, stream=None):
-    """Causal attention for q.shape[1] query tokens a sequence; plan: DecodePlan over
-    verify_lengths(seq_lens, q_len)."""
+    """Causal attention for q.shape[1] query tokens a sequence; plan: DecodePlan(..., q_len=q.shape[1])."""
+    if plan.q_len != q.shape[1]:
+        raise ValueError(f"the plan is for q_len {plan.q_len}, q has {q.shape[1]} query tokens")
     flags = ((B.KVQ_CHECKED if checked else 0) | (B.KVQ_SKIP_MERGE if skip_merge else 0)
              | (B.KVQ_EARLY_START if early_start else 0))
     B.kvq_paged_verify_attention(cache.struct, q, sm_scale, block_tables, seq_lens, plan.plan, plan.total_splits,

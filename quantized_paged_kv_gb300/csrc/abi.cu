@@ -71,8 +71,6 @@ int check_cache(const kvq_cache* c, bool pointers) {
   if (c->page_size != 16) return fail(KVQ_ERR_UNSUPPORTED, "page_size %d: only 16 is implemented", c->page_size);
   if (c->head_dim != 128 && c->head_dim != 256)
     return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d: only 128 and 256 are implemented", c->head_dim);
-  if (c->format == KVQ_FMT_NVFP4 && c->head_dim != 256)
-    return fail(KVQ_ERR_UNSUPPORTED, "NVFP4 is implemented for head_dim 256 only");
   if (c->num_kv_heads < 1) return fail(KVQ_ERR_INVALID_ARG, "num_kv_heads %d < 1", c->num_kv_heads);
   if (c->num_pages < 1) return fail(KVQ_ERR_INVALID_ARG, "num_pages %d < 1", c->num_pages);
   if ((int64_t)c->num_pages * c->num_kv_heads * c->page_size > 0x7FFFFFFFLL)
@@ -115,15 +113,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // halves (stride 128), KV heads (stride 16 * row_bytes), pages.  One box = the
 // `hg` consecutive heads of one page, landing in shared memory as
 // [head][half][row][128 bytes] with the 128-byte swizzle the decode kernel's
-// ldmatrix addressing expects.
+// ldmatrix addressing expects.  Rows of 64 bytes (NVFP4 at head_dim 128): a head
+// block of 16 rows is read as 8 rows of 128 bytes (token pairs), one half.
 int make_code_map(CUtensorMap* map, void* base, int64_t num_pages, int64_t hkv, int64_t rbytes, int hg) {
   auto fn = encode_fn();
   if (!fn) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[5] = {128, 16, static_cast<cuuint64_t>(rbytes / 128), static_cast<cuuint64_t>(hkv),
-                              static_cast<cuuint64_t>(num_pages)};
-  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(rbytes), 128, static_cast<cuuint64_t>(16 * rbytes),
+  if (rbytes != 64 && rbytes % 128 != 0) return fail(KVQ_ERR_UNSUPPORTED, "code rows of %lld bytes", (long long)rbytes);
+  const int64_t rows = rbytes >= 128 ? 16 : 16 * rbytes / 128;  // 128-byte rows of a head block
+  const int64_t halves = rbytes >= 128 ? rbytes / 128 : 1;
+  const int64_t row_stride = rbytes >= 128 ? rbytes : 128;
+  const cuuint64_t dims[5] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(halves),
+                              static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(row_stride), 128, static_cast<cuuint64_t>(16 * rbytes),
                                  static_cast<cuuint64_t>(16 * rbytes * hkv)};
-  const cuuint32_t box[5] = {128, 16, static_cast<cuuint32_t>(rbytes / 128), static_cast<cuuint32_t>(hg), 1};
+  const cuuint32_t box[5] = {128, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(halves),
+                             static_cast<cuuint32_t>(hg), 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, base, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -176,7 +180,7 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
       cudaFuncAttributes fa;
       e = cudaFuncGetAttributes(&fa, kern);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(decode kernel)");
-      if (fa.numRegs != inst->launch_regs)
+      if (inst->launch_regs > 0 && fa.numRegs != inst->launch_regs)
         return fail(KVQ_ERR_UNSUPPORTED, "decode kernel built with %d registers a thread, its register split assumes %d",
                     fa.numRegs, inst->launch_regs);
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, inst->smem_bytes);
@@ -460,6 +464,24 @@ int kvq_plan_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t bat
   return succeed();
 }
 
+int kvq_plan_verify_splits(const kvq_cache* cache, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                           int32_t split_override, int32_t target_ctas, int32_t* plan, int64_t plan_capacity,
+                           int32_t* total_splits, int32_t* num_ctas) {
+  if (batch < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", batch);
+  if (q_len < 1) return fail(KVQ_ERR_INVALID_ARG, "q_len %d < 1", q_len);
+  if (!seq_lens) return fail(KVQ_ERR_INVALID_ARG, "seq_lens is NULL");
+  if ((int64_t)batch * q_len > 0x7FFFFFFF / 4) return fail(KVQ_ERR_UNSUPPORTED, "batch x q_len too large");
+  // query token i of sequence b sees the first L_b - q_len + 1 + i tokens (causal)
+  std::vector<int32_t> lens((size_t)batch * q_len);
+  for (int32_t b = 0; b < batch; ++b) {
+    if (seq_lens[b] < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_lens[%d] = %d < 0", b, seq_lens[b]);
+    for (int32_t i = 0; i < q_len; ++i)
+      lens[(size_t)b * q_len + i] = std::max(0, seq_lens[b] - q_len + 1 + i);
+  }
+  return kvq_plan_splits(cache, lens.data(), batch * q_len, split_override, target_ctas, plan, plan_capacity,
+                         total_splits, num_ctas);
+}
+
 size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int32_t head_dim) {
   if (total_splits < 0 || num_q_heads < 0 || head_dim < 0) return 0;
   const size_t rows = (size_t)total_splits * num_q_heads;
@@ -486,10 +508,13 @@ namespace {
 // launch works on batch = nseq x q_len virtual sequences (query token i of cache
 // sequence b is virtual sequence b * q_len + i, with b's block table and
 // L_b - q_len + 1 + i visible tokens).
+// clear_status: zero the workspace's status block on the stream once every
+// argument has been checked, just before the first launch (a rejected call
+// leaves the block as it was).
 int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_len, int32_t num_q_heads,
                 float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* seq_lens,
                 const int32_t* plan, int32_t total_splits, int32_t num_ctas, void* workspace, size_t workspace_bytes,
-                void* out, int32_t out_dtype, float* lse_out, uint32_t flags, void* stream) {
+                void* out, int32_t out_dtype, float* lse_out, uint32_t flags, void* stream, bool clear_status = false) {
   int rc = check_cache(cache, true);
   if (rc) return rc;
   if (nseq < 1) return fail(KVQ_ERR_INVALID_ARG, "batch %d < 1", nseq);
@@ -589,6 +614,13 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   int32_t q_host = 0;
   rc = memory_kind(q, "q", &q_host);
   if (rc) return rc;
+  int32_t out_host = 0;
+  rc = memory_kind(out, "out", &out_host);
+  if (rc) return rc;
+  if (clear_status) {
+    const cudaError_t ec = cudaMemsetAsync(workspace, 0, 256, st);
+    if (ec != cudaSuccess) return cuda_fail(ec, "clearing the status block");
+  }
   const void* q_dev = q;
   if (q_host) {
     const size_t rows = (size_t)total_splits * num_q_heads;
@@ -621,8 +653,7 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   p.drop_copies = (flags & KVQ_TEST_STALL) ? 1 : 0;
   p.wait_limit_ns = (flags & KVQ_TEST_STALL) ? 2000000ull : 2000000000ull;  // 2 ms / 2 s
   p.q_len = q_len;
-  rc = memory_kind(out, "out", &p.out_host);
-  if (rc) return rc;
+  p.out_host = out_host;
   p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
   p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
   p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
@@ -643,6 +674,15 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
 }
 
 }  // namespace
+
+int kvq::decode_clearing_status(const kvq_cache* cache, const void* q, int32_t batch, int32_t num_q_heads,
+                                float sm_scale, const int32_t* block_tables, int32_t max_pages_per_seq,
+                                const int32_t* seq_lens, const int32_t* plan, int32_t total_splits, int32_t num_ctas,
+                                void* workspace, size_t workspace_bytes, void* out, int32_t out_dtype, float* lse_out,
+                                uint32_t flags, void* stream) {
+  return decode_impl(cache, q, batch, 1, num_q_heads, sm_scale, block_tables, max_pages_per_seq, seq_lens, plan,
+                     total_splits, num_ctas, workspace, workspace_bytes, out, out_dtype, lse_out, flags, stream, true);
+}
 
 extern "C" {
 

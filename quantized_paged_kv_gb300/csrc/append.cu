@@ -372,7 +372,8 @@ cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaS
       return head_dim == 256 ? launch_append_t<KVQ_FMT_BF16, 256>(p, stream)
                              : launch_append_t<KVQ_FMT_BF16, 128>(p, stream);
     case KVQ_FMT_NVFP4:
-      return launch_append_t<KVQ_FMT_NVFP4, 256>(p, stream);
+      return head_dim == 256 ? launch_append_t<KVQ_FMT_NVFP4, 256>(p, stream)
+                             : launch_append_t<KVQ_FMT_NVFP4, 128>(p, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -95,11 +95,11 @@ struct DecodeTraits<KVQ_FMT_BF16, D> {
   static constexpr int kScaleRow = 0;
 };
 
-template <>
-struct DecodeTraits<KVQ_FMT_NVFP4, 256> {
+template <int D>
+struct DecodeTraits<KVQ_FMT_NVFP4, D> {
   static constexpr bool kBf16Mma = false;
-  static constexpr int kRow = 128;
-  static constexpr int kScaleRow = 16;  // one E4M3 byte per 16 elements
+  static constexpr int kRow = D / 2;        // two E2M1 codes a byte
+  static constexpr int kScaleRow = D / 16;  // one E4M3 byte per 16 elements
 };
 
 // consumer warps per CTA: 8 at D = 256 (+1 producer = 9 warps: at most 3 per
@@ -143,8 +143,9 @@ struct DecodeLayout {
   // one q tile per head of the group (kAvail bytes together; the ring gets what
   // the group's hg tiles leave), then the barriers and the page-id buffer.
   static constexpr int kIdBytes = kMaxProducers * 2 * 32 * 4;
-  static constexpr int kAvail = (227 * 1024 - 1024 - 2 * kMaxStages * 8 - kIdBytes) / 1024 * 1024;
-  static constexpr int kSmemBytes = 1024 + kAvail + 2 * kMaxStages * 8 + kIdBytes;
+  static constexpr int kBadBytes = kMaxStages * 4;  // per stage: its page id was out of range
+  static constexpr int kAvail = (227 * 1024 - 1024 - 2 * kMaxStages * 8 - kIdBytes - kBadBytes) / 1024 * 1024;
+  static constexpr int kSmemBytes = 1024 + kAvail + 2 * kMaxStages * 8 + kIdBytes + kBadBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static __host__ __device__ constexpr int ring_bytes(int hg) { return (kAvail - hg * kQBytes) / 1024 * 1024; }
   // the smallest ring (a group of kCW heads): the epilogue's buffers fit in any
@@ -223,6 +224,16 @@ __device__ __forceinline__ uint32_t swz(uint32_t block, int t, int chunk) {
   return block + (chunk >> 3) * (kPage * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
 }
 
+// The same for a head block of any row size: rows of 128 bytes or more as above;
+// 64-byte rows (NVFP4 at D = 128) travel as 8 rows of 128 bytes, each holding a
+// token pair (token t is the low or high half of row t / 2), under the same
+// 128-byte swizzle.
+template <int ROW>
+__device__ __forceinline__ uint32_t swz_row(uint32_t block, int t, int chunk) {
+  if constexpr (ROW >= 128) return swz(block, t, chunk);
+  else return swz(block, t >> 1, 4 * (t & 1) + chunk);
+}
+
 __device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }  // k in [-126, 127]
 
 // PLO: the P' operand carries a lo term (fp32 output); the launcher picks the
@@ -268,6 +279,9 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo::kAvail);
   uint64_t* empty = full + kMaxStages;
   int* pid_s = reinterpret_cast<int*>(empty + kMaxStages);  // [producer][2][32] page ids
+  // per stage, set by its producer before the stage's full barrier completes:
+  // the page id was out of range, so the consumers mask every token of it
+  int* bad_s = pid_s + Lo::kIdBytes / 4;
 
   // ---- plan: split offsets [batch + 1], C = gridDim.x, then (16-byte aligned) the
   // first item descriptor of every CTA, the CTAs' offsets into the list of their
@@ -441,6 +455,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
               if (p.drop_copies) {
                 // failure-path test: the stage is never filled, so its consumers' wait runs out
               } else if (pg >= 0) {
+                bad_s[st] = 0;  // read by the consumers after this stage's full barrier completes
                 uint8_t* kc = codes + st * stage_code;
                 mbar_arrive_expect_tx(&full[st], stage_code + stage_scale);
                 tma_load_5d(kc, &tm_k, 0, 0, 0, static_cast<int>(head0), pg, &full[st]);
@@ -452,7 +467,11 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
                   bulk_load(ks + HG * Lo::kHeadScale, p.v_scales + off, HG * Lo::kHeadScale, &full[st]);
                 }
               } else {
-                mbar_arrive(&full[st]);  // nothing to load; the stage keeps stale bytes (status flagged)
+                // an out-of-range page id (flagged in the status word): nothing is
+                // loaded, and the consumers mask every token of the stage, so the
+                // page contributes nothing whatever stale bytes the stage holds
+                bad_s[st] = 1;
+                mbar_arrive(&full[st]);
               }
               st += NP;
               if (st >= NST) {
@@ -634,7 +653,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
       const uint8_t* ksc = scales + st * stage_scale + hl * Lo::kHeadScale;
       const uint8_t* vsc = ksc + HG * Lo::kHeadScale;
       const int tok0 = (page_begin + idx) * kPage;
-      const int nvalid = min(kPage, L - tok0);
+      const int nvalid = bad_s[st] ? 0 : min(kPage, L - tok0);  // a bad page id: no valid token
 
     // ---------------------------------------------------------- S = q K^T
     float sacc[2][2][4];
@@ -655,8 +674,13 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     if constexpr (FMT == KVQ_FMT_NVFP4) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const uint4 srow = *reinterpret_cast<const uint4*>(ksc + (8 * i + r) * 16);
-        ksw[i][0] = srow.x; ksw[i][1] = srow.y; ksw[i][2] = srow.z; ksw[i][3] = srow.w;
+        if constexpr (D == 256) {
+          const uint4 srow = *reinterpret_cast<const uint4*>(ksc + (8 * i + r) * 16);
+          ksw[i][0] = srow.x; ksw[i][1] = srow.y; ksw[i][2] = srow.z; ksw[i][3] = srow.w;
+        } else {  // D = 128: 8 group scales a token
+          const uint2 srow = *reinterpret_cast<const uint2*>(ksc + (8 * i + r) * 8);
+          ksw[i][0] = srow.x; ksw[i][1] = srow.y; ksw[i][2] = ksw[i][3] = 0u;
+        }
       }
     }
 #pragma unroll
@@ -677,7 +701,7 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         uint32_t w[4];
-        ldsm_x4(swz(kblk, 8 * i + (lane & 7), 4 * cg + (lane >> 3)), w[0], w[1], w[2], w[3]);
+        ldsm_x4(swz_row<T::kRow>(kblk, 8 * i + (lane & 7), 4 * cg + (lane >> 3)), w[0], w[1], w[2], w[3]);
         if constexpr (FMT == KVQ_FMT_INT8) {
           // chunk = 16 d's = one k-step; lane gets bytes 4c..4c+3 of row 8i+r:
           // k (2c, 2c+1) <- d 16ch+4c+{0,1}, k (2c+8, 2c+9) <- d 16ch+4c+{2,3}.
@@ -757,13 +781,16 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
     pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 1));
     pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 2));
     const float m_new = fmaxf(m_run, pmax);
-    const float alpha = exp2f(m_run - m_new);  // m_run = -inf -> 0
+    // no valid token so far (only a page with a bad id): keep the state empty
+    // instead of forming exp2(-inf - -inf)
+    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = exp2f(m_run - m_use);  // m_run = -inf -> 0
     m_run = m_new;
     float pr[4];
     float psum = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      pr[u] = exp2f(z[u] - m_new);  // masked tokens: exp2(-inf) = 0
+      pr[u] = exp2f(z[u] - m_use);  // masked tokens: exp2(-inf) = 0
       psum += pr[u];
     }
     l_run = l_run * alpha + psum;
@@ -863,6 +890,52 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
         }
         mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], phi[0], phi[1]);
         if constexpr (p_lo) mma16816<true>(oacc[mt], w[0], w[1], w[2], w[3], plo[0], plo[1]);
+      }
+    } else if constexpr (D == 128) {
+      // NVFP4 at D = 128 (64-byte rows): lane (r, c) reads the 8 bytes r (d
+      // 16r..16r+15, scale group r) of token rows 2c, 2c+1 (MMA k 2c, 2c+1) and
+      // 2c+8, 2c+9 (k 2c+8, 2c+9).  As at D = 256, the words of a token pair at
+      // the same d merge into bytes that each hold one d for both tokens, first
+      // token in the low nibble.  m-tile 4j+k takes d = 16r+8j+2k (row r) and d+1
+      // (row r+8); every m-tile of the lane is in group r.
+      uint2 vw[2][2];  // [token pair][first / second token]
+#pragma unroll
+      for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 8 * tb + 2 * c + e;
+          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                       : "=r"(vw[tb][e].x), "=r"(vw[tb][e].y)
+                       : "r"(swz_row<T::kRow>(vblk, t, r >> 1) + 8 * (r & 1)));
+        }
+      uint32_t svp[2];  // [token pair]: f16x2 of group r over the pair's tokens
+#pragma unroll
+      for (int tb = 0; tb < 2; ++tb) {
+        const int t = 8 * tb + 2 * c;
+        const uint32_t sw = (uint32_t)vsc[t * 8 + r] | ((uint32_t)vsc[(t + 1) * 8 + r] << 8);
+        const uint32_t vm = (t < nvalid ? 0x0000FFFFu : 0u) | (t + 1 < nvalid ? 0xFFFF0000u : 0u);
+        svp[tb] = e4m3x2_to_h2(sw) & vm;  // unwritten slots may hold NaN scales
+      }
+      const __half2 sa = u32_as_h2(svp[0]), sb = u32_as_h2(svp[1]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t f[2][2][4];  // [token pair][even / odd d][byte k]
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb) {
+          const uint32_t w0 = j == 0 ? vw[tb][0].x : vw[tb][0].y;
+          const uint32_t w1 = j == 0 ? vw[tb][1].x : vw[tb][1].y;
+          e2m1x8_to_h2x4(bitsel(w0, w1 << 4, 0x0F0F0F0Fu), f[tb][0]);
+          e2m1x8_to_h2x4(bitsel(w0 >> 4, w1, 0x0F0F0F0Fu), f[tb][1]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t a0 = h2_as_u32(__hmul2(u32_as_h2(f[0][0][k]), sa));
+          const uint32_t a1 = h2_as_u32(__hmul2(u32_as_h2(f[0][1][k]), sa));
+          const uint32_t a2 = h2_as_u32(__hmul2(u32_as_h2(f[1][0][k]), sb));
+          const uint32_t a3 = h2_as_u32(__hmul2(u32_as_h2(f[1][1][k]), sb));
+          mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, phi[0], phi[1]);
+          if constexpr (p_lo) mma16816<false>(oacc[4 * j + k], a0, a1, a2, a3, plo[0], plo[1]);
+        }
       }
     } else {
       // NVFP4: lane (r, c) reads 16-byte chunk r (d 32r..32r+31) of token rows
@@ -1037,8 +1110,8 @@ __global__ void __launch_bounds__(DecodeLayout<FMT, D>::kThreads, 1)
           } else if constexpr (FMT == KVQ_FMT_BF16) {
             put(hr, 16 * mt + r, oacc[mt][e], 0.f, false);
             put(hr, 16 * mt + 8 + r, oacc[mt][2 + e], 0.f, false);
-          } else {
-            put(hr, 32 * r + 8 * (mt >> 2) + 2 * (mt & 3), oacc[mt][e], oacc[mt][2 + e], true);
+          } else {  // NVFP4: m-tile 4j+k of lane row r holds d = (D/8) r + 8j + 2k and d+1
+            put(hr, (D / 8) * r + 8 * (mt >> 2) + 2 * (mt & 3), oacc[mt][e], oacc[mt][2 + e], true);
           }
         }
       }

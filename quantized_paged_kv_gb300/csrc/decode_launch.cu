@@ -14,7 +14,7 @@ DecodeInstance instance_of() {
                         Lo::kCW,
                         DecodeTraits<FMT, D>::kRow,
                         &decode_head_group<FMT, D>,
-                        Lo::kLaunchRegs};
+                        Lo::kRegSplit ? Lo::kLaunchRegs : 0};
 }
 
 template <int FMT, int D>
@@ -48,6 +48,7 @@ bool decode_instance(int format, int head_dim, DecodeInstance* out) {
   else if (format == KVQ_FMT_BF16 && head_dim == 256) *out = instance_of<KVQ_FMT_BF16, 256>();
   else if (format == KVQ_FMT_BF16 && head_dim == 128) *out = instance_of<KVQ_FMT_BF16, 128>();
   else if (format == KVQ_FMT_NVFP4 && head_dim == 256) *out = instance_of<KVQ_FMT_NVFP4, 256>();
+  else if (format == KVQ_FMT_NVFP4 && head_dim == 128) *out = instance_of<KVQ_FMT_NVFP4, 128>();
   else return false;
   return true;
 }
@@ -61,6 +62,7 @@ cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const
   if (format == KVQ_FMT_BF16 && head_dim == 256) return launch_t<KVQ_FMT_BF16, 256>(tk, tv, p, grid, stream);
   if (format == KVQ_FMT_BF16 && head_dim == 128) return launch_t<KVQ_FMT_BF16, 128>(tk, tv, p, grid, stream);
   if (format == KVQ_FMT_NVFP4 && head_dim == 256) return launch_t<KVQ_FMT_NVFP4, 256>(tk, tv, p, grid, stream);
+  if (format == KVQ_FMT_NVFP4 && head_dim == 128) return launch_t<KVQ_FMT_NVFP4, 128>(tk, tv, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -78,7 +78,7 @@ struct DecodeInstance {
   int consumer_warps;          // consumer warps per CTA
   int row_bytes;               // code bytes per token row
   int (*head_group)(int hkv);  // KV heads per work item for num_kv_heads = hkv (0: none fits)
-  int launch_regs;             // registers a thread the kernel's register split assumes at launch
+  int launch_regs;             // registers a thread the kernel's register split assumes at launch (0: no split)
 };
 
 bool decode_instance(int format, int head_dim, DecodeInstance* out);
@@ -103,6 +103,14 @@ cudaError_t launch_decode(int format, int head_dim, const CUtensorMap& tk, const
 cudaError_t launch_append(int format, int head_dim, const AppendParams& p, cudaStream_t stream);
 // Record a printf-style message as the calling thread's last error; returns code.
 int record_error(int code, const char* fmt, ...);
+// kvq_paged_decode_attention that, once every argument has passed its checks,
+// zeroes the workspace's 256-byte status block on the stream before launching
+// (the static-scratch entry point's region keeps the previous call's bits).
+int decode_clearing_status(const kvq_cache* cache, const void* q, int32_t batch, int32_t num_q_heads, float sm_scale,
+                           const int32_t* block_tables, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                           const int32_t* plan, int32_t total_splits, int32_t num_ctas, void* workspace,
+                           size_t workspace_bytes, void* out, int32_t out_dtype, float* lse_out, uint32_t flags,
+                           void* stream);
 // offsets: split offsets [batch + 1], or null when every sequence has
 // uniform_splits splits (rows b * uniform_splits ...).  offsets_ready: the
 // offsets are not written by the preceding kernel on the stream (read before

@@ -293,9 +293,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float ksv = 0.f, vsv = 0.f;
       uint2 kgs = make_uint2(0, 0), vgs = make_uint2(0, 0);  // NVFP4: this half row's group scale bytes
       if constexpr (FMT == KVQ_FMT_NVFP4) {
-        if (ro >= 0) {
-          kgs = __ldg(reinterpret_cast<const uint2*>(p.k_scales + ro * 16 + half * 8));
-          vgs = __ldg(reinterpret_cast<const uint2*>(p.v_scales + ro * 16 + half * 8));
+        if (ro >= 0) {  // D/32 scale bytes a half row: 8 at D = 256, 4 at D = 128
+          if constexpr (D == 256) {
+            kgs = __ldg(reinterpret_cast<const uint2*>(p.k_scales + ro * 16 + half * 8));
+            vgs = __ldg(reinterpret_cast<const uint2*>(p.v_scales + ro * 16 + half * 8));
+          } else {
+            kgs.x = __ldg(reinterpret_cast<const uint32_t*>(p.k_scales + ro * 8 + half * 4));
+            vgs.x = __ldg(reinterpret_cast<const uint32_t*>(p.v_scales + ro * 8 + half * 4));
+          }
         }
       }
       if constexpr (FMT == KVQ_FMT_INT8) {
@@ -590,6 +595,7 @@ PrefillInstance tc_instance_of() {
 
 bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out) {
   if (format == KVQ_FMT_NVFP4 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_NVFP4, 256>();
+  else if (format == KVQ_FMT_NVFP4 && head_dim == 128) *out = tc_instance_of<KVQ_FMT_NVFP4, 128>();
   else if (format == KVQ_FMT_INT8 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_INT8, 256>();
   else if (format == KVQ_FMT_INT8 && head_dim == 128) *out = tc_instance_of<KVQ_FMT_INT8, 128>();
   else if (format == KVQ_FMT_BF16 && head_dim == 256) *out = tc_instance_of<KVQ_FMT_BF16, 256>();
@@ -600,6 +606,7 @@ bool prefill_tc_instance(int format, int head_dim, PrefillInstance* out) {
 
 cudaError_t launch_prefill_tc(int format, int head_dim, const PrefillParams& p, int grid, cudaStream_t stream) {
   if (format == KVQ_FMT_NVFP4 && head_dim == 256) return launch_tc_t<KVQ_FMT_NVFP4, 256>(p, grid, stream);
+  if (format == KVQ_FMT_NVFP4 && head_dim == 128) return launch_tc_t<KVQ_FMT_NVFP4, 128>(p, grid, stream);
   if (format == KVQ_FMT_INT8 && head_dim == 256) return launch_tc_t<KVQ_FMT_INT8, 256>(p, grid, stream);
   if (format == KVQ_FMT_INT8 && head_dim == 128) return launch_tc_t<KVQ_FMT_INT8, 128>(p, grid, stream);
   if (format == KVQ_FMT_BF16 && head_dim == 256) return launch_tc_t<KVQ_FMT_BF16, 256>(p, grid, stream);

@@ -9,12 +9,18 @@
 // can still size a plan on the host; neither can find room for a workspace.
 //
 // The region is one file-scope __device__ array.  Its address on a device is
-// taken once, with that device current, by the first call made there
-// (cudaGetSymbolAddress); that first call should therefore come before any
-// stream capture.  Every call on a device shares the region and finds the last
-// call's contents in it: the call clears the status block (the only part that
+// taken with that device current, by the first call made there
+// (cudaGetSymbolAddress), and kept together with the ID of the CUDA context it
+// was taken in; a later call in another context (after cudaDeviceReset, or once
+// the primary context has been released and created again, which loads the
+// module anew) looks the address up again.  The first call on a device should
+// therefore come before any stream capture.  Every call on a device shares the
+// region and finds the last call's contents in it: once its arguments have
+// passed their checks, the call clears the status block (the only part that
 // must start at zero; every partial row the merge reads is written by the
 // decode first), and calls whose kernels overlap on the GPU race on it.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "kvq_internal.h"
@@ -25,9 +31,38 @@ static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_STATIC_SCRAT
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // CUDA context the address belongs to (0: none yet)
+  void* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Address of the region on the current device (set up on first use there).
+// ID of the calling thread's current CUDA context, 0 if there is none or the
+// driver does not say (the address is then looked up again).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Address of the region on the current device, in the current context.
 int scratch_on_current_device(void** ptr) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -35,15 +70,17 @@ int scratch_on_current_device(void** ptr) {
   if (dev < 0 || dev >= kMaxDevices)
     return kvq::record_error(KVQ_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long id = current_context_id();
+  if (id == 0 || g_scratch[dev].ctx_id != id || !g_scratch[dev].ptr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // makes the device's primary context current if needed
     if (e != cudaSuccess || !p)
       return kvq::record_error(KVQ_ERR_CUDA, "cudaGetSymbolAddress(static decode scratch): %s",
                                cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
+    g_scratch[dev].ptr = p;
+    g_scratch[dev].ctx_id = current_context_id();
   }
-  *ptr = g_scratch_ptr[dev];
+  *ptr = g_scratch[dev].ptr;
   return KVQ_OK;
 }
 
@@ -66,11 +103,11 @@ extern "C" int kvq_paged_decode_attention_static(const kvq_cache* cache, const v
                              "the static region holds %zu: use kvq_paged_decode_attention with a workspace",
                              need, total_splits, num_q_heads, cache->head_dim, (size_t)KVQ_STATIC_SCRATCH_BYTES);
   void* scratch = nullptr;
-  int rc = scratch_on_current_device(&scratch);
+  const int rc = scratch_on_current_device(&scratch);
   if (rc) return rc;
-  cudaError_t e = cudaMemsetAsync(scratch, 0, 256, reinterpret_cast<cudaStream_t>(stream));  // status block
-  if (e != cudaSuccess) return kvq::record_error(KVQ_ERR_CUDA, "clearing the status block: %s", cudaGetErrorString(e));
-  return kvq_paged_decode_attention(cache, q, batch, num_q_heads, sm_scale, block_tables, max_pages_per_seq, seq_lens,
-                                    plan, total_splits, num_ctas, scratch, (size_t)KVQ_STATIC_SCRATCH_BYTES, out,
-                                    out_dtype, lse_out, flags, stream);
+  // the status block is cleared on `stream` only once the arguments have passed
+  // the decode's checks, so a rejected call leaves an earlier call's bits in place
+  return kvq::decode_clearing_status(cache, q, batch, num_q_heads, sm_scale, block_tables, max_pages_per_seq,
+                                     seq_lens, plan, total_splits, num_ctas, scratch,
+                                     (size_t)KVQ_STATIC_SCRATCH_BYTES, out, out_dtype, lse_out, flags, stream);
 }

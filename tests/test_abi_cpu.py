@@ -182,6 +182,31 @@ def test_planner_override_and_auto(kvq):
     assert nctas == 152
 
 
+def test_verify_plan_computes_the_causal_lengths(kvq):
+    s = _struct(kvq)
+    # query token i of a sequence of L tokens (q_len T) sees L - T + 1 + i tokens,
+    # none when that is not positive; worked by hand:
+    cases = [([5, 40], 3, [3, 4, 5, 38, 39, 40]),
+             ([1], 3, [0, 0, 1]),
+             ([2, 0, 17], 2, [1, 2, 0, 0, 16, 17]),
+             ([33], 1, [33])]
+    for lens, T, virtual in cases:
+        for ov, tc in ((0, 152), (3, 152), (0, 7)):
+            got, total, nctas = kvq.kvq_plan_verify_splits(s, lens, T, ov, tc)
+            ref, rtotal, rctas = kvq.kvq_plan_splits(s, virtual, ov, tc)
+            assert (total, nctas) == (rtotal, rctas)
+            assert np.array_equal(got.numpy()[:ref.numel()], ref.numpy())
+            _check_plan(got.numpy(), virtual, total, nctas, 1, ov or None)
+    L = kvq.lib()
+    total, nctas = ctypes.c_int32(), ctypes.c_int32()
+    lens = (ctypes.c_int32 * 2)(5, 9)
+    assert L.kvq_plan_verify_splits(ctypes.byref(s), lens, 2, 0, 0, 152, None, 0, ctypes.byref(total),
+                                    ctypes.byref(nctas)) == 1 and "q_len" in kvq.kvq_last_error()
+    bad = (ctypes.c_int32 * 2)(5, -1)
+    assert L.kvq_plan_verify_splits(ctypes.byref(s), bad, 2, 2, 0, 152, None, 0, ctypes.byref(total),
+                                    ctypes.byref(nctas)) == 1 and "seq_lens" in kvq.kvq_last_error()
+
+
 def test_workspace_layout(kvq):
     n = kvq.kvq_decode_workspace_bytes(38, 24, 256)
     # status, lse partials (padded), o partials (padded), a bf16 copy of q
@@ -198,9 +223,12 @@ def test_host_validation_errors(kvq):
     assert rc == 2 and "page_size" in kvq.kvq_last_error()
     s.page_size = 16
     s.format = 2
-    s.head_dim = 128
+    s.head_dim = 64
     rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))
-    assert rc == 2
+    assert rc == 2 and "head_dim" in kvq.kvq_last_error()
+    s.head_dim = 128  # NVFP4 at head_dim 128 is planned like any other cache
+    rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 152, None, 0, ctypes.byref(total), ctypes.byref(mx))
+    assert rc == 3 and total.value == 1
     s.head_dim = 256
     s.k_global_scale = 0.0
     rc = L.kvq_plan_splits(ctypes.byref(s), lens, 1, 1, 0, None, 0, ctypes.byref(total), ctypes.byref(mx))

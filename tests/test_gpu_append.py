@@ -78,12 +78,13 @@ def test_int8_g32_append_bit_exact(D, kind):
 
 @pytest.mark.parametrize("kind", ["normal", "outliers", "spikes", "edge"])
 @pytest.mark.parametrize("gs", [(1.0, 1.0), "tensor", (0.37, 1234.5)])
-def test_nvfp4_append_bit_exact(kind, gs):
-    _append_and_compare("nvfp4", 2, 256, kind, gs=gs)
+@pytest.mark.parametrize("D", [128, 256])
+def test_nvfp4_append_bit_exact(kind, gs, D):
+    _append_and_compare("nvfp4", 2, D, kind, gs=gs)
 
 
-@pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("int8_g32", 128), ("int8_g32", 256), ("nvfp4", 256),
-                                   ("bf16", 256)])
+@pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("int8_g32", 128), ("int8_g32", 256), ("nvfp4", 128),
+                                   ("nvfp4", 256), ("bf16", 256)])
 @pytest.mark.parametrize("n", [1, 5, 33, 301])
 def test_append_ragged_token_counts(fmt, D, n):
     # a block carries several rows a thread group: token counts that leave the
@@ -197,7 +198,8 @@ def test_int8_g32_append_dense_quotients():
 
 
 @pytest.mark.parametrize("gs", [1.0, 0.37, 1234.5])
-def test_nvfp4_append_dense_quotients(gs):
+@pytest.mark.parametrize("D", [128, 256])
+def test_nvfp4_append_dense_quotients(gs, D):
     """Groups of 16 holding their maximum and 15 bf16 values up to it, so that
     every value up to each maximum meets the group's E4M3 scale."""
     rng = np.random.default_rng(12)
@@ -209,7 +211,7 @@ def test_nvfp4_append_dense_quotients(gs):
         groups.append(np.concatenate([np.full((len(g), 1), a, np.float32), g], axis=1))
     g = np.concatenate(groups)
     g = np.concatenate([g, np.zeros(((-len(g)) % 16, 16), np.float32)])
-    x = g.reshape(-1, 256)
+    x = g.reshape(-1, D)
     got_c, got_s = _append_rows("nvfp4", x, gs)
     c_exp, s_exp = oatt.quantize_rows("nvfp4", x, gs)
     assert np.array_equal(got_s, s_exp)

@@ -58,8 +58,6 @@ def test_tiny_int8(split):
 @pytest.mark.parametrize("D,Hq,Hkv", [(256, 24, 4), (128, 32, 8), (256, 8, 8), (128, 16, 2)])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 def test_ragged_batch(fmt, D, Hq, Hkv, out_dtype):
-    if fmt == "nvfp4" and D != 256:
-        pytest.skip("NVFP4 is implemented for D = 256")
     wl = W.make("serving_int8", lens=("list", [1, 17, 300, 0, 64, 1000]), seed=7)
     wl.Hq, wl.Hkv, wl.D = Hq, Hkv, D
     if out_dtype == "f32":  # large values; the bf16-output cases keep N(0, 0.5^2) as the bf16 workloads do
@@ -173,6 +171,52 @@ def test_checked_mode_reports_bad_metadata():
     decode(cache, good, q, bt, sl, out, wl.sm_scale, checked=True)
 
 
+@pytest.mark.parametrize("fmt", ["int8", "int8_g32", "nvfp4", "bf16"])
+def test_raw_mode_bad_page_ids_contribute_nothing(fmt):
+    """Raw mode: a block-table entry outside the pool is skipped and flagged, and
+    its page's tokens are left out of the softmax (whatever the stage held before:
+    the pool is sentinel-filled, so stale bytes would show as NaN or garbage).
+    The result equals the oracle's attention over the sequence without those
+    tokens; a sequence whose every page is bad gives 0 and -inf."""
+    from oracle import attention as oatt
+    from oracle import layout as olay
+    from quantized_paged_kv_gb300 import DecodePlan, decode, kvq_read_status
+
+    wl = W.make("tiny_int8", lens=("list", [700, 64, 20]), seed=14)
+    gs = H.global_scales(wl, fmt)
+    cache = H.gpu_cache(wl, fmt, gs)
+    q = wl.q()
+    bad = wl.block_tables.copy()
+    drop = {0: [0, 5, 43], 1: [0, 1, 2, 3], 2: []}  # pages made bad (sequence 1: all of them)
+    for b, js in drop.items():
+        for j in js:
+            bad[b, j] = wl.num_pages + 7 + j
+    for split in (1, 3):
+        plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=split)
+        out = torch.full((wl.B, wl.Hq, wl.D), float("nan"), device="cuda")
+        lse = torch.full((wl.B, wl.Hq), float("nan"), device="cuda")
+        decode(cache, plan, torch.from_numpy(q).to(torch.bfloat16).cuda(), torch.from_numpy(bad).cuda(),
+               torch.from_numpy(wl.seq_lens).cuda(), out, wl.sm_scale, lse_out=lse)
+        rc, bits = kvq_read_status(plan.workspace)
+        assert rc == 5 and bits == 1  # KVQ_DEV_BAD_PAGE only
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        pools = H.oracle_pools(wl, fmt, gs)
+        for b in range(wl.B):
+            L = int(wl.seq_lens[b])
+            keep = np.array([t for t in range(L) if t // 16 not in drop[b]], dtype=np.int64)
+            slots = olay.token_slots(wl.block_tables[b], L, 16)[keep]
+            for h in range(wl.Hkv):
+                k = oatt.cache_rows(fmt, pools["k_codes"], pools.get("k_scales"), slots, h, gs[0])
+                v = oatt.cache_rows(fmt, pools["v_codes"], pools.get("v_scales"), slots, h, gs[1])
+                ro, rl = oatt.attend(q[b, h * wl.G:(h + 1) * wl.G], k, v, wl.sm_scale)
+                rows = slice(h * wl.G, (h + 1) * wl.G)
+                assert np.all(np.abs(o[b, rows] - ro) <= H.bound("f32", ro)), (fmt, split, b, h)
+                if len(keep) == 0:
+                    assert np.all(o[b, rows] == 0) and np.all(np.isneginf(l[b, rows]))
+                else:
+                    assert np.abs(l[b, rows] - rl).max() < 1e-3
+
+
 def test_nan_sentinels_in_unwritten_tail_slots_do_not_leak():
     for fmt in ("int8", "int8_g32", "nvfp4", "bf16"):
         wl = W.make("tiny_int8", lens=("list", [33, 5, 47]), seed=6)
@@ -236,6 +280,30 @@ def test_long_nvfp4_full_size_sampled():
     order = np.argsort(wl.seq_lens)
     units = [(int(order[0]), 1), (int(order[-1]), 2)]
     _check(wl, "nvfp4", 0, units=units)
+
+
+def test_serving_nvfp4_full_size_sampled():
+    # the batch-64 serving mix (D = 128, G = 4) in NVFP4 with the tensor global
+    # scales 448 * 6 / amax, bf16 output, the bench's automatic plan
+    wl = W.make("serving_int8")
+    order = np.argsort(wl.seq_lens)
+    units = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 4)]
+    _check(wl, "nvfp4", 0, units=units)
+
+
+def test_long_context_nvfp4_full_size_sampled():
+    # the 32K batch-1 workload in NVFP4 (D = 256, G = 6) with tensor global scales, fp32 output
+    wl = W.make("long_int8")
+    _check(wl, "nvfp4", 0, units=[(0, 0), (0, 3)])
+
+
+def test_nvfp4_d128_gqa_shapes_and_splits():
+    # D = 128 with 1, 3, 5 and 8 query heads a KV head; page-crossing lengths
+    for G in (1, 3, 5, 8):
+        wl = W.make("serving_int8", lens=("list", [1, 15, 16, 17, 333, 2049]), seed=60 + G)
+        wl.Hkv, wl.Hq = 2, 2 * G
+        for split in (1, 4, 0):
+            _check(wl, "nvfp4", split, out_dtype="f32")
 
 
 def test_early_start_chain_in_a_graph_matches_plain_calls():

@@ -50,7 +50,7 @@ def test_prefill_d256_gqa6(fmt, T):
         _check(wl, fmt, T, splits)
 
 
-@pytest.mark.parametrize("fmt", ["int8", "bf16"])
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
 def test_prefill_d128_gqa4_bf16_out(fmt):
     wl = W.make("serving_int8", lens=("list", [1500]), seed=42)
     _check(wl, fmt, 200, 0, "bf16")

@@ -142,7 +142,7 @@ def _fused_rows(rng, n, Hkv, D):
 
 
 @pytest.mark.parametrize("fmt,D", [("int8", 128), ("int8", 256), ("int8_g32", 128), ("int8_g32", 256),
-                                   ("nvfp4", 256), ("bf16", 128), ("bf16", 256)])
+                                   ("nvfp4", 128), ("nvfp4", 256), ("bf16", 128), ("bf16", 256)])
 @pytest.mark.parametrize("n", [5, 301])
 def test_fused_rotated_append_bit_exact(fmt, D, n):
     # KVQ_ROTATE on the append: codes and scales equal the oracle's quantization of

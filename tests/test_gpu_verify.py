@@ -18,10 +18,10 @@ def _lib():
 
 
 def _run(wl, fmt, T, split=0, out_dtype="f32", gs=(1.0, 1.0), checked=True):
-    from quantized_paged_kv_gb300 import DecodePlan, verify, verify_lengths
+    from quantized_paged_kv_gb300 import DecodePlan, verify
 
     cache = H.gpu_cache(wl, fmt, gs)
-    plan = DecodePlan(cache, verify_lengths(wl.seq_lens, T), wl.Hq, split_override=split)
+    plan = DecodePlan(cache, wl.seq_lens, wl.Hq, split_override=split, q_len=T)
     q = wl.q_tokens(T)
     qt = torch.from_numpy(q).to(torch.bfloat16).cuda()
     od = {"f32": torch.float32, "bf16": torch.bfloat16}[out_dtype]
@@ -58,9 +58,11 @@ def test_verify_matches_the_oracle(fmt, T):
         _compare(wl, fmt, T, split, "f32", gs)
 
 
-def test_verify_bf16_output_and_gqa_4():
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_verify_bf16_output_and_gqa_4(fmt):
+    # D = 128, 4 query heads a KV head (the serving mix's shape)
     wl = W.make("serving_int8", lens=("list", [300, 1000, 2, 2500]), seed=32)
-    _compare(wl, "int8", 3, 0, "bf16")
+    _compare(wl, fmt, 3, 0, "bf16", H.global_scales(wl, fmt))
 
 
 def test_single_token_verify_is_the_decode():

@@ -1,5 +1,6 @@
 """kvq_paged_decode_attention_static (library-owned scratch, no allocation)
-against kvq_paged_decode_attention (caller's workspace), through the C ABI.
+against the CPU oracle and against kvq_paged_decode_attention (caller's
+workspace), through the C ABI.
 
 The file name makes pytest collect it last, so that it runs both after every
 other test in one process and, alone, in a fresh one.  Calls come in a row with
@@ -53,6 +54,13 @@ def _compare(wl, fmt, split, out_dtype):
     o_s, l_s, o_w, l_w, total = _both(wl, fmt, split, out_dtype)
     assert total > wl.B  # the merge reads partials out of the static region
     assert np.all(np.isfinite(o_s))
+    # against the oracle (float64 attention over the oracle's own pools)
+    ref, ref_lse = H.oracle_decode(wl, fmt, H.oracle_pools(wl, fmt, H.global_scales(wl, fmt)))
+    assert np.all(np.abs(o_s - ref) <= H.bound(out_dtype, ref))
+    fin_ref = np.isfinite(ref_lse)
+    assert np.array_equal(fin_ref, np.isfinite(l_s))
+    assert fin_ref.sum() == 0 or np.abs(l_s[fin_ref] - ref_lse[fin_ref]).max() < 1e-3
+    # and against the workspace entry point on the same inputs
     assert np.abs(o_s - o_w).max() <= H.tol(out_dtype)
     fin = np.isfinite(l_w)
     assert np.array_equal(fin, np.isfinite(l_s))
@@ -66,8 +74,8 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
     wl2 = W.make("tiny_int8", lens=("list", [700, 33, 4096]), seed=12)
     _compare(wl1, "int8", 3, "bf16")
     _compare(wl2, "int8", 5, "f32")
-    # and back, now over the larger call's leftovers
-    _compare(wl1, "int8", 3, "bf16")
+    # and back, now over the larger call's leftovers, in NVFP4 (tensor global scales)
+    _compare(wl1, "nvfp4", 3, "bf16")
 
 
 def test_status_block_is_cleared_between_calls():
