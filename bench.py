@@ -35,6 +35,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attention µs/step and KV GB/s read (fraction of GB300 HBM peak)"
 UNIT = "GB/s"
 WORKLOAD = "long_int8"
+HEADLINE_WORKLOAD = ("long-context batch-1 INT8 decode: B=1, Hq=24, Hkv=4, D=256, context 32768, page 16, "
+                     "permuted pages, fp32 out")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -190,9 +192,13 @@ class LayerSet:
         return int(self.wl.seq_lens.sum()) * kvq.kvq_bytes_per_token(self.fmt, self.wl.Hkv, self.wl.D)
 
 
-def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=None):
+MIN_TIMED_S = 1.0  # the headline's timed region lasts at least this long, whatever --steps says
+
+
+def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=None, min_seconds=0.0):
     """Capture R consecutive calls in a CUDA graph; replay to run `steps` calls
-    (rounded up to whole replays); returns (seconds per call, calls timed)."""
+    (rounded up to whole replays, and to at least `min_seconds` of replays);
+    returns (seconds per call, calls timed, clock record)."""
     import torch
 
     stream = torch.cuda.Stream()
@@ -207,10 +213,16 @@ def time_graph(ls, plan, steps, warmup, skip_merge=False, barrier=None, sampler=
             ls.call(r, plan, skip_merge)
     reps = max(1, math.ceil(steps / ls.R))
     wreps = max(1, math.ceil(warmup / ls.R))
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        w0.record(stream)
         for _ in range(wreps):
             g.replay()
+        w1.record(stream)
     stream.synchronize()
+    if min_seconds > 0:  # enough replays to fill the minimum timed region (estimated from the warm-up)
+        per_replay = max(w0.elapsed_time(w1) * 1e-3 / wreps, 1e-7)
+        reps = max(reps, math.ceil(min_seconds / per_replay))
     if barrier:
         barrier()
     torch.cuda.synchronize()
@@ -505,74 +517,193 @@ def time_e2e(ls, plan, steps, warmup=3):
     return t, h2d, d2h
 
 
+def time_e2e_eager(ls, plan, seconds=0.3):
+    """The e2e step without a graph: the public API called from the host for
+    every step (pinned host buffers as in time_e2e); seconds per step."""
+    import torch
+
+    import quantized_paged_kv_gb300 as kvq
+
+    q_h = ls.q.cpu().pin_memory()
+    bt_h = ls.bt.cpu().pin_memory()
+    sl_h = ls.sl.cpu().pin_memory()
+    out_h = torch.empty(ls.out.shape, dtype=ls.out.dtype).pin_memory()
+    stream = torch.cuda.Stream()
+
+    def run(n):
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                kvq.decode(ls.caches[i % ls.R], plan, q_h, bt_h, sl_h, out_h, ls.wl.sm_scale, early_start=True,
+                           stream=stream)
+
+    run(ls.R)  # warm-up
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(ls.R)
+    e1.record(stream)
+    stream.synchronize()
+    n = max(ls.R, int(seconds / max(e0.elapsed_time(e1) * 1e-3 / ls.R, 1e-7)))
+    e0.record(stream)
+    run(n)
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / n
+
+
 def layers_for(bytes_per_layer, l2_bytes, floor=8):
     return max(floor, math.ceil(4 * l2_bytes / max(bytes_per_layer, 1)))
 
 
-def cpu_baseline(seconds=12.0):
-    """Time the oracle on the host's cores (bounded sample): one single-threaded
-    worker process per core, all at once, each decoding one KV head of the
-    32,768-token sequence over and over for `seconds`; the throughput is the
-    workers' sum."""
-    code = f"""
-import json, os, sys, time
-sys.path.insert(0, {ROOT!r})
+# The oracle's timed sample: one (sequence, KV head) unit a worker process, its
+# context truncated to at most this many tokens (the oracle's work per token is
+# the same at any length), decoded over and over; for the append, the new
+# tokens of one KV head quantized over and over.
+ORACLE_CAP_TOKENS = 8192
+ORACLE_CONFIGS = (("tiny_int8", "int8", "decode"), ("long_int8", "int8", "decode"),
+                  ("serving_int8", "int8", "decode"), ("append_int8", "int8", "decode"),
+                  ("append_int8", "int8", "append"), ("long_nvfp4", "nvfp4", "decode"))
+
+_ORACLE_WORKER = """
+import json, sys, time
+sys.path.insert(0, ROOT)
 import numpy as np
 from oracle import attention as oatt, layout as olay
 from quantized_paged_kv_gb300 import workloads as W
-h = int(sys.argv[1])
-wl = W.make({WORKLOAD!r})
-h = h % wl.Hkv
-k, v = wl.kv(0)
-slots = wl.slots(0)
-pools = {{}}
-for name, x in (("k", k), ("v", v)):
-    c = np.zeros((wl.num_pages, wl.Hkv, 16, wl.D), np.uint8); s = np.zeros((wl.num_pages, wl.Hkv, 16), np.float32)
-    cc, ss = oatt.quantize_rows("int8", x[:, h, :])
-    olay.scatter_rows(c, slots, h, cc); olay.scatter_rows(s, slots, h, ss)
-    pools[name + "_codes"], pools[name + "_scales"] = c, s
-q = wl.q()
-sys.stdout.write("ready\\n"); sys.stdout.flush()
-sys.stdin.readline()
-t0 = time.perf_counter(); n = 0
-while time.perf_counter() - t0 < {seconds}:
-    oatt.paged_decode("int8", pools, q, wl.block_tables, wl.seq_lens, wl.sm_scale, heads=[(0, h)]); n += 1
-dt = (time.perf_counter() - t0) / n
-nbytes = int(wl.seq_lens.sum()) * 2 * (wl.D + 4)
-print(json.dumps({{"sec_per_unit": dt, "bytes_per_unit": nbytes, "units": n}}))
+idx, cap = int(sys.argv[1]), int(sys.argv[2])
+
+def sample(name, fmt, mode):
+    base = W.make(name)
+    b = idx % base.B
+    h = (idx // base.B) % base.Hkv
+    L = base.append_tail if mode == "append" else min(int(base.seq_lens[b]), cap)
+    wl = W.make(name, lens=("list", [L]), seed=base.seed + 1000 * b)
+    k, v = wl.kv(0)
+    k, v = k[:, h, :], v[:, h, :]
+    gs = 1.0
+    if fmt == "nvfp4":
+        gs = float(np.float32(2688.0) / np.float32(max(np.abs(k).max(), np.abs(v).max())))
+    if mode == "append":
+        def work():
+            oatt.quantize_rows(fmt, k, gs)
+            oatt.quantize_rows(fmt, v, gs)
+        return L, work
+    P = (L + 15) // 16
+    row = {"int8": wl.D, "nvfp4": wl.D // 2}[fmt]
+    sshape = (P, 1, 16) if fmt == "int8" else (P, 1, 16, wl.D // 16)
+    sdt = np.float32 if fmt == "int8" else np.uint8
+    pools = {"k_global_scale": gs, "v_global_scale": gs}
+    for nm, x in (("k", k), ("v", v)):
+        c = np.zeros((P, 1, 16, row), np.uint8)
+        sc = np.zeros(sshape, sdt)
+        cc, ss = oatt.quantize_rows(fmt, x, gs)
+        olay.scatter_rows(c, np.arange(L), 0, cc)
+        olay.scatter_rows(sc, np.arange(L), 0, ss)
+        pools[nm + "_codes"], pools[nm + "_scales"] = c, sc
+    q = wl.q()[:, h * wl.G:(h + 1) * wl.G]
+    bt = np.arange(P, dtype=np.int32)[None]
+    lens = np.array([L])
+    def work():
+        oatt.paged_decode(fmt, pools, q, bt, lens, wl.sm_scale)
+    return L, work
+
+for line in sys.stdin:  # commands: "<workload> <fmt> <mode> <seconds>", then "go"
+    name, fmt, mode, seconds = line.split()
+    L, work = sample(name, fmt, mode)
+    work()
+    sys.stdout.write("ready\\n"); sys.stdout.flush()
+    sys.stdin.readline()
+    t0 = time.perf_counter(); n = 0
+    while time.perf_counter() - t0 < float(seconds):
+        work(); n += 1
+    dt = time.perf_counter() - t0
+    sys.stdout.write(json.dumps({"token_heads_per_s": n * L / dt, "units": n, "tokens": L}) + "\\n")
+    sys.stdout.flush()
 """
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
-    procs = [subprocess.Popen([sys.executable, "-c", code, str(i)], stdin=subprocess.PIPE, stdout=subprocess.PIPE,
-                              stderr=subprocess.PIPE, text=True, env=env) for i in range(cores)]
-    try:
-        for pr in procs:  # every worker has built its pools: start them together
-            if pr.stdout.readline().strip() != "ready":
-                raise RuntimeError(pr.stderr.read()[-300:])
-        for pr in procs:
+
+
+class _OracleWorkers:
+    """Single-threaded oracle worker processes (one per core), reused for every
+    workload; rates(n, ...) times a sample on the first n of them at once."""
+
+    def __init__(self, count):
+        code = _ORACLE_WORKER.replace("sys.path.insert(0, ROOT)", f"sys.path.insert(0, {ROOT!r})")
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                   CUDA_VISIBLE_DEVICES="")
+        self.procs = [subprocess.Popen([sys.executable, "-c", code, str(i), str(ORACLE_CAP_TOKENS)],
+                                       stdin=subprocess.PIPE, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                       text=True, env=env) for i in range(count)]
+
+    def _line(self, pr):
+        ln = pr.stdout.readline()
+        if not ln:
+            pr.wait(timeout=60)
+            raise RuntimeError(pr.stderr.read()[-300:])
+        return ln.strip()
+
+    def rates(self, n, name, fmt, mode, seconds):
+        sel = self.procs[:n]
+        for pr in sel:
+            pr.stdin.write(f"{name} {fmt} {mode} {seconds}\n")
+            pr.stdin.flush()
+        for pr in sel:  # every worker has built its sample: start them together
+            if self._line(pr) != "ready":
+                raise RuntimeError("oracle worker out of step")
+        for pr in sel:
             pr.stdin.write("go\n")
             pr.stdin.flush()
-        results = []
-        for pr in procs:
-            out, err = pr.communicate(timeout=600)
-            if pr.returncode != 0:
-                raise RuntimeError(err[-300:])
-            results.append(json.loads(out.strip().splitlines()[-1]))
-    except Exception as e:  # noqa: BLE001
-        for pr in procs:
-            if pr.poll() is None:
+        return [json.loads(self._line(pr)) for pr in sel]
+
+    def close(self):
+        for pr in self.procs:
+            try:
+                pr.stdin.close()
+                pr.wait(timeout=30)
+            except Exception:  # noqa: BLE001
                 pr.kill()
-        return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle", "error": str(e)[-300:]}
-    gbps = sum(r["bytes_per_unit"] / r["sec_per_unit"] for r in results) / 1e9
-    units = sum(r["units"] for r in results)
-    one = results[0]["bytes_per_unit"] / results[0]["sec_per_unit"] / 1e9
-    return {"value": gbps, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"float64 numpy oracle, {cores} single-threaded worker processes at once, each decoding one "
-                      f"KV head of the 32,768-token sequence (1/4 of one step) for {seconds:.0f} s: "
-                      f"{units} head-decodes in all",
-            "per_core_value": round(one, 4),
-            "us_per_step_equiv": 68157440 / (gbps * 1e9) * 1e6}
+
+
+def cpu_baseline(seconds=2.0):
+    """The oracle timed on the host's cores, per workload: one single-threaded
+    worker process per core at once (all cores), then one worker alone (one
+    core).  Each worker times a bounded sample (ORACLE_CAP_TOKENS above) and
+    reports token-heads per second; the call time of a workload is its
+    token-heads over that rate (the sum of the workers' rates for all cores)."""
+    import quantized_paged_kv_gb300 as kvq
+    from quantized_paged_kv_gb300 import workloads as W
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    configs = {}
+    workers = _OracleWorkers(cores)
+    try:
+        for name, fmt, mode in ORACLE_CONFIGS:
+            wl = W.make(name)
+            if mode == "append":
+                token_heads = wl.append_tail * wl.B * wl.Hkv
+                nbytes = token_heads * 4 * wl.D + wl.append_tail * wl.B * kvq.kvq_bytes_per_token(fmt, wl.Hkv, wl.D)
+            else:
+                token_heads = int(wl.seq_lens.sum()) * wl.Hkv
+                nbytes = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token(fmt, wl.Hkv, wl.D)
+            r_all = sum(r["token_heads_per_s"] for r in workers.rates(cores, name, fmt, mode, seconds))
+            r_one = workers.rates(1, name, fmt, mode, seconds)[0]["token_heads_per_s"]
+            t_all, t_one = token_heads / r_all, token_heads / r_one
+            configs[f"{name}/{fmt}/{mode}"] = {
+                "us_per_call_all_cores": round(t_all * 1e6, 1), "us_per_call_1_core": round(t_one * 1e6, 1),
+                "GBps_all_cores": round(nbytes / t_all / 1e9, 4), "GBps_1_core": round(nbytes / t_one / 1e9, 4),
+                "token_heads_per_call": token_heads, "bytes_per_call": nbytes}
+    except Exception as e:  # noqa: BLE001
+        return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle", "error": str(e)[-300:],
+                "configs": configs}
+    finally:
+        workers.close()
+    head = configs[f"{WORKLOAD}/int8/decode"]
+    return {"value": head["GBps_all_cores"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"float64 numpy oracle, {cores} single-threaded worker processes at once (and one alone); "
+                      f"each times one (sequence, KV head) unit of the workload, its context cut to at most "
+                      f"{ORACLE_CAP_TOKENS} tokens, decoded over and over for {seconds:.0f} s (the append: that "
+                      f"head's new tokens quantized); call time = the workload's token-heads / the measured rate",
+            "per_core_value": head["GBps_1_core"], "us_per_step_equiv": head["us_per_call_all_cores"],
+            "configs": configs}
 
 
 def run_ours(args, rank, world, barrier, allmax):
@@ -601,16 +732,16 @@ def run_ours(args, rank, world, barrier, allmax):
     ls = LayerSet(wl, "int8", R, dev)
     plan = ls.plan(0)
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
-    t_call, calls, clocks = time_graph(ls, plan, args.steps, args.warmup, barrier=barrier, sampler=sampler)
+    t_call, calls, clocks = time_graph(ls, plan, args.steps, args.warmup, barrier=barrier, sampler=sampler,
+                                       min_seconds=MIN_TIMED_S)
     t_call = allmax(t_call)
-    if clocks is not None and clocks.get("samples", 0) < 3:  # timed region too short: extend by an untimed soak
-        _, _, c2 = time_graph(ls, plan, max(args.steps, int(1.5 / max(t_call, 1e-7))), 0,
-                              sampler=ClockSampler(local))
-        clocks = dict(c2 or clocks, window="timed region too short; sampled over a 1.5 s soak of the same step")
+    if clocks is not None:
+        clocks["window"] = f"sampled every 20 ms during the timed region ({calls * t_call:.2f} s)"
     t_dec, _, _ = time_graph(ls, plan, args.steps, args.warmup, skip_merge=True)
     t_dec = allmax(t_dec)
     e2e_t, h2d, d2h = time_e2e(ls, plan, args.steps, args.warmup)
     e2e_t = allmax(e2e_t)
+    e2e_eager_t = allmax(time_e2e_eager(ls, plan))
 
     bytes_step = ls.kv_bytes()
     value = world * bytes_step / t_call / 1e9
@@ -619,14 +750,14 @@ def run_ours(args, rank, world, barrier, allmax):
     tr = traffic_record(WORKLOAD)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": calls,
-        "warmup": args.warmup, "ms_per_step": t_call * 1e3, "us_per_step": round(t_call * 1e6, 3),
+        "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": t_call * 1e3, "us_per_step": round(t_call * 1e6, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded N(0,1) K/V with 4 outlier channels x8, quantized by kvq_quant_append)",
-        "config": {"workload": "long-context batch-1 INT8 decode: B=1, Hq=24, Hkv=4, D=256, context 32768, "
-                               "page 16, permuted pages, fp32 out",
+        "config": {"workload": HEADLINE_WORKLOAD,
                    "split_plan": f"auto: {plan.total_splits} splits", "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer pools x {per_layer / 1e6:.1f} MB visited round-robin",
-                   "timing": "CUDA graph of R consecutive calls (decode + merge), CUDA events",
+                   "timing": f"CUDA graph of R consecutive calls (decode + merge), replayed for at least "
+                             f"{MIN_TIMED_S:.1f} s (every call counted in steps), CUDA events",
                    "parallelism": f"dp{world}: one independent problem per rank, no data-path collective", "kv_bytes_per_step": bytes_step,
                    "us_per_16_layer_step": round(16 * t_call * 1e6, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -639,7 +770,11 @@ def run_ours(args, rank, world, barrier, allmax):
                 "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_t * 1e6, 3),
                 "how": "public API per step with pinned host buffers for q, block table, seq_lens and out, read and "
                        "written by the kernels over NVLink-C2C (no separate copy); R steps in one CUDA graph, "
-                       "CUDA events"},
+                       "CUDA events",
+                "eager": {"value": round(world * bytes_step / e2e_eager_t / 1e9, 1), "unit": UNIT,
+                          "us_per_step": round(e2e_eager_t * 1e6, 3),
+                          "how": "the same public call made from the host every step, no graph: argument checks, "
+                                 "two tensor-map encodes and the pointer queries run on the host each call"}},
         "gpu_launches": calls * (2 if plan.total_splits > wl.B else 1),
         "clocks": clocks,
     }
@@ -774,21 +909,27 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
         gc.collect()
         torch.cuda.empty_cache()
 
+    def tensor_gs(wl):  # the NVFP4 per-tensor global scales 448 * 6 / amax of K and of V
+        ka, va = wl.tensor_amax()
+        return (float(np.float32(2688.0) / np.float32(ka)), float(np.float32(2688.0) / np.float32(va)))
+
     wl = W.make("tiny_int8")
     measure(wl, "int8", (1, 4, 0))
     wl = W.make("long_int8")
     measure(wl, "int8", (1, 2, 4, 8, 16, 32, 38, 64, 0))
     measure(wl, "bf16", (16, 38, 64, 0))
     measure(wl, "int8_g32", (0,))  # INT8 with one scale per 32 values
+    measure(wl, "nvfp4", (0,), tensor_gs(wl))  # the same workload in NVFP4
     wl = W.make("serving_int8")
     measure(wl, "int8", (0, 1))
     measure(wl, "int8_g32", (0,))
+    measure(wl, "nvfp4", (0,), tensor_gs(wl))
     # the decode that follows the append workload's append: B = 8, contexts 4K..16K
     wl = W.make("append_int8")
     measure(wl, "int8", (0,))
     wl = W.make("long_nvfp4")
-    gs = (1.0, 1.0)
-    measure(wl, "nvfp4", (0,), gs, tag="long_nvfp4(gs=1)")
+    measure(wl, "nvfp4", (0,), tensor_gs(wl))
+    measure(wl, "nvfp4", (0,), (1.0, 1.0), tag="long_nvfp4(gs=1)")
     measure(wl, "int8", (0,))
     measure(wl, "bf16", (0,))
     # verify step: 6 query tokens a sequence over the 32K context (the pages' verify shape)
@@ -856,7 +997,7 @@ def run_reference(args):
         pools[name + "_codes"], pools[name + "_scales"] = c, s
     q = wl.q()
     steps = max(1, min(args.steps, 40))
-    warm = max(1, min(args.warmup, 3))
+    warm = max(1, min(args.warmup, 40))
     for i in range(warm):
         oatt.paged_decode("int8", pools, q, wl.block_tables, wl.seq_lens, wl.sm_scale, heads=[(0, i % 4)])
     t0 = _t.perf_counter()
@@ -870,11 +1011,11 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
         "steps": steps, "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload)",
-        "config": {"workload": "long-context batch-1 INT8 decode: B=1, Hq=24, Hkv=4, D=256, context 32768, "
-                               "page 16 (reference arm: one KV head per step)"},
+        "config": {"workload": HEADLINE_WORKLOAD},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"float64 numpy oracle; each step = decode of one KV head (6 query heads) over "
-                                   f"32,768 tokens; BLAS may use up to {cores} threads"},
+                         "sample": f"float64 numpy oracle; each step decodes one KV head (6 query heads) of the "
+                                   f"32,768-token sequence, a quarter of the workload's step, and GB/s counts that "
+                                   f"head's bytes; BLAS may use up to {cores} threads"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

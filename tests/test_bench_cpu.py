@@ -24,7 +24,7 @@ def test_reference_arm_prints_one_contract_line():
         assert k in d, k
     assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 1
     assert d["value"] > 0 and d["higher_is_better"] is True
-    assert "workload" in d["config"]
+    assert d["config"] == {"workload": bench.HEADLINE_WORKLOAD}  # the same config string as our arm's
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -58,3 +58,30 @@ def test_traffic_record_only_for_the_current_decode_source(tmp_path, monkeypatch
     assert bench.traffic_record("long_int8") is None
     (fake / "traffic.json").write_text(json.dumps({"long_int8": dict(committed, kernel_sha=bench.kernel_sha())}))
     assert bench.traffic_record("long_int8")["dram_bytes_per_launch"] == committed["dram_bytes_per_launch"]
+
+
+def test_reference_arm_honours_the_warmup_count():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "5"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["steps"] == 2 and d["warmup"] == 5
+
+
+def test_oracle_workers_time_every_kind_of_sample():
+    """The per-workload oracle timing: decode samples of both formats and the
+    append sample, on two workers at once and on one alone."""
+    w = bench._OracleWorkers(2)
+    try:
+        for name, fmt, mode in (("tiny_int8", "int8", "decode"), ("append_int8", "int8", "append"),
+                                ("serving_int8", "int8", "decode")):
+            two = w.rates(2, name, fmt, mode, 0.2)
+            one = w.rates(1, name, fmt, mode, 0.2)
+            assert len(two) == 2 and len(one) == 1
+            for r in two + one:
+                assert r["token_heads_per_s"] > 0 and r["units"] >= 1
+                assert r["tokens"] <= bench.ORACLE_CAP_TOKENS
+            if mode == "append":
+                assert one[0]["tokens"] == 1024
+    finally:
+        w.close()
