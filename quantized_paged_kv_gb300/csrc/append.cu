@@ -21,9 +21,9 @@
 // append, without the rotated rows' round trip through memory.
 //
 // A thread handles EPT consecutive elements of a row (one or two 16-byte loads):
-// 16 for NVFP4 (a thread holds one whole scale group), 8 for the other formats;
+// 16 for NVFP4 (a thread holds one whole scale group) and INT8, 8 for the others;
 // D/EPT threads share a row and reduce its maxima with shuffles, and each thread
-// carries kAppendRows rows whose loads go out together.  A row is one (token, KV
+// carries append_rows<FMT>() rows whose loads go out together.  A row is one (token, KV
 // head, K-or-V) triple; a block's rows share the KV head and K-or-V.  Coalesced
 // stores: codes EPT (INT8) / EPT/2 (NVFP4) / 2 EPT (BF16) bytes per thread,
 // contiguous across the row.
@@ -36,11 +36,13 @@ namespace {
 constexpr int kAppendThreads = 256;
 
 // Elements a thread, per format.  Measured on 8,192 tokens (D = 256), 8 against
-// 16: INT8 14.7 / 14.7 us, INT8 per 32 values 19.1 / 22.1, BF16 12.7 / 12.9,
-// NVFP4 20.9 / 19.7.
+// 16 (two rows a thread group): INT8 14.7 / 14.7 us, INT8 per 32 values 19.1 /
+// 22.1, BF16 12.7 / 12.9, NVFP4 20.9 / 19.7.  INT8 with 16 elements and one row a
+// thread group (two rows a warp share each warp instruction of the row-scale
+// arithmetic): 13.99 against 14.18 us for 8 elements and two rows (same run).
 template <int FMT>
 __host__ __device__ constexpr int append_ept() {
-  return FMT == KVQ_FMT_NVFP4 ? 16 : 8;
+  return FMT == KVQ_FMT_NVFP4 || FMT == KVQ_FMT_INT8 ? 16 : 8;
 }
 
 template <int EPT>
@@ -302,11 +304,14 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int h, int whi
 }
 
 // Rows a thread group carries: their loads (rows and slot ids) are all issued
-// before the first row is quantized, so each thread keeps EPT/8 kAppendRows
-// 16-byte loads in flight.  Measured on 8,192 tokens (D = 256,
-// 16 elements a thread): 2 rows 14.7 us (INT8), 3 rows 15.8, 4 rows 16.7 (fewer
-// resident blocks).
-constexpr int kAppendRows = 2;
+// before the first row is quantized, so each thread keeps EPT/8 x append_rows
+// 16-byte loads in flight (two for every format).  Measured on 8,192 tokens
+// (D = 256, 16 elements a thread, INT8): 2 rows 14.7 us, 3 rows 15.8, 4 rows 16.7
+// (fewer resident blocks), 1 row 14.0.
+template <int FMT>
+__host__ __device__ constexpr int append_rows() {
+  return FMT == KVQ_FMT_INT8 ? 1 : 2;
+}
 
 // Grid: x over token blocks, y over (KV head, K or V) = 2 h + which, so that no
 // index needs a division.
@@ -321,13 +326,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   const int t = threadIdx.x % TPR;
   const int which = blockIdx.y & 1;
   const int h = blockIdx.y >> 1;
-  const int64_t n0 = (int64_t)blockIdx.x * ROWS * kAppendRows + threadIdx.x / TPR;
+  const int64_t n0 = (int64_t)blockIdx.x * ROWS * append_rows<FMT>() + threadIdx.x / TPR;
   const uint16_t* src = (which ? p.v_new : p.k_new) + (int64_t)h * D + t * EPT;
   const int64_t stride = (int64_t)p.num_kv_heads * D;  // elements between tokens
-  Piece<EPT> raw[kAppendRows];
-  int64_t slot[kAppendRows];
+  Piece<EPT> raw[append_rows<FMT>()];
+  int64_t slot[append_rows<FMT>()];
 #pragma unroll
-  for (int u = 0; u < kAppendRows; ++u) {
+  for (int u = 0; u < append_rows<FMT>(); ++u) {
     const int64_t n = n0 + (int64_t)u * ROWS;
     const int64_t nn = n < p.n_tokens ? n : 0;
     const uint4* s4 = reinterpret_cast<const uint4*>(src + nn * stride);
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   Piece<EPT> sgn{};
   if constexpr (ROT) sgn = rot_sign_masks<EPT>(t);
 #pragma unroll
-  for (int u = 0; u < kAppendRows; ++u) {
+  for (int u = 0; u < append_rows<FMT>(); ++u) {
     const int64_t n = n0 + (int64_t)u * ROWS;
     append_row<FMT, D, ROT>(p, h, which, n < p.n_tokens, slot[u], raw[u], t, sgn);
   }
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 
 template <int FMT, int D>
 cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
-  constexpr int TOKENS = kAppendThreads / (D / append_ept<FMT>()) * kAppendRows;  // tokens a block covers
+  constexpr int TOKENS = kAppendThreads / (D / append_ept<FMT>()) * append_rows<FMT>();  // tokens a block covers
   const int64_t blocks = (p.n_tokens + TOKENS - 1) / TOKENS;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF || 2 * p.num_kv_heads > 65535) return cudaErrorInvalidValue;
