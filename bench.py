@@ -48,7 +48,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true", help="also measure the other workloads and the split sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler and its soak")
+    ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
+    ap.add_argument("--min-seconds", type=float, default=MIN_TIMED_S,
+                    help="shortest timed region of the headline (0: exactly the whole replays --steps asks for, "
+                         "e.g. for a profiler's launch list)")
     ap.add_argument("--ncu-case", default=None, metavar="WORKLOAD",
                     help="profiling case: build the workload's pools (just over L2 in total), run --calls eager "
                          "decode calls over them and exit (no timing); for append_int8, --calls appends")
@@ -733,7 +736,7 @@ def run_ours(args, rank, world, barrier, allmax):
     plan = ls.plan(0)
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     t_call, calls, clocks = time_graph(ls, plan, args.steps, args.warmup, barrier=barrier, sampler=sampler,
-                                       min_seconds=MIN_TIMED_S)
+                                       min_seconds=args.min_seconds)
     t_call = allmax(t_call)
     if clocks is not None:
         clocks["window"] = f"sampled every 20 ms during the timed region ({calls * t_call:.2f} s)"
@@ -741,7 +744,7 @@ def run_ours(args, rank, world, barrier, allmax):
     t_dec = allmax(t_dec)
     e2e_t, h2d, d2h = time_e2e(ls, plan, args.steps, args.warmup)
     e2e_t = allmax(e2e_t)
-    e2e_eager_t = allmax(time_e2e_eager(ls, plan))
+    e2e_eager_t = allmax(time_e2e_eager(ls, plan, seconds=0.3 if args.min_seconds > 0 else 0.0))
 
     bytes_step = ls.kv_bytes()
     value = world * bytes_step / t_call / 1e9
@@ -757,7 +760,7 @@ def run_ours(args, rank, world, barrier, allmax):
                    "split_plan": f"auto: {plan.total_splits} splits", "layers_rotated": R,
                    "l2": f"inputs larger than L2: {R} layer pools x {per_layer / 1e6:.1f} MB visited round-robin",
                    "timing": f"CUDA graph of R consecutive calls (decode + merge), replayed for at least "
-                             f"{MIN_TIMED_S:.1f} s (every call counted in steps), CUDA events",
+                             f"{args.min_seconds:.1f} s (every call counted in steps), CUDA events",
                    "parallelism": f"dp{world}: one independent problem per rank, no data-path collective", "kv_bytes_per_step": bytes_step,
                    "us_per_16_layer_step": round(16 * t_call * 1e6, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
