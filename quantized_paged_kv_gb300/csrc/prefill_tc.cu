@@ -46,22 +46,24 @@ struct TcLayout {
   static constexpr int kQBytes = kTcRows * D * 2;        // [atom][128 rows][128 B]
   static constexpr int kKBytes = kTcKeys * D * 2;        // [atom][64 keys][128 B]
   static constexpr int kVBytes = kTcKeys * D * 2;        // [8-key group][d atom][8 keys][128 B]
-  static constexpr int kPBytes = kTcRows * kTcKeys * 2;  // [128 rows][128 B]
   static constexpr int kQAt = 0;
   static constexpr int kKAt = kQAt + kQBytes;            // two K tiles
   static constexpr int kVAt = kKAt + 2 * kKBytes;        // two V tiles
-  static constexpr int kPAt = kVAt + 2 * kVBytes;        // P hi, then P lo
   static constexpr int kScRing = 3;                      // scale buffers (tiles in flight)
-  static constexpr int kScAt = kPAt + 2 * kPBytes;       // float k scales [3][64], v scales [3][64]
+  static constexpr int kScAt = kVAt + 2 * kVBytes;       // float k scales [3][64], v scales [3][64]
   static constexpr int kBarAt = kScAt + 2 * kScRing * kTcKeys * 4;
   static constexpr int kNumBars = 14;
   static constexpr int kSlotAt = kBarAt + kNumBars * 8;
   static constexpr int kSmemBytes = 1024 + kSlotAt + 16;
-  static_assert(kNumBars >= 13, "barriers");
+  static_assert(kNumBars >= 14, "barriers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t kTmemO = 0;          // O: D columns
   static constexpr uint32_t kTmemS = D;          // S: two buffers of 64 columns
-  static constexpr uint32_t kTmemCols = D + 2 * kTcKeys <= 256 ? 256 : 512;
+  // P: two buffers of 64 columns, each the hi terms (32 columns of f16 / bf16
+  // pairs) then the lo terms, the A operand of O += P V read from TMEM
+  static constexpr uint32_t kTmemP = D + 2 * kTcKeys;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kTmemP + 2 * kTcKeys <= kTmemCols, "TMEM columns");
   // MN-major V: byte offset between d atoms (leading) and between 8-key groups (strided)
   static constexpr uint32_t kVLbo = 1024, kVSbo = kAtoms * 1024;
 };
@@ -70,7 +72,8 @@ struct TcLayout {
 // so that no waiter can see a barrier two phases ahead of the one it waits for.
 enum : int {
   kBarQ = 0,
-  kBarP,       // P(i) written (softmax warps)
+  kBarP0,      // P(i) written into TMEM buffer 0 / 1 (softmax warps)
+  kBarP1,
   kBarK0,      // K(i) converted, buffers 0 / 1 (converter warps)
   kBarK1,
   kBarV0,      // V(i) converted
@@ -183,21 +186,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (i > 0) {
           const int j = i - 1;
-          if (!wait(kBarP, j & 1) || !wait(kBarV0 + (j & 1), (j >> 1) & 1)) break;
+          if (!wait(kBarP0 + (j & 1), (j >> 1) & 1) || !wait(kBarV0 + (j & 1), (j >> 1) & 1)) break;
           tc_fence_after();
           const uint32_t vb = sbase + Lo::kVAt + (uint32_t)(j & 1) * Lo::kVBytes;
+          const uint32_t pa = tmem + Lo::kTmemP + (uint32_t)(j & 1) * kTcKeys;  // P(j): hi, then lo 32 columns on
 #pragma unroll
           for (int k = 0; k < kTcKeys / 16; ++k) {
-            const uint64_t ad = umma_desc_sw128(sbase + Lo::kPAt + 32 * k, 16, 1024);
             const uint64_t bd = umma_desc_sw128(vb + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
-            umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+            umma_f16_ta(tmem + Lo::kTmemO, pa + 8 * k, bd, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
           }
           if constexpr (PLO) {
 #pragma unroll
             for (int k = 0; k < kTcKeys / 16; ++k) {
-              const uint64_t ad = umma_desc_sw128(sbase + Lo::kPAt + Lo::kPBytes + 32 * k, 16, 1024);
               const uint64_t bd = umma_desc_sw128(vb + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
-              umma_f16(tmem + Lo::kTmemO, ad, bd, kIdescPV, 1u);
+              umma_f16_ta(tmem + Lo::kTmemO, pa + kTcKeys / 2 + 8 * k, bd, kIdescPV, 1u);
             }
           }
           umma_commit(&bars[kBarO0 + (j & 1)]);
@@ -216,12 +218,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kChunks = kHalfBytes / 16;  // 16-byte source chunks of a half row
     uint8_t* ktiles = smem + Lo::kKAt;
     uint8_t* vtiles = smem + Lo::kVAt;
-    // pool row of key n of tile i (-1: a key past the range or the sequence, or a bad page id)
-    auto tile_row = [&](int i) -> int64_t {
+    // pool row of key n of tile i (-1: a key past the range or the sequence, or a
+    // bad page id), in two steps so that the block-table read can run ahead:
+    // page_of(i) reads the page id, row_from(i, id) validates it
+    auto page_of = [&](int i) -> int {
       const int jp = i * kTcPages + (n >> 4);  // page of the range
       const int tok = (pg0 + jp) * kPage + (n & 15);
       if (jp >= npg || tok >= key_end) return -1;
-      const int pg = p.block_table[pg0 + jp];
+      return p.block_table[pg0 + jp];
+    };
+    auto row_from = [&](int i, int pg) -> int64_t {
+      const int jp = i * kTcPages + (n >> 4);
+      const int tok = (pg0 + jp) * kPage + (n & 15);
+      if (jp >= npg || tok >= key_end) return -1;
       if (pg < 0 || pg >= p.num_pages) {
         if (half == 0 && (n & 15) == 0) atomicOr(p.status, KVQ_DEV_BAD_PAGE);
         return -1;
@@ -284,12 +293,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     };
-    // one tensor's loads are in flight while the other is written: K(i+1) while
-    // V(i) is written, V(i) while K(i) is written
-    uint4 rk[kChunks], rv[kChunks];
-    int64_t ro = nt > 0 ? tile_row(0) : -1;
-    if (nt > 0) load(p.k_codes, ro, rk);
-    for (int i = 0; i < nt; ++i) {
+    // Loads run a tile ahead of the conversions: at the start of tile i the
+    // converters issue K(i + 1) and V(i + 1) (two register sets a tensor, used in
+    // turn) and read the page ids of tile i + 2, so that no code load waits for
+    // its block-table read and every load has a whole tile to land.  Where two
+    // sets a tensor would not fit in the registers (8-bit rows of 256 values and
+    // wider), V(i) is issued at the start of tile i and K(i + 1) once K(i) is
+    // written.
+    constexpr bool kAhead = kChunks <= 4;
+    uint4 rk0[kChunks], rv0[kChunks], rk1[kAhead ? kChunks : 1], rv1[kAhead ? kChunks : 1];
+    int64_t ro = nt > 0 ? row_from(0, page_of(0)) : -1;
+    int pg_next = nt > 1 ? page_of(1) : -1;  // page id of tile i + 1
+    if (nt > 0) {
+      load(p.k_codes, ro, rk0);
+      if constexpr (kAhead) load(p.v_codes, ro, rv0);
+    }
+    auto step = [&](int i, uint4 (&rk)[kChunks], uint4 (&rv)[kChunks], uint4 (&rk_next)[kChunks],
+                    uint4 (&rv_next)[kChunks]) -> bool {
+      const int64_t ro_next = i + 1 < nt ? row_from(i + 1, pg_next) : -1;
+      pg_next = i + 2 < nt ? page_of(i + 2) : -1;
       float ksv = 0.f, vsv = 0.f;
       uint2 kgs = make_uint2(0, 0), vgs = make_uint2(0, 0);  // NVFP4: this half row's group scale bytes
       if constexpr (FMT == KVQ_FMT_NVFP4) {
@@ -309,9 +331,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           vsv = __ldg(reinterpret_cast<const float*>(p.v_scales) + ro);
         }
       }
-      load(p.v_codes, ro, rv);
+      if constexpr (kAhead) {
+        if (i + 1 < nt) {
+          load(p.k_codes, ro_next, rk_next);
+          load(p.v_codes, ro_next, rv_next);
+        }
+      } else {
+        load(p.v_codes, ro, rv);
+      }
       // K buffer i & 1 is free once S(i-2) is done
-      if (i > 1 && !wait_warp(kBarKF0 + (i & 1), ((i - 2) >> 1) & 1)) break;
+      if (i > 1 && !wait_warp(kBarKF0 + (i & 1), ((i - 2) >> 1) & 1)) return false;
       if constexpr (FMT == KVQ_FMT_INT8) {
         // both scales of the tile go out with K: the softmax reads them once S is
         // done.  Ring of three: the last reader of this slot, the softmax of tile
@@ -325,15 +354,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       fence_proxy_async_smem();  // the tile's bytes become visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarK0 + (i & 1)]);
-      const int64_t ro_next = i + 1 < nt ? tile_row(i + 1) : -1;
-      if (i + 1 < nt) load(p.k_codes, ro_next, rk);
+      if (!kAhead && i + 1 < nt) load(p.k_codes, ro_next, rk_next);  // rk_next is rk: after it is written
       // V buffer i & 1 is free once P(i-2) V(i-2) is done
-      if (i > 1 && !wait_warp(kBarO0 + (i & 1), ((i - 2) >> 1) & 1)) break;
+      if (i > 1 && !wait_warp(kBarO0 + (i & 1), ((i - 2) >> 1) & 1)) return false;
       put(1, i & 1, rv, vgs);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarV0 + (i & 1)]);
       ro = ro_next;
+      return true;
+    };
+    if constexpr (kAhead) {
+      for (int i = 0; i < nt; i += 2) {  // the two register sets take turns
+        if (!step(i, rk0, rv0, rk1, rv1)) break;
+        if (i + 1 < nt && !step(i + 1, rk1, rv1, rk0, rv0)) break;
+      }
+    } else {
+      for (int i = 0; i < nt; ++i)
+        if (!step(i, rk0, rv0, rk0, rv0)) break;
     }
   } else {
     // ================================================================== softmax
@@ -432,13 +470,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * rs;  // log2 units
-      // the P tile and O may be touched once P(i-1) V(i-1) has completed
-      if (i > 0) {
-        if (!wait_warp(kBarO0 + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
-        tc_fence_after();
-      }
       const bool resc = m_run != -INFINITY && mx > m_run + kTcRescale;
       if (__any_sync(0xffffffffu, resc)) {
+        // O is rescaled once it holds P(i-1) V(i-1), before P(i) V(i) adds to it
+        if (i > 0) {
+          if (!wait_warp(kBarO0 + ((i - 1) & 1), ((i - 1) >> 1) & 1)) break;
+          tc_fence_after();
+        }
         const float alpha = resc ? exp2f(m_run - mx) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -456,15 +494,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (m_run == -INFINITY) m_run = mx;  // first visible keys (still -inf if none)
-      uint8_t* prow = smem + Lo::kPAt + rl * 128;
-      uint8_t* plrow = prow + Lo::kPBytes;
+      // P buffer i & 1 (TMEM) is free once P(i-2) V(i-2) has completed: the
+      // softmax of tile i no longer waits for the product of tile i-1
+      if (i > 1) {
+        if (!wait_warp(kBarO0 + (i & 1), ((i - 2) >> 1) & 1)) break;
+        tc_fence_after();
+      }
+      const uint32_t tp = tq + Lo::kTmemP + (uint32_t)(i & 1) * kTcKeys;  // this row's P(i): hi, lo 32 columns on
       // pass 2: p = 2^(z - m) <= 2^8 (ex2.approx.ftz: results below 2^-126 are 0,
       // a masked key's z = -inf gives exactly 0), P' = p v_scale, packed hi (+ lo)
       float psums[4] = {0.f, 0.f, 0.f, 0.f};
       const float msub = m_run == -INFINITY ? 0.f : m_run;  // a row with no visible key: every z is -inf
+      uint32_t ph[8], pl[8];  // two groups of 8 keys: 8 words of key pairs, hi and lo
 #pragma unroll
       for (int c8 = 0; c8 < kTcKeys / 8; ++c8) {
-        uint32_t hw[4], lw[4];
+        uint32_t* hw = ph + 4 * (c8 & 1);
+        [[maybe_unused]] uint32_t* lw = pl + 4 * (c8 & 1);
         float v8[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
         if constexpr (FMT == KVQ_FMT_INT8) {
           const float4 va = *reinterpret_cast<const float4*>(vs + 8 * c8);
@@ -498,15 +543,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if constexpr (PLO) lw[e] = h2_as_u32(__floats2half2_rn(pv[0] - __low2float(hv), pv[1] - __high2float(hv)));
           }
         }
-        const int off = (c8 ^ (rl & 7)) << 4;
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        if constexpr (PLO) *reinterpret_cast<uint4*>(plrow + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        if (c8 & 1) {  // keys 16 (c8 / 2) .. +15: columns 8 (c8 / 2) .. +7
+          tmem_st8(tp + 8 * (c8 >> 1), ph);
+          if constexpr (PLO) tmem_st8(tp + kTcKeys / 2 + 8 * (c8 >> 1), pl);
+        }
       }
       l_run += (psums[0] + psums[1]) + (psums[2] + psums[3]);
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarP]);
+      if (lane == 0) mbar_arrive(&bars[kBarP0 + (i & 1)]);
       done = i + 1;
     }
     // ================================================================ epilogue
