@@ -301,12 +301,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // wider), V(i) is issued at the start of tile i and K(i + 1) once K(i) is
     // written.
     constexpr bool kAhead = kChunks <= 4;
-    uint4 rk0[kChunks], rv0[kChunks], rk1[kAhead ? kChunks : 1], rv1[kAhead ? kChunks : 1];
+    constexpr bool kVAhead = !kAhead && kChunks <= 8;  // V alone a tile ahead
+    uint4 rk0[kChunks], rv0[kChunks], rk1[kAhead ? kChunks : 1], rv1[(kAhead || kVAhead) ? kChunks : 1];
     int64_t ro = nt > 0 ? row_from(0, page_of(0)) : -1;
     int pg_next = nt > 1 ? page_of(1) : -1;  // page id of tile i + 1
     if (nt > 0) {
       load(p.k_codes, ro, rk0);
-      if constexpr (kAhead) load(p.v_codes, ro, rv0);
+      if constexpr (kAhead || kVAhead) load(p.v_codes, ro, rv0);
     }
     auto step = [&](int i, uint4 (&rk)[kChunks], uint4 (&rv)[kChunks], uint4 (&rk_next)[kChunks],
                     uint4 (&rv_next)[kChunks]) -> bool {
@@ -336,6 +337,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           load(p.k_codes, ro_next, rk_next);
           load(p.v_codes, ro_next, rv_next);
         }
+      } else if constexpr (kVAhead) {
+        if (i + 1 < nt) load(p.v_codes, ro_next, rv_next);
       } else {
         load(p.v_codes, ro, rv);
       }
@@ -368,6 +371,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int i = 0; i < nt; i += 2) {  // the two register sets take turns
         if (!step(i, rk0, rv0, rk1, rv1)) break;
         if (i + 1 < nt && !step(i + 1, rk1, rv1, rk0, rv0)) break;
+      }
+    } else if constexpr (kVAhead) {
+      for (int i = 0; i < nt; i += 2) {  // the two V register sets take turns; K has one
+        if (!step(i, rk0, rv0, rk0, rv1)) break;
+        if (i + 1 < nt && !step(i + 1, rk0, rv1, rk0, rv0)) break;
       }
     } else {
       for (int i = 0; i < nt; ++i)
