@@ -269,6 +269,17 @@ int kvq_plan_verify_splits(const kvq_cache* cache, const int32_t* seq_lens, int3
  * into it and kvq_read_status clears it. */
 size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int32_t head_dim);
 
+/* Workspace bytes for kvq_paged_verify_attention: the larger of
+ * kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim) and, for a
+ * call the prefill kernel takes (batch = 1, q_len x query heads a KV head >= 32),
+ * kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, S) for the largest
+ * key split count S it may use: about one CTA per SM, at most 64.
+ * target_ctas: the SM count of the device the calls run on (0: the current
+ * device's).  A smaller workspace keeps such a call on the decode kernel.
+ * 0 for bad arguments (the reason in kvq_last_error). */
+size_t kvq_verify_workspace_bytes(const kvq_cache* cache, int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                  int32_t total_splits, int32_t target_ctas);
+
 /* Device pointers to the partials inside a workspace (host pointer arithmetic). */
 int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_heads,
                            int32_t head_dim, float** o_part, float** lse_part);
@@ -323,12 +334,21 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
  * MMA tile holds the G query heads of one token (8-row granularity), and the
  * q_len tokens' items cover the same pages at about the same time, so a page
  * read for one token is mostly still in L2 for the others.
+ * One sequence (batch = 1) whose q_len x (num_q_heads / num_kv_heads) query rows
+ * number 32 or more goes instead to the tensor-core kernel of
+ * kvq_paged_prefill_attention ([int8-kv] "Read the prompt using a small temporary
+ * buffer": a block of query rows reads each key once), with the sequence length
+ * read on the device and about one CTA per SM in key splits, when q and out are
+ * device memory, neither KVQ_SKIP_MERGE nor KVQ_TEST_STALL is set and the
+ * workspace holds kvq_verify_workspace_bytes; the plan is still required (and
+ * checked under KVQ_CHECKED), the result is the same up to rounding order.
  *   q              device bf16 [batch][q_len][num_q_heads][head_dim]
  *   seq_lens       device int32 [batch]: tokens in the cache, the q_len new ones included
  *   plan           kvq_plan_verify_splits(seq_lens, batch, q_len, ...): the plan
  *                  over the batch * q_len virtual lengths max(0, seq_lens[b] -
  *                  q_len + 1 + i), in order b * q_len + i
- *   workspace      >= kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim)
+ *   workspace      >= kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim);
+ *                  kvq_verify_workspace_bytes(...) also covers the routed call
  *   out            device [batch][q_len][num_q_heads][head_dim] float or bf16
  *   lse_out        device float [batch][q_len][num_q_heads] (nullable)
  * Everything else (flags included) as for kvq_paged_decode_attention; q_len = 1

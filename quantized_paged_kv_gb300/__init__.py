@@ -16,6 +16,6 @@ from ._binding import (  # noqa: F401
     kvq_quant_append,
     kvq_paged_decode_attention_static, kvq_paged_prefill_attention, kvq_paged_verify_attention,
     kvq_prefill_splits, kvq_prefill_workspace_bytes, kvq_read_status, kvq_rotate_rows, kvq_split_merge,
-    kvq_workspace_partials, lib,
+    kvq_verify_workspace_bytes, kvq_workspace_partials, lib,
 )
 from .cache import DecodePlan, KVCache, decode, prefill, verify  # noqa: F401

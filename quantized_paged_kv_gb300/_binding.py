@@ -29,7 +29,7 @@ FORMATS = {"bf16": KVQ_FMT_BF16, "int8": KVQ_FMT_INT8, "nvfp4": KVQ_FMT_NVFP4, "
 # every symbol include/kvq.h declares
 EXPORTS = (
     "kvq_bytes_per_token", "kvq_cache_array_bytes", "kvq_quant_append", "kvq_plan_splits", "kvq_plan_verify_splits",
-    "kvq_decode_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
+    "kvq_decode_workspace_bytes", "kvq_verify_workspace_bytes", "kvq_workspace_partials", "kvq_paged_decode_attention",
     "kvq_paged_decode_attention_static", "kvq_paged_verify_attention", "kvq_prefill_splits",
     "kvq_prefill_workspace_bytes", "kvq_paged_prefill_attention", "kvq_split_merge", "kvq_read_status",
     "kvq_last_error", "kvq_rotate_rows",
@@ -72,6 +72,8 @@ def lib():
         "kvq_plan_verify_splits": (c_int32, [POINTER(KvqCacheStruct), POINTER(c_int32), c_int32, c_int32, c_int32,
                                              c_int32, POINTER(c_int32), c_int64, POINTER(c_int32), POINTER(c_int32)]),
         "kvq_decode_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
+        "kvq_verify_workspace_bytes": (c_size_t, [POINTER(KvqCacheStruct), c_int32, c_int32, c_int32, c_int32,
+                                                  c_int32]),
         "kvq_workspace_partials": (c_int32, [P, c_int32, c_int32, c_int32, POINTER(c_void_p), POINTER(c_void_p)]),
         "kvq_paged_decode_attention": (c_int32, [POINTER(KvqCacheStruct), P, c_int32, c_int32, c_float, P, c_int32,
                                                  P, P, c_int32, c_int32, P, c_size_t, P, c_int32, P, c_uint32, P]),
@@ -110,6 +112,22 @@ def _check(rc, name):
         raise KvqError(rc, f"{name}: {lib().kvq_last_error().decode()}")
 
 
+def _shapes(q, out, lse_out, block_tables, seq_lens, cache_struct):
+    """The buffers a device call writes or indexes, against q's shape (q is [B, ..., Hq, D]):
+    out holds q's element count, lse_out one value a query row, block_tables and
+    seq_lens a row per sequence."""
+    if out.numel() != q.numel():
+        raise ValueError(f"out must hold {q.numel()} values (q's shape {tuple(q.shape)}), got {tuple(out.shape)}")
+    if lse_out is not None and lse_out.numel() != q.numel() // q.shape[-1]:
+        raise ValueError(f"lse_out must hold {q.numel() // q.shape[-1]} values, got {tuple(lse_out.shape)}")
+    if q.shape[-1] != cache_struct.head_dim:
+        raise ValueError(f"q's head_dim {q.shape[-1]} != the cache's {cache_struct.head_dim}")
+    if block_tables is not None and (block_tables.dim() != 2 or block_tables.shape[0] < q.shape[0]):
+        raise ValueError(f"block_tables must be [>= {q.shape[0]}, max_pages]")
+    if seq_lens is not None and seq_lens.numel() < q.shape[0]:
+        raise ValueError(f"seq_lens must hold {q.shape[0]} lengths")
+
+
 def _need(t, dtype, name, device=True):
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -133,6 +151,15 @@ def kvq_cache_array_bytes(fmt, num_pages, page_size, num_kv_heads, head_dim):
 
 def kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim):
     return int(lib().kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim))
+
+
+def kvq_verify_workspace_bytes(cache_struct, batch, q_len, num_q_heads, total_splits, target_ctas=0):
+    """Workspace bytes of a verify call, the tensor-core route of a one-sequence call included."""
+    n = int(lib().kvq_verify_workspace_bytes(ctypes.byref(cache_struct), batch, q_len, num_q_heads, total_splits,
+                                             target_ctas))
+    if n == 0:
+        raise KvqError(1, f"kvq_verify_workspace_bytes: {lib().kvq_last_error().decode()}")
+    return n
 
 
 def _plan(call, name, cache_struct, seq_lens, lead, split_override, target_ctas, virtual_batch):
@@ -211,6 +238,7 @@ def kvq_paged_decode_attention(cache_struct, q, sm_scale, block_tables, seq_lens
     _need(out, out.dtype, "out")
     if lse_out is not None:
         _need(lse_out, torch.float32, "lse_out")
+    _shapes(q, out, lse_out, block_tables, seq_lens, cache_struct)
     B, Hq, _ = q.shape
     od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
     _check(lib().kvq_paged_decode_attention(
@@ -232,6 +260,7 @@ def kvq_paged_decode_attention_static(cache_struct, q, sm_scale, block_tables, s
     _need(out, out.dtype, "out")
     if lse_out is not None:
         _need(lse_out, torch.float32, "lse_out")
+    _shapes(q, out, lse_out, block_tables, seq_lens, cache_struct)
     B, Hq, _ = q.shape
     od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
     _check(lib().kvq_paged_decode_attention_static(
@@ -253,6 +282,7 @@ def kvq_paged_verify_attention(cache_struct, q, sm_scale, block_tables, seq_lens
     _need(out, out.dtype, "out")
     if lse_out is not None:
         _need(lse_out, torch.float32, "lse_out")
+    _shapes(q, out, lse_out, block_tables, seq_lens, cache_struct)
     B, T, Hq, _ = q.shape
     od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
     _check(lib().kvq_paged_verify_attention(
@@ -283,6 +313,7 @@ def kvq_paged_prefill_attention(cache_struct, q, sm_scale, block_table, seq_len,
     _need(out, out.dtype, "out")
     if lse_out is not None:
         _need(lse_out, torch.float32, "lse_out")
+    _shapes(q, out, lse_out, None, None, cache_struct)
     T, Hq, _ = q.shape
     od = KVQ_OUT_BF16 if out.dtype == torch.bfloat16 else KVQ_OUT_F32
     _check(lib().kvq_paged_prefill_attention(

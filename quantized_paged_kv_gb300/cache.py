@@ -71,8 +71,11 @@ class DecodePlan:
         self.batch = len(seq_lens) * q_len
         self.num_q_heads = num_q_heads
         self.head_dim = cache.head_dim
-        self.workspace = torch.zeros(B.kvq_decode_workspace_bytes(self.total_splits, num_q_heads, cache.head_dim),
-                                     dtype=torch.uint8, device=device)
+        if q_len == 1:
+            ws = B.kvq_decode_workspace_bytes(self.total_splits, num_q_heads, cache.head_dim)
+        else:  # room for the tensor-core route of a one-sequence verify call as well
+            ws = B.kvq_verify_workspace_bytes(cache.struct, len(seq_lens), q_len, num_q_heads, self.total_splits)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
 
     def partials(self):
         """(o_part pointer, lse_part pointer) inside the workspace."""

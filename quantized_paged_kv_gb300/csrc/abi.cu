@@ -193,6 +193,32 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// A verify call of one sequence whose query rows (q_len x query heads a KV head)
+// fill at least a quarter of the tensor-core tile's 128 rows goes to the prefill
+// kernel: it reads every key once for all q_len query tokens, where the decode
+// kernel reads the keys once a query token.  The key splits of that launch: about
+// one CTA per SM, capped by the block table's width (at least 4 pages a split)
+// and by 64.  0: the call stays on the decode kernel.
+constexpr int kVerifyRouteRows = 32;
+
+// sms <= 0: the current device's SM count.
+int verify_route_splits(const kvq_cache* cache, int32_t nseq, int32_t q_len, int32_t num_q_heads, int32_t max_pages,
+                        int32_t sms) {
+  if (nseq != 1 || q_len < 2 || num_q_heads % cache->num_kv_heads) return 0;
+  const int64_t G = num_q_heads / cache->num_kv_heads;
+  if ((int64_t)q_len * G < kVerifyRouteRows) return 0;
+  kvq::PrefillInstance inst;
+  if (!kvq::prefill_tc_instance(cache->format, cache->head_dim, &inst)) return 0;
+  int dev = 0;
+  if (sms <= 0 && (cudaGetDevice(&dev) != cudaSuccess ||
+                   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess))
+    return 0;
+  const int64_t items = ((int64_t)q_len * G + inst.rows - 1) / inst.rows * cache->num_kv_heads;
+  int64_t S = std::max<int64_t>(1, sms / items);
+  S = std::min<int64_t>({S, 64, std::max<int64_t>(1, max_pages / 4)});
+  return static_cast<int>(S);
+}
+
 }  // namespace
 
 int kvq::record_error(int code, const char* fmt, ...) {
@@ -489,6 +515,31 @@ size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int
   return 256 + align256(rows * sizeof(float)) + align256(rows * head_dim * sizeof(float)) + rows * head_dim * 2;
 }
 
+size_t kvq_verify_workspace_bytes(const kvq_cache* cache, int32_t batch, int32_t q_len, int32_t num_q_heads,
+                                  int32_t total_splits, int32_t target_ctas) {
+  if (batch < 1 || q_len < 1 || num_q_heads < 1 || total_splits < 0) {
+    fail(KVQ_ERR_INVALID_ARG, "bad batch %d / q_len %d / num_q_heads %d / total_splits %d", batch, q_len, num_q_heads,
+         total_splits);
+    return 0;
+  }
+  if (check_cache(cache, false)) return 0;  // the reason is recorded
+  if (target_ctas <= 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&target_ctas, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "querying the SM count");
+      return 0;
+    }
+  }
+  const size_t decode_need = kvq_decode_workspace_bytes(total_splits, num_q_heads, cache->head_dim);
+  // the routed call's splits never exceed those of the widest block table
+  const int S = verify_route_splits(cache, batch, q_len, num_q_heads, 0x7FFFFFFF, target_ctas);
+  succeed();
+  if (S <= 0) return decode_need;
+  return std::max(decode_need, kvq_prefill_workspace_bytes(q_len, num_q_heads, cache->head_dim, S));
+}
+
 int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_heads, int32_t head_dim,
                            float** o_part, float** lse_part) {
   if (!workspace || !o_part || !lse_part || total_splits < 0 || num_q_heads < 0 || head_dim < 0)
@@ -503,6 +554,88 @@ int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_
 }  // extern "C"
 
 namespace {
+
+// The tensor-core prefill launch (and its merge) once every argument has been
+// checked: q_len query tokens of one sequence, the sequence length from the host
+// (seq_len) or, when seq_len_dev is not null, read by the kernel from device
+// memory (a verify call).
+int prefill_launch(const kvq_cache* cache, const void* q, int32_t q_len, int32_t num_q_heads, float sm_scale,
+                   const int32_t* block_table, int32_t max_pages, int32_t seq_len, const int32_t* seq_len_dev,
+                   int32_t splits, void* workspace, void* out, int32_t out_dtype, float* lse_out, uint32_t flags,
+                   void* stream) {
+  const int D = cache->head_dim;
+  const int G = num_q_heads / cache->num_kv_heads;
+  kvq::PrefillInstance inst;
+  if (!kvq::prefill_tc_instance(cache->format, D, &inst))
+    return fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, D);
+  {
+    static std::mutex mu;
+    static bool done[64][4][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    bool& d = done[dev][cache->format][D == 256 ? 1 : 0];
+    if (!d) {
+      for (const void* kern : inst.kernels) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(prefill kernel)");
+        if (inst.launch_regs > 0 && fa.numRegs != inst.launch_regs)
+          return fail(KVQ_ERR_UNSUPPORTED,
+                      "prefill kernel built with %d registers a thread, its register split assumes %d", fa.numRegs,
+                      inst.launch_regs);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, inst.smem_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+      }
+      d = true;
+    }
+  }
+  kvq::PrefillParams p{};
+  p.q = q;
+  p.block_table = block_table;
+  p.k_codes = static_cast<const uint8_t*>(cache->k_codes);
+  p.v_codes = static_cast<const uint8_t*>(cache->v_codes);
+  p.k_scales = static_cast<const uint8_t*>(cache->k_scales);
+  p.v_scales = static_cast<const uint8_t*>(cache->v_scales);
+  const size_t rows = splits > 1 ? (size_t)q_len * splits * num_q_heads : 0;
+  char* ws = static_cast<char*>(workspace);
+  p.status = reinterpret_cast<int32_t*>(ws);
+  p.lse_part = reinterpret_cast<float*>(ws + 256);
+  p.o_part = reinterpret_cast<float*>(ws + 256 + align256(rows * sizeof(float)));
+  p.out = out;
+  p.lse_out = lse_out;
+  p.q_len = q_len;
+  p.seq_len = seq_len;
+  p.seq_len_dev = seq_len_dev;
+  p.max_pages = max_pages;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.num_pages = cache->num_pages;
+  p.splits = splits;
+  p.row_blocks = (q_len * G + inst.rows - 1) / inst.rows;
+  p.out_bf16 = out_dtype == KVQ_OUT_BF16;
+  p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+  p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
+  p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t grid = (int64_t)p.row_blocks * cache->num_kv_heads * splits;
+  if (grid > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
+  cudaError_t e = kvq::launch_prefill_tc(cache->format, D, p, static_cast<int>(grid), st);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  if (splits > 1) {
+    e = kvq::launch_merge(p.o_part, p.lse_part, nullptr, splits, q_len, num_q_heads, D, out, p.out_bf16, lse_out,
+                          false, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  if (flags & KVQ_CHECKED) {
+    int32_t bits = 0;
+    const int rc = kvq_read_status(workspace, stream, &bits);
+    if (rc) return rc;
+  }
+  return succeed();
+}
 
 // Decode (q_len = 1) or causal verification of q_len tokens a sequence: the
 // launch works on batch = nseq x q_len virtual sequences (query token i of cache
@@ -598,6 +731,19 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
       seen[key] = 1;
     }
   }
+  int32_t q_host = 0, out_host = 0;
+  rc = memory_kind(q, "q", &q_host);
+  if (rc) return rc;
+  rc = memory_kind(out, "out", &out_host);
+  if (rc) return rc;
+  // one sequence, many query rows: the tensor-core prefill kernel (the plan was
+  // checked above all the same, so a call is accepted or refused alike on both paths)
+  if (!clear_status && !q_host && !out_host && !(flags & (KVQ_SKIP_MERGE | KVQ_TEST_STALL))) {
+    const int S = verify_route_splits(cache, nseq, q_len, num_q_heads, max_pages_per_seq, 0);
+    if (S > 0 && workspace_bytes >= kvq_prefill_workspace_bytes(q_len, num_q_heads, D, S))
+      return prefill_launch(cache, q, q_len, num_q_heads, sm_scale, block_tables, max_pages_per_seq, 0, seq_lens, S,
+                            workspace, out, out_dtype, lse_out, flags, stream);
+  }
   kvq::DecodeInstance inst;
   rc = prepare_instance(cache->format, D, &inst);
   if (rc) return rc;
@@ -610,17 +756,11 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   if (rc) return rc;
   float *o_part = nullptr, *lse_part = nullptr;
   kvq_workspace_partials(workspace, total_splits, num_q_heads, D, &o_part, &lse_part);
-  // q in pinned host memory: one copy into the workspace, read by the decode
-  int32_t q_host = 0;
-  rc = memory_kind(q, "q", &q_host);
-  if (rc) return rc;
-  int32_t out_host = 0;
-  rc = memory_kind(out, "out", &out_host);
-  if (rc) return rc;
   if (clear_status) {
     const cudaError_t ec = cudaMemsetAsync(workspace, 0, 256, st);
     if (ec != cudaSuccess) return cuda_fail(ec, "clearing the status block");
   }
+  // q in pinned host memory: one copy into the workspace, read by the decode
   const void* q_dev = q;
   if (q_host) {
     const size_t rows = (size_t)total_splits * num_q_heads;
@@ -760,76 +900,10 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
   const int D = cache->head_dim;
   const size_t need = kvq_prefill_workspace_bytes(q_len, num_q_heads, D, splits);
   if (workspace_bytes < need) return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
-  kvq::PrefillInstance inst;
-  if (!kvq::prefill_tc_instance(cache->format, D, &inst))
-    return fail(KVQ_ERR_UNSUPPORTED, "no prefill kernel for format %d head_dim %d", cache->format, D);
-  {
-    static std::mutex mu;
-    static bool done[64][4][2] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "device index %d", dev);
-    std::lock_guard<std::mutex> lock(mu);
-    bool& d = done[dev][cache->format][D == 256 ? 1 : 0];
-    if (!d) {
-      for (const void* kern : inst.kernels) {
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(prefill kernel)");
-        if (inst.launch_regs > 0 && fa.numRegs != inst.launch_regs)
-          return fail(KVQ_ERR_UNSUPPORTED,
-                      "prefill kernel built with %d registers a thread, its register split assumes %d", fa.numRegs,
-                      inst.launch_regs);
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, inst.smem_bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
-      }
-      d = true;
-    }
-  }
-  kvq::PrefillParams p{};
-  p.q = q;
-  p.block_table = block_table;
-  p.k_codes = static_cast<const uint8_t*>(cache->k_codes);
-  p.v_codes = static_cast<const uint8_t*>(cache->v_codes);
-  p.k_scales = static_cast<const uint8_t*>(cache->k_scales);
-  p.v_scales = static_cast<const uint8_t*>(cache->v_scales);
-  const size_t rows = splits > 1 ? (size_t)q_len * splits * num_q_heads : 0;
-  char* ws = static_cast<char*>(workspace);
-  p.status = reinterpret_cast<int32_t*>(ws);
-  p.lse_part = reinterpret_cast<float*>(ws + 256);
-  p.o_part = reinterpret_cast<float*>(ws + 256 + align256(rows * sizeof(float)));
-  p.out = out;
-  p.lse_out = lse_out;
-  p.q_len = q_len;
-  p.seq_len = seq_len;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = cache->num_kv_heads;
-  p.num_pages = cache->num_pages;
-  p.splits = splits;
-  p.row_blocks = (q_len * G + inst.rows - 1) / inst.rows;
-  p.out_bf16 = out_dtype == KVQ_OUT_BF16;
-  p.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
-  p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
-  p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
   rc = memory_kind(out, "out", nullptr);
   if (rc) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t grid = (int64_t)p.row_blocks * cache->num_kv_heads * splits;
-  if (grid > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
-  cudaError_t e = kvq::launch_prefill_tc(cache->format, D, p, static_cast<int>(grid), st);
-  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  if (splits > 1) {
-    e = kvq::launch_merge(p.o_part, p.lse_part, nullptr, splits, q_len, num_q_heads, D, out, p.out_bf16, lse_out,
-                          false, st);
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  }
-  if (flags & KVQ_CHECKED) {
-    int32_t bits = 0;
-    rc = kvq_read_status(workspace, stream, &bits);
-    if (rc) return rc;
-  }
-  return succeed();
+  return prefill_launch(cache, q, q_len, num_q_heads, sm_scale, block_table, max_pages, seq_len, nullptr, splits,
+                        workspace, out, out_dtype, lse_out, flags, stream);
 }
 
 int kvq_split_merge(const float* o_part, const float* lse_part, const int32_t* split_offsets, int32_t batch,

@@ -47,7 +47,8 @@ struct PrefillParams {
   void* out;                   // [q_len][Hq][D] f32 or bf16 (splits == 1)
   float* lse_out;              // [q_len][Hq] or null
   int32_t* status;             // device status word
-  int32_t q_len, seq_len, num_q_heads, num_kv_heads, num_pages;
+  const int32_t* seq_len_dev;  // device [1]: the sequence length, read by the kernel (null: seq_len)
+  int32_t q_len, seq_len, num_q_heads, num_kv_heads, num_pages, max_pages;
   int32_t splits, row_blocks, out_bf16;
   float sm_scale_log2;
   float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scales (1 otherwise)

@@ -121,6 +121,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the sequence length: from the launch, or (a verify call) from device memory,
+  // clamped to the block table (an out-of-range value is flagged)
+  int seq_len = p.seq_len;
+  if (p.seq_len_dev) {
+    seq_len = *p.seq_len_dev;
+    if (seq_len < 0 || seq_len > p.max_pages * kPage) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
+      seq_len = seq_len < 0 ? 0 : p.max_pages * kPage;
+    }
+  }
   const int G = p.num_q_heads / p.num_kv_heads;
   const int TG = p.q_len * G;
   const int it = blockIdx.x;
@@ -130,12 +140,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int rb = p.row_blocks - 1 - rest / p.num_kv_heads;  // heaviest row blocks first
   const int row0 = rb * kTcRows;
   const int last_tok = min(p.q_len - 1, (row0 + kTcRows - 1) / G);
-  const int kmax = p.seq_len - p.q_len + last_tok + 1;  // keys the block's last row sees
-  const int np_all = (kmax + kPage - 1) / kPage;
+  const int kmax = seq_len - p.q_len + last_tok + 1;  // keys the block's last row sees
+  const int np_all = kmax > 0 ? (kmax + kPage - 1) / kPage : 0;
   const int pg0 = (int)((int64_t)s * np_all / p.splits);
   const int npg = (int)((int64_t)(s + 1) * np_all / p.splits) - pg0;
   const int nt = (npg + kTcPages - 1) / kTcPages;
-  const int key_end = min(p.seq_len, (pg0 + npg) * kPage);  // keys of this range (exclusive)
+  const int key_end = min(seq_len, (pg0 + npg) * kPage);  // keys of this range (exclusive)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < kBarCount; ++b) mbar_init(&bars[b], b <= kBarV1 ? 4 : 1);
@@ -429,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarQ]);
     }
-    const int lim = live ? p.seq_len - p.q_len + ti + 1 : 0;  // keys this row sees (exclusive)
+    const int lim = live ? max(0, seq_len - p.q_len + ti + 1) : 0;  // keys this row sees (exclusive)
     const int kend = min(lim, key_end);
     // logit (log2 units) = S x kfac x rs with rs = the row's power of two (q was
     // scaled by 1/rs to be exact in fp16; 1 for BF16): INT8 kfac = the key's scale

@@ -263,3 +263,47 @@ def test_prefill_split_choice_and_workspace(kvq):
     g32 = _struct(kvq, fmt="int8_g32")
     with pytest.raises(kvq.KvqError, match="no prefill kernel"):  # per-32 scales: decode and verify only
         kvq.kvq_prefill_splits(g32, 10, 24, 500, 152)
+
+
+def test_verify_workspace_covers_the_tensor_core_route(kvq):
+    """A one-sequence verify call with 32+ query rows a KV head may take the
+    prefill kernel with about one CTA per SM in key splits (at most 64): its
+    workspace covers both routes; any other call needs the decode workspace."""
+    s = _struct(kvq)  # INT8, Hkv = 4, D = 256
+    dec = kvq.kvq_decode_workspace_bytes
+    pre = kvq.kvq_prefill_workspace_bytes
+    vws = lambda st, b, T, hq, ts: kvq.kvq_verify_workspace_bytes(st, b, T, hq, ts, 152)
+    # 6 tokens x 6 heads = 36 rows: one row block a KV head, 4 items -> 38 splits
+    assert vws(s, 1, 6, 24, 40) == max(dec(40, 24, 256), pre(6, 24, 256, 38)) == pre(6, 24, 256, 38)
+    assert vws(s, 1, 6, 24, 4000) == dec(4000, 24, 256)  # a wide decode plan needs more
+    assert vws(s, 2, 6, 24, 40) == dec(40, 24, 256)  # two sequences: the decode kernel
+    assert vws(s, 1, 5, 24, 40) == dec(40, 24, 256)  # 30 rows: the decode kernel
+    assert vws(s, 1, 4, 32, 40) == max(dec(40, 32, 256), pre(4, 32, 256, 38))  # 4 x 8 = 32 rows
+    assert vws(s, 1, 43, 24, 43) == max(dec(43, 24, 256), pre(43, 24, 256, 12))  # 258 rows: 3 blocks, 12 items
+    assert vws(s, 1, 8, 8, 8) == dec(8, 8, 256)  # G = 2, 16 rows: no route
+    assert kvq.kvq_verify_workspace_bytes(s, 1, 16, 8, 16, 152) == max(dec(16, 8, 256), pre(16, 8, 256, 38))
+    assert kvq.kvq_verify_workspace_bytes(s, 1, 16, 8, 16, 1000) == max(dec(16, 8, 256), pre(16, 8, 256, 64))
+    g32 = _struct(kvq, fmt="int8_g32")  # no prefill kernel: the decode kernel
+    assert vws(g32, 1, 6, 24, 40) == dec(40, 24, 256)
+    with pytest.raises(kvq.KvqError):
+        vws(s, 1, 0, 24, 40)
+
+
+def test_binding_refuses_undersized_buffers(kvq):
+    """The Python binding checks the buffers a device call writes against q's shape
+    before anything reaches the library (host tensors stand in for device ones)."""
+    import torch
+
+    s = _struct(kvq)  # D = 256
+    chk = kvq._binding._shapes
+    q = torch.zeros(3, 6, 24, 256)
+    bt, sl = torch.zeros(3, 10, dtype=torch.int32), torch.zeros(3, dtype=torch.int32)
+    chk(q, torch.zeros(3, 6, 24, 256), torch.zeros(3, 6, 24), bt, sl, s)
+    chk(q, torch.zeros(18, 24 * 256), None, bt, sl, s)  # a view of the same size is accepted
+    for bad in (dict(out=torch.zeros(1, 6, 24, 256)), dict(lse=torch.zeros(1, 6, 24)),
+                dict(bt=torch.zeros(2, 10, dtype=torch.int32)), dict(sl=torch.zeros(2, dtype=torch.int32)),
+                dict(q=torch.zeros(3, 6, 24, 128), out=torch.zeros(3, 6, 24, 128))):
+        args = dict(q=q, out=torch.zeros(3, 6, 24, 256), lse=None, bt=bt, sl=sl)
+        args.update(bad)
+        with pytest.raises(ValueError):
+            chk(args["q"], args["out"], args["lse"], args["bt"], args["sl"], s)

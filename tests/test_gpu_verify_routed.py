@@ -1,0 +1,173 @@
+"""Verify calls of one sequence whose query rows (q_len x query heads a KV head)
+number 32 or more run on the tensor-core prefill kernel, with the sequence length
+read on the device.  Checked against the float64 oracle's paged_verify (max-abs
+2e-3 for fp32 output, 1e-2 or half a bf16 ulp for bf16 output), against the same
+call kept on the decode kernel by a workspace too small for the route, through a
+CUDA graph, and for the flag the kernel raises when the device length runs past
+the block table."""
+import numpy as np
+import pytest
+import torch
+
+from quantized_paged_kv_gb300 import workloads as W
+from tests import harness as H
+from oracle import attention as oatt
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    H.ensure_built()
+
+
+class _Call:
+    """One verify call's tensors; run(workspace) calls it and returns (out, lse) as numpy."""
+
+    def __init__(self, wl, fmt, T, gs=(1.0, 1.0), out_dtype="f32", split=0, seq_len=None):
+        from quantized_paged_kv_gb300 import DecodePlan
+
+        self.wl, self.T = wl, T
+        self.cache = H.gpu_cache(wl, fmt, gs)
+        self.plan = DecodePlan(self.cache, wl.seq_lens, wl.Hq, split_override=split, q_len=T)
+        self.q = wl.q_tokens(T)
+        self.qt = torch.from_numpy(self.q).to(torch.bfloat16).cuda()
+        od = {"f32": torch.float32, "bf16": torch.bfloat16}[out_dtype]
+        self.out = torch.full((wl.B, T, wl.Hq, wl.D), float("nan"), dtype=od, device="cuda")
+        self.lse = torch.full((wl.B, T, wl.Hq), float("nan"), device="cuda")
+        self.bt = torch.from_numpy(wl.block_tables).cuda()
+        lens = wl.seq_lens if seq_len is None else np.array([seq_len], np.int32)
+        self.sl = torch.from_numpy(lens).cuda()
+
+    def launch(self, workspace=None, checked=True):
+        from quantized_paged_kv_gb300 import _binding as B
+
+        ws = self.plan.workspace if workspace is None else workspace
+        B.kvq_paged_verify_attention(self.cache.struct, self.qt, self.wl.sm_scale, self.bt, self.sl, self.plan.plan,
+                                     self.plan.total_splits, self.plan.num_ctas, ws, self.out, self.lse,
+                                     B.KVQ_CHECKED if checked else 0, None)
+
+    def run(self, workspace=None, checked=True):
+        self.out.fill_(float("nan"))
+        self.lse.fill_(float("nan"))
+        self.launch(workspace, checked)
+        torch.cuda.synchronize()
+        return self.out.float().cpu().numpy(), self.lse.cpu().numpy()
+
+    def decode_only_workspace(self):
+        """A workspace that holds the decode plan's partials but not the routed call's."""
+        from quantized_paged_kv_gb300 import _binding as B
+
+        n = B.kvq_decode_workspace_bytes(self.plan.total_splits, self.wl.Hq, self.wl.D)
+        assert n < self.plan.workspace.numel()
+        return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def _compare(wl, fmt, T, out, lse, gs, out_dtype="f32", units=None):
+    pools = H.oracle_pools(wl, fmt, gs)
+    ref, ref_lse = oatt.paged_verify(fmt, pools, wl.q_tokens(T), wl.block_tables, wl.seq_lens, wl.sm_scale,
+                                     units=units)
+    sel = ~np.isnan(ref_lse)
+    rows = sel[..., None].repeat(wl.D, -1)
+    assert np.all(np.isfinite(out[rows]))
+    err = np.abs(out - ref)[rows]
+    assert np.all(err <= H.bound(out_dtype, ref[rows])), (fmt, T, err.max())
+    fin = sel & np.isfinite(ref_lse)
+    if fin.any():
+        assert np.abs(lse[fin] - ref_lse[fin]).max() < 1e-3
+    assert np.all(np.isneginf(lse[sel & ~np.isfinite(ref_lse)]))
+    assert np.all(out[sel & ~np.isfinite(ref_lse)] == 0)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
+@pytest.mark.parametrize("T", [6, 8, 22, 43])
+@pytest.mark.parametrize("L", [3, 700, 5000])
+def test_routed_verify_matches_the_oracle(fmt, T, L):
+    """6 query heads a KV head: 36 to 258 rows (one to three 128-row blocks); L < T
+    leaves the first tokens with no visible key; the key splits cover a ragged last page."""
+    wl = W.make("tiny_int8", lens=("list", [L]), seed=51)
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, T, gs)
+    out, lse = c.run()
+    _compare(wl, fmt, T, out, lse, gs)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_routed_verify_d128_gqa4_bf16_output(fmt):
+    # 8 tokens x 4 query heads a KV head = 32 rows, D = 128
+    wl = W.make("serving_int8", lens=("list", [2500]), seed=52)
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, 8, gs, out_dtype="bf16")
+    out, lse = c.run()
+    _compare(wl, fmt, 8, out, lse, gs, out_dtype="bf16")
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_route_and_decode_kernel_agree(fmt):
+    """The same call on both kernels: each within the tolerance of the oracle, so
+    within twice of each other; the two routes round differently, so the outputs
+    are not bit-equal (the route was taken)."""
+    wl = W.make("tiny_int8", lens=("list", [1500]), seed=53)
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, 6, gs, split=1)
+    routed = c.run()
+    kept = c.run(c.decode_only_workspace())
+    _compare(wl, fmt, 6, routed[0], routed[1], gs)
+    _compare(wl, fmt, 6, kept[0], kept[1], gs)
+    assert np.abs(routed[0] - kept[0]).max() <= 4e-3
+    assert not np.array_equal(routed[0], kept[0])
+
+
+def test_below_the_row_threshold_the_decode_kernel_runs():
+    """5 tokens x 6 heads = 30 rows: the decode kernel whatever the workspace (bit-equal)."""
+    wl = W.make("tiny_int8", lens=("list", [1500]), seed=54)
+    c = _Call(wl, "int8", 5, split=1)
+    a = c.run()
+    big = torch.zeros(c.plan.workspace.numel() + (8 << 20), dtype=torch.uint8, device="cuda")
+    b = c.run(big)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_routed_verify_in_a_cuda_graph():
+    """Captured once, replayed: the same bits as the eager call."""
+    wl = W.make("tiny_int8", lens=("list", [3000]), seed=55)
+    c = _Call(wl, "int8", 6)
+    ref = c.run(checked=False)
+    c.out.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            c.launch(checked=False)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(c.out.cpu().numpy(), ref[0])
+    assert np.array_equal(c.lse.cpu().numpy(), ref[1])
+
+
+def test_device_length_past_the_block_table_is_flagged():
+    """Unchecked call whose device seq_len runs past the block table: the kernel
+    clamps it to the table's width (every read stays inside the table) and raises
+    KVQ_DEV_BAD_SEQLEN in the status word."""
+    from quantized_paged_kv_gb300 import _binding as B
+
+    wl = W.make("tiny_int8", lens=("list", [700]), seed=56)
+    width = wl.block_tables.shape[1]
+    c = _Call(wl, "int8", 6, seq_len=width * 16 + 40)
+    c.run(checked=False)
+    rc, bits = B.kvq_read_status(c.plan.workspace, None)
+    assert rc != 0 and bits & B.KVQ_DEV_BAD_SEQLEN
+
+
+@pytest.mark.parametrize("fmt,T", [("int8", 6), ("nvfp4", 8)])
+def test_routed_verify_32k_sampled(fmt, T):
+    """The pages' verify shape (6 query tokens x 6 heads, 32K context) and 8 tokens
+    in NVFP4, on sampled (token, KV head) units."""
+    wl = W.make("long_int8")
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, T, gs)
+    out, lse = c.run()
+    units = [(0, i, h) for i in (0, T // 2, T - 1) for h in (0, 3)]
+    _compare(wl, fmt, T, out, lse, gs, units=units)
