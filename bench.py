@@ -940,8 +940,15 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token("int8", wl.Hkv, wl.D)
     R = layers_for(per_layer, l2, floor=2)
     ls = LayerSet(wl, "int8", R, dev)
-    for T in (2, 6):
+    for T in (2, 4, 6, 8):  # from 4 tokens a one-sequence call runs on the tensor-core kernel
         res[f"verify_long_int8/T={T}"] = time_verify(ls, T, steps)
+    del ls
+    gc.collect()
+    torch.cuda.empty_cache()
+    per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token("nvfp4", wl.Hkv, wl.D)
+    ls = LayerSet(wl, "nvfp4", layers_for(per_layer, l2, floor=2), dev, tensor_gs(wl))
+    for T in (2, 3, 6):  # NVFP4 from 3 tokens
+        res[f"verify_long_int8(nvfp4)/T={T}"] = time_verify(ls, T, steps)
     del ls
     gc.collect()
     torch.cuda.empty_cache()

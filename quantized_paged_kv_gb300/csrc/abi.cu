@@ -193,20 +193,29 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// A verify call of one sequence whose query rows (q_len x query heads a KV head)
-// fill at least a quarter of the tensor-core tile's 128 rows goes to the prefill
+// A verify call of one sequence with enough query tokens goes to the prefill
 // kernel: it reads every key once for all q_len query tokens, where the decode
-// kernel reads the keys once a query token.  The key splits of that launch: about
-// one CTA per SM, capped by the block table's width (at least 4 pages a split)
-// and by 64.  0: the call stays on the decode kernel.
-constexpr int kVerifyRouteRows = 32;
+// kernel reads the keys once a query token, but it has the larger fixed cost
+// (measured at 32K keys: the decode kernel ~11 + 9.6 q_len us, the prefill kernel
+// ~46 us for INT8, ~38 us for NVFP4, whatever q_len up to a 128-row tile; at 8K
+// keys ~9 + 2.6 q_len against ~22 us).  The query-token threshold therefore
+// falls with the context, known on the host only through the block table's
+// width: 4 tokens from 1,024 pages (16K tokens) up, 6 below, one fewer for NVFP4
+// (cheaper to convert on the tensor-core path).  The key splits of that launch:
+// about one CTA per SM, capped by the block table's width (at least 4 pages a
+// split) and by 64.  0: the call stays on the decode kernel.
+constexpr int kVerifyLongPages = 1024;
+
+int verify_route_min_tokens(int format, int64_t max_pages) {
+  return (max_pages >= kVerifyLongPages ? 4 : 6) - (format == KVQ_FMT_NVFP4 ? 1 : 0);
+}
 
 // sms <= 0: the current device's SM count.
 int verify_route_splits(const kvq_cache* cache, int32_t nseq, int32_t q_len, int32_t num_q_heads, int32_t max_pages,
                         int32_t sms) {
-  if (nseq != 1 || q_len < 2 || num_q_heads % cache->num_kv_heads) return 0;
+  if (nseq != 1 || num_q_heads % cache->num_kv_heads) return 0;
+  if (q_len < verify_route_min_tokens(cache->format, max_pages)) return 0;
   const int64_t G = num_q_heads / cache->num_kv_heads;
-  if ((int64_t)q_len * G < kVerifyRouteRows) return 0;
   kvq::PrefillInstance inst;
   if (!kvq::prefill_tc_instance(cache->format, cache->head_dim, &inst)) return 0;
   int dev = 0;
@@ -533,7 +542,7 @@ size_t kvq_verify_workspace_bytes(const kvq_cache* cache, int32_t batch, int32_t
     }
   }
   const size_t decode_need = kvq_decode_workspace_bytes(total_splits, num_q_heads, cache->head_dim);
-  // the routed call's splits never exceed those of the widest block table
+  // the widest block table: the lowest token threshold and the most splits
   const int S = verify_route_splits(cache, batch, q_len, num_q_heads, 0x7FFFFFFF, target_ctas);
   succeed();
   if (S <= 0) return decode_need;
@@ -736,7 +745,7 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   if (rc) return rc;
   rc = memory_kind(out, "out", &out_host);
   if (rc) return rc;
-  // one sequence, many query rows: the tensor-core prefill kernel (the plan was
+  // one sequence, enough query tokens: the tensor-core prefill kernel (the plan was
   // checked above all the same, so a call is accepted or refused alike on both paths)
   if (!clear_status && !q_host && !out_host && !(flags & (KVQ_SKIP_MERGE | KVQ_TEST_STALL))) {
     const int S = verify_route_splits(cache, nseq, q_len, num_q_heads, max_pages_per_seq, 0);

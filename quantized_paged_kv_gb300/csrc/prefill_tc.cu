@@ -121,6 +121,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the merge of the key splits may be scheduled now (it waits for this grid)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kBarCount; ++b) mbar_init(&bars[b], b <= kBarV1 ? 4 : 1);
+    slot[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(slot, Lo::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // The launch is a programmatic dependent of the preceding kernel: the barriers
+  // and the TMEM are set up while that kernel drains, and nothing it may write
+  // (q, the block table, the sequence length, the pool) is read before it completes.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the sequence length: from the launch, or (a verify call) from device memory,
   // clamped to the block table (an out-of-range value is flagged)
   int seq_len = p.seq_len;
@@ -146,19 +164,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int npg = (int)((int64_t)(s + 1) * np_all / p.splits) - pg0;
   const int nt = (npg + kTcPages - 1) / kTcPages;
   const int key_end = min(seq_len, (pg0 + npg) * kPage);  // keys of this range (exclusive)
-
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < kBarCount; ++b) mbar_init(&bars[b], b <= kBarV1 ? 4 : 1);
-    slot[1] = 0;
-    fence_mbar_init();
-  }
-  if (warp == 8) {
-    tmem_alloc(slot, Lo::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = slot[0];
   volatile uint32_t* abort_flag = slot + 1;
   auto wait = [&](int b, uint32_t parity) -> bool {  // one thread
@@ -639,9 +644,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int FMT, int D>
 cudaError_t launch_tc_t(const PrefillParams& p, int grid, cudaStream_t stream) {
   using Lo = TcLayout<FMT, D>;
-  if (p.out_bf16) prefill_tc_kernel<FMT, D, false><<<grid, kTcThreads, Lo::kSmemBytes, stream>>>(p);
-  else prefill_tc_kernel<FMT, D, true><<<grid, kTcThreads, Lo::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = Lo::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return p.out_bf16 ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<FMT, D, false>, p)
+                    : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<FMT, D, true>, p);
 }
 
 template <int FMT, int D>

@@ -266,7 +266,7 @@ def test_prefill_split_choice_and_workspace(kvq):
 
 
 def test_verify_workspace_covers_the_tensor_core_route(kvq):
-    """A one-sequence verify call with 32+ query rows a KV head may take the
+    """A one-sequence verify call with 4+ query tokens (3+ for NVFP4) may take the
     prefill kernel with about one CTA per SM in key splits (at most 64): its
     workspace covers both routes; any other call needs the decode workspace."""
     s = _struct(kvq)  # INT8, Hkv = 4, D = 256
@@ -277,12 +277,14 @@ def test_verify_workspace_covers_the_tensor_core_route(kvq):
     assert vws(s, 1, 6, 24, 40) == max(dec(40, 24, 256), pre(6, 24, 256, 38)) == pre(6, 24, 256, 38)
     assert vws(s, 1, 6, 24, 4000) == dec(4000, 24, 256)  # a wide decode plan needs more
     assert vws(s, 2, 6, 24, 40) == dec(40, 24, 256)  # two sequences: the decode kernel
-    assert vws(s, 1, 5, 24, 40) == dec(40, 24, 256)  # 30 rows: the decode kernel
-    assert vws(s, 1, 4, 32, 40) == max(dec(40, 32, 256), pre(4, 32, 256, 38))  # 4 x 8 = 32 rows
+    assert vws(s, 1, 4, 24, 40) == pre(4, 24, 256, 38)  # 4 tokens: routed on a long context
+    assert vws(s, 1, 3, 24, 40) == dec(40, 24, 256)  # 3 INT8 tokens: the decode kernel
     assert vws(s, 1, 43, 24, 43) == max(dec(43, 24, 256), pre(43, 24, 256, 12))  # 258 rows: 3 blocks, 12 items
-    assert vws(s, 1, 8, 8, 8) == dec(8, 8, 256)  # G = 2, 16 rows: no route
-    assert kvq.kvq_verify_workspace_bytes(s, 1, 16, 8, 16, 152) == max(dec(16, 8, 256), pre(16, 8, 256, 38))
+    assert vws(s, 1, 8, 8, 8) == max(dec(8, 8, 256), pre(8, 8, 256, 38))  # G = 2: one row block a head
     assert kvq.kvq_verify_workspace_bytes(s, 1, 16, 8, 16, 1000) == max(dec(16, 8, 256), pre(16, 8, 256, 64))
+    nv = _struct(kvq, fmt="nvfp4")
+    assert vws(nv, 1, 3, 24, 40) == pre(3, 24, 256, 38)  # NVFP4 from 3 tokens
+    assert vws(nv, 1, 2, 24, 40) == dec(40, 24, 256)
     g32 = _struct(kvq, fmt="int8_g32")  # no prefill kernel: the decode kernel
     assert vws(g32, 1, 6, 24, 40) == dec(40, 24, 256)
     with pytest.raises(kvq.KvqError):

@@ -1,6 +1,6 @@
-"""Verify calls of one sequence whose query rows (q_len x query heads a KV head)
-number 32 or more run on the tensor-core prefill kernel, with the sequence length
-read on the device.  Checked against the float64 oracle's paged_verify (max-abs
+"""Verify calls of one sequence with enough query tokens (6 on a block table
+under 1,024 pages, 4 from there on, one fewer for NVFP4) run on the tensor-core
+prefill kernel, with the sequence length read on the device.  Checked against the float64 oracle's paged_verify (max-abs
 2e-3 for fp32 output, 1e-2 or half a bf16 ulp for bf16 output), against the same
 call kept on the decode kernel by a workspace too small for the route, through a
 CUDA graph, and for the flag the kernel raises when the device length runs past
@@ -55,11 +55,11 @@ class _Call:
         return self.out.float().cpu().numpy(), self.lse.cpu().numpy()
 
     def decode_only_workspace(self):
-        """A workspace that holds the decode plan's partials but not the routed call's."""
+        """A workspace that holds the decode plan's partials only (too small for a routed call's)."""
         from quantized_paged_kv_gb300 import _binding as B
 
         n = B.kvq_decode_workspace_bytes(self.plan.total_splits, self.wl.Hq, self.wl.D)
-        assert n < self.plan.workspace.numel()
+        assert n <= self.plan.workspace.numel()
         return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
@@ -118,14 +118,31 @@ def test_route_and_decode_kernel_agree(fmt):
     assert not np.array_equal(routed[0], kept[0])
 
 
-def test_below_the_row_threshold_the_decode_kernel_runs():
-    """5 tokens x 6 heads = 30 rows: the decode kernel whatever the workspace (bit-equal)."""
+@pytest.mark.parametrize("fmt,T", [("int8", 5), ("nvfp4", 4)])
+def test_below_the_token_threshold_the_decode_kernel_runs(fmt, T):
+    """A 94-page block table: fewer than 6 tokens (5 for NVFP4) stay on the decode
+    kernel whatever the workspace (bit-equal)."""
     wl = W.make("tiny_int8", lens=("list", [1500]), seed=54)
-    c = _Call(wl, "int8", 5, split=1)
+    c = _Call(wl, fmt, T, H.global_scales(wl, fmt), split=1)
     a = c.run()
     big = torch.zeros(c.plan.workspace.numel() + (8 << 20), dtype=torch.uint8, device="cuda")
     b = c.run(big)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("fmt,T,routed", [("int8", 4, True), ("int8", 3, False), ("nvfp4", 3, True)])
+def test_long_context_threshold(fmt, T, routed):
+    """A 32K context (2,048-page block table): 4 tokens are routed (3 for NVFP4);
+    sampled units against the oracle on either kernel, and the route decides
+    whether the call's bits differ from the decode kernel's."""
+    wl = W.make("long_int8")
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, T, gs, split=1)
+    auto = c.run()
+    kept = c.run(c.decode_only_workspace())
+    units = [(0, i, h) for i in (0, T - 1) for h in (1, 2)]
+    _compare(wl, fmt, T, auto[0], auto[1], gs, units=units)
+    assert np.array_equal(auto[0], kept[0]) != routed
 
 
 def test_routed_verify_in_a_cuda_graph():
