@@ -21,12 +21,13 @@
 //   * warp 8, lane 0 (MMA): S(i) = Q K(i)^T into one of two TMEM buffers, then
 //     O += P(i-1) V(i-1); each group of MMAs is committed to an mbarrier.
 //   * warps 0..3 (softmax, one query row a thread): the q row (INT8: scaled by a
-//     power of two so that it is exact in fp16) into the A tile; per tile, S from
-//     TMEM (tcgen05.ld), the online softmax with the row's causal limit, and P'
-//     (INT8: the V scale of each key folded in) as the fp16 / bf16 A operand of
-//     the P V product, in hi + lo terms for fp32 output.  The running maximum is
-//     raised only when a row's new maximum exceeds it by more than 2^8 (then the
-//     row of O in TMEM is rescaled), so p <= 256.
+//     power of two so that it is exact in fp16) into Q in TMEM, the A operand of
+//     S = Q K^T; per tile, S from TMEM (tcgen05.ld), the online softmax with the
+//     row's causal limit, and P' (INT8: the V scale of each key folded in),
+//     written over S(i) in TMEM as the fp16 / bf16 A operand of the P V product,
+//     in hi + lo terms for fp32 output.  The running maximum is raised only when
+//     a row's new maximum exceeds it by more than 2^8 (then the row of O in TMEM
+//     is rescaled), so p <= 256.
 // Every wait is bounded (%globaltimer); a timeout sets KVQ_DEV_TIMEOUT, the CTA
 // waits for its issued MMAs, frees its TMEM and returns.
 #include "decode.cuh"
@@ -43,11 +44,9 @@ constexpr float kTcRescale = 8.0f;  // log2 of the largest p a stale maximum may
 template <int FMT, int D>
 struct TcLayout {
   static constexpr int kAtoms = D / 64;                  // 128-byte swizzle atoms along D (fp16)
-  static constexpr int kQBytes = kTcRows * D * 2;        // [atom][128 rows][128 B]
   static constexpr int kKBytes = kTcKeys * D * 2;        // [atom][64 keys][128 B]
   static constexpr int kVBytes = kTcKeys * D * 2;        // [8-key group][d atom][8 keys][128 B]
-  static constexpr int kQAt = 0;
-  static constexpr int kKAt = kQAt + kQBytes;            // two K tiles
+  static constexpr int kKAt = 0;                         // two K tiles
   static constexpr int kVAt = kKAt + 2 * kKBytes;        // two V tiles
   static constexpr int kScRing = 3;                      // scale buffers (tiles in flight)
   static constexpr int kScAt = kVAt + 2 * kVBytes;       // float k scales [3][64], v scales [3][64]
@@ -57,13 +56,15 @@ struct TcLayout {
   static constexpr int kSmemBytes = 1024 + kSlotAt + 16;
   static_assert(kNumBars >= 14, "barriers");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  static constexpr uint32_t kTmemO = 0;          // O: D columns
-  static constexpr uint32_t kTmemS = D;          // S: two buffers of 64 columns
-  // P: two buffers of 64 columns, each the hi terms (32 columns of f16 / bf16
-  // pairs) then the lo terms, the A operand of O += P V read from TMEM
-  static constexpr uint32_t kTmemP = D + 2 * kTcKeys;
+  // TMEM columns: O (D), two S buffers of 64, and Q (D / 2: f16 / bf16 pairs).
+  // P(i) is written over S(i) once the softmax has read S(i): the hi terms (32
+  // columns of pairs) then the lo terms, the A operand of O += P V.  Q is the A
+  // operand of S = Q K^T, so neither product reads an A operand from shared memory.
+  static constexpr uint32_t kTmemO = 0;
+  static constexpr uint32_t kTmemS = D;
+  static constexpr uint32_t kTmemQ = D + 2 * kTcKeys;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kTmemP + 2 * kTcKeys <= kTmemCols, "TMEM columns");
+  static_assert(kTmemQ + D / 2 <= kTmemCols, "TMEM columns");
   // MN-major V: byte offset between d atoms (leading) and between 8-key groups (strided)
   static constexpr uint32_t kVLbo = 1024, kVSbo = kAtoms * 1024;
 };
@@ -190,11 +191,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t ds = tmem + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys;
           const uint32_t kb = sbase + Lo::kKAt + (uint32_t)(i & 1) * Lo::kKBytes;
 #pragma unroll
-          for (int k = 0; k < KS; ++k) {
+          for (int k = 0; k < KS; ++k) {  // k-step of 16 elements: 8 columns of Q
             const int a = k >> 2, kk = k & 3;
-            const uint64_t ad = umma_desc_sw128(sbase + Lo::kQAt + a * kTcRows * 128 + 32 * kk, 16, 1024);
             const uint64_t bd = umma_desc_sw128(kb + a * kTcKeys * 128 + 32 * kk, 16, 1024);
-            umma_f16(ds, ad, bd, kIdescS, k > 0 ? 1u : 0u);
+            umma_f16_ta(ds, tmem + Lo::kTmemQ + 8 * k, bd, kIdescS, k > 0 ? 1u : 0u);
           }
           umma_commit(&bars[kBarS0 + (i & 1)]);
           umma_commit(&bars[kBarKF0 + (i & 1)]);
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!wait(kBarP0 + (j & 1), (j >> 1) & 1) || !wait(kBarV0 + (j & 1), (j >> 1) & 1)) break;
           tc_fence_after();
           const uint32_t vb = sbase + Lo::kVAt + (uint32_t)(j & 1) * Lo::kVBytes;
-          const uint32_t pa = tmem + Lo::kTmemP + (uint32_t)(j & 1) * kTcKeys;  // P(j): hi, then lo 32 columns on
+          const uint32_t pa = tmem + Lo::kTmemS + (uint32_t)(j & 1) * kTcKeys;  // P(j) over S(j): hi, then lo
 #pragma unroll
           for (int k = 0; k < kTcKeys / 16; ++k) {
             const uint64_t bd = umma_desc_sw128(vb + 2 * k * Lo::kVSbo, Lo::kVLbo, Lo::kVSbo);
@@ -402,7 +402,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = row0 + rl;
     const bool live = row < TG;
     const int ti = live ? row / G : 0, g = live ? row - (row / G) * G : 0;
-    // ---- q row -> the A tile (INT8: scaled by 2^k so its largest |q| is in [2^14, 2^15))
+    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+    // ---- q row -> Q in TMEM, this thread's lane (INT8: scaled by 2^k so its
+    // largest |q| is in [2^14, 2^15)); column c holds elements 2c (low half), 2c + 1
     float row_scale = 1.f;
     {
       const uint4* qrow =
@@ -427,20 +429,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         up = pow2f(k);
         row_scale = pow2f(-k);
       }
-      for (int c8 = 0; c8 < D / 8; ++c8) {
-        const uint4 v = live ? __ldg(qrow + c8) : make_uint4(0, 0, 0, 0);
-        uint4 o = v;
-        if constexpr (!kBf16) {
+#pragma unroll 1
+      for (int c16 = 0; c16 < D / 16; ++c16) {  // 16 elements: 8 columns
+        uint32_t cols[8];
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const uint4 v = live ? __ldg(qrow + 2 * c16 + h8) : make_uint4(0, 0, 0, 0);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t r4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            r4[e] = h2_as_u32(__floats2half2_rn(__uint_as_float(w[e] << 16) * up, __uint_as_float(w[e] & 0xFFFF0000u) * up));
-          o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+            cols[4 * h8 + e] = kBf16 ? w[e]
+                                     : h2_as_u32(__floats2half2_rn(__uint_as_float(w[e] << 16) * up,
+                                                                   __uint_as_float(w[e] & 0xFFFF0000u) * up));
         }
-        *reinterpret_cast<uint4*>(smem + Lo::kQAt + kmajor_off(rl, 8 * c8, kTcRows)) = o;
+        tmem_st8(tq + Lo::kTmemQ + 8 * c16, cols);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarQ]);
     }
@@ -454,7 +459,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // maximum logit.
     const float rs = row_scale;
     const float kconst = p.sm_scale_log2 * p.k_gs_inv;  // kfac of the non-INT8 formats
-    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     float m_run = -INFINITY, l_run = 0.f;
 
     int done = 0;  // tiles completed
@@ -517,13 +521,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (m_run == -INFINITY) m_run = mx;  // first visible keys (still -inf if none)
-      // P buffer i & 1 (TMEM) is free once P(i-2) V(i-2) has completed: the
-      // softmax of tile i no longer waits for the product of tile i-1
-      if (i > 1) {
-        if (!wait_warp(kBarO0 + (i & 1), ((i - 2) >> 1) & 1)) break;
-        tc_fence_after();
-      }
-      const uint32_t tp = tq + Lo::kTmemP + (uint32_t)(i & 1) * kTcKeys;  // this row's P(i): hi, lo 32 columns on
+      // P(i) goes over S(i), which this thread has read.  The last reader of those
+      // columns before S(i), P(i-2) V(i-2), was issued before S(i), so the commit
+      // that reported S(i) done covered it too.
+      const uint32_t tp = tq + Lo::kTmemS + (uint32_t)(i & 1) * kTcKeys;  // this row's P(i): hi, lo 32 columns on
       // pass 2: p = 2^(z - m) <= 2^8 (ex2.approx.ftz: results below 2^-126 are 0,
       // a masked key's z = -inf gives exactly 0), P' = p v_scale, packed hi (+ lo)
       float psums[4] = {0.f, 0.f, 0.f, 0.f};
