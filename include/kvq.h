@@ -273,7 +273,7 @@ size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int
  * kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim) and, for a
  * call the prefill kernel may take (batch = 1, q_len >= 4, or >= 3 for NVFP4),
  * kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, S) for the largest
- * key split count S it may use: about one CTA per SM, at most 64.
+ * key split count S it may use (at most 64; see kvq_prefill_splits).
  * target_ctas: the SM count of the device the calls run on (0: the current
  * device's).  A smaller workspace keeps such a call on the decode kernel.
  * 0 for bad arguments (the reason in kvq_last_error). */
@@ -338,8 +338,9 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
  * spans 1,024 pages or more, >= 6 below that (one fewer for NVFP4), goes instead
  * to the tensor-core kernel of kvq_paged_prefill_attention ([int8-kv] "Read the
  * prompt using a small temporary buffer": a block of query rows reads each key
- * once), with the sequence length read on the device and about one CTA per SM
- * in key splits, when q and out are device memory, neither KVQ_SKIP_MERGE nor
+ * once), with the sequence length read on the device and the key splits that
+ * kvq_prefill_splits picks for the block table's width as the context, when q
+ * and out are device memory, neither KVQ_SKIP_MERGE nor
  * KVQ_TEST_STALL is set and the workspace holds kvq_verify_workspace_bytes; the
  * plan is still required (and checked under KVQ_CHECKED), the result is the same
  * up to rounding order.
@@ -386,7 +387,12 @@ int kvq_paged_verify_attention(const kvq_cache* cache, const void* q, int32_t ba
  *   q              device bf16 [q_len][num_q_heads][head_dim]
  *   block_table    device int32 [max_pages]: the sequence's pages
  *   seq_len        host: tokens of the sequence, the q_len new ones included
- *   splits         1 .. 64 key ranges (kvq_prefill_splits gives a default)
+ *   splits         1 .. 64 key ranges.  kvq_prefill_splits gives a default: the S
+ *                  that minimises a model of the call fitted to measured calls,
+ *                  waves(S) x (10 us + 1.9 us a 64-key tile of a split) plus, for
+ *                  S > 1, the merge (3.5 us + the partials written and read at
+ *                  6 TB/s), waves(S) = ceil(CTAs / target_ctas), at least one
+ *                  tile a split
  *   workspace      device, >= kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, splits),
  *                  256-byte aligned; its first word is the device status word
  *   out            device [q_len][num_q_heads][head_dim] float or bf16

@@ -193,6 +193,29 @@ int prepare_instance(int format, int D, kvq::DecodeInstance* inst) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Key splits of a prefill-kernel launch: the split count S in [1, 64] (at least
+// one 64-key tile a split) that minimises a model of the call's time, fitted to
+// measured prefill calls at 32K keys (2,048 / 512 / 6 tokens, S = 1 .. 64):
+//   waves(S) x (10 us + 1.9 us x tiles a split) + [S > 1] (3.5 us + partials)
+// with waves(S) = ceil(items x S / CTAs a wave), one CTA an SM, and the merge's
+// partials written and read once at 6 TB/s.  Ties go to the smaller S.
+int64_t pick_key_splits(int64_t items, int64_t pages, int64_t partial_bytes_per_split, int64_t ctas) {
+  const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(64, pages / 4));
+  int64_t best = 1;
+  double best_us = 0.0;
+  for (int64_t S = 1; S <= cap; ++S) {
+    const int64_t waves = (items * S + ctas - 1) / ctas;
+    const int64_t tiles = (pages + 4 * S - 1) / (4 * S);
+    double us = (double)waves * (10.0 + 1.9 * (double)tiles);
+    if (S > 1) us += 3.5 + 2.0 * (double)partial_bytes_per_split * (double)S / 6.0e6;
+    if (S == 1 || us < best_us) {
+      best = S;
+      best_us = us;
+    }
+  }
+  return best;
+}
+
 // A verify call of one sequence with enough query tokens goes to the prefill
 // kernel: it reads every key once for all q_len query tokens, where the decode
 // kernel reads the keys once a query token, but it has the larger fixed cost
@@ -201,9 +224,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // keys ~9 + 2.6 q_len against ~22 us).  The query-token threshold therefore
 // falls with the context, known on the host only through the block table's
 // width: 4 tokens from 1,024 pages (16K tokens) up, 6 below, one fewer for NVFP4
-// (cheaper to convert on the tensor-core path).  The key splits of that launch:
-// about one CTA per SM, capped by the block table's width (at least 4 pages a
-// split) and by 64.  0: the call stays on the decode kernel.
+// (cheaper to convert on the tensor-core path).  The key splits of that launch
+// come from pick_key_splits with the block table's width as the context.
+// 0: the call stays on the decode kernel.
 constexpr int kVerifyLongPages = 1024;
 
 int verify_route_min_tokens(int format, int64_t max_pages) {
@@ -223,9 +246,7 @@ int verify_route_splits(const kvq_cache* cache, int32_t nseq, int32_t q_len, int
                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess))
     return 0;
   const int64_t items = ((int64_t)q_len * G + inst.rows - 1) / inst.rows * cache->num_kv_heads;
-  int64_t S = std::max<int64_t>(1, sms / items);
-  S = std::min<int64_t>({S, 64, std::max<int64_t>(1, max_pages / 4)});
-  return static_cast<int>(S);
+  return static_cast<int>(pick_key_splits(items, max_pages, (int64_t)q_len * num_q_heads * cache->head_dim * 4, sms));
 }
 
 }  // namespace
@@ -542,8 +563,9 @@ size_t kvq_verify_workspace_bytes(const kvq_cache* cache, int32_t batch, int32_t
     }
   }
   const size_t decode_need = kvq_decode_workspace_bytes(total_splits, num_q_heads, cache->head_dim);
-  // the widest block table: the lowest token threshold and the most splits
-  const int S = verify_route_splits(cache, batch, q_len, num_q_heads, 0x7FFFFFFF, target_ctas);
+  // a block table of 2^20 pages (16M tokens): the lowest token threshold, and as
+  // many splits as any shorter table gets
+  const int S = verify_route_splits(cache, batch, q_len, num_q_heads, 1 << 20, target_ctas);
   succeed();
   if (S <= 0) return decode_need;
   return std::max(decode_need, kvq_prefill_workspace_bytes(q_len, num_q_heads, cache->head_dim, S));
@@ -873,9 +895,7 @@ int32_t kvq_prefill_splits(const kvq_cache* cache, int32_t q_len, int32_t num_q_
   const int64_t G = num_q_heads / cache->num_kv_heads;
   const int64_t items = (q_len * G + inst.rows - 1) / inst.rows * cache->num_kv_heads;
   const int64_t pages = (seq_len + cache->page_size - 1) / cache->page_size;
-  // about two CTAs' worth of items per SM, at least 16 pages a split, at most 16 splits
-  int64_t S = (2 * target + items - 1) / items;
-  S = std::max<int64_t>(1, std::min<int64_t>({S, 16, std::max<int64_t>(1, pages / 16)}));
+  const int64_t S = pick_key_splits(items, pages, (int64_t)q_len * num_q_heads * cache->head_dim * 4, target);
   succeed();
   return static_cast<int32_t>(S);
 }

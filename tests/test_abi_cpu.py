@@ -247,11 +247,17 @@ def test_host_validation_errors(kvq):
 
 def test_prefill_split_choice_and_workspace(kvq):
     s = _struct(kvq)  # INT8, Hkv = 4, D = 256
-    # 2048 tokens x 6 heads = 96 row blocks of 128 a KV head: enough work, one split
-    assert kvq.kvq_prefill_splits(s, 2048, 24, 32768, 152) == 1
-    # 6 tokens: one row block a head -> more splits (at most 16, at least 16 pages each)
-    assert kvq.kvq_prefill_splits(s, 6, 24, 32768, 152) == 16
-    assert kvq.kvq_prefill_splits(s, 6, 24, 100, 152) == 1
+    # 2048 tokens x 6 heads = 96 row blocks of 128 a KV head, 384 CTAs: 2.5 waves;
+    # three splits make eight even waves of a third (measured 2,783 against 2,918 us)
+    assert kvq.kvq_prefill_splits(s, 2048, 24, 32768, 152) == 3
+    assert kvq.kvq_prefill_splits(s, 512, 24, 32768, 152) == 3  # 723 against 818 us at 4
+    # 6 tokens: one row block a head, 4 CTAs a split -> one wave of ~37 splits
+    # (measured 47.5 us at 38 splits, 83.2 at 16)
+    assert kvq.kvq_prefill_splits(s, 6, 24, 32768, 152) == 37
+    assert kvq.kvq_prefill_splits(s, 6, 24, 100, 152) == 1  # 7 pages: under two tiles
+    for T, L in ((1, 700), (6, 8192), (2048, 32768), (100, 5000)):  # never past 64, at least a tile a split
+        S = kvq.kvq_prefill_splits(s, T, 24, L, 152)
+        assert 1 <= S <= min(64, max(1, -(-L // 16) // 4))
     assert kvq.kvq_prefill_workspace_bytes(6, 24, 256, 1) == 256
     n = kvq.kvq_prefill_workspace_bytes(6, 24, 256, 3)
     rows = 6 * 3 * 24
@@ -259,7 +265,7 @@ def test_prefill_split_choice_and_workspace(kvq):
     with pytest.raises(kvq.KvqError):
         kvq.kvq_prefill_splits(s, 10, 24, 5, 152)  # q_len > seq_len
     nv = _struct(kvq, fmt="nvfp4")
-    assert kvq.kvq_prefill_splits(nv, 10, 24, 500, 152) == 2  # NVFP4 runs on the same prefill kernel
+    assert kvq.kvq_prefill_splits(nv, 10, 24, 500, 152) == 8  # NVFP4 runs on the same prefill kernel
     g32 = _struct(kvq, fmt="int8_g32")
     with pytest.raises(kvq.KvqError, match="no prefill kernel"):  # per-32 scales: decode and verify only
         kvq.kvq_prefill_splits(g32, 10, 24, 500, 152)
@@ -267,8 +273,9 @@ def test_prefill_split_choice_and_workspace(kvq):
 
 def test_verify_workspace_covers_the_tensor_core_route(kvq):
     """A one-sequence verify call with 4+ query tokens (3+ for NVFP4) may take the
-    prefill kernel with about one CTA per SM in key splits (at most 64): its
-    workspace covers both routes; any other call needs the decode workspace."""
+    prefill kernel with the key splits kvq_prefill_splits picks (at most 64; the
+    workspace is sized for the longest context): its workspace covers both
+    routes; any other call needs the decode workspace."""
     s = _struct(kvq)  # INT8, Hkv = 4, D = 256
     dec = kvq.kvq_decode_workspace_bytes
     pre = kvq.kvq_prefill_workspace_bytes
@@ -279,7 +286,7 @@ def test_verify_workspace_covers_the_tensor_core_route(kvq):
     assert vws(s, 2, 6, 24, 40) == dec(40, 24, 256)  # two sequences: the decode kernel
     assert vws(s, 1, 4, 24, 40) == pre(4, 24, 256, 38)  # 4 tokens: routed on a long context
     assert vws(s, 1, 3, 24, 40) == dec(40, 24, 256)  # 3 INT8 tokens: the decode kernel
-    assert vws(s, 1, 43, 24, 43) == max(dec(43, 24, 256), pre(43, 24, 256, 12))  # 258 rows: 3 blocks, 12 items
+    assert vws(s, 1, 43, 24, 43) == max(dec(43, 24, 256), pre(43, 24, 256, 38))  # 258 rows: 12 CTAs a split
     assert vws(s, 1, 8, 8, 8) == max(dec(8, 8, 256), pre(8, 8, 256, 38))  # G = 2: one row block a head
     assert kvq.kvq_verify_workspace_bytes(s, 1, 16, 8, 16, 1000) == max(dec(16, 8, 256), pre(16, 8, 256, 64))
     nv = _struct(kvq, fmt="nvfp4")
