@@ -271,7 +271,8 @@ size_t kvq_decode_workspace_bytes(int32_t total_splits, int32_t num_q_heads, int
 
 /* Workspace bytes for kvq_paged_verify_attention: the larger of
  * kvq_decode_workspace_bytes(total_splits, num_q_heads, head_dim) and, for a
- * call the prefill kernel may take (batch = 1, q_len >= 4, or >= 3 for NVFP4),
+ * call the prefill kernel may take (q_len >= 4 for one sequence, >= 6 for a
+ * batch; NVFP4 3 and 4),
  * kvq_prefill_workspace_bytes(q_len, num_q_heads, head_dim, S) for the largest
  * key split count S it may use (at most 64; see kvq_prefill_splits).
  * target_ctas: the SM count of the device the calls run on (0: the current
@@ -334,16 +335,17 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
  * MMA tile holds the G query heads of one token (8-row granularity), and the
  * q_len tokens' items cover the same pages at about the same time, so a page
  * read for one token is mostly still in L2 for the others.
- * One sequence (batch = 1) with q_len >= 4 query tokens when the block table
- * spans 1,024 pages or more, >= 6 below that (one fewer for NVFP4), goes instead
- * to the tensor-core kernel of kvq_paged_prefill_attention ([int8-kv] "Read the
- * prompt using a small temporary buffer": a block of query rows reads each key
- * once), with the sequence length read on the device and the key splits that
- * kvq_prefill_splits picks for the block table's width as the context, when q
- * and out are device memory, neither KVQ_SKIP_MERGE nor
- * KVQ_TEST_STALL is set and the workspace holds kvq_verify_workspace_bytes; the
- * plan is still required (and checked under KVQ_CHECKED), the result is the same
- * up to rounding order.
+ * A call with enough query tokens a sequence goes instead, as one launch for
+ * the batch, to the tensor-core kernel of kvq_paged_prefill_attention ([int8-kv]
+ * "Read the prompt using a small temporary buffer": a block of query rows reads
+ * each key once): q_len >= 4 for one sequence whose block table spans 1,024
+ * pages or more, >= 6 otherwise (NVFP4: 3, 5 for one sequence on a shorter
+ * table, 4 for a batch).  The kernel reads the sequence lengths on the device
+ * and takes the key splits that kvq_prefill_splits picks with the block table's
+ * width as the context.  This happens when q and out are device memory, neither
+ * KVQ_SKIP_MERGE nor KVQ_TEST_STALL is set and the workspace holds
+ * kvq_verify_workspace_bytes; the plan is still required (and checked under
+ * KVQ_CHECKED), and the result is the same up to rounding order.
  *   q              device bf16 [batch][q_len][num_q_heads][head_dim]
  *   seq_lens       device int32 [batch]: tokens in the cache, the q_len new ones included
  *   plan           kvq_plan_verify_splits(seq_lens, batch, q_len, ...): the plan

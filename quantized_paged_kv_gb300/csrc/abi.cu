@@ -216,28 +216,35 @@ int64_t pick_key_splits(int64_t items, int64_t pages, int64_t partial_bytes_per_
   return best;
 }
 
-// A verify call of one sequence with enough query tokens goes to the prefill
-// kernel: it reads every key once for all q_len query tokens, where the decode
-// kernel reads the keys once a query token, but it has the larger fixed cost
+// A verify call with enough query tokens a sequence goes to the prefill kernel,
+// one launch for the whole batch: it reads every key once for all q_len query
+// tokens, where the decode kernel reads the keys once a query token, but it has
+// the larger fixed cost
 // (measured at 32K keys: the decode kernel ~11 + 9.6 q_len us, the prefill kernel
 // ~46 us for INT8, ~38 us for NVFP4, whatever q_len up to a 128-row tile; at 8K
 // keys ~9 + 2.6 q_len against ~22 us).  The query-token threshold therefore
 // falls with the context, known on the host only through the block table's
-// width: 4 tokens from 1,024 pages (16K tokens) up, 6 below, one fewer for NVFP4
-// (cheaper to convert on the tensor-core path).  The key splits of that launch
-// come from pick_key_splits with the block table's width as the context.
+// width: for one sequence 4 tokens from 1,024 pages (16K tokens) up, 6 below,
+// one fewer for NVFP4 (cheaper to convert on the tensor-core path).  A batch
+// splits every sequence as its longest, so short sequences' CTAs idle while long
+// ones finish (8 sequences of 4K-16K, INT8: 148 us at 4 tokens against 123 on
+// the decode kernel, 153 against 175 at 6; 64 sequences of 0.5K-8K: 407 against
+// 483 at 6): 6 tokens, 4 for NVFP4.  The key splits of that launch come from
+// pick_key_splits with the block table's width as the context.
 // 0: the call stays on the decode kernel.
 constexpr int kVerifyLongPages = 1024;
 
-int verify_route_min_tokens(int format, int64_t max_pages) {
-  return (max_pages >= kVerifyLongPages ? 4 : 6) - (format == KVQ_FMT_NVFP4 ? 1 : 0);
+int verify_route_min_tokens(int format, int32_t nseq, int64_t max_pages) {
+  const bool nv = format == KVQ_FMT_NVFP4;
+  if (nseq == 1 && max_pages >= kVerifyLongPages) return nv ? 3 : 4;
+  return nv ? (nseq == 1 ? 5 : 4) : 6;
 }
 
 // sms <= 0: the current device's SM count.
 int verify_route_splits(const kvq_cache* cache, int32_t nseq, int32_t q_len, int32_t num_q_heads, int32_t max_pages,
                         int32_t sms) {
-  if (nseq != 1 || num_q_heads % cache->num_kv_heads) return 0;
-  if (q_len < verify_route_min_tokens(cache->format, max_pages)) return 0;
+  if (nseq < 1 || num_q_heads % cache->num_kv_heads) return 0;
+  if (q_len < verify_route_min_tokens(cache->format, nseq, max_pages)) return 0;
   const int64_t G = num_q_heads / cache->num_kv_heads;
   kvq::PrefillInstance inst;
   if (!kvq::prefill_tc_instance(cache->format, cache->head_dim, &inst)) return 0;
@@ -245,8 +252,9 @@ int verify_route_splits(const kvq_cache* cache, int32_t nseq, int32_t q_len, int
   if (sms <= 0 && (cudaGetDevice(&dev) != cudaSuccess ||
                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess))
     return 0;
-  const int64_t items = ((int64_t)q_len * G + inst.rows - 1) / inst.rows * cache->num_kv_heads;
-  return static_cast<int>(pick_key_splits(items, max_pages, (int64_t)q_len * num_q_heads * cache->head_dim * 4, sms));
+  const int64_t items = (int64_t)nseq * (((int64_t)q_len * G + inst.rows - 1) / inst.rows) * cache->num_kv_heads;
+  return static_cast<int>(
+      pick_key_splits(items, max_pages, (int64_t)nseq * q_len * num_q_heads * cache->head_dim * 4, sms));
 }
 
 }  // namespace
@@ -568,7 +576,7 @@ size_t kvq_verify_workspace_bytes(const kvq_cache* cache, int32_t batch, int32_t
   const int S = verify_route_splits(cache, batch, q_len, num_q_heads, 1 << 20, target_ctas);
   succeed();
   if (S <= 0) return decode_need;
-  return std::max(decode_need, kvq_prefill_workspace_bytes(q_len, num_q_heads, cache->head_dim, S));
+  return std::max(decode_need, kvq_prefill_workspace_bytes(batch * q_len, num_q_heads, cache->head_dim, S));
 }
 
 int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_heads, int32_t head_dim,
@@ -587,13 +595,13 @@ int kvq_workspace_partials(void* workspace, int32_t total_splits, int32_t num_q_
 namespace {
 
 // The tensor-core prefill launch (and its merge) once every argument has been
-// checked: q_len query tokens of one sequence, the sequence length from the host
-// (seq_len) or, when seq_len_dev is not null, read by the kernel from device
-// memory (a verify call).
-int prefill_launch(const kvq_cache* cache, const void* q, int32_t q_len, int32_t num_q_heads, float sm_scale,
-                   const int32_t* block_table, int32_t max_pages, int32_t seq_len, const int32_t* seq_len_dev,
-                   int32_t splits, void* workspace, void* out, int32_t out_dtype, float* lse_out, uint32_t flags,
-                   void* stream) {
+// checked: q_len query tokens of each of `batch` sequences (block_table
+// [batch][max_pages]), the length from the host (seq_len, batch 1) or, when
+// seq_len_dev is not null, read by the kernel from device memory (a verify call).
+int prefill_launch(const kvq_cache* cache, const void* q, int32_t batch, int32_t q_len, int32_t num_q_heads,
+                   float sm_scale, const int32_t* block_table, int32_t max_pages, int32_t seq_len,
+                   const int32_t* seq_len_dev, int32_t splits, void* workspace, void* out, int32_t out_dtype,
+                   float* lse_out, uint32_t flags, void* stream) {
   const int D = cache->head_dim;
   const int G = num_q_heads / cache->num_kv_heads;
   kvq::PrefillInstance inst;
@@ -630,13 +638,14 @@ int prefill_launch(const kvq_cache* cache, const void* q, int32_t q_len, int32_t
   p.v_codes = static_cast<const uint8_t*>(cache->v_codes);
   p.k_scales = static_cast<const uint8_t*>(cache->k_scales);
   p.v_scales = static_cast<const uint8_t*>(cache->v_scales);
-  const size_t rows = splits > 1 ? (size_t)q_len * splits * num_q_heads : 0;
+  const size_t rows = splits > 1 ? (size_t)batch * q_len * splits * num_q_heads : 0;
   char* ws = static_cast<char*>(workspace);
   p.status = reinterpret_cast<int32_t*>(ws);
   p.lse_part = reinterpret_cast<float*>(ws + 256);
   p.o_part = reinterpret_cast<float*>(ws + 256 + align256(rows * sizeof(float)));
   p.out = out;
   p.lse_out = lse_out;
+  p.batch = batch;
   p.q_len = q_len;
   p.seq_len = seq_len;
   p.seq_len_dev = seq_len_dev;
@@ -651,13 +660,13 @@ int prefill_launch(const kvq_cache* cache, const void* q, int32_t q_len, int32_t
   p.k_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->k_global_scale : 1.0f;
   p.v_gs_inv = cache->format == KVQ_FMT_NVFP4 ? 1.0f / cache->v_global_scale : 1.0f;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t grid = (int64_t)p.row_blocks * cache->num_kv_heads * splits;
+  const int64_t grid = (int64_t)batch * p.row_blocks * cache->num_kv_heads * splits;
   if (grid > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "grid too large");
   cudaError_t e = kvq::launch_prefill_tc(cache->format, D, p, static_cast<int>(grid), st);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   if (splits > 1) {
-    e = kvq::launch_merge(p.o_part, p.lse_part, nullptr, splits, q_len, num_q_heads, D, out, p.out_bf16, lse_out,
-                          false, st);
+    e = kvq::launch_merge(p.o_part, p.lse_part, nullptr, splits, batch * q_len, num_q_heads, D, out, p.out_bf16,
+                          lse_out, false, st);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (flags & KVQ_CHECKED) {
@@ -767,13 +776,13 @@ int decode_impl(const kvq_cache* cache, const void* q, int32_t nseq, int32_t q_l
   if (rc) return rc;
   rc = memory_kind(out, "out", &out_host);
   if (rc) return rc;
-  // one sequence, enough query tokens: the tensor-core prefill kernel (the plan was
-  // checked above all the same, so a call is accepted or refused alike on both paths)
+  // enough query tokens: the tensor-core prefill kernel (the plan was checked
+  // above all the same, so a call is accepted or refused alike on both paths)
   if (!clear_status && !q_host && !out_host && !(flags & (KVQ_SKIP_MERGE | KVQ_TEST_STALL))) {
     const int S = verify_route_splits(cache, nseq, q_len, num_q_heads, max_pages_per_seq, 0);
-    if (S > 0 && workspace_bytes >= kvq_prefill_workspace_bytes(q_len, num_q_heads, D, S))
-      return prefill_launch(cache, q, q_len, num_q_heads, sm_scale, block_tables, max_pages_per_seq, 0, seq_lens, S,
-                            workspace, out, out_dtype, lse_out, flags, stream);
+    if (S > 0 && workspace_bytes >= kvq_prefill_workspace_bytes(nseq * q_len, num_q_heads, D, S))
+      return prefill_launch(cache, q, nseq, q_len, num_q_heads, sm_scale, block_tables, max_pages_per_seq, 0,
+                            seq_lens, S, workspace, out, out_dtype, lse_out, flags, stream);
   }
   kvq::DecodeInstance inst;
   rc = prepare_instance(cache->format, D, &inst);
@@ -931,7 +940,7 @@ int kvq_paged_prefill_attention(const kvq_cache* cache, const void* q, int32_t q
   if (workspace_bytes < need) return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   rc = memory_kind(out, "out", nullptr);
   if (rc) return rc;
-  return prefill_launch(cache, q, q_len, num_q_heads, sm_scale, block_table, max_pages, seq_len, nullptr, splits,
+  return prefill_launch(cache, q, 1, q_len, num_q_heads, sm_scale, block_table, max_pages, seq_len, nullptr, splits,
                         workspace, out, out_dtype, lse_out, flags, stream);
 }
 

@@ -36,19 +36,19 @@ struct DecodeParams {
 };
 
 struct PrefillParams {
-  const void* q;               // bf16 [q_len][Hq][D]
-  const int32_t* block_table;  // [max_pages] of the sequence
+  const void* q;               // bf16 [batch][q_len][Hq][D]
+  const int32_t* block_table;  // [batch][max_pages]
   const uint8_t* k_codes;      // pool code arrays [num_pages][Hkv][16][row bytes]
   const uint8_t* v_codes;
   const uint8_t* k_scales;     // pool scale arrays (INT8)
   const uint8_t* v_scales;
-  float* o_part;               // [q_len * splits][Hq][D] (splits > 1)
-  float* lse_part;             // [q_len * splits][Hq]
-  void* out;                   // [q_len][Hq][D] f32 or bf16 (splits == 1)
-  float* lse_out;              // [q_len][Hq] or null
+  float* o_part;               // [batch * q_len * splits][Hq][D] (splits > 1)
+  float* lse_part;             // [batch * q_len * splits][Hq]
+  void* out;                   // [batch][q_len][Hq][D] f32 or bf16 (splits == 1)
+  float* lse_out;              // [batch][q_len][Hq] or null
   int32_t* status;             // device status word
-  const int32_t* seq_len_dev;  // device [1]: the sequence length, read by the kernel (null: seq_len)
-  int32_t q_len, seq_len, num_q_heads, num_kv_heads, num_pages, max_pages;
+  const int32_t* seq_len_dev;  // device [batch]: the sequence lengths, read by the kernel (null: seq_len, batch 1)
+  int32_t batch, q_len, seq_len, num_q_heads, num_kv_heads, num_pages, max_pages;
   int32_t splits, row_blocks, out_bf16;
   float sm_scale_log2;
   float k_gs_inv, v_gs_inv;    // NVFP4: 1 / global scales (1 otherwise)

@@ -8,10 +8,12 @@
 //
 // The chunk's T tokens are the last T entries of one sequence's cache (L tokens
 // in all); query token i sits at position L - T + i and sees tokens 0 .. L-T+i.
+// A launch covers one chunk, or (a verify call) T tokens of each of a batch of
+// sequences, each with its own block-table row and its length read on the device.
 //
-// Work item (one CTA): 128 query rows (token, query head) of one KV head — the
-// MMA's M — against one key range (a split; splits are merged by the merge
-// kernel), in tiles of 64 keys (four pages).  Warp roles:
+// Work item (one CTA): 128 query rows (token, query head) of one KV head of one
+// sequence — the MMA's M — against one key range (a split; splits are merged by
+// the merge kernel), in tiles of 64 keys (four pages).  Warp roles:
 //   * warps 4..7 (converters): per tile, K codes -> fp16 (NVFP4: codes x group
 //     scale, exact in fp16; INT8: the codes) in the canonical K-major
 //     layout with the 128-byte swizzle (the B operand of S = Q K^T) and V codes
@@ -140,23 +142,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // and the TMEM are set up while that kernel drains, and nothing it may write
   // (q, the block table, the sequence length, the pool) is read before it completes.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the sequence length: from the launch, or (a verify call) from device memory,
-  // clamped to the block table (an out-of-range value is flagged)
-  int seq_len = p.seq_len;
-  if (p.seq_len_dev) {
-    seq_len = *p.seq_len_dev;
-    if (seq_len < 0 || seq_len > p.max_pages * kPage) {
-      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
-      seq_len = seq_len < 0 ? 0 : p.max_pages * kPage;
-    }
-  }
-  const int G = p.num_q_heads / p.num_kv_heads;
-  const int TG = p.q_len * G;
+  // work item: (sequence b, row block rb, KV head h, key split s), split fastest
   const int it = blockIdx.x;
   const int s = it % p.splits;
   const int rest = it / p.splits;
   const int h = rest % p.num_kv_heads;
-  const int rb = p.row_blocks - 1 - rest / p.num_kv_heads;  // heaviest row blocks first
+  const int rest2 = rest / p.num_kv_heads;
+  const int rb = p.row_blocks - 1 - rest2 % p.row_blocks;  // heaviest row blocks first
+  const int b = rest2 / p.row_blocks;
+  // the sequence length: from the launch, or (a verify call) from device memory,
+  // clamped to the block table (an out-of-range value is flagged once a sequence)
+  int seq_len = p.seq_len;
+  if (p.seq_len_dev) {
+    seq_len = p.seq_len_dev[b];
+    if (seq_len < 0 || seq_len > p.max_pages * kPage) {
+      if (threadIdx.x == 0 && s == 0 && h == 0 && rb == p.row_blocks - 1) atomicOr(p.status, KVQ_DEV_BAD_SEQLEN);
+      seq_len = seq_len < 0 ? 0 : p.max_pages * kPage;
+    }
+  }
+  const int32_t* btab = p.block_table + (size_t)b * p.max_pages;  // this sequence's block table
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int TG = p.q_len * G;
+  const size_t tok_base = (size_t)b * p.q_len;  // the sequence's first query token in q, out and the partials
   const int row0 = rb * kTcRows;
   const int last_tok = min(p.q_len - 1, (row0 + kTcRows - 1) / G);
   const int kmax = seq_len - p.q_len + last_tok + 1;  // keys the block's last row sees
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int jp = i * kTcPages + (n >> 4);  // page of the range
       const int tok = (pg0 + jp) * kPage + (n & 15);
       if (jp >= npg || tok >= key_end) return -1;
-      return p.block_table[pg0 + jp];
+      return btab[pg0 + jp];
     };
     auto row_from = [&](int i, int pg) -> int64_t {
       const int jp = i * kTcPages + (n >> 4);
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     {
       const uint4* qrow =
           reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                         ((size_t)ti * p.num_q_heads + h * G + g) * D);
+                                         ((tok_base + ti) * p.num_q_heads + h * G + g) * D);
       float up = 1.f;
       if constexpr (!kBf16) {
         float amax = 0.f;
@@ -595,7 +602,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float lse = any ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     const bool direct = p.splits == 1;
     const size_t qh = (size_t)h * G + g;
-    const size_t orow = direct ? (size_t)ti * p.num_q_heads + qh : ((size_t)ti * p.splits + s) * p.num_q_heads + qh;
+    const size_t orow =
+        direct ? (tok_base + ti) * p.num_q_heads + qh : ((tok_base + ti) * p.splits + s) * p.num_q_heads + qh;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t ov[32];

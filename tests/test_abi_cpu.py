@@ -272,10 +272,11 @@ def test_prefill_split_choice_and_workspace(kvq):
 
 
 def test_verify_workspace_covers_the_tensor_core_route(kvq):
-    """A one-sequence verify call with 4+ query tokens (3+ for NVFP4) may take the
-    prefill kernel with the key splits kvq_prefill_splits picks (at most 64; the
-    workspace is sized for the longest context): its workspace covers both
-    routes; any other call needs the decode workspace."""
+    """A verify call with 4+ query tokens a sequence (3+ for NVFP4) may take the
+    prefill kernel, one launch for the batch, with the key splits
+    kvq_prefill_splits picks (at most 64; the workspace is sized for the longest
+    context): its workspace covers both routes; any other call needs the decode
+    workspace."""
     s = _struct(kvq)  # INT8, Hkv = 4, D = 256
     dec = kvq.kvq_decode_workspace_bytes
     pre = kvq.kvq_prefill_workspace_bytes
@@ -283,7 +284,8 @@ def test_verify_workspace_covers_the_tensor_core_route(kvq):
     # 6 tokens x 6 heads = 36 rows: one row block a KV head, 4 items -> 38 splits
     assert vws(s, 1, 6, 24, 40) == max(dec(40, 24, 256), pre(6, 24, 256, 38)) == pre(6, 24, 256, 38)
     assert vws(s, 1, 6, 24, 4000) == dec(4000, 24, 256)  # a wide decode plan needs more
-    assert vws(s, 2, 6, 24, 40) == dec(40, 24, 256)  # two sequences: the decode kernel
+    assert vws(s, 2, 6, 24, 40) == pre(12, 24, 256, 19)  # two sequences: one launch, 8 CTAs a split
+    assert vws(s, 2, 5, 24, 40) == dec(40, 24, 256)  # a batch: 6 INT8 tokens a sequence at least
     assert vws(s, 1, 4, 24, 40) == pre(4, 24, 256, 38)  # 4 tokens: routed on a long context
     assert vws(s, 1, 3, 24, 40) == dec(40, 24, 256)  # 3 INT8 tokens: the decode kernel
     assert vws(s, 1, 43, 24, 43) == max(dec(43, 24, 256), pre(43, 24, 256, 38))  # 258 rows: 12 CTAs a split
@@ -292,6 +294,8 @@ def test_verify_workspace_covers_the_tensor_core_route(kvq):
     nv = _struct(kvq, fmt="nvfp4")
     assert vws(nv, 1, 3, 24, 40) == pre(3, 24, 256, 38)  # NVFP4 from 3 tokens
     assert vws(nv, 1, 2, 24, 40) == dec(40, 24, 256)
+    assert vws(nv, 3, 3, 24, 40) == dec(40, 24, 256)  # a batch: 4 NVFP4 tokens a sequence at least
+    assert vws(nv, 3, 4, 24, 40) > dec(40, 24, 256)
     g32 = _struct(kvq, fmt="int8_g32")  # no prefill kernel: the decode kernel
     assert vws(g32, 1, 6, 24, 40) == dec(40, 24, 256)
     with pytest.raises(kvq.KvqError):

@@ -1,6 +1,7 @@
-"""Verify calls of one sequence with enough query tokens (6 on a block table
-under 1,024 pages, 4 from there on, one fewer for NVFP4) run on the tensor-core
-prefill kernel, with the sequence length read on the device.  Checked against the float64 oracle's paged_verify (max-abs
+"""Verify calls with enough query tokens a sequence (6 on a block table under
+1,024 pages, 4 from there on, one fewer for NVFP4) run on the tensor-core
+prefill kernel, one launch for the whole batch, with the sequence lengths read
+on the device.  Checked against the float64 oracle's paged_verify (max-abs
 2e-3 for fp32 output, 1e-2 or half a bf16 ulp for bf16 output), against the same
 call kept on the decode kernel by a workspace too small for the route, through a
 CUDA graph, and for the flag the kernel raises when the device length runs past
@@ -36,7 +37,7 @@ class _Call:
         self.out = torch.full((wl.B, T, wl.Hq, wl.D), float("nan"), dtype=od, device="cuda")
         self.lse = torch.full((wl.B, T, wl.Hq), float("nan"), device="cuda")
         self.bt = torch.from_numpy(wl.block_tables).cuda()
-        lens = wl.seq_lens if seq_len is None else np.array([seq_len], np.int32)
+        lens = wl.seq_lens if seq_len is None else np.array(np.atleast_1d(seq_len), np.int32)
         self.sl = torch.from_numpy(lens).cuda()
 
     def launch(self, workspace=None, checked=True):
@@ -188,3 +189,57 @@ def test_routed_verify_32k_sampled(fmt, T):
     out, lse = c.run()
     units = [(0, i, h) for i in (0, T // 2, T - 1) for h in (0, 3)]
     _compare(wl, fmt, T, out, lse, gs, units=units)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
+@pytest.mark.parametrize("T", [6, 22])
+def test_batched_routed_verify_matches_the_oracle(fmt, T):
+    """Four sequences in one launch: lengths 5 to 5,000 (one shorter than T, ragged
+    last pages, a block table wider than most of them)."""
+    wl = W.make("tiny_int8", lens=("list", [700, 5, 5000, 1300]), seed=57)
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, T, gs)
+    out, lse = c.run()
+    _compare(wl, fmt, T, out, lse, gs)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_batched_route_and_decode_kernel_agree_d128_bf16_output(fmt):
+    """Three sequences of the serving shape (4 query heads a KV head, D = 128), bf16
+    output: both kernels within the oracle's tolerance, and the route was taken."""
+    wl = W.make("serving_int8", lens=("list", [300, 2500, 1000]), seed=58)
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, 8, gs, out_dtype="bf16", split=1)
+    routed = c.run()
+    kept = c.run(c.decode_only_workspace())
+    _compare(wl, fmt, 8, routed[0], routed[1], gs, out_dtype="bf16")
+    _compare(wl, fmt, 8, kept[0], kept[1], gs, out_dtype="bf16")
+    assert not np.array_equal(routed[0], kept[0])
+
+
+def test_batched_bad_device_length_is_flagged():
+    """One of two sequences has a device length past the block table: flagged, and
+    every read stays inside the table (clamped)."""
+    from quantized_paged_kv_gb300 import _binding as B
+
+    wl = W.make("tiny_int8", lens=("list", [700, 400]), seed=59)
+    width = wl.block_tables.shape[1]
+    c = _Call(wl, "int8", 6, seq_len=[700, width * 16 + 40])
+    c.run(checked=False)
+    rc, bits = B.kvq_read_status(c.plan.workspace, None)
+    assert rc != 0 and bits & B.KVQ_DEV_BAD_SEQLEN
+
+
+@pytest.mark.parametrize("fmt,T,routed", [("int8", 5, False), ("int8", 6, True), ("nvfp4", 3, False), ("nvfp4", 4, True)])
+def test_batch_token_threshold(fmt, T, routed):
+    """Two sequences: 6 query tokens a sequence take the tensor-core kernel (4 for
+    NVFP4), fewer stay on the decode kernel; either way within the oracle's
+    tolerance, and the route decides whether the bits differ from the decode
+    kernel's."""
+    wl = W.make("tiny_int8", lens=("list", [1500, 900]), seed=60)
+    gs = H.global_scales(wl, fmt)
+    c = _Call(wl, fmt, T, gs, split=1)
+    auto = c.run()
+    kept = c.run(c.decode_only_workspace())
+    _compare(wl, fmt, T, auto[0], auto[1], gs)
+    assert np.array_equal(auto[0], kept[0]) != routed
