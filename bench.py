@@ -952,6 +952,16 @@ def sweep(args, dev, l2, peak, peak_tf=1937.0):
     del ls
     gc.collect()
     torch.cuda.empty_cache()
+    # a batch: the 8 sequences of 4K..16K of the append workload, 4 and 6 tokens a
+    # sequence (the batch takes the tensor-core route from 6)
+    wl = W.make("append_int8")
+    per_layer = int(wl.seq_lens.sum()) * kvq.kvq_bytes_per_token("int8", wl.Hkv, wl.D)
+    ls = LayerSet(wl, "int8", layers_for(per_layer, l2, floor=2), dev)
+    for T in (4, 6, 8):
+        res[f"verify_append_int8/T={T}"] = time_verify(ls, T, steps)
+    del ls
+    gc.collect()
+    torch.cuda.empty_cache()
     # prefill: a 2,048-token chunk at the end of the 32K context (and the first chunk)
     wl = W.make("long_int8")
     for fmt, Ts in (("int8", (512, 2048)), ("nvfp4", (2048,))):
