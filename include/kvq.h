@@ -44,7 +44,9 @@
  *   - Errors found on the device (an out-of-range page id or slot, a bounded
  *     wait that ran out) never fault or trap: the kernel skips the access, sets a
  *     bit in a device status word and finishes.  KVQ_CHECKED reads that word
- *     before returning; raw callers read it with kvq_read_status().
+ *     before returning; raw callers read it with kvq_read_status().  The tokens of
+ *     a page with an out-of-range id are left out of the softmax by every
+ *     attention kernel (decode, verify on either kernel, prefill).
  */
 #ifndef KVQ_H
 #define KVQ_H

@@ -52,7 +52,9 @@ struct TcLayout {
   static constexpr int kVAt = kKAt + 2 * kKBytes;        // two V tiles
   static constexpr int kScRing = 3;                      // scale buffers (tiles in flight)
   static constexpr int kScAt = kVAt + 2 * kVBytes;       // float k scales [3][64], v scales [3][64]
-  static constexpr int kBarAt = kScAt + 2 * kScRing * kTcKeys * 4;
+  // key-validity masks: uint16 [3][4 converter warps], bit k = key 16 w + k read
+  static constexpr int kMaskAt = kScAt + 2 * kScRing * kTcKeys * 4;
+  static constexpr int kBarAt = kMaskAt + 32;
   static constexpr int kNumBars = 14;
   static constexpr int kSlotAt = kBarAt + kNumBars * 8;
   static constexpr int kSmemBytes = 1024 + kSlotAt + 16;
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Lo::kSlotAt);  // [0] TMEM base, [1] abort flag
   float* ksc = reinterpret_cast<float*>(smem + Lo::kScAt);            // [3][64]
   float* vsc = ksc + Lo::kScRing * kTcKeys;                           // [3][64]
+  uint16_t* kmask = reinterpret_cast<uint16_t*>(smem + Lo::kMaskAt);  // [3][4]
   const uint32_t sbase = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -366,6 +369,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // K buffer i & 1 is free once S(i-2) is done
       if (i > 1 && !wait_warp(kBarKF0 + (i & 1), ((i - 2) >> 1) & 1)) return false;
+      {
+        // which of the warp's 16 keys were read (a bad page id or a key past the
+        // range is not): the softmax leaves the others out, as the decode does
+        uint32_t m = __ballot_sync(0xffffffffu, ro >= 0) & 0x55555555u;  // half 0 lanes: one bit a key
+        m = (m | (m >> 1)) & 0x33333333u;
+        m = (m | (m >> 2)) & 0x0F0F0F0Fu;
+        m = (m | (m >> 4)) & 0x00FF00FFu;
+        m = (m | (m >> 8)) & 0x0000FFFFu;
+        if (lane == 0) kmask[(i % Lo::kScRing) * 4 + (warp - 4)] = static_cast<uint16_t>(m);
+      }
       if constexpr (FMT == KVQ_FMT_INT8) {
         // both scales of the tile go out with K: the softmax reads them once S is
         // done.  Ring of three: the last reader of this slot, the softmax of tile
@@ -481,7 +494,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float* vs = vsc + (i % Lo::kScRing) * kTcKeys;
       // pass 1: z = S x kfac (the logit before the row factor rs > 0) and the tile
       // maximum (four independent chains); only a tile that crosses the row's
-      // limit is masked
+      // limit, or holds keys that were not read (a bad page id), is masked
+      const uint64_t km = *reinterpret_cast<const uint64_t*>(kmask + (i % Lo::kScRing) * 4);
       float z[kTcKeys];
 #pragma unroll
       for (int t = 0; t < kTcKeys; ++t) z[t] = __uint_as_float(sv[t >> 5][t & 31]);
@@ -501,6 +515,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (nvis < kTcKeys) zz = t < nvis ? zz : -INFINITY;
           z[t] = zz;
           mxs[e] = fmaxf(mxs[e], zz);
+        }
+      }
+      if (km != ~0ull) {  // keys that were not read (the same for the whole tile): out, and the maximum again
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mxs[e] = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < kTcKeys; ++t) {
+          if (!((km >> t) & 1ull)) z[t] = -INFINITY;
+          mxs[t & 3] = fmaxf(mxs[t & 3], z[t]);
         }
       }
       const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * rs;  // log2 units

@@ -243,3 +243,47 @@ def test_batch_token_threshold(fmt, T, routed):
     kept = c.run(c.decode_only_workspace())
     _compare(wl, fmt, T, auto[0], auto[1], gs)
     assert np.array_equal(auto[0], kept[0]) != routed
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4", "bf16"])
+def test_routed_raw_mode_bad_page_ids_contribute_nothing(fmt):
+    """Raw mode on the tensor-core route: block-table entries outside the pool are
+    flagged and their pages' tokens are left out of the softmax, as on the decode
+    kernel (the pool is sentinel-filled, so a page read anyway would show); each
+    query token's result equals the oracle's attention over its visible tokens
+    without those pages, and a token that sees only bad pages gives 0 and -inf."""
+    from oracle import layout as olay
+    from quantized_paged_kv_gb300 import _binding as B
+
+    wl = W.make("tiny_int8", lens=("list", [700, 64, 300]), seed=61)
+    gs = H.global_scales(wl, fmt)
+    T = 6
+    c = _Call(wl, fmt, T, gs)
+    drop = {0: [0, 5, 43], 1: [0, 1, 2, 3], 2: [18]}  # sequence 1: every page; sequence 2: the last
+    bad = wl.block_tables.copy()
+    for b, js in drop.items():
+        for j in js:
+            bad[b, j] = wl.num_pages + 7 + j
+    c.bt = torch.from_numpy(bad).cuda()
+    out, lse = c.run(checked=False)
+    rc, bits = B.kvq_read_status(c.plan.workspace, None)
+    assert rc != 0 and bits == B.KVQ_DEV_BAD_PAGE
+    pools = H.oracle_pools(wl, fmt, gs)
+    q = wl.q_tokens(T)
+    G = wl.Hq // wl.Hkv
+    for b in range(wl.B):
+        L = int(wl.seq_lens[b])
+        for i in range(T):
+            vis = max(0, L - T + 1 + i)
+            keep = np.array([t for t in range(vis) if t // 16 not in drop[b]], dtype=np.int64)
+            slots = olay.token_slots(wl.block_tables[b], vis, 16)[keep]
+            for h in range(wl.Hkv):
+                k = oatt.cache_rows(fmt, pools["k_codes"], pools.get("k_scales"), slots, h, gs[0])
+                v = oatt.cache_rows(fmt, pools["v_codes"], pools.get("v_scales"), slots, h, gs[1])
+                ro, rl = oatt.attend(q[b, i, h * G:(h + 1) * G], k, v, wl.sm_scale)
+                rows = slice(h * G, (h + 1) * G)
+                assert np.all(np.abs(out[b, i, rows] - ro) <= H.bound("f32", ro)), (fmt, b, i, h)
+                if len(keep) == 0:
+                    assert np.all(out[b, i, rows] == 0) and np.all(np.isneginf(lse[b, i, rows]))
+                else:
+                    assert np.abs(lse[b, i, rows] - rl).max() < 1e-3
