@@ -225,12 +225,12 @@ int64_t pick_key_splits(int64_t items, int64_t pages, int64_t partial_bytes_per_
 // keys ~9 + 2.6 q_len against ~22 us).  The query-token threshold therefore
 // falls with the context, known on the host only through the block table's
 // width: for one sequence 4 tokens from 1,024 pages (16K tokens) up, 6 below,
-// one fewer for NVFP4 (cheaper to convert on the tensor-core path).  A batch
-// splits every sequence as its longest, so short sequences' CTAs idle while long
-// ones finish (8 sequences of 4K-16K, INT8: 148 us at 4 tokens against 123 on
-// the decode kernel, 153 against 175 at 6; 64 sequences of 0.5K-8K: 407 against
-// 483 at 6): 6 tokens, 4 for NVFP4.  The key splits of that launch come from
-// pick_key_splits with the block table's width as the context.
+// one fewer for NVFP4 (cheaper to convert on the tensor-core path).  For a batch
+// the crossover comes later (8 sequences of 4K-16K, INT8: 148 us at 4 tokens
+// against 123 on the decode kernel, 153 against 175 at 6; 64 sequences of
+// 0.5K-8K: 407 against 483 at 6): 6 tokens, 4 for NVFP4.  The key splits of
+// that launch come from pick_key_splits with the block table's width as the
+// context.
 // 0: the call stays on the decode kernel.
 constexpr int kVerifyLongPages = 1024;
 
