@@ -18,8 +18,10 @@
 //     scale, exact in fp16; INT8: the codes) in the canonical K-major
 //     layout with the 128-byte swizzle (the B operand of S = Q K^T) and V codes
 //     -> fp16 in the MN-major layout (the B operand of O = P V, no transpose); the
-//     INT8 scales go to shared memory.  Keys past the range or the sequence are
-//     written as zeros.
+//     INT8 scales go to shared memory.  Keys past the range or the sequence, or
+//     on a page whose id is out of the pool, are written as zeros, and a per-tile
+//     mask of the keys read goes out with the scales: the softmax leaves the
+//     others out, as the decode kernel does.
 //   * warp 8, lane 0 (MMA): S(i) = Q K(i)^T into one of two TMEM buffers, then
 //     O += P(i-1) V(i-1); each group of MMAs is committed to an mbarrier.
 //   * warps 0..3 (softmax, one query row a thread): the q row (INT8: scaled by a
