@@ -248,16 +248,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // pool row of key n of tile i (-1: a key past the range or the sequence, or a
     // bad page id), in two steps so that the block-table read can run ahead:
     // page_of(i) reads the page id, row_from(i, id) validates it
-    auto page_of = [&](int i) -> int {
+    auto in_range = [&](int i) {  // key n of tile i lies in the range and the sequence
       const int jp = i * kTcPages + (n >> 4);  // page of the range
-      const int tok = (pg0 + jp) * kPage + (n & 15);
-      if (jp >= npg || tok >= key_end) return -1;
-      return btab[pg0 + jp];
+      return jp < npg && (pg0 + jp) * kPage + (n & 15) < key_end;
     };
+    auto page_of = [&](int i) -> int { return in_range(i) ? btab[pg0 + i * kTcPages + (n >> 4)] : -1; };
     auto row_from = [&](int i, int pg) -> int64_t {
-      const int jp = i * kTcPages + (n >> 4);
-      const int tok = (pg0 + jp) * kPage + (n & 15);
-      if (jp >= npg || tok >= key_end) return -1;
+      if (!in_range(i)) return -1;
       if (pg < 0 || pg >= p.num_pages) {
         if (half == 0 && (n & 15) == 0) atomicOr(p.status, KVQ_DEV_BAD_PAGE);
         return -1;
@@ -331,6 +328,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr bool kVAhead = !kAhead && kChunks <= 8;  // V alone a tile ahead
     uint4 rk0[kChunks], rv0[kChunks], rk1[kAhead ? kChunks : 1], rv1[(kAhead || kVAhead) ? kChunks : 1];
     int64_t ro = nt > 0 ? row_from(0, page_of(0)) : -1;
+    // every key-mask entry of this warp starts full (published with K(0))
+    uint32_t partial_slots = 0;  // ring slots whose entry holds a partial mask
+    if (lane == 0)
+      for (int sl = 0; sl < Lo::kScRing; ++sl) kmask[sl * 4 + (warp - 4)] = 0xFFFFu;
     int pg_next = nt > 1 ? page_of(1) : -1;  // page id of tile i + 1
     if (nt > 0) {
       load(p.k_codes, ro, rk0);
@@ -372,14 +373,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // K buffer i & 1 is free once S(i-2) is done
       if (i > 1 && !wait_warp(kBarKF0 + (i & 1), ((i - 2) >> 1) & 1)) return false;
       {
-        // which of the warp's 16 keys were read (a bad page id or a key past the
-        // range is not): the softmax leaves the others out, as the decode does
-        uint32_t m = __ballot_sync(0xffffffffu, ro >= 0) & 0x55555555u;  // half 0 lanes: one bit a key
-        m = (m | (m >> 1)) & 0x33333333u;
-        m = (m | (m >> 2)) & 0x0F0F0F0Fu;
-        m = (m | (m >> 4)) & 0x00FF00FFu;
-        m = (m | (m >> 8)) & 0x0000FFFFu;
-        if (lane == 0) kmask[(i % Lo::kScRing) * 4 + (warp - 4)] = static_cast<uint16_t>(m);
+        // keys on a page whose id is out of the pool (keys past the range are cut
+        // by the rows' limits): the softmax leaves them out, as the decode does.
+        // A warp rewrites its mask entry only for such a tile, and once after it.
+        const bool bad = ro < 0 && in_range(i);
+        const int slot = i % Lo::kScRing;
+        if (__any_sync(0xffffffffu, bad)) {
+          uint32_t m = __ballot_sync(0xffffffffu, !bad) & 0x55555555u;  // half 0 lanes: one bit a key
+          m = (m | (m >> 1)) & 0x33333333u;
+          m = (m | (m >> 2)) & 0x0F0F0F0Fu;
+          m = (m | (m >> 4)) & 0x00FF00FFu;
+          m = (m | (m >> 8)) & 0x0000FFFFu;
+          if (lane == 0) kmask[slot * 4 + (warp - 4)] = static_cast<uint16_t>(m);
+          partial_slots |= 1u << slot;
+        } else if (partial_slots & (1u << slot)) {
+          if (lane == 0) kmask[slot * 4 + (warp - 4)] = 0xFFFFu;
+          partial_slots &= ~(1u << slot);
+        }
       }
       if constexpr (FMT == KVQ_FMT_INT8) {
         // both scales of the tile go out with K: the softmax reads them once S is
