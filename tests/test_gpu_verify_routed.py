@@ -287,3 +287,27 @@ def test_routed_raw_mode_bad_page_ids_contribute_nothing(fmt):
                     assert np.all(out[b, i, rows] == 0) and np.all(np.isneginf(lse[b, i, rows]))
                 else:
                     assert np.abs(lse[b, i, rows] - rl).max() < 1e-3
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_routed_verify_equals_the_prefill_call(fmt):
+    """One sequence whose block table is exactly as wide as its pages: the routed
+    verify call and kvq_paged_prefill_attention of the same tokens pick the same
+    key splits and run the same kernel, so their outputs are the same bits."""
+    from quantized_paged_kv_gb300 import _binding as B
+    from quantized_paged_kv_gb300 import prefill
+
+    wl = W.make("tiny_int8", lens=("list", [700]), seed=62)
+    assert wl.block_tables.shape[1] == -(-700 // 16)
+    gs = H.global_scales(wl, fmt)
+    T = 8
+    c = _Call(wl, fmt, T, gs)
+    out_v, lse_v = c.run()
+    S = B.kvq_prefill_splits(c.cache.struct, T, wl.Hq, 700)
+    out_p = torch.full((T, wl.Hq, wl.D), float("nan"), device="cuda")
+    lse_p = torch.full((T, wl.Hq), float("nan"), device="cuda")
+    prefill(c.cache, c.qt[0].contiguous(), c.bt[0].contiguous(), 700, out_p, wl.sm_scale, lse_out=lse_p, splits=S,
+            checked=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(out_v[0], out_p.cpu().numpy())
+    assert np.array_equal(lse_v[0], lse_p.cpu().numpy())
