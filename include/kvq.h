@@ -347,7 +347,10 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
  * width as the context.  This happens when q and out are device memory, neither
  * KVQ_SKIP_MERGE nor KVQ_TEST_STALL is set and the workspace holds
  * kvq_verify_workspace_bytes; the plan is still required (and checked under
- * KVQ_CHECKED), and the result is the same up to rounding order.
+ * KVQ_CHECKED), and the result is the same up to rounding order.  With q_len
+ * the length of a prompt chunk, the call is a chunked prefill of the same number
+ * of tokens for every sequence of a batch (kvq_paged_prefill_attention takes
+ * one sequence).
  *   q              device bf16 [batch][q_len][num_q_heads][head_dim]
  *   seq_lens       device int32 [batch]: tokens in the cache, the q_len new ones included
  *   plan           kvq_plan_verify_splits(seq_lens, batch, q_len, ...): the plan
