@@ -311,3 +311,17 @@ def test_routed_verify_equals_the_prefill_call(fmt):
     torch.cuda.synchronize()
     assert np.array_equal(out_v[0], out_p.cpu().numpy())
     assert np.array_equal(lse_v[0], lse_p.cpu().numpy())
+
+
+@pytest.mark.parametrize("fmt", ["int8", "nvfp4"])
+def test_verify_entry_as_a_batched_chunked_prefill(fmt):
+    """Two sequences, the last 200 tokens of each as query tokens (1,200 query
+    rows a KV head, ten 128-row blocks): a chunked prefill of a batch through the
+    verify entry, against the oracle on sampled (sequence, token, KV head) units."""
+    wl = W.make("tiny_int8", lens=("list", [900, 1300]), seed=63)
+    gs = H.global_scales(wl, fmt)
+    T = 200
+    c = _Call(wl, fmt, T, gs)
+    out, lse = c.run()
+    units = [(b, i, h) for b in (0, 1) for i in (0, 57, 128, 199) for h in (0, 3)]
+    _compare(wl, fmt, T, out, lse, gs, units=units)
