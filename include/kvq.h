@@ -340,9 +340,9 @@ int kvq_paged_decode_attention(const kvq_cache* cache, const void* q, int32_t ba
  * A call with enough query tokens a sequence goes instead, as one launch for
  * the batch, to the tensor-core kernel of kvq_paged_prefill_attention ([int8-kv]
  * "Read the prompt using a small temporary buffer": a block of query rows reads
- * each key once): q_len >= 4 for one sequence whose block table spans 1,024
- * pages or more, >= 6 otherwise (NVFP4: 3, 5 for one sequence on a shorter
- * table, 4 for a batch).  The kernel reads the sequence lengths on the device
+ * each key once): for one sequence q_len >= 4 when its block table spans
+ * 2,048 pages or more, >= 5 from 1,024, >= 6 from 512, >= 10 below (NVFP4: 3,
+ * 3, 4, 8); for a batch q_len >= 6 (NVFP4: 4).  The kernel reads the sequence lengths on the device
  * and takes the key splits that kvq_prefill_splits picks with the block table's
  * width as the context.  This happens when q and out are device memory, neither
  * KVQ_SKIP_MERGE nor KVQ_TEST_STALL is set and the workspace holds

@@ -224,8 +224,9 @@ int64_t pick_key_splits(int64_t items, int64_t pages, int64_t partial_bytes_per_
 // ~46 us for INT8, ~38 us for NVFP4, whatever q_len up to a 128-row tile; at 8K
 // keys ~9 + 2.6 q_len against ~22 us).  The query-token threshold therefore
 // falls with the context, known on the host only through the block table's
-// width: for one sequence 4 tokens from 1,024 pages (16K tokens) up, 6 below,
-// one fewer for NVFP4 (cheaper to convert on the tensor-core path).  For a batch
+// width: for one sequence 4 tokens from 2,048 pages (32K tokens) up, 5 from
+// 1,024, 6 from 512, 10 below, fewer for NVFP4 (cheaper to convert on the
+// tensor-core path: 3, 3, 4, 8).  For a batch
 // the crossover comes later (8 sequences of 4K-16K, INT8: 148 us at 4 tokens
 // against 123 on the decode kernel, 153 against 175 at 6; 64 sequences of
 // 0.5K-8K: 407 against 483 at 6): 6 tokens, 4 for NVFP4.  The key splits of
@@ -236,8 +237,13 @@ constexpr int kVerifyLongPages = 1024;
 
 int verify_route_min_tokens(int format, int32_t nseq, int64_t max_pages) {
   const bool nv = format == KVQ_FMT_NVFP4;
-  if (nseq == 1 && max_pages >= kVerifyLongPages) return nv ? 3 : 4;
-  return nv ? (nseq == 1 ? 5 : 4) : 6;
+  if (nseq > 1) return nv ? 4 : 6;
+  // one sequence (measured crossovers: 2K keys, the decode kernel still wins at 6
+  // tokens; 8K from 6, NVFP4 4; 16K from 5, NVFP4 3; 32K from 4, NVFP4 3)
+  if (max_pages >= 2 * kVerifyLongPages) return nv ? 3 : 4;
+  if (max_pages >= kVerifyLongPages) return nv ? 3 : 5;
+  if (max_pages >= kVerifyLongPages / 2) return nv ? 4 : 6;
+  return nv ? 8 : 10;
 }
 
 // sms <= 0: the current device's SM count.
